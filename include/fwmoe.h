@@ -1,0 +1,167 @@
+/*
+ * fwmoe — the routed mixture-of-experts feed-forward step over Q8_0 weights,
+ * on one NVIDIA GB300 (sm_103a). C ABI.
+ *
+ * The step (the Flyweight README, "flyweight-llm" 0.2.0, §Features: "sparse
+ * MoE execution"; §Quantization: grouped routed-expert GPU kernels for Q8_0
+ * among other formats; the pages print no formula, and the reading used here
+ * is the standard top-k softmax router):
+ *
+ *   z[t,e]   = sum_h x[t,h] * router_w[e,h] + router_bias[e]        (fp32)
+ *   ids[t,:] = the k largest z[t,.]; ties go to the lower expert id; ordered
+ *              by descending z (equal z: lower id first)
+ *   gates    = softmax of z[t,.] restricted to ids[t,:], renormalised to sum 1
+ *   y_e(x)   = W_down,e ( SiLU(W_gate,e x) * (W_up,e x) ),  SiLU(a) = a/(1+e^-a)
+ *   out[t]   = sum_j gates[t,j] * y_{ids[t,j]}(x_t)  (+ y_shared(x_t), weight 1)
+ *
+ * There is no residual add: out is the MoE output only.
+ *
+ * Q8_0 weight layout accepted by fw_moe_init (GGUF convention; the pages name
+ * the format, §Quantization): each matrix row is cut along its input dimension
+ * into blocks of 32 values, each block 34 bytes: a little-endian IEEE binary16
+ * scale d, then 32 int8 codes q; the weight is d*q. Expert matrices are stored
+ * back to back, expert-major: w_gate / w_up are E x [I rows x H/32 blocks],
+ * w_down is E x [H rows x I/32 blocks].
+ *
+ * Conventions for every call:
+ *  - Pointers named "device" are CUDA device pointers owned by the caller.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Calls enqueue
+ *    asynchronously; none synchronises except fw_moe_init, fw_moe_free,
+ *    fw_moe_status and fw_moe_forward_host.
+ *  - Argument errors are reported before anything is enqueued. A failed call
+ *    returns a negative fw_status and fw_moe_last_error() describes it.
+ *  - There is no CPU fallback: without an sm_103 device, fw_moe_init fails
+ *    with FW_EUNSUPPORTED.
+ */
+#ifndef FWMOE_H
+#define FWMOE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  FW_OK = 0,
+  FW_EINVAL = -1,       /* bad argument (null pointer, size, alignment) */
+  FW_ENOMEM = -2,       /* device allocation failed */
+  FW_ECUDA = -3,        /* a CUDA call or launch failed */
+  FW_EUNSUPPORTED = -4, /* no sm_103 device, or a shape this build does not handle */
+  FW_ESTATE = -5,       /* call order broken (e.g. ffn with a T other than the last route's) */
+  FW_ETIMEOUT = -6,     /* a kernel gave up a bounded wait (see fw_moe_status) */
+  FW_EDEVICE = -7       /* a kernel reported a failed index or layout check */
+} fw_status;
+
+typedef struct fw_moe_handle fw_moe_handle; /* opaque; one handle = one MoE layer */
+
+typedef struct {
+  int32_t H;            /* hidden size; multiple of 64 */
+  int32_t I;            /* per-expert intermediate size; multiple of 64 */
+  int32_t E;            /* routed experts, 1..1024 */
+  int32_t k;            /* experts per token, 1..min(E, 16) */
+  int32_t n_shared;     /* always-on shared experts: 0 or 1 */
+  int32_t T_max;        /* largest T any call on this handle may pass (sizes the workspace) */
+  int32_t decode_T_max; /* T <= this takes the decode (grouped GEMV) path; 0 = 16; at most 16 */
+} fw_moe_config;
+
+typedef struct { /* all DEVICE pointers, read only during fw_moe_init */
+  const float *router_w;       /* [E, H] fp32 row-major */
+  const float *router_bias;    /* [E] fp32 or NULL; added to the logits (selection and gates) */
+  const uint8_t *w_gate;       /* E x [I x H/32] Q8_0 blocks */
+  const uint8_t *w_up;         /* E x [I x H/32] Q8_0 blocks */
+  const uint8_t *w_down;       /* E x [H x I/32] Q8_0 blocks */
+  const uint8_t *shared_gate;  /* [I x H/32] Q8_0, or NULL when n_shared == 0 */
+  const uint8_t *shared_up;    /* [I x H/32] Q8_0, or NULL when n_shared == 0 */
+  const uint8_t *shared_down;  /* [H x I/32] Q8_0, or NULL when n_shared == 0 */
+} fw_moe_weights;
+
+/* Create a layer: validates the shapes, copies the router and repacks every
+ * Q8_0 matrix into the handle's own device memory (a byte-preserving change of
+ * layout: int8 code planes plus binary16 scale planes), allocates the
+ * workspace for T_max tokens and synchronises `stream` once. The caller may
+ * free its weight buffers afterwards. *out receives the handle. */
+fw_status fw_moe_init(const fw_moe_config *cfg, const fw_moe_weights *w, void *stream, fw_moe_handle **out);
+
+/* Routing for T tokens (0 <= T <= T_max): x is DEVICE bf16 [T, H] row-major.
+ * Writes expert_ids (DEVICE int32 [T, k]) and gates (DEVICE fp32 [T, k], may be
+ * NULL), and keeps the routing and the token-to-expert grouping in the handle
+ * for the next fw_moe_ffn. T == 0 is a no-op. */
+fw_status fw_moe_route(fw_moe_handle *h, const void *x, int32_t T, int32_t *expert_ids, float *gates,
+                       void *stream);
+
+/* Experts and combine for the routing made by the last fw_moe_route on this
+ * handle: same x, same T, same stream. out is DEVICE bf16 [T, H] row-major.
+ * A T different from the last route's returns FW_ESTATE. */
+fw_status fw_moe_ffn(fw_moe_handle *h, const void *x, int32_t T, void *out, void *stream);
+
+/* fw_moe_route followed by fw_moe_ffn (expert_ids may not be NULL; gates may). */
+fw_status fw_moe_forward(fw_moe_handle *h, const void *x, int32_t T, int32_t *expert_ids, float *gates, void *out,
+                         void *stream);
+
+/* The whole step from and to HOST memory: copies x (bf16 [T, H]) to the device,
+ * runs fw_moe_forward on the handle's own device buffers, copies expert_ids
+ * (int32 [T, k]) and out (bf16 [T, H]) back and synchronises `stream`. Host
+ * buffers should be pinned for the copies to be asynchronous. */
+fw_status fw_moe_forward_host(fw_moe_handle *h, const void *x_host, int32_t T, int32_t *expert_ids_host,
+                              void *out_host, void *stream);
+
+/* Token-to-expert grouping of the last route (for tests and tools): offsets
+ * DEVICE int32 [E + 1], the exclusive prefix sum of the per-expert counts;
+ * perm DEVICE int32 [T*k], the slot ids s = t*k + j grouped by ascending expert
+ * and, within an expert, by ascending token; inv DEVICE int32 [T*k] (may be
+ * NULL), inv[perm[p]] = p. */
+fw_status fw_moe_get_permutation(fw_moe_handle *h, int32_t *offsets, int32_t *perm, int32_t *inv, void *stream);
+
+/* Copy one repacked matrix of one expert back out in the GGUF Q8_0 layout
+ * (which: 0 gate, 1 up, 2 down; expert E is the shared expert). blocks is
+ * DEVICE memory of rows x K/32 x 34 bytes. Round-trips fw_moe_init's input. */
+fw_status fw_moe_export_q8_0(fw_moe_handle *h, int32_t expert, int32_t which, uint8_t *blocks, void *stream);
+
+/* Synchronise `stream`, read and clear the handle's device status word.
+ * FW_OK, FW_ETIMEOUT or FW_EDEVICE. */
+fw_status fw_moe_status(fw_moe_handle *h, void *stream);
+
+/* Kernel kinds reported by fw_moe_profile_end. */
+enum {
+  FW_KERNEL_ROUTE_DECODE = 0, /* decode router: GEMV, top-k, gates, grouping */
+  FW_KERNEL_ROUTE_TILES = 1,  /* prefill router: tiled GEMM, top-k, per-tile counts */
+  FW_KERNEL_ROUTE_SCAN = 2,   /* prefill grouping: offsets, tile lists */
+  FW_KERNEL_ROUTE_SCATTER = 3,/* prefill grouping: stable scatter */
+  FW_KERNEL_DECODE_GATEUP = 4,/* decode gate/up grouped GEMV + SiLU */
+  FW_KERNEL_DECODE_DOWN = 5,  /* decode down grouped GEMV + combine */
+  FW_KERNEL_PREFILL_GATEUP = 6,
+  FW_KERNEL_PREFILL_DOWN = 7,
+  FW_KERNEL_PREFILL_COMBINE = 8,
+  FW_KERNEL_KINDS = 16
+};
+
+/* Optional per-kernel timing, for measurement tools. After
+ * fw_moe_profile_begin, every kernel this handle launches (up to max_launches)
+ * is bracketed by CUDA events recorded on its own stream; this serialises the
+ * kernels (no programmatic overlap), so profile in a pass of its own.
+ * fw_moe_profile_end synchronises, writes per kind (arrays of n_kinds, at most
+ * FW_KERNEL_KINDS) the summed milliseconds and the launch count, and stops
+ * recording. Creating the events happens in begin, not on the launch path. */
+fw_status fw_moe_profile_begin(fw_moe_handle *h, int32_t max_launches);
+fw_status fw_moe_profile_end(fw_moe_handle *h, int32_t n_kinds, float *total_ms, int32_t *launches);
+
+/* Release the handle (synchronises its device first). NULL is a no-op; a
+ * handle already freed is detected (FW_EINVAL) as long as its memory has not
+ * been reused. */
+fw_status fw_moe_free(fw_moe_handle *h);
+
+/* Text of the last failed call on this thread ("" if none). */
+const char *fw_moe_last_error(void);
+
+/* Quantise fp32 weights to Q8_0 on the GPU: w DEVICE [rows, K] row-major fp32,
+ * K % 32 == 0; blocks DEVICE rows x K/32 x 34 bytes. Per block of 32:
+ * amax = max|w|, d = amax/127 (fp64), q = round-half-away-from-zero(w/d)
+ * clamped to +-127 (fp64), d stored as binary16 (round to nearest even);
+ * an all-zero block stores zeros. */
+fw_status fw_q8_0_quantize(const float *w, int64_t rows, int64_t K, uint8_t *blocks, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

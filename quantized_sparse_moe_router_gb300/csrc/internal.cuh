@@ -1,0 +1,257 @@
+// Internal declarations of the fwmoe library: the handle, the device layout of
+// the repacked weights and workspace, and the small PTX helpers (mbarrier,
+// bulk asynchronous copies, bounded waits) the kernels share.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/fwmoe.h"
+
+namespace fw {
+
+constexpr uint32_t kHandleMagic = 0x4D6F4531u;  // "1EoM"
+constexpr uint32_t kHandleFreed = 0xDEADF00Du;
+constexpr int kQBlock = 32;        // Q8_0 block length
+constexpr int kQBlockBytes = 34;   // fp16 scale + 32 int8
+constexpr int kGUGroup = 64;       // gate/up rows are interleaved in groups of 64
+constexpr int kMaxK = 16;          // experts per token
+constexpr int kMaxDecodeT = 16;    // decode path token limit (one lane per token in the combine)
+constexpr int kRouteTileM = 32;    // tokens per CTA in the tiled router
+
+// Status bits written by kernels into the handle's device status word.
+constexpr int kStatusTimeout = 1;
+constexpr int kStatusBadIndex = 2;
+
+// Scale rows are padded to a multiple of 16 bytes so each row can be fetched
+// with one bulk copy.
+__host__ __device__ inline int64_t scale_pitch_bytes(int64_t K) { return ((K / kQBlock) * 2 + 15) / 16 * 16; }
+
+// Row of gate/up matrix row i in the interleaved [2I, H] code plane:
+// groups of 64 gate rows followed by the 64 up rows of the same i range.
+__host__ __device__ inline int64_t gu_row_gate(int64_t i) { return (i / kGUGroup) * 2 * kGUGroup + (i % kGUGroup); }
+__host__ __device__ inline int64_t gu_row_up(int64_t i) { return gu_row_gate(i) + kGUGroup; }
+
+// Device-side routing metadata (one small struct per handle, device memory).
+struct Meta {
+  int32_t n_unique;     // experts with at least one row, shared included
+  uint32_t ticket;      // last-CTA detection in the router (self-resetting)
+  int32_t status;       // kStatus* bits
+  int32_t T;            // T of the last route
+  int32_t n_mtiles;     // prefill: number of (expert, 128-row) tiles
+  int32_t pad[3];
+};
+
+// Host-side event pool of the optional per-kernel timing.
+struct Timing {
+  cudaEvent_t* ev = nullptr;  // 2 * cap events
+  int* kind = nullptr;        // kind of each recorded pair
+  int cap = 0;
+  int next = 0;
+};
+
+struct Handle {
+  uint32_t magic;
+  Timing* timing;     // null unless profiling
+  fw_moe_config cfg;
+  int S, EU;          // shared experts, routed + shared
+  int device;
+  int num_sms;
+  int last_T;         // T of the last fw_moe_route, -1 before any
+  // ---- repacked weights (device)
+  int8_t* q_gu;       // [EU][2I][H] codes, gate/up interleaved per 64-row group
+  uint8_t* s_gu;      // [EU][2I][pitch(H)] binary16 scales, row-major (padded rows)
+  uint16_t* st_gu;    // [EU][H/32][2I] binary16 scales, transposed
+  int8_t* q_d;        // [EU][H][I]
+  uint8_t* s_d;       // [EU][H][pitch(I)]
+  uint16_t* st_d;     // [EU][I/32][H]
+  float* wr;          // [E][H]
+  float* bias;        // [E] (zeros when none)
+  // ---- workspace (device), sized for T_max
+  int64_t rows_max;   // T_max * (k + S)
+  int32_t* ids;       // [T_max][k]
+  float* gates;       // [T_max][k]
+  float* logits;      // [T_max][E] (decode router)
+  int32_t* counts;    // [EU]
+  int32_t* offsets;   // [EU + 1]
+  int32_t* perm;      // [rows_max]  slot of each grouped row (routed t*k+j, shared T*k+t)
+  int32_t* inv;       // [rows_max]
+  int32_t* row_token; // [rows_max]
+  float* row_gate;    // [rows_max]
+  int32_t* uexp;      // [EU] experts with rows, ascending (shared = E last)
+  int32_t* hist;      // [ceil(T_max/32)][EU] per-tile counts, then per-tile bases
+  int32_t* mtiles;    // [rows_max/128 + EU] prefill tiles: expert << 20 | tile index
+  void* hbuf;         // [rows_max][I] fp32 (decode) or bf16 (prefill)
+  __nv_bfloat16* yp;  // [rows_max][H] bf16 (prefill)
+  Meta* meta;
+  // ---- device staging for fw_moe_forward_host
+  void* x_dev;
+  void* out_dev;
+  int32_t* ids_dev;
+};
+
+// Brackets one kernel launch with events when the handle is profiling.
+struct KernelTimer {
+  Timing* t;
+  int slot;
+  cudaStream_t s;
+  KernelTimer(const Handle* h, int kind, cudaStream_t st) : t(h->timing), slot(-1), s(st) {
+    if (t && t->next < t->cap) {
+      slot = t->next++;
+      t->kind[slot] = kind;
+      cudaEventRecord(t->ev[2 * slot], s);
+    }
+  }
+  ~KernelTimer() {
+    if (slot >= 0) cudaEventRecord(t->ev[2 * slot + 1], s);
+  }
+};
+
+// Allow a kernel the device's full opt-in shared memory (done at init, never on
+// the launch path, so that launches stay legal inside stream capture).
+template <typename K>
+inline cudaError_t allow_max_dynamic_smem(K kernel) {
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa;
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kernel);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
+  return e;
+}
+
+// ---------------------------------------------------------------- launchers
+cudaError_t configure_route_kernels();
+cudaError_t configure_decode_kernels();
+cudaError_t configure_prefill_kernels();
+// Each returns cudaGetLastError() of its launches.
+cudaError_t launch_quantize_q8_0(const float* w, int64_t rows, int64_t K, uint8_t* blocks, cudaStream_t s);
+cudaError_t launch_repack(const Handle* h, int which, int expert0, int count, const uint8_t* blocks,
+                          cudaStream_t s);
+cudaError_t launch_export(const Handle* h, int which, int expert, uint8_t* blocks, cudaStream_t s);
+cudaError_t launch_route_decode(Handle* h, const __nv_bfloat16* x, int T, int32_t* ids_out, float* gates_out,
+                                cudaStream_t s);
+cudaError_t launch_route_prefill(Handle* h, const __nv_bfloat16* x, int T, int32_t* ids_out, float* gates_out,
+                                 cudaStream_t s);
+cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfloat16* out, cudaStream_t s);
+cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bfloat16* out, cudaStream_t s);
+cudaError_t launch_get_permutation(const Handle* h, int T, int32_t* offsets, int32_t* perm, int32_t* inv,
+                                   cudaStream_t s);
+
+}  // namespace fw
+
+// ---------------------------------------------------------------- device helpers
+namespace fw {
+namespace dev {
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Every wait in these kernels gives up after this long and reports kStatusTimeout.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait for the phase with the given parity to complete. false = gave up.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0 = globaltimer_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// One bulk asynchronous copy global -> shared (16-byte aligned, size % 16 == 0),
+// completion counted in bytes on `bar`.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel in the stream start its
+// prologue, and wait for the previous kernel's results.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Four int8 codes packed in a word -> four exact floats, without a conversion
+// instruction: byte b of (w ^ 0x80808080) is q_b + 128; placing it in the low
+// mantissa byte of 2^23 gives the float 2^23 + q_b + 128 exactly, and
+// subtracting 2^23 + 128 leaves q_b.
+__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float& a, float& b, float& c, float& d) {
+  const uint32_t u = w ^ 0x80808080u;
+  const float bias = 8388736.0f;  // 2^23 + 128
+  a = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - bias;
+  b = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - bias;
+  c = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7652)) - bias;
+  d = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7653)) - bias;
+}
+
+// Two bf16 packed in a word -> two floats (exact).
+__device__ __forceinline__ void bf16x2_to_f32(uint32_t w, float& lo, float& hi) {
+  lo = __uint_as_float(w << 16);
+  hi = __uint_as_float(w & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ float half_bits_to_f32(uint16_t b) { return __half2float(__ushort_as_half(b)); }
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ void report(Meta* m, int bits) { atomicOr(&m->status, bits); }
+
+}  // namespace dev
+}  // namespace fw

@@ -1,0 +1,157 @@
+// Q8_0 on the device: the quantiser, and the one-time repack of GGUF-style
+// 34-byte blocks into the handle's aligned planes (and back, for checking).
+//
+// Q8_0 is named on the pages as one of the GGUF tensor formats the grouped
+// routed-expert kernels read (Flyweight README, §Quantization); its layout is
+// the GGUF one: per 32 consecutive values of a row, a binary16 scale d then 32
+// int8 codes, value = d * q.
+#include "internal.cuh"
+
+namespace fw {
+namespace {
+
+__device__ __forceinline__ double round_half_away(double v) {
+  double a = fabs(v);
+  double fl = floor(a);
+  double r = (a - fl >= 0.5) ? fl + 1.0 : fl;
+  return v < 0.0 ? -r : r;
+}
+
+// One thread per 32-value block. The decisions (d and every code) are taken in
+// fp64: d = amax/127, q = round-half-away(w/d), clamp to +-127; d is stored
+// rounded to binary16 (nearest even).
+__global__ void quantize_q8_0_kernel(const float* __restrict__ w, int64_t nblocks, uint8_t* __restrict__ out) {
+  int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (blk >= nblocks) return;
+  const float4* src = reinterpret_cast<const float4*>(w + blk * kQBlock);
+  float v[kQBlock];
+#pragma unroll
+  for (int i = 0; i < kQBlock / 4; ++i) {
+    float4 f = src[i];
+    v[4 * i] = f.x;
+    v[4 * i + 1] = f.y;
+    v[4 * i + 2] = f.z;
+    v[4 * i + 3] = f.w;
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < kQBlock; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  double d = (double)amax / 127.0;
+  uint16_t dbits = __half_as_ushort(__double2half(d));
+  uint16_t* dst = reinterpret_cast<uint16_t*>(out + blk * kQBlockBytes);  // 34-byte blocks are 2-byte aligned
+  dst[0] = dbits;
+#pragma unroll
+  for (int i = 0; i < kQBlock; i += 2) {
+    int q0 = 0, q1 = 0;
+    if (amax > 0.0f) {
+      q0 = (int)fmin(127.0, fmax(-127.0, round_half_away((double)v[i] / d)));
+      q1 = (int)fmin(127.0, fmax(-127.0, round_half_away((double)v[i + 1] / d)));
+    }
+    dst[1 + i / 2] = (uint16_t)((uint8_t)(int8_t)q0 | ((uint16_t)(uint8_t)(int8_t)q1 << 8));
+  }
+}
+
+struct PlaneView {
+  int8_t* q;       // code plane of this matrix kind, expert 0
+  uint8_t* s;      // row-major scale plane (padded rows)
+  uint16_t* st;    // transposed scale plane
+  int64_t rows;    // rows of one expert's matrix (I for gate/up, H for down)
+  int64_t prows;   // rows of one expert in the plane (2I for gate/up, H for down)
+  int64_t K;       // row length (H for gate/up, I for down)
+  int which;       // 0 gate, 1 up, 2 down
+};
+
+__device__ __forceinline__ int64_t plane_row(const PlaneView& p, int64_t r) {
+  return p.which == 0 ? gu_row_gate(r) : (p.which == 1 ? gu_row_up(r) : r);
+}
+
+// One thread per block of one expert range: GGUF block -> code plane + both scale planes.
+__global__ void repack_kernel(PlaneView p, int expert0, int64_t nblocks, const uint8_t* __restrict__ src) {
+  int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (blk >= nblocks) return;
+  const int64_t nb = p.K / kQBlock;
+  const int64_t per_expert = p.rows * nb;
+  const int64_t e = expert0 + blk / per_expert;
+  const int64_t r = (blk % per_expert) / nb;
+  const int64_t b = blk % nb;
+  const uint16_t* in = reinterpret_cast<const uint16_t*>(src + blk * kQBlockBytes);
+  uint32_t words[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) words[i] = (uint32_t)in[1 + 2 * i] | ((uint32_t)in[2 + 2 * i] << 16);
+  const int64_t prow = e * p.prows + plane_row(p, r);
+  uint4* qd = reinterpret_cast<uint4*>(p.q + prow * p.K + b * kQBlock);
+  qd[0] = make_uint4(words[0], words[1], words[2], words[3]);
+  qd[1] = make_uint4(words[4], words[5], words[6], words[7]);
+  reinterpret_cast<uint16_t*>(p.s + prow * scale_pitch_bytes(p.K))[b] = in[0];
+  p.st[(e * nb + b) * p.prows + plane_row(p, r)] = in[0];
+}
+
+__global__ void export_kernel(PlaneView p, int expert, int64_t nblocks, uint8_t* __restrict__ dst) {
+  int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (blk >= nblocks) return;
+  const int64_t nb = p.K / kQBlock;
+  const int64_t r = blk / nb, b = blk % nb;
+  const int64_t prow = (int64_t)expert * p.prows + plane_row(p, r);
+  const uint4* qs = reinterpret_cast<const uint4*>(p.q + prow * p.K + b * kQBlock);
+  uint4 a = qs[0], c = qs[1];
+  uint32_t words[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+  uint16_t* out = reinterpret_cast<uint16_t*>(dst + blk * kQBlockBytes);
+  out[0] = reinterpret_cast<const uint16_t*>(p.s + prow * scale_pitch_bytes(p.K))[b];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    out[1 + 2 * i] = (uint16_t)(words[i] & 0xFFFF);
+    out[2 + 2 * i] = (uint16_t)(words[i] >> 16);
+  }
+}
+
+PlaneView view_of(const Handle* h, int which) {
+  PlaneView p;
+  const int64_t H = h->cfg.H, I = h->cfg.I;
+  p.which = which;
+  if (which == 2) {
+    p.q = h->q_d;
+    p.s = h->s_d;
+    p.st = h->st_d;
+    p.rows = H;
+    p.prows = H;
+    p.K = I;
+  } else {
+    p.q = h->q_gu;
+    p.s = h->s_gu;
+    p.st = h->st_gu;
+    p.rows = I;
+    p.prows = 2 * I;
+    p.K = H;
+  }
+  return p;
+}
+
+unsigned grid_1d(int64_t n, int threads) { return (unsigned)((n + threads - 1) / threads); }
+
+}  // namespace
+
+cudaError_t launch_quantize_q8_0(const float* w, int64_t rows, int64_t K, uint8_t* blocks, cudaStream_t s) {
+  int64_t nblocks = rows * (K / kQBlock);
+  if (nblocks == 0) return cudaSuccess;
+  quantize_q8_0_kernel<<<grid_1d(nblocks, 256), 256, 0, s>>>(w, nblocks, blocks);
+  return cudaGetLastError();
+}
+
+// Repack `count` consecutive experts starting at `expert0` (count experts of GGUF blocks at `blocks`).
+cudaError_t launch_repack(const Handle* h, int which, int expert0, int count, const uint8_t* blocks,
+                          cudaStream_t s) {
+  PlaneView p = view_of(h, which);
+  int64_t nblocks = (int64_t)count * p.rows * (p.K / kQBlock);
+  if (nblocks == 0) return cudaSuccess;
+  repack_kernel<<<grid_1d(nblocks, 256), 256, 0, s>>>(p, expert0, nblocks, blocks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_export(const Handle* h, int which, int expert, uint8_t* blocks, cudaStream_t s) {
+  PlaneView p = view_of(h, which);
+  int64_t nblocks = p.rows * (p.K / kQBlock);
+  export_kernel<<<grid_1d(nblocks, 256), 256, 0, s>>>(p, expert, nblocks, blocks);
+  return cudaGetLastError();
+}
+
+}  // namespace fw
