@@ -67,7 +67,7 @@ struct Allocator {
 
 void free_handle_memory(Handle* h) {
   void* ptrs[] = {h->q_gu, h->s_gu, h->st_gu, h->q_d, h->s_d, h->st_d, h->wr, h->bias, h->ids, h->gates,
-                  h->logits, h->counts, h->offsets, h->perm, h->inv, h->row_token, h->row_gate, h->uexp,
+                  h->logits, h->counts, h->offsets, h->perm, h->inv, h->row_token, h->row_gate, h->uinfo,
                   h->hist, h->mtiles, h->hbuf, h->yp, h->meta, h->x_dev, h->out_dev, h->ids_dev};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -163,7 +163,7 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
       {(void**)&h->inv, (size_t)(h->rows_max * 4)},
       {(void**)&h->row_token, (size_t)(h->rows_max * 4)},
       {(void**)&h->row_gate, (size_t)(h->rows_max * 4)},
-      {(void**)&h->uexp, (size_t)(EU * 4)},
+      {(void**)&h->uinfo, (size_t)(EU * 16)},
       {(void**)&h->hist, (size_t)(n_route_tiles * EU * 4)},
       {(void**)&h->mtiles, (size_t)(n_mtiles_max * 4)},
       {(void**)&h->hbuf, hbuf_bytes},

@@ -80,7 +80,7 @@ struct Handle {
   int32_t* inv;       // [rows_max]
   int32_t* row_token; // [rows_max]
   float* row_gate;    // [rows_max]
-  int32_t* uexp;      // [EU] experts with rows, ascending (shared = E last)
+  int4* uinfo;        // [EU] (expert, first grouped row, rows, 0) of the experts with rows, ascending id
   int32_t* hist;      // [ceil(T_max/32)][EU] per-tile counts, then per-tile bases
   int32_t* mtiles;    // [rows_max/128 + EU] prefill tiles: expert << 20 | tile index
   void* hbuf;         // [rows_max][I] fp32 (decode) or bf16 (prefill)

@@ -68,11 +68,13 @@ __device__ __forceinline__ float warp_gate(float my_z, int k, int lane) {
   return ex / sum;
 }
 
-// Exclusive scan of n <= 1024 ints in shared memory by the whole block
-// (blockDim.x == 128). Returns the total.
-__device__ int block_exclusive_scan_128(int* v, int n, int* warp_tot) {
+// Exclusive scan of n ints in shared memory by the whole block of NT threads.
+// Returns the total.
+template <int NT>
+__device__ int block_exclusive_scan(int* v, int n, int* warp_tot) {
+  constexpr int NW = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int per = (n + 127) / 128;
+  const int per = (n + NT - 1) / NT;
   const int b = tid * per, e = min(n, b + per);
   int s = 0;
   for (int i = b; i < e; ++i) s += v[i];
@@ -85,7 +87,8 @@ __device__ int block_exclusive_scan_128(int* v, int n, int* warp_tot) {
   if (lane == 31) warp_tot[w] = incl;
   __syncthreads();
   int wbase = 0, total = 0;
-  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+  for (int i = 0; i < NW; ++i) {
     if (i < w) wbase += warp_tot[i];
     total += warp_tot[i];
   }
@@ -116,65 +119,89 @@ struct RouteArgs {
   int32_t* inv;
   int32_t* row_token;
   float* row_gate;
-  int32_t* uexp;
+  int4* uinfo;
   Meta* meta;
 };
 
-// Grid: ceil(E / 4) CTAs of 4 warps, one warp per expert row of the router.
-// The last CTA to finish (atomic ticket, no waiting) does the selection, the
-// gates and the grouping for all T <= 16 tokens.
-__global__ void __launch_bounds__(128) route_decode_kernel(RouteArgs a) {
+constexpr int kRouteThreads = 256;
+constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kRouteUnroll = 8;  // float4 loads of the router row in flight per lane
+
+// Grid: E CTAs of 8 warps; CTA e computes z[t][e] for the T <= 16 tokens, its
+// warps splitting H with all of a lane's loads issued before any use. The
+// last CTA to finish (atomic ticket, no waiting) selects, makes the gates and
+// groups the (token, slot) pairs for all tokens.
+__global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a) {
+  __shared__ float s_part[kRouteWarps][kMaxDecodeT];
   __shared__ int s_cnt[kMaxE + 2];
+  __shared__ int s_c2[kMaxE + 1];
   __shared__ uint32_t s_mask[kMaxE + 1];
   __shared__ int s_nz[kMaxE + 2];
   __shared__ int s_ids[kMaxDecodeT * kMaxK];
   __shared__ float s_gates[kMaxDecodeT * kMaxK];
-  __shared__ int s_wtot[4];
+  __shared__ int s_wtot[kRouteWarps];
   __shared__ bool s_last;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int e = blockIdx.x * 4 + warp;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int e = blockIdx.x;
   const int T = a.T, H = a.H;
   pdl_launch_dependents();  // the expert kernels wait for this grid's completion before reading
-  if (e < a.E) {
+  {
     float acc[kMaxDecodeT];
 #pragma unroll
     for (int t = 0; t < kMaxDecodeT; ++t) acc[t] = 0.0f;
     const float* wrow = a.wr + (int64_t)e * H;
-    for (int h0 = 4 * lane; h0 < H; h0 += 128) {
-      float4 w = __ldg(reinterpret_cast<const float4*>(wrow + h0));
+    for (int base = 4 * tid; base < H; base += 4 * kRouteThreads * kRouteUnroll) {
+      float4 w[kRouteUnroll];
 #pragma unroll
-      for (int t = 0; t < kMaxDecodeT; ++t) {
-        if (t < T) {
-          uint2 xv = __ldg(reinterpret_cast<const uint2*>(a.x + (int64_t)t * H + h0));
-          float x0, x1, x2, x3;
-          bf16x2_to_f32(xv.x, x0, x1);
-          bf16x2_to_f32(xv.y, x2, x3);
-          acc[t] = fmaf(x0, w.x, acc[t]);
-          acc[t] = fmaf(x1, w.y, acc[t]);
-          acc[t] = fmaf(x2, w.z, acc[t]);
-          acc[t] = fmaf(x3, w.w, acc[t]);
+      for (int u = 0; u < kRouteUnroll; ++u) {
+        int h = base + 4 * kRouteThreads * u;
+        w[u] = h < H ? __ldg(reinterpret_cast<const float4*>(wrow + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kRouteUnroll; ++u) {
+        int h = base + 4 * kRouteThreads * u;
+        if (h < H) {
+#pragma unroll
+          for (int t = 0; t < kMaxDecodeT; ++t) {
+            if (t < T) {
+              uint2 xv = __ldg(reinterpret_cast<const uint2*>(a.x + (int64_t)t * H + h));
+              float x0, x1, x2, x3;
+              bf16x2_to_f32(xv.x, x0, x1);
+              bf16x2_to_f32(xv.y, x2, x3);
+              acc[t] = fmaf(x0, w[u].x, acc[t]);
+              acc[t] = fmaf(x1, w[u].y, acc[t]);
+              acc[t] = fmaf(x2, w[u].z, acc[t]);
+              acc[t] = fmaf(x3, w[u].w, acc[t]);
+            }
+          }
         }
       }
     }
-    const float b = a.bias[e];
 #pragma unroll
     for (int t = 0; t < kMaxDecodeT; ++t) {
       if (t < T) {
         float v = warp_sum(acc[t]);
-        if (lane == 0) a.logits[t * a.E + e] = v + b;
+        if (lane == 0) s_part[warp][t] = v;
       }
     }
+  }
+  __syncthreads();
+  if (tid < T) {
+    float z = 0.f;
+#pragma unroll
+    for (int w = 0; w < kRouteWarps; ++w) z += s_part[w][tid];
+    a.logits[tid * a.E + e] = z + a.bias[e];
     __threadfence();
   }
   __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicInc(&a.meta->ticket, gridDim.x - 1) == gridDim.x - 1;
+  if (tid == 0) s_last = atomicInc(&a.meta->ticket, gridDim.x - 1) == gridDim.x - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
 
   // ---- selection and gates: one warp per token
   const int k = a.k, E = a.E;
-  for (int t = warp; t < T; t += 4) {
+  for (int t = warp; t < T; t += kRouteWarps) {
     float zl[kMaxEPerLane];
 #pragma unroll
     for (int m = 0; m < kMaxEPerLane; ++m) {
@@ -196,24 +223,25 @@ __global__ void __launch_bounds__(128) route_decode_kernel(RouteArgs a) {
   }
   // ---- grouping: counts, offsets, stable ranks via per-expert token masks
   const int EU = E + a.S;
-  for (int i = threadIdx.x; i < EU + 1; i += 128) s_cnt[i] = 0;
-  for (int i = threadIdx.x; i < EU; i += 128) s_mask[i] = 0;
+  for (int i = tid; i < EU + 1; i += kRouteThreads) s_cnt[i] = 0;
+  for (int i = tid; i < EU; i += kRouteThreads) s_mask[i] = 0;
   __syncthreads();
-  for (int p = threadIdx.x; p < T * k; p += 128) {
+  for (int p = tid; p < T * k; p += kRouteThreads) {
     int ee = s_ids[p];
     atomicAdd(&s_cnt[ee], 1);
     atomicOr(&s_mask[ee], 1u << (p / k));
   }
-  if (a.S && threadIdx.x == 0) s_cnt[E] = T;
+  if (a.S && tid == 0) s_cnt[E] = T;
   __syncthreads();
-  for (int i = threadIdx.x; i < EU; i += 128) {
+  for (int i = tid; i < EU; i += kRouteThreads) {
     a.counts[i] = s_cnt[i];
+    s_c2[i] = s_cnt[i];
     s_nz[i] = s_cnt[i] > 0;
   }
   __syncthreads();
-  block_exclusive_scan_128(s_cnt, EU + 1, s_wtot);  // s_cnt[EU] = total rows
-  for (int i = threadIdx.x; i < EU + 1; i += 128) a.offsets[i] = s_cnt[i];
-  for (int p = threadIdx.x; p < T * k; p += 128) {
+  block_exclusive_scan<kRouteThreads>(s_cnt, EU + 1, s_wtot);  // s_cnt[EU] = total rows
+  for (int i = tid; i < EU + 1; i += kRouteThreads) a.offsets[i] = s_cnt[i];
+  for (int p = tid; p < T * k; p += kRouteThreads) {
     int t = p / k, ee = s_ids[p];
     int pos = s_cnt[ee] + __popc(s_mask[ee] & ((1u << t) - 1u));
     a.perm[pos] = p;
@@ -222,7 +250,7 @@ __global__ void __launch_bounds__(128) route_decode_kernel(RouteArgs a) {
     a.row_gate[pos] = s_gates[p];
   }
   if (a.S) {
-    for (int t = threadIdx.x; t < T; t += 128) {
+    for (int t = tid; t < T; t += kRouteThreads) {
       int pos = s_cnt[E] + t;
       a.perm[pos] = T * k + t;
       a.inv[T * k + t] = pos;
@@ -231,10 +259,10 @@ __global__ void __launch_bounds__(128) route_decode_kernel(RouteArgs a) {
     }
   }
   __syncthreads();
-  int n_unique = block_exclusive_scan_128(s_nz, EU, s_wtot);
-  for (int i = threadIdx.x; i < EU; i += 128)
-    if (a.counts[i] > 0) a.uexp[s_nz[i]] = i;
-  if (threadIdx.x == 0) {
+  int n_unique = block_exclusive_scan<kRouteThreads>(s_nz, EU, s_wtot);
+  for (int i = tid; i < EU; i += kRouteThreads)
+    if (s_c2[i] > 0) a.uinfo[s_nz[i]] = make_int4(i, s_cnt[i], s_c2[i], 0);
+  if (tid == 0) {
     a.meta->n_unique = n_unique;
     a.meta->T = T;
   }
@@ -392,7 +420,7 @@ __global__ void __launch_bounds__(256) route_scan_kernel(RouteArgs a, int32_t* h
   for (int e = tid; e < EU + 1; e += 256) a.offsets[e] = s_off[e];
   for (int e = tid; e < EU; e += 256) {
     int cnt = a.counts[e];
-    if (cnt > 0) a.uexp[s_nz[e]] = e;
+    if (cnt > 0) a.uinfo[s_nz[e]] = make_int4(e, s_off[e], cnt, 0);
     int nt = (cnt + 127) / 128;
     for (int i = 0; i < nt; ++i) mtiles[s_nt[e] + i] = (e << 16) | i;
   }
@@ -459,7 +487,7 @@ RouteArgs route_args(Handle* h, const __nv_bfloat16* x, int T, int32_t* ids_out,
   a.inv = h->inv;
   a.row_token = h->row_token;
   a.row_gate = h->row_gate;
-  a.uexp = h->uexp;
+  a.uinfo = h->uinfo;
   a.meta = h->meta;
   return a;
 }
@@ -491,7 +519,7 @@ cudaError_t launch_route_decode(Handle* h, const __nv_bfloat16* x, int T, int32_
                                 cudaStream_t s) {
   RouteArgs a = route_args(h, x, T, ids_out, gates_out);
   KernelTimer tm(h, FW_KERNEL_ROUTE_DECODE, s);
-  route_decode_kernel<<<(h->cfg.E + 3) / 4, 128, 0, s>>>(a);
+  route_decode_kernel<<<h->cfg.E, kRouteThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
