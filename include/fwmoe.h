@@ -130,9 +130,10 @@ enum {
   FW_KERNEL_ROUTE_SCATTER = 3,/* prefill grouping: stable scatter */
   FW_KERNEL_DECODE_GATEUP = 4,/* decode gate/up grouped GEMV + SiLU */
   FW_KERNEL_DECODE_DOWN = 5,  /* decode down grouped GEMV + combine */
-  FW_KERNEL_PREFILL_GATEUP = 6,
-  FW_KERNEL_PREFILL_DOWN = 7,
-  FW_KERNEL_PREFILL_COMBINE = 8,
+  FW_KERNEL_PREFILL_GATEUP = 6,  /* prefill gate/up grouped GEMM (tcgen05) + SiLU */
+  FW_KERNEL_PREFILL_DOWN = 7,    /* prefill down grouped GEMM (tcgen05) x gate */
+  FW_KERNEL_PREFILL_COMBINE = 8, /* prefill un-permute and sum */
+  FW_KERNEL_PREFILL_GATHER = 9, /* prefill: x rows gathered into grouped order */
   FW_KERNEL_KINDS = 16
 };
 

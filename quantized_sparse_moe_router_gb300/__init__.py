@@ -53,7 +53,7 @@ EXPORTED = ("fw_moe_init", "fw_moe_route", "fw_moe_ffn", "fw_moe_forward", "fw_m
             "fw_q8_0_quantize", "fw_moe_profile_begin", "fw_moe_profile_end")
 
 KERNEL_KINDS = ("route_decode", "route_tiles", "route_scan", "route_scatter", "decode_gateup", "decode_down",
-                "prefill_gateup", "prefill_down", "prefill_combine")
+                "prefill_gateup", "prefill_down", "prefill_combine", "prefill_gather")
 
 
 def lib():

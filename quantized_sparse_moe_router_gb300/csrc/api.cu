@@ -68,7 +68,7 @@ struct Allocator {
 void free_handle_memory(Handle* h) {
   void* ptrs[] = {h->q_gu, h->s_gu, h->st_gu, h->q_d, h->s_d, h->st_d, h->wr, h->bias, h->ids, h->gates,
                   h->logits, h->counts, h->offsets, h->perm, h->inv, h->row_token, h->row_gate, h->uinfo,
-                  h->hist, h->mtiles, h->hbuf, h->yp, h->meta, h->x_dev, h->out_dev, h->ids_dev};
+                  h->hist, h->minfo, h->xperm, h->hbuf, h->yp, h->meta, h->x_dev, h->out_dev, h->ids_dev};
   for (void* p : ptrs)
     if (p) cudaFree(p);
 }
@@ -165,7 +165,8 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
       {(void**)&h->row_gate, (size_t)(h->rows_max * 4)},
       {(void**)&h->uinfo, (size_t)(EU * 16)},
       {(void**)&h->hist, (size_t)(n_route_tiles * EU * 4)},
-      {(void**)&h->mtiles, (size_t)(n_mtiles_max * 4)},
+      {(void**)&h->minfo, (size_t)(n_mtiles_max * 16)},
+      {(void**)&h->xperm, (size_t)(Tm > decode_limit(h) ? h->rows_max * H * 2 : 256)},
       {(void**)&h->hbuf, hbuf_bytes},
       {(void**)&h->yp, (size_t)(Tm > decode_limit(h) ? h->rows_max * H * 2 : 256)},
       {(void**)&h->meta, sizeof(Meta)},
@@ -199,9 +200,16 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
     if (e == cudaSuccess) e = launch_repack(h, 1, (int)E, 1, w->shared_up, s);
     if (e == cudaSuccess) e = launch_repack(h, 2, (int)E, 1, w->shared_down, s);
   }
+  if (e == cudaSuccess && Tm > decode_limit(h)) {
+    // rows past the valid ones of a tile are read (and masked); keep them finite
+    e = cudaMemsetAsync(h->xperm, 0, (size_t)h->rows_max * H * 2, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(h->hbuf, 0, hbuf_bytes, s);
+    if (e == cudaSuccess) e = prepare_prefill(h);
+  }
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);
   if (e != cudaSuccess) {
     A.release();
+    delete h->maps;
     delete h;
     return cuda_fail(e, "fw_moe_init");
   }
@@ -235,7 +243,7 @@ fw_status fw_moe_route(fw_moe_handle* hh, const void* x, int32_t T, int32_t* exp
   if (T == 0) return FW_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  cudaError_t e = T <= decode_limit(h) ? launch_route_decode(h, xb, T, expert_ids, gates, s)
+  cudaError_t e = T <= decode_limit(h) ? launch_route_decode(h, xb, T, expert_ids, gates, true, s)
                                         : launch_route_prefill(h, xb, T, expert_ids, gates, s);
   if (e != cudaSuccess) {
     h->last_T = -1;
@@ -255,17 +263,40 @@ fw_status fw_moe_ffn(fw_moe_handle* hh, const void* x, int32_t T, void* out, voi
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out);
-  cudaError_t e = T <= decode_limit(h) ? launch_ffn_decode(h, xb, T, ob, s) : launch_ffn_prefill(h, xb, T, ob, s);
+  cudaError_t e = T <= decode_limit(h) ? launch_ffn_decode(h, xb, T, ob, false, nullptr, nullptr, s)
+                                        : launch_ffn_prefill(h, xb, T, ob, s);
   if (e == cudaErrorNotSupported) return fail(FW_EUNSUPPORTED, "fw_moe_ffn: prefill path not available in this build");
   if (e != cudaSuccess) return cuda_fail(e, "fw_moe_ffn launch");
   return FW_OK;
 }
 
-fw_status fw_moe_forward(fw_moe_handle* h, const void* x, int32_t T, int32_t* expert_ids, float* gates, void* out,
+fw_status fw_moe_forward(fw_moe_handle* hh, const void* x, int32_t T, int32_t* expert_ids, float* gates, void* out,
                          void* stream) {
-  fw_status st = fw_moe_route(h, x, T, expert_ids, gates, stream);
+  Handle* h = reinterpret_cast<Handle*>(hh);
+  fw_status st = check_call(h, x, T, "fw_moe_forward");
   if (st != FW_OK) return st;
-  return fw_moe_ffn(h, x, T, out, stream);
+  if (T > 0 && (!expert_ids || !aligned(expert_ids, 4) || (gates && !aligned(gates, 4))))
+    return fail(FW_EINVAL, "fw_moe_forward: expert_ids must be a 4-byte aligned device pointer");
+  if (T > 0 && (!out || !aligned(out, 16)))
+    return fail(FW_EINVAL, "fw_moe_forward: out must be a 16-byte aligned device pointer");
+  if (T > decode_limit(h)) {
+    st = fw_moe_route(hh, x, T, expert_ids, gates, stream);
+    return st != FW_OK ? st : fw_moe_ffn(hh, x, T, out, stream);
+  }
+  h->last_T = T;
+  if (T == 0) return FW_OK;
+  // decode: the router only makes logits; the expert kernels select and group
+  // (in shared memory) and the gate/up kernel publishes ids, gates and grouping
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  cudaError_t e = launch_route_decode(h, xb, T, expert_ids, gates, false, s);
+  if (e == cudaSuccess)
+    e = launch_ffn_decode(h, xb, T, static_cast<__nv_bfloat16*>(out), true, expert_ids, gates, s);
+  if (e != cudaSuccess) {
+    h->last_T = -1;
+    return cuda_fail(e, "fw_moe_forward launch");
+  }
+  return FW_OK;
 }
 
 fw_status fw_moe_forward_host(fw_moe_handle* hh, const void* x_host, int32_t T, int32_t* ids_host, void* out_host,
@@ -395,6 +426,7 @@ fw_status fw_moe_free(fw_moe_handle* hh) {
   cudaError_t e = cudaDeviceSynchronize();
   drop_timing(h);
   free_handle_memory(h);
+  delete h->maps;
   h->magic = kHandleFreed;
   delete h;
   if (e != cudaSuccess) return cuda_fail(e, "fw_moe_free");

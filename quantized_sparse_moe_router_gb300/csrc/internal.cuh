@@ -3,6 +3,7 @@
 // bulk asynchronous copies, bounded waits) the kernels share.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -52,9 +53,20 @@ struct Timing {
   int next = 0;
 };
 
+// TMA descriptors of the prefill GEMMs (host copies, passed by value).
+struct PrefillMaps {
+  CUtensorMap a_x;    // xperm [rows_max][H] bf16, box 64 x 128, 128B swizzle
+  CUtensorMap a_h;    // hbuf  [rows_max][I] bf16, box 64 x 128, 128B swizzle
+  CUtensorMap q_gu;   // code plane [EU*2I][H] u8, box 64 x 256
+  CUtensorMap s_gu;   // scale plane [EU*H/32][2I] u16, box 256 x 2
+  CUtensorMap q_d;    // [EU*H][I] u8
+  CUtensorMap s_d;    // [EU*I/32][H] u16
+};
+
 struct Handle {
   uint32_t magic;
   Timing* timing;     // null unless profiling
+  PrefillMaps* maps;  // null unless T_max exceeds the decode limit
   fw_moe_config cfg;
   int S, EU;          // shared experts, routed + shared
   int device;
@@ -82,7 +94,8 @@ struct Handle {
   float* row_gate;    // [rows_max]
   int4* uinfo;        // [EU] (expert, first grouped row, rows, 0) of the experts with rows, ascending id
   int32_t* hist;      // [ceil(T_max/32)][EU] per-tile counts, then per-tile bases
-  int32_t* mtiles;    // [rows_max/128 + EU] prefill tiles: expert << 20 | tile index
+  int4* minfo;        // [rows_max/128 + EU] prefill 128-row tiles: (expert, first row, valid rows, 0)
+  __nv_bfloat16* xperm; // [rows_max][H] x gathered into grouped order (prefill)
   void* hbuf;         // [rows_max][I] fp32 (decode) or bf16 (prefill)
   __nv_bfloat16* yp;  // [rows_max][H] bf16 (prefill)
   Meta* meta;
@@ -127,16 +140,22 @@ inline cudaError_t allow_max_dynamic_smem(K kernel) {
 cudaError_t configure_route_kernels();
 cudaError_t configure_decode_kernels();
 cudaError_t configure_prefill_kernels();
+cudaError_t prepare_prefill(Handle* h);  // tensor maps; needs the planes and workspace allocated
 // Each returns cudaGetLastError() of its launches.
 cudaError_t launch_quantize_q8_0(const float* w, int64_t rows, int64_t K, uint8_t* blocks, cudaStream_t s);
 cudaError_t launch_repack(const Handle* h, int which, int expert0, int count, const uint8_t* blocks,
                           cudaStream_t s);
 cudaError_t launch_export(const Handle* h, int which, int expert, uint8_t* blocks, cudaStream_t s);
+// select: publish ids/gates/grouping from the router itself (standalone
+// route); otherwise only logits, and the decode expert kernels route.
 cudaError_t launch_route_decode(Handle* h, const __nv_bfloat16* x, int T, int32_t* ids_out, float* gates_out,
-                                cudaStream_t s);
+                                bool select, cudaStream_t s);
 cudaError_t launch_route_prefill(Handle* h, const __nv_bfloat16* x, int T, int32_t* ids_out, float* gates_out,
                                  cudaStream_t s);
-cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfloat16* out, cudaStream_t s);
+// publish: the gate/up kernel also writes ids (to ids_out/gates_out, which may
+// be null) and the grouping, for a forward whose router did not select.
+cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfloat16* out, bool publish,
+                              int32_t* ids_out, float* gates_out, cudaStream_t s);
 cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bfloat16* out, cudaStream_t s);
 cudaError_t launch_get_permutation(const Handle* h, int T, int32_t* offsets, int32_t* perm, int32_t* inv,
                                    cudaStream_t s);

@@ -8,99 +8,12 @@
 // lower id, ordered by descending z, gates = softmax restricted to the k and
 // renormalised; then the (token, slot) pairs grouped by expert, stable in
 // token order, with every count and offset kept on the device.
-#include "internal.cuh"
+#include "routing.cuh"
 
 namespace fw {
 namespace {
 
 using namespace dev;
-
-constexpr int kMaxE = 256;               // experts supported by the register layouts below
-constexpr int kMaxEPerLane = kMaxE / 32;
-
-// --------------------------------------------------------------- top-k
-// One warp selects the k largest of z[0..E) (lane l holds z[l + 32 m]),
-// ties to the lower id, in descending order; lane j < k ends with
-// (id_j, z_j) in (*out_id, *out_z).
-__device__ __forceinline__ void warp_topk(const float (&zl)[kMaxEPerLane], int E, int k, int lane, int* out_id,
-                                          float* out_z) {
-  uint32_t taken = 0;  // bit m: z[lane + 32 m] already selected
-  int my_id = -1;
-  float my_z = 0.0f;
-  for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-#pragma unroll
-    for (int m = 0; m < kMaxEPerLane; ++m) {
-      int e = lane + 32 * m;
-      if (e < E && !((taken >> m) & 1u)) {
-        float v = zl[m];
-        if (v > bv || (v == bv && e < bi)) {
-          bv = v;
-          bi = e;
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-      int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (lane == j) {
-      my_id = bi;
-      my_z = bv;
-    }
-  }
-  *out_id = my_id;
-  *out_z = my_z;
-}
-
-// Gates of the selection held by lanes 0..k-1: exp(z_j - z_0) / sum.
-__device__ __forceinline__ float warp_gate(float my_z, int k, int lane) {
-  float z0 = __shfl_sync(0xFFFFFFFFu, my_z, 0);
-  float ex = lane < k ? expf(my_z - z0) : 0.0f;
-  float sum = warp_sum(ex);
-  return ex / sum;
-}
-
-// Exclusive scan of n ints in shared memory by the whole block of NT threads.
-// Returns the total.
-template <int NT>
-__device__ int block_exclusive_scan(int* v, int n, int* warp_tot) {
-  constexpr int NW = NT / 32;
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int per = (n + NT - 1) / NT;
-  const int b = tid * per, e = min(n, b + per);
-  int s = 0;
-  for (int i = b; i < e; ++i) s += v[i];
-  int incl = s;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  if (lane == 31) warp_tot[w] = incl;
-  __syncthreads();
-  int wbase = 0, total = 0;
-#pragma unroll
-  for (int i = 0; i < NW; ++i) {
-    if (i < w) wbase += warp_tot[i];
-    total += warp_tot[i];
-  }
-  int run = wbase + incl - s;
-  for (int i = b; i < e; ++i) {
-    int c = v[i];
-    v[i] = run;
-    run += c;
-  }
-  __syncthreads();
-  return total;
-}
 
 // ------------------------------------------------------ decode router
 struct RouteArgs {
@@ -128,18 +41,13 @@ constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kRouteUnroll = 8;  // float4 loads of the router row in flight per lane
 
 // Grid: E CTAs of 8 warps; CTA e computes z[t][e] for the T <= 16 tokens, its
-// warps splitting H with all of a lane's loads issued before any use. The
-// last CTA to finish (atomic ticket, no waiting) selects, makes the gates and
-// groups the (token, slot) pairs for all tokens.
-__global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a) {
+// warps splitting H with all of a lane's loads issued before any use. With
+// `select`, the last CTA to finish (atomic ticket, no waiting) also selects,
+// makes the gates and groups the (token, slot) pairs and publishes them;
+// without it the logits are the only output (the expert kernels rebuild the
+// routing from them).
+__global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a, int select) {
   __shared__ float s_part[kRouteWarps][kMaxDecodeT];
-  __shared__ int s_cnt[kMaxE + 2];
-  __shared__ int s_c2[kMaxE + 1];
-  __shared__ uint32_t s_mask[kMaxE + 1];
-  __shared__ int s_nz[kMaxE + 2];
-  __shared__ int s_ids[kMaxDecodeT * kMaxK];
-  __shared__ float s_gates[kMaxDecodeT * kMaxK];
-  __shared__ int s_wtot[kRouteWarps];
   __shared__ bool s_last;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int e = blockIdx.x;
@@ -191,81 +99,19 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
 #pragma unroll
     for (int w = 0; w < kRouteWarps; ++w) z += s_part[w][tid];
     a.logits[tid * a.E + e] = z + a.bias[e];
-    __threadfence();
+    if (select) __threadfence();
   }
+  if (!select) return;
   __syncthreads();
   if (tid == 0) s_last = atomicInc(&a.meta->ticket, gridDim.x - 1) == gridDim.x - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-
-  // ---- selection and gates: one warp per token
-  const int k = a.k, E = a.E;
-  for (int t = warp; t < T; t += kRouteWarps) {
-    float zl[kMaxEPerLane];
-#pragma unroll
-    for (int m = 0; m < kMaxEPerLane; ++m) {
-      int ee = lane + 32 * m;
-      zl[m] = ee < E ? __ldcg(a.logits + t * E + ee) : -INFINITY;
-    }
-    int id;
-    float zv;
-    warp_topk(zl, E, k, lane, &id, &zv);
-    float g = warp_gate(zv, k, lane);
-    if (lane < k) {
-      s_ids[t * k + lane] = id;
-      s_gates[t * k + lane] = g;
-      a.ids[t * k + lane] = id;
-      a.gates[t * k + lane] = g;
-      a.ids_out[t * k + lane] = id;
-      if (a.gates_out) a.gates_out[t * k + lane] = g;
-    }
-  }
-  // ---- grouping: counts, offsets, stable ranks via per-expert token masks
-  const int EU = E + a.S;
-  for (int i = tid; i < EU + 1; i += kRouteThreads) s_cnt[i] = 0;
-  for (int i = tid; i < EU; i += kRouteThreads) s_mask[i] = 0;
-  __syncthreads();
-  for (int p = tid; p < T * k; p += kRouteThreads) {
-    int ee = s_ids[p];
-    atomicAdd(&s_cnt[ee], 1);
-    atomicOr(&s_mask[ee], 1u << (p / k));
-  }
-  if (a.S && tid == 0) s_cnt[E] = T;
-  __syncthreads();
-  for (int i = tid; i < EU; i += kRouteThreads) {
-    a.counts[i] = s_cnt[i];
-    s_c2[i] = s_cnt[i];
-    s_nz[i] = s_cnt[i] > 0;
-  }
-  __syncthreads();
-  block_exclusive_scan<kRouteThreads>(s_cnt, EU + 1, s_wtot);  // s_cnt[EU] = total rows
-  for (int i = tid; i < EU + 1; i += kRouteThreads) a.offsets[i] = s_cnt[i];
-  for (int p = tid; p < T * k; p += kRouteThreads) {
-    int t = p / k, ee = s_ids[p];
-    int pos = s_cnt[ee] + __popc(s_mask[ee] & ((1u << t) - 1u));
-    a.perm[pos] = p;
-    a.inv[p] = pos;
-    a.row_token[pos] = t;
-    a.row_gate[pos] = s_gates[p];
-  }
-  if (a.S) {
-    for (int t = tid; t < T; t += kRouteThreads) {
-      int pos = s_cnt[E] + t;
-      a.perm[pos] = T * k + t;
-      a.inv[T * k + t] = pos;
-      a.row_token[pos] = t;
-      a.row_gate[pos] = 1.0f;
-    }
-  }
-  __syncthreads();
-  int n_unique = block_exclusive_scan<kRouteThreads>(s_nz, EU, s_wtot);
-  for (int i = tid; i < EU; i += kRouteThreads)
-    if (s_c2[i] > 0) a.uinfo[s_nz[i]] = make_int4(i, s_cnt[i], s_c2[i], 0);
-  if (tid == 0) {
-    a.meta->n_unique = n_unique;
-    a.meta->T = T;
-  }
+  __shared__ SmemRouting r;
+  route_in_smem<kRouteThreads>(a.logits, T, a.E, a.k, a.S, r);
+  RoutingOut o{a.ids_out, a.gates_out, a.ids,      a.gates,    a.counts, a.offsets,
+               a.perm,    a.inv,       a.row_token, a.row_gate, a.uinfo,  a.meta};
+  publish_routing<kRouteThreads>(r, T, a.E, a.k, a.S, o);
 }
 
 // ------------------------------------------------------ prefill router
@@ -372,7 +218,7 @@ __global__ void __launch_bounds__(256) route_tiles_kernel(RouteArgs a, int32_t* 
 // per-tile absolute bases (in place of the tile counts), the list of experts
 // with rows, and the list of 128-row tiles per expert for the prefill GEMMs.
 __global__ void __launch_bounds__(256) route_scan_kernel(RouteArgs a, int32_t* hist, int n_tiles,
-                                                         int32_t* mtiles) {
+                                                         int4* minfo) {
   __shared__ int s_off[kMaxE + 2];
   __shared__ int s_nz[kMaxE + 2];
   __shared__ int s_nt[kMaxE + 2];
@@ -422,7 +268,7 @@ __global__ void __launch_bounds__(256) route_scan_kernel(RouteArgs a, int32_t* h
     int cnt = a.counts[e];
     if (cnt > 0) a.uinfo[s_nz[e]] = make_int4(e, s_off[e], cnt, 0);
     int nt = (cnt + 127) / 128;
-    for (int i = 0; i < nt; ++i) mtiles[s_nt[e] + i] = (e << 16) | i;
+    for (int i = 0; i < nt; ++i) minfo[s_nt[e] + i] = make_int4(e, s_off[e] + 128 * i, min(128, cnt - 128 * i), 0);
   }
   __syncthreads();
   for (int e = tid; e < E; e += 256) {
@@ -516,10 +362,10 @@ cudaError_t configure_route_kernels() {
 }
 
 cudaError_t launch_route_decode(Handle* h, const __nv_bfloat16* x, int T, int32_t* ids_out, float* gates_out,
-                                cudaStream_t s) {
+                                bool select, cudaStream_t s) {
   RouteArgs a = route_args(h, x, T, ids_out, gates_out);
   KernelTimer tm(h, FW_KERNEL_ROUTE_DECODE, s);
-  route_decode_kernel<<<h->cfg.E, kRouteThreads, 0, s>>>(a);
+  route_decode_kernel<<<h->cfg.E, kRouteThreads, 0, s>>>(a, select ? 1 : 0);
   return cudaGetLastError();
 }
 
@@ -545,7 +391,7 @@ cudaError_t launch_route_prefill(Handle* h, const __nv_bfloat16* x, int T, int32
   if (err != cudaSuccess) return err;
   {
     KernelTimer tm(h, FW_KERNEL_ROUTE_SCAN, s);
-    route_scan_kernel<<<1, 256, 0, s>>>(a, h->hist, n_tiles, h->mtiles);
+    route_scan_kernel<<<1, 256, 0, s>>>(a, h->hist, n_tiles, h->minfo);
   }
   {
     KernelTimer tm(h, FW_KERNEL_ROUTE_SCATTER, s);
