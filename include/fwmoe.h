@@ -128,8 +128,8 @@ enum {
   FW_KERNEL_ROUTE_TILES = 1,  /* prefill router: tiled GEMM, top-k, per-tile counts */
   FW_KERNEL_ROUTE_SCAN = 2,   /* prefill grouping: offsets, tile lists */
   FW_KERNEL_ROUTE_SCATTER = 3,/* prefill grouping: stable scatter */
-  FW_KERNEL_DECODE_GATEUP = 4,/* decode gate/up grouped GEMV + SiLU */
-  FW_KERNEL_DECODE_DOWN = 5,  /* decode down grouped GEMV + combine */
+  FW_KERNEL_DECODE_EXPERTS = 4, /* decode experts: gate/up GEMV + SiLU, grid barrier, down GEMV + combine */
+  FW_KERNEL_RESERVED_5 = 5,
   FW_KERNEL_PREFILL_GATEUP = 6,  /* prefill gate/up grouped GEMM (tcgen05) + SiLU */
   FW_KERNEL_PREFILL_DOWN = 7,    /* prefill down grouped GEMM (tcgen05) x gate */
   FW_KERNEL_PREFILL_COMBINE = 8, /* prefill un-permute and sum */
@@ -154,6 +154,29 @@ fw_status fw_moe_free(fw_moe_handle *h);
 
 /* Text of the last failed call on this thread ("" if none). */
 const char *fw_moe_last_error(void);
+
+/* Routing only (logits, top-k with ties to the lower id, renormalised gates)
+ * for callers that must not allocate device memory: code that runs inside a
+ * framework whose memory manager owns every byte of the device (a serving
+ * engine's pool or a fixed arena), or on a latency path where cudaMalloc's
+ * implicit synchronisation is not acceptable. It needs no handle: x is DEVICE
+ * bf16 [T, H], router_w DEVICE fp32 [E, H] (16-byte aligned), router_bias
+ * DEVICE fp32 [E] or NULL; writes expert_ids DEVICE int32 [T, k] and gates
+ * DEVICE fp32 [T, k] (may be NULL), the same values fw_moe_route writes.
+ * The pages have no counterpart: this is a convenience of this library.
+ *
+ * Its only scratch (the T x E logits and a ticket counter, 16.25 KiB) is a
+ * file-scope __device__ array that every GPU loading this library holds until
+ * process exit; limits: T <= 16, E <= 256, k <= min(E, 16), H % 4 == 0, beyond
+ * which it returns FW_EINVAL with text. The first call on a device looks the
+ * array's device address up (cudaGetSymbolAddress, with that device
+ * current); make that first call before any stream capture. Each call clears
+ * the ticket in stream order. All calls share the one array and it keeps the
+ * last call's contents: calls that can overlap on the GPU (other streams, or
+ * other threads' streams) race and must be serialised by the caller. It calls
+ * no cudaMalloc, cudaFree or allocating library routine. */
+fw_status fw_moe_route_noalloc(const void *x, int32_t T, int32_t H, const float *router_w, const float *router_bias,
+                               int32_t E, int32_t k, int32_t *expert_ids, float *gates, void *stream);
 
 /* Quantise fp32 weights to Q8_0 on the GPU: w DEVICE [rows, K] row-major fp32,
  * K % 32 == 0; blocks DEVICE rows x K/32 x 34 bytes. Per block of 32:

@@ -50,9 +50,9 @@ _lib = None
 
 EXPORTED = ("fw_moe_init", "fw_moe_route", "fw_moe_ffn", "fw_moe_forward", "fw_moe_forward_host",
             "fw_moe_get_permutation", "fw_moe_export_q8_0", "fw_moe_status", "fw_moe_free", "fw_moe_last_error",
-            "fw_q8_0_quantize", "fw_moe_profile_begin", "fw_moe_profile_end")
+            "fw_q8_0_quantize", "fw_moe_profile_begin", "fw_moe_profile_end", "fw_moe_route_noalloc")
 
-KERNEL_KINDS = ("route_decode", "route_tiles", "route_scan", "route_scatter", "decode_gateup", "decode_down",
+KERNEL_KINDS = ("route_decode", "route_tiles", "route_scan", "route_scatter", "decode_experts", "reserved",
                 "prefill_gateup", "prefill_down", "prefill_combine", "prefill_gather")
 
 
@@ -78,6 +78,7 @@ def lib():
             "fw_q8_0_quantize": [vp, i64, i64, vp, vp],
             "fw_moe_profile_begin": [vp, i32],
             "fw_moe_profile_end": [vp, i32, vp, vp],
+            "fw_moe_route_noalloc": [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -139,6 +140,12 @@ def fw_moe_free(h):
 
 def fw_q8_0_quantize(w, rows, K, blocks, stream):
     _check(lib().fw_q8_0_quantize(w, rows, K, blocks, stream), "fw_q8_0_quantize")
+
+
+def fw_moe_route_noalloc(x, T, H, router_w, router_bias, E, k, expert_ids, gates, stream):
+    """Routing without a handle or any device allocation (see include/fwmoe.h)."""
+    _check(lib().fw_moe_route_noalloc(x, T, H, router_w, router_bias, E, k, expert_ids, gates, stream),
+           "fw_moe_route_noalloc")
 
 
 def fw_moe_profile_begin(h, max_launches):

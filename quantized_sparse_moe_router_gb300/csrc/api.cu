@@ -88,6 +88,10 @@ fw_status check_config(const fw_moe_config* c) {
 int decode_limit(const Handle* h) { return h->cfg.decode_T_max ? h->cfg.decode_T_max : kMaxDecodeT; }
 
 }  // namespace
+
+// Record the text of a failed call for fw_moe_last_error (other source files).
+fw_status set_error(fw_status st, const char* text) { return fail(st, "%s", text); }
+
 }  // namespace fw
 
 using namespace fw;
@@ -347,12 +351,16 @@ fw_status fw_moe_status(fw_moe_handle* hh, void* stream) {
   Handle* h = reinterpret_cast<Handle*>(hh);
   if (!live(h)) return fail(FW_EINVAL, "fw_moe_status: not a live handle");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int32_t word = 0;
+  int32_t word = 0, diag[4] = {0, 0, 0, 0};
   cudaError_t e = cudaStreamSynchronize(s);
   if (e == cudaSuccess) e = cudaMemcpy(&word, &h->meta->status, 4, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(diag, h->meta->diag, sizeof(diag), cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(&h->meta->status, 0, 4);
+  if (e == cudaSuccess) e = cudaMemset(h->meta->diag, 0, sizeof(diag));
   if (e != cudaSuccess) return cuda_fail(e, "fw_moe_status");
-  if (word & kStatusTimeout) return fail(FW_ETIMEOUT, "a kernel gave up a bounded wait (status 0x%x)", word);
+  if (word & kStatusTimeout)
+    return fail(FW_ETIMEOUT, "a kernel gave up a bounded wait (status 0x%x; site %d, block %d, stage %d, detail %d)",
+                word, diag[0], diag[1], diag[2], diag[3]);
   if (word) return fail(FW_EDEVICE, "a kernel reported a failed check (status 0x%x)", word);
   return FW_OK;
 }

@@ -1,25 +1,26 @@
-// Decode path (T <= 16): the experts as grouped, HBM-bound GEMVs.
+// Decode path (T <= 16): the experts of one call as one fused, HBM-bound
+// grouped GEMV kernel.
 //
 // The pages' runtime runs routed experts through grouped GPU kernels per
 // quantisation format, Q8_0 among them (Flyweight README, §Quantization), and
 // fuses the gate and up projections so they share one activation load (its
-// CPU expert kernels, §Current limitations). Here every selected expert's Q8_0
-// rows are streamed from HBM exactly once per call, in large bulk asynchronous
-// copies (many contiguous rows per copy) into a shared-memory ring fed by one
-// producer warp, and dequantised in registers by eight consumer warps.
+// CPU expert kernels, §Current limitations). Here every selected expert's
+// Q8_0 rows are streamed from HBM exactly once per call, in large bulk
+// asynchronous copies into a shared-memory ring fed by one producer warp, and
+// dequantised in registers by sixteen consumer warps.
 //
-// Both kernels first rebuild the batch's routing from the router logits in
-// shared memory (top-k, gates and grouping are deterministic, so every CTA
-// gets the same answer) instead of waiting for a published table.
-//
-//   gate/up kernel: unit = (expert, i): gate row i and up row i share the
-//     x loads; h = SiLU(g) * u for each of the expert's tokens -> hbuf (fp32).
-//     With `publish`, CTA 0 also writes the routing outputs.
-//   down kernel: each CTA owns a block of output rows; it routes and starts
-//     streaming W_down rows *before* waiting for the gate/up kernel
-//     (programmatic dependent launch), then visits the touched experts in
-//     ascending id (shared last): lane t accumulates gate * (W_down h) for
-//     token t, so the combine is fused and its order fixed (no atomics).
+// One persistent CTA per SM, launched cooperatively (all CTAs resident):
+//   0. after the router's grid completes (programmatic dependent launch), each
+//      CTA rebuilds the batch's routing from the logits in shared memory
+//      (bitonic top-k per token; deterministic, so every CTA agrees); CTA 0
+//      publishes it;
+//   1. gate/up: the CTA's slice of the (touched expert, i) units; for each of
+//      the expert's tokens h = SiLU(g) * u -> hbuf (fp32, grouped row order);
+//   2. grid-wide barrier (every h written) -- meanwhile the producer keeps
+//      streaming this CTA's W_down rows into the ring;
+//   3. down + combine: the CTA's block of output rows, every touched expert in
+//      ascending id (shared last); lane t accumulates gate * (W_down h) for
+//      token t and writes out[t] (bf16): fixed order, no atomics.
 #include <algorithm>
 
 #include "routing.cuh"
@@ -29,307 +30,333 @@ namespace {
 
 using namespace dev;
 
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;  // + one producer warp
-constexpr int kProducer = kConsumerWarps;            // warp index of the producer
+constexpr int kCW = 16;                    // consumer warps
+constexpr int kThreads = (kCW + 1) * 32;   // + one producer warp
+constexpr int kProducer = kCW;
 constexpr int kMaxStages = 16;
-constexpr int kDownRowBlock = 16;                    // output rows per down stage
-constexpr int kMaxDownBlocks = 4;                    // row blocks a CTA may own
+constexpr int kRowBlock = 16;              // output rows per W_down stage
+constexpr int kMaxRowBlocks = 4;           // row blocks a CTA may own
+constexpr uint32_t kConsumerBarrier = 1;   // named barrier of the 16 consumer warps
 
-struct GateUpArgs {
-  const int8_t* q;        // q_gu
-  const uint8_t* s;       // s_gu
+enum XMode { kXGlobal = 0, kXSmemF32 = 1, kXSmemBf16 = 2 };
+
+struct DecodeArgs {
+  const uint8_t* q_gu;   // codes + 128
+  const uint8_t* s_gu;   // row-major binary16 scales, padded rows
+  const uint8_t* q_d;
+  const uint8_t* s_d;
   const __nv_bfloat16* x;
   const float* logits;
-  float* hbuf;
-  RoutingOut out;         // routing outputs (publish only; meta always)
-  int H, I, E, k, S, T;
-  int publish;
-  int stages;
-  int units_per_stage;    // consecutive i of one expert per stage (divides 64)
-  uint32_t stage_bytes;
-  int x_in_smem;
-};
-
-struct DownArgs {
-  const int8_t* q;        // q_d
-  const uint8_t* s;       // s_d
-  const float* logits;
-  const float* hbuf;
+  float* hbuf;           // [rows][I] fp32
   __nv_bfloat16* out;
+  RoutingOut ro;
   Meta* meta;
   int H, I, E, k, S, T;
+  int publish;
+  int R;                 // gate/up units per stage (divides 64)
+  uint32_t stage_bytes;  // ring slot size (max of a gate/up and a down stage)
   int stages;
-  uint32_t stage_bytes;   // kDownRowBlock * (I + pitch(I))
-  int h_in_smem;
+  int x_mode;
+  int h_smem;            // h staged in shared memory (fp32)
+  uint32_t act_bytes;    // shared-memory area for x, then for h
 };
 
-// sum_{i<16} q_i * x_i for 16 int8 codes (one uint4) and 16 floats.
-__device__ __forceinline__ float dot16(const uint4 q, const float (&xv)[16]) {
-  float c[16];
-  i8x4_to_f32(q.x, c[0], c[1], c[2], c[3]);
-  i8x4_to_f32(q.y, c[4], c[5], c[6], c[7]);
-  i8x4_to_f32(q.z, c[8], c[9], c[10], c[11]);
-  i8x4_to_f32(q.w, c[12], c[13], c[14], c[15]);
-  float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-  for (int i = 0; i < 16; i += 2) {
-    a0 = fmaf(c[i], xv[i], a0);
-    a1 = fmaf(c[i + 1], xv[i + 1], a1);
-  }
-  return a0 + a1;
+// ------------------------------------------------------------- packed fp32
+typedef unsigned long long f2;
+
+__device__ __forceinline__ f2 f2_pack(float a, float b) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ f2 f2_pack_bits(uint32_t a, uint32_t b) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ float f2_hsum(f2 v) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+  return a + b;
+}
+__device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
+  f2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
+  f2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
 }
 
-__device__ __forceinline__ void unpack_x16(uint4 a, uint4 b, float (&xv)[16]) {
-  bf16x2_to_f32(a.x, xv[0], xv[1]);
-  bf16x2_to_f32(a.y, xv[2], xv[3]);
-  bf16x2_to_f32(a.z, xv[4], xv[5]);
-  bf16x2_to_f32(a.w, xv[6], xv[7]);
-  bf16x2_to_f32(b.x, xv[8], xv[9]);
-  bf16x2_to_f32(b.y, xv[10], xv[11]);
-  bf16x2_to_f32(b.z, xv[12], xv[13]);
-  bf16x2_to_f32(b.w, xv[14], xv[15]);
+// Four offset-binary codes of a word times four x values (two pairs), added
+// to a pair accumulator: the byte permute makes the float 2^23 + q + 128 and
+// one packed subtraction leaves q exactly.
+__device__ __forceinline__ f2 dot4(uint32_t w, f2 x01, f2 x23, f2 acc) {
+  const f2 bias = f2_pack(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+  const f2 m01 = f2_pack_bits(__byte_perm(w, 0x4B000000u, 0x7650), __byte_perm(w, 0x4B000000u, 0x7651));
+  const f2 m23 = f2_pack_bits(__byte_perm(w, 0x4B000000u, 0x7652), __byte_perm(w, 0x4B000000u, 0x7653));
+  acc = f2_fma(f2_add(m01, bias), x01, acc);
+  return f2_fma(f2_add(m23, bias), x23, acc);
 }
 
-__device__ __forceinline__ void load_h16(const float* p, bool shared, float (&hv)[16]) {
+// sum_{i<16} q_i x_i for one 16-code segment; x as 8 pairs.
+__device__ __forceinline__ float dot16(const uint4 q, const f2 (&x)[8]) {
+  f2 a = dot4(q.x, x[0], x[1], 0ull);
+  f2 b = dot4(q.y, x[2], x[3], 0ull);
+  a = dot4(q.z, x[4], x[5], a);
+  b = dot4(q.w, x[6], x[7], b);
+  return f2_hsum(f2_add(a, b));
+}
+
+__device__ __forceinline__ void x16_from_f32(const float* p, f2 (&x)[8]) {
   const float4* q = reinterpret_cast<const float4*>(p);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    float4 v = shared ? q[i] : __ldg(q + i);
-    hv[4 * i] = v.x;
-    hv[4 * i + 1] = v.y;
-    hv[4 * i + 2] = v.z;
-    hv[4 * i + 3] = v.w;
+    const float4 v = q[i];
+    x[2 * i] = f2_pack(v.x, v.y);
+    x[2 * i + 1] = f2_pack(v.z, v.w);
+  }
+}
+
+__device__ __forceinline__ void x16_from_bf16(uint4 a, uint4 b, f2 (&x)[8]) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = f2_pack_bits(w[i] << 16, w[i] & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ void x16_from_f32_global(const float* p, f2 (&x)[8]) {
+  const float4* q = reinterpret_cast<const float4*>(p);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 v = __ldg(q + i);
+    x[2 * i] = f2_pack(v.x, v.y);
+    x[2 * i + 1] = f2_pack(v.z, v.w);
   }
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
-__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+__device__ __forceinline__ void consumer_sync() {
+  asm volatile("bar.sync %0, %1;" ::"r"(kConsumerBarrier), "r"(kCW * 32) : "memory");
 }
 
-// Dynamic shared memory: [activation (x or h)][ring], 128-byte aligned.
-__host__ __device__ inline uint32_t ring_offset(uint32_t act_bytes) { return (act_bytes + 127) / 128 * 128; }
+__device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
 
-// ------------------------------------------------------------- gate / up
-// CTA c takes units [lo, hi) of the (expert with rows) x I unit space; a stage
-// is up to R = units_per_stage consecutive units of one expert (R divides 64,
-// so a stage never crosses a 64-row gate/up group): 4 bulk copies (gate codes,
-// up codes, gate scales, up scales). Unit g goes to consumer warp g % 8,
-// which arrives on its stage's empty barrier with a weight chosen so that each
-// stage's arrivals sum to R.
-__global__ void __launch_bounds__(kThreads, 1) decode_gateup_kernel(GateUpArgs a) {
+__host__ __device__ inline uint32_t align128(uint32_t v) { return (v + 127) / 128 * 128; }
+
+// ------------------------------------------------------------- the kernel
+__global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], xbar;
+  __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], actbar;
   __shared__ SmemRouting r;
-  __shared__ int s_fail;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = a.H, I = a.I, T = a.T;
-  const uint32_t pitch = (uint32_t)scale_pitch_bytes(H);
-  const uint32_t x_bytes = a.x_in_smem ? (uint32_t)T * H * 2 : 0;
-  const __nv_bfloat16* s_x = reinterpret_cast<const __nv_bfloat16*>(smem);
-  uint8_t* ring = smem + ring_offset(x_bytes);
-  const int R = a.units_per_stage;
+  const int H = a.H, I = a.I, T = a.T, R = a.R;
+  const uint32_t pitch_h = (uint32_t)scale_pitch_bytes(H), pitch_i = (uint32_t)scale_pitch_bytes(I);
+  uint8_t* ring = smem + align128(a.act_bytes);
   if (tid == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], R);
+      mbar_init(&empty[s], kCW);
     }
-    mbar_init(&xbar, 1);
-    s_fail = 0;
+    mbar_init(&actbar, 1);
     fence_mbar_init();
   }
-  pdl_wait();  // the router's logits
-  if (tid == 0 && x_bytes) {
-    mbar_arrive_expect_tx(&xbar, x_bytes);
-    bulk_g2s(smem, a.x, x_bytes, &xbar);
-  }
+  pdl_wait();  // the router's logits (and its reset of the grid barrier)
   route_in_smem<kThreads>(a.logits, T, a.E, a.k, a.S, r);
-  pdl_launch_dependents();
-  if (a.publish && blockIdx.x == 0) publish_routing<kThreads>(r, T, a.E, a.k, a.S, a.out);
+  if (a.publish && blockIdx.x == 0) publish_routing<kThreads>(r, T, a.E, a.k, a.S, a.ro);
 
-  const int64_t n_units = (int64_t)r.n_unique * I;
+  const int nU = r.n_unique;
+  // gate/up stages: units [lo, hi) of the nU x I unit space, R consecutive per stage
+  const int64_t n_units = (int64_t)nU * I;
   const int64_t lo = n_units * blockIdx.x / gridDim.x, hi = n_units * (blockIdx.x + 1) / gridDim.x;
-  const int64_t b0 = lo / R;  // stage j covers [max(lo, R(b0+j)), min(hi, R(b0+j+1)))
-  const int64_t n_stages = hi > lo ? (hi + R - 1) / R - b0 : 0;
+  const int64_t b0 = lo / R;
+  const int64_t n_gu = hi > lo ? (hi + R - 1) / R - b0 : 0;
+  // down stages: output rows [o0, o1), blocks of 16 rows, every touched expert (block fastest)
+  const int o0 = (int)((int64_t)H * blockIdx.x / gridDim.x), o1 = (int)((int64_t)H * (blockIdx.x + 1) / gridDim.x);
+  const int n_blk = (o1 - o0 + kRowBlock - 1) / kRowBlock;
+  const int64_t n_dn = (int64_t)nU * n_blk;
+  const int64_t n_all = n_gu + n_dn;
 
   if (warp == kProducer) {
+    // ------------------------------------------------------ producer
     if (lane == 0) {
       int64_t j = 0;
-      for (; j < n_stages; ++j) {
+      for (; j < n_all; ++j) {
         const int st = (int)(j % a.stages);
         if (j >= a.stages && !mbar_wait(&empty[st], (uint32_t)(((j / a.stages) - 1) & 1))) {
-          s_fail = 1;
+          report_wait(a.meta, kSiteGuEmpty, j, (int)n_all);
           break;
         }
-        const int64_t u0 = std::max<int64_t>(lo, (b0 + j) * R), u1 = std::min<int64_t>(hi, (b0 + j + 1) * R);
-        const int n = (int)(u1 - u0);
-        const int e = r.u[u0 / I].x, i0 = (int)(u0 % I);
-        const int64_t rg = (int64_t)e * 2 * I + gu_row_gate(i0), ru = (int64_t)e * 2 * I + gu_row_up(i0);
         uint8_t* sb = ring + (size_t)st * a.stage_bytes;
-        const uint32_t qb = (uint32_t)n * H, sbb = (uint32_t)n * pitch;
-        mbar_arrive_expect_tx(&full[st], 2 * qb + 2 * sbb);
-        bulk_g2s(sb, a.q + rg * H, qb, &full[st]);
-        bulk_g2s(sb + (size_t)R * H, a.q + ru * H, qb, &full[st]);
-        bulk_g2s(sb + (size_t)2 * R * H, a.s + rg * pitch, sbb, &full[st]);
-        bulk_g2s(sb + (size_t)2 * R * H + (size_t)R * pitch, a.s + ru * pitch, sbb, &full[st]);
+        if (j < n_gu) {
+          const int64_t u0 = std::max<int64_t>(lo, (b0 + j) * R), u1 = std::min<int64_t>(hi, (b0 + j + 1) * R);
+          const int n = (int)(u1 - u0);
+          const int e = r.u[u0 / I].x, i0 = (int)(u0 % I);
+          const int64_t rg = (int64_t)e * 2 * I + gu_row_gate(i0), ru = (int64_t)e * 2 * I + gu_row_up(i0);
+          const uint32_t qb = (uint32_t)n * H, sbb = (uint32_t)n * pitch_h;
+          mbar_arrive_expect_tx(&full[st], 2 * qb + 2 * sbb);
+          bulk_g2s(sb, a.q_gu + rg * H, qb, &full[st]);
+          bulk_g2s(sb + (size_t)R * H, a.q_gu + ru * H, qb, &full[st]);
+          bulk_g2s(sb + (size_t)2 * R * H, a.s_gu + rg * pitch_h, sbb, &full[st]);
+          bulk_g2s(sb + (size_t)2 * R * H + (size_t)R * pitch_h, a.s_gu + ru * pitch_h, sbb, &full[st]);
+        } else {
+          const int64_t jd = j - n_gu;
+          const int e = r.u[jd / n_blk].x, blk = (int)(jd % n_blk);
+          const int r0 = o0 + blk * kRowBlock, nr = ::min(kRowBlock + 0, o1 - r0);
+          const int64_t row = (int64_t)e * H + r0;
+          mbar_arrive_expect_tx(&full[st], (uint32_t)nr * (I + pitch_i));
+          bulk_g2s(sb, a.q_d + row * I, (uint32_t)nr * I, &full[st]);
+          bulk_g2s(sb + (size_t)kRowBlock * I, a.s_d + row * pitch_i, (uint32_t)nr * pitch_i, &full[st]);
+        }
       }
       // every copy issued has landed before the CTA may leave
       for (int64_t q = std::max<int64_t>(0, j - a.stages); q < j; ++q)
         mbar_wait(&full[q % a.stages], (uint32_t)((q / a.stages) & 1));
     }
   } else {
-    bool ok = !x_bytes || mbar_wait(&xbar, 0);
-    const int nseg = H / 16;
-    for (int64_t g = lo + warp; g < hi && ok; g += kConsumerWarps) {
-      const int64_t j = g / R - b0;
+    // ------------------------------------------------------ consumers
+    bool ok = true;
+    // x for this batch: fp32 or bf16 in shared memory, else read from global
+    if (a.x_mode == kXSmemF32) {
+      float* xs = reinterpret_cast<float*>(smem);
+      for (int i = tid; i < T * H / 8; i += kCW * 32) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
+        float4 lo4, hi4;
+        bf16x2_to_f32(v.x, lo4.x, lo4.y);
+        bf16x2_to_f32(v.y, lo4.z, lo4.w);
+        bf16x2_to_f32(v.z, hi4.x, hi4.y);
+        bf16x2_to_f32(v.w, hi4.z, hi4.w);
+        reinterpret_cast<float4*>(xs)[2 * i] = lo4;
+        reinterpret_cast<float4*>(xs)[2 * i + 1] = hi4;
+      }
+    } else if (a.x_mode == kXSmemBf16) {
+      for (int i = tid; i < T * H / 8; i += kCW * 32)
+        reinterpret_cast<uint4*>(smem)[i] = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
+    }
+    consumer_sync();
+
+    // ---- phase 1: gate/up. Every consumer warp passes every stage in order
+    // (no wait is ever more than one phase ahead of its barrier) and computes
+    // the units g of the stage with (g - lo) % 16 == warp.
+    const int nseg_h = H / 16;
+    for (int64_t j = 0; j < n_gu && ok; ++j) {
       const int st = (int)(j % a.stages);
       if (!mbar_wait(&full[st], (uint32_t)((j / a.stages) & 1))) {
+        report_wait(a.meta, kSiteGuFull, j, warp);
         ok = false;
         break;
       }
       const int64_t u0 = std::max<int64_t>(lo, (b0 + j) * R), u1 = std::min<int64_t>(hi, (b0 + j + 1) * R);
-      const size_t off = (size_t)(g - u0);
       const uint8_t* sb = ring + (size_t)st * a.stage_bytes;
-      const uint8_t* qg_row = sb + off * H;
-      const uint8_t* qu_row = sb + (size_t)R * H + off * H;
-      const uint16_t* sg = reinterpret_cast<const uint16_t*>(sb + (size_t)2 * R * H + off * pitch);
-      const uint16_t* su = reinterpret_cast<const uint16_t*>(sb + (size_t)2 * R * H + (size_t)R * pitch + off * pitch);
-      const int4 ui = r.u[g / I];
-      const int i = (int)(g % I);
-      for (int rr = 0; rr < ui.z; ++rr) {
-        const int pos = ui.y + rr;
-        const int t = r.tok[pos];
-        float accg = 0.f, accu = 0.f;
-        for (int seg = lane; seg < nseg; seg += 32) {
-          uint4 x0, x1;
-          if (x_bytes) {
-            const uint4* xp = reinterpret_cast<const uint4*>(s_x + (size_t)t * H + seg * 16);
-            x0 = xp[0];
-            x1 = xp[1];
-          } else {
-            const uint4* xp = reinterpret_cast<const uint4*>(a.x + (size_t)t * H + seg * 16);
-            x0 = __ldg(xp);
-            x1 = __ldg(xp + 1);
+      for (int64_t g = u0 + ((warp - (u0 - lo)) % kCW + kCW) % kCW; g < u1; g += kCW) {
+        const size_t off = (size_t)(g - u0);
+        const uint8_t* qg_row = sb + off * H;
+        const uint8_t* qu_row = sb + (size_t)R * H + off * H;
+        const uint16_t* sg = reinterpret_cast<const uint16_t*>(sb + (size_t)2 * R * H + off * pitch_h);
+        const uint16_t* su =
+            reinterpret_cast<const uint16_t*>(sb + (size_t)2 * R * H + (size_t)R * pitch_h + off * pitch_h);
+        const int4 ui = r.u[g / I];
+        const int i = (int)(g % I);
+        for (int rr = 0; rr < ui.z; ++rr) {
+          const int pos = ui.y + rr;
+          const int t = r.tok[pos];
+          float accg = 0.f, accu = 0.f;
+          for (int seg = lane; seg < nseg_h; seg += 32) {
+            f2 xv[8];
+            if (a.x_mode == kXSmemF32) {
+              x16_from_f32(reinterpret_cast<const float*>(smem) + (size_t)t * H + seg * 16, xv);
+            } else {
+              const uint4* xp = a.x_mode == kXSmemBf16
+                                    ? reinterpret_cast<const uint4*>(smem + ((size_t)t * H + seg * 16) * 2)
+                                    : reinterpret_cast<const uint4*>(a.x + (size_t)t * H + seg * 16);
+              const uint4 x0 = a.x_mode == kXSmemBf16 ? xp[0] : __ldg(xp);
+              const uint4 x1 = a.x_mode == kXSmemBf16 ? xp[1] : __ldg(xp + 1);
+              x16_from_bf16(x0, x1, xv);
+            }
+            const uint4 qg = *reinterpret_cast<const uint4*>(qg_row + seg * 16);
+            const uint4 qu = *reinterpret_cast<const uint4*>(qu_row + seg * 16);
+            accg = fmaf(half_bits_to_f32(sg[seg >> 1]), dot16(qg, xv), accg);
+            accu = fmaf(half_bits_to_f32(su[seg >> 1]), dot16(qu, xv), accu);
           }
-          float xv[16];
-          unpack_x16(x0, x1, xv);
-          const uint4 qg = *reinterpret_cast<const uint4*>(qg_row + seg * 16);
-          const uint4 qu = *reinterpret_cast<const uint4*>(qu_row + seg * 16);
-          accg = fmaf(half_bits_to_f32(sg[seg >> 1]), dot16(qg, xv), accg);
-          accu = fmaf(half_bits_to_f32(su[seg >> 1]), dot16(qu, xv), accu);
+          accg = warp_sum(accg);
+          accu = warp_sum(accu);
+          if (lane == 0) a.hbuf[(int64_t)pos * I + i] = silu(accg) * accu;
         }
-        accg = warp_sum(accg);
-        accu = warp_sum(accu);
-        if (lane == 0) a.hbuf[(int64_t)pos * I + i] = silu(accg) * accu;
       }
       __syncwarp();
-      if (lane == 0) mbar_arrive_cnt(&empty[st], g == u0 ? (uint32_t)(R - (u1 - u0) + 1) : 1u);
+      if (lane == 0) mbar_arrive(&empty[st]);
     }
-    if (!ok && lane == 0) s_fail = 1;
-  }
-  __syncthreads();
-  if (tid == 0 && s_fail) report(a.out.meta, kStatusTimeout);
-}
 
-// ------------------------------------------------------------- down + combine
-// CTA c owns output rows [o0, o1) in blocks of up to 16; a stage is one block
-// of rows of one touched expert (2 bulk copies: codes, scales). Consumer warp
-// w owns rows w and w + 8 of every block and keeps their per-token sums in
-// registers (lane t: token t) across all experts.
-__global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(DownArgs a) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], hbar;
-  __shared__ SmemRouting r;
-  __shared__ int s_fail;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = a.H, I = a.I, T = a.T;
-  const uint32_t pitch = (uint32_t)scale_pitch_bytes(I);
-  const int rows_all = T * (a.k + a.S);
-  const uint32_t h_bytes = a.h_in_smem ? (uint32_t)rows_all * I * 4 : 0;
-  const float* hsrc = h_bytes ? reinterpret_cast<const float*>(smem) : a.hbuf;
-  uint8_t* ring = smem + ring_offset(h_bytes);
-  if (tid == 0) {
-    for (int s = 0; s < a.stages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kConsumerWarps);
-    }
-    mbar_init(&hbar, 1);
-    s_fail = 0;
-    fence_mbar_init();
-  }
-  // The router finished before the gate/up kernel let this grid start, so its
-  // logits are final: route and start streaming W_down before h exists.
-  route_in_smem<kThreads>(a.logits, T, a.E, a.k, a.S, r);
-  const int o0 = (int)((int64_t)H * blockIdx.x / gridDim.x), o1 = (int)((int64_t)H * (blockIdx.x + 1) / gridDim.x);
-  const int n_blocks = (o1 - o0 + kDownRowBlock - 1) / kDownRowBlock;
-  const int nU = r.n_unique;
-  const int64_t n_stages = (int64_t)nU * n_blocks;  // (expert, block), block fastest
-
-  if (warp == kProducer) {
-    if (lane == 0) {
-      int64_t j = 0;
-      for (; j < n_stages; ++j) {
-        const int st = (int)(j % a.stages);
-        if (j >= a.stages && !mbar_wait(&empty[st], (uint32_t)(((j / a.stages) - 1) & 1))) {
-          s_fail = 1;
+    // ---- phase 2: every CTA's h is written before any CTA reads it
+    consumer_sync();
+    if (tid == 0) {
+      __threadfence();
+      atomicAdd(reinterpret_cast<unsigned long long*>(&a.meta->gbar), 1ull);
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_u64(reinterpret_cast<const unsigned long long*>(&a.meta->gbar)) < gridDim.x) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          report_wait(a.meta, kSiteGrid, 0, gridDim.x);
           break;
         }
-        const int e = r.u[j / n_blocks].x, blk = (int)(j % n_blocks);
-        const int r0 = o0 + blk * kDownRowBlock, nr = ::min(kDownRowBlock + 0, o1 - r0);
-        const int64_t row = (int64_t)e * H + r0;
-        uint8_t* sb = ring + (size_t)st * a.stage_bytes;
-        mbar_arrive_expect_tx(&full[st], (uint32_t)nr * (I + pitch));
-        bulk_g2s(sb, a.q + row * I, (uint32_t)nr * I, &full[st]);
-        bulk_g2s(sb + (size_t)kDownRowBlock * I, a.s + row * pitch, (uint32_t)nr * pitch, &full[st]);
+        __nanosleep(64);
       }
-      for (int64_t q = std::max<int64_t>(0, j - a.stages); q < j; ++q)
-        mbar_wait(&full[q % a.stages], (uint32_t)((q / a.stages) & 1));
+      if (a.h_smem) {  // x is no longer read: the area now takes h
+        fence_proxy_async_smem();
+        const uint32_t hb = (uint32_t)r.rows * I * 4;
+        mbar_arrive_expect_tx(&actbar, hb);
+        bulk_g2s(smem, a.hbuf, hb, &actbar);
+      }
     }
-  }
-  pdl_wait();  // h from the gate/up kernel
-  pdl_launch_dependents();
-  if (tid == 0 && h_bytes) {
-    mbar_arrive_expect_tx(&hbar, h_bytes);
-    bulk_g2s(smem, a.hbuf, h_bytes, &hbar);
-  }
-  if (warp != kProducer) {
-    bool ok = !h_bytes || mbar_wait(&hbar, 0);
-    const int nseg = I / 16;
-    float acc[kMaxDownBlocks][2];
+    consumer_sync();
+    if (a.h_smem && ok && !mbar_wait(&actbar, 0)) {
+      report_wait(a.meta, kSiteDnH, 0, r.rows);
+      ok = false;
+    }
+
+    // ---- phase 3: down + combine. Warp w owns row w of every 16-row block.
+    const float* hsrc = a.h_smem ? reinterpret_cast<const float*>(smem) : a.hbuf;
+    const int nseg_i = I / 16;
+    float acc[kMaxRowBlocks];
 #pragma unroll
-    for (int b = 0; b < kMaxDownBlocks; ++b) acc[b][0] = acc[b][1] = 0.f;
-    for (int64_t j = 0; j < n_stages && ok; ++j) {
+    for (int b = 0; b < kMaxRowBlocks; ++b) acc[b] = 0.f;
+    for (int64_t jd = 0; jd < n_dn && ok; ++jd) {
+      const int64_t j = n_gu + jd;
       const int st = (int)(j % a.stages);
       if (!mbar_wait(&full[st], (uint32_t)((j / a.stages) & 1))) {
+        report_wait(a.meta, kSiteDnFull, j, warp);
         ok = false;
         break;
       }
-      const int4 ui = r.u[j / n_blocks];
-      const int blk = (int)(j % n_blocks);
-      const int nr = ::min(kDownRowBlock + 0, o1 - (o0 + blk * kDownRowBlock));
-      const uint8_t* sb = ring + (size_t)st * a.stage_bytes;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int rr = warp + q * kConsumerWarps;
-        if (rr >= nr) continue;
-        const uint8_t* qrow = sb + (size_t)rr * I;
-        const uint16_t* sc = reinterpret_cast<const uint16_t*>(sb + (size_t)kDownRowBlock * I + (size_t)rr * pitch);
+      const int4 ui = r.u[jd / n_blk];
+      const int blk = (int)(jd % n_blk);
+      const int nr = ::min(kRowBlock + 0, o1 - (o0 + blk * kRowBlock));
+      if (warp < nr) {
+        const uint8_t* sb = ring + (size_t)st * a.stage_bytes;
+        const uint8_t* qrow = sb + (size_t)warp * I;
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(sb + (size_t)kRowBlock * I + (size_t)warp * pitch_i);
         for (int m = 0; m < ui.z; ++m) {
           const int pos = ui.y + m;
           const float* hrow = hsrc + (size_t)pos * I;
           float d = 0.f;
-          for (int seg = lane; seg < nseg; seg += 32) {
-            float hv[16];
-            load_h16(hrow + seg * 16, h_bytes != 0, hv);
+          for (int seg = lane; seg < nseg_i; seg += 32) {
+            f2 hv[8];
+            if (a.h_smem)
+              x16_from_f32(hrow + seg * 16, hv);
+            else
+              x16_from_f32_global(hrow + seg * 16, hv);
             const uint4 qq = *reinterpret_cast<const uint4*>(qrow + seg * 16);
             d = fmaf(half_bits_to_f32(sc[seg >> 1]), dot16(qq, hv), d);
           }
           d = warp_sum(d);
 #pragma unroll
-          for (int b = 0; b < kMaxDownBlocks; ++b)
-            if (b == blk && lane == r.tok[pos]) acc[b][q] = fmaf(r.rg[pos], d, acc[b][q]);
+          for (int b = 0; b < kMaxRowBlocks; ++b)
+            if (b == blk && lane == r.tok[pos]) acc[b] = fmaf(r.rg[pos], d, acc[b]);
         }
       }
       __syncwarp();
@@ -337,48 +364,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_down_kernel(DownArgs a) {
     }
     if (ok && lane < T) {
 #pragma unroll
-      for (int b = 0; b < kMaxDownBlocks; ++b) {
-        if (b >= n_blocks) break;
-        const int r0 = o0 + b * kDownRowBlock, nr = ::min(kDownRowBlock + 0, o1 - r0);
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int rr = warp + q * kConsumerWarps;
-          if (rr < nr) a.out[(int64_t)lane * H + r0 + rr] = __float2bfloat16_rn(acc[b][q]);
-        }
+      for (int b = 0; b < kMaxRowBlocks; ++b) {
+        const int row = o0 + b * kRowBlock + warp;
+        if (b < n_blk && row < o1) a.out[(int64_t)lane * H + row] = __float2bfloat16_rn(acc[b]);
       }
     }
-    if (!ok && lane == 0) s_fail = 1;
   }
   __syncthreads();
-  if (tid == 0 && s_fail) report(a.meta, kStatusTimeout);
 }
 
-template <typename K, typename A>
-cudaError_t launch_pdl(K kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t s, A args) {
+cudaError_t launch(const DecodeArgs& a, unsigned grid, size_t smem, cudaStream_t s, bool pdl) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = grid;
-  cfg.blockDim = block;
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;  // the grid-wide barrier needs every CTA resident
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, args);
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, decode_experts_kernel, a);
 }
 
-// The gate/up and down CTAs are sized to fit on one SM together (so the down
-// kernel can start streaming while gate/up runs): each takes at most this
-// much dynamic shared memory.
-constexpr uint32_t kDynSmemEach = 96 * 1024;
-constexpr uint32_t kActSmemMax = 32 * 1024;  // x or h staged in shared memory up to this size
+int g_smem_optin = 0;
+constexpr uint32_t kActMax = 80 * 1024;     // x or h in shared memory up to this size
+constexpr uint32_t kStageTarget = 24 * 1024;
 
 }  // namespace
 
 cudaError_t configure_decode_kernels() {
-  cudaError_t e = allow_max_dynamic_smem(decode_gateup_kernel);
-  if (e == cudaSuccess) e = allow_max_dynamic_smem(decode_down_kernel);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncAttributes fa;
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, decode_experts_kernel);
+  if (e == cudaSuccess) {
+    g_smem_optin -= (int)fa.sharedSizeBytes;
+    e = cudaFuncSetAttribute(decode_experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_optin);
+  }
   return e;
 }
 
@@ -386,63 +412,47 @@ cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfl
                               int32_t* ids_out, float* gates_out, cudaStream_t s) {
   const int H = h->cfg.H, I = h->cfg.I, k = h->cfg.k, S = h->S;
   const int rows = T * (k + S);
-  if ((H + h->num_sms - 1) / h->num_sms > kDownRowBlock * kMaxDownBlocks) return cudaErrorNotSupported;
-  cudaError_t err;
-  {
-    GateUpArgs a;
-    a.q = h->q_gu;
-    a.s = h->s_gu;
-    a.x = x;
-    a.logits = h->logits;
-    a.hbuf = static_cast<float*>(h->hbuf);
-    a.out = RoutingOut{ids_out, gates_out, h->ids,      h->gates,    h->counts, h->offsets,
-                       h->perm, h->inv,    h->row_token, h->row_gate, h->uinfo,  h->meta};
-    a.H = H;
-    a.I = I;
-    a.E = h->cfg.E;
-    a.k = k;
-    a.S = S;
-    a.T = T;
-    a.publish = publish ? 1 : 0;
-    const uint32_t x_bytes = (uint32_t)T * H * 2;
-    a.x_in_smem = x_bytes <= kActSmemMax;
-    const uint32_t act = a.x_in_smem ? x_bytes : 0;
-    const uint32_t unit_bytes = (uint32_t)(2 * H + 2 * scale_pitch_bytes(H));
-    int R = 8;
-    while (R > 1 && (uint64_t)R * unit_bytes * 3 > kDynSmemEach - ring_offset(act)) R /= 2;
-    a.units_per_stage = R;
-    a.stage_bytes = (uint32_t)R * unit_bytes;
-    const uint32_t ring_off = ring_offset(act);
-    a.stages = (int)std::min<int64_t>(kMaxStages, (kDynSmemEach - ring_off) / a.stage_bytes);
-    if (a.stages < 2) return cudaErrorInvalidConfiguration;
-    size_t smem = ring_off + (size_t)a.stages * a.stage_bytes;
-    KernelTimer tm(h, FW_KERNEL_DECODE_GATEUP, s);
-    err = launch_pdl(decode_gateup_kernel, dim3((unsigned)h->num_sms), dim3(kThreads), smem, s, a);
-    if (err != cudaSuccess) return err;
-  }
-  {
-    DownArgs a;
-    a.q = h->q_d;
-    a.s = h->s_d;
-    a.logits = h->logits;
-    a.hbuf = static_cast<const float*>(h->hbuf);
-    a.out = out;
-    a.meta = h->meta;
-    a.H = H;
-    a.I = I;
-    a.E = h->cfg.E;
-    a.k = k;
-    a.S = S;
-    a.T = T;
-    const uint32_t h_bytes = (uint32_t)rows * I * 4;
-    a.h_in_smem = h_bytes <= kActSmemMax;
-    a.stage_bytes = (uint32_t)(kDownRowBlock * (I + scale_pitch_bytes(I)));
-    const uint32_t ring_off = ring_offset(a.h_in_smem ? h_bytes : 0);
-    a.stages = (int)std::min<int64_t>(kMaxStages, (kDynSmemEach - ring_off) / a.stage_bytes);
-    if (a.stages < 2) return cudaErrorInvalidConfiguration;
-    size_t smem = ring_off + (size_t)a.stages * a.stage_bytes;
-    KernelTimer tm(h, FW_KERNEL_DECODE_DOWN, s);
-    err = launch_pdl(decode_down_kernel, dim3((unsigned)std::min(h->num_sms, H)), dim3(kThreads), smem, s, a);
+  const int grid = h->num_sms;
+  if ((H + grid - 1) / grid > kRowBlock * kMaxRowBlocks) return cudaErrorNotSupported;
+  DecodeArgs a;
+  a.q_gu = reinterpret_cast<const uint8_t*>(h->q_gu);
+  a.s_gu = h->s_gu;
+  a.q_d = reinterpret_cast<const uint8_t*>(h->q_d);
+  a.s_d = h->s_d;
+  a.x = x;
+  a.logits = h->logits;
+  a.hbuf = static_cast<float*>(h->hbuf);
+  a.out = out;
+  a.ro = RoutingOut{ids_out, gates_out, h->ids,      h->gates,    h->counts, h->offsets,
+                    h->perm, h->inv,    h->row_token, h->row_gate, h->uinfo,  h->meta};
+  a.meta = h->meta;
+  a.H = H;
+  a.I = I;
+  a.E = h->cfg.E;
+  a.k = k;
+  a.S = S;
+  a.T = T;
+  a.publish = publish ? 1 : 0;
+  const uint32_t x32 = (uint32_t)T * H * 4, x16 = (uint32_t)T * H * 2, hb = (uint32_t)rows * I * 4;
+  a.x_mode = x32 <= 32 * 1024 ? kXSmemF32 : (x16 <= kActMax ? kXSmemBf16 : kXGlobal);
+  a.h_smem = hb <= kActMax;
+  const uint32_t xb = a.x_mode == kXSmemF32 ? x32 : (a.x_mode == kXSmemBf16 ? x16 : 0);
+  a.act_bytes = std::max(xb, a.h_smem ? hb : 0u);
+  const uint32_t unit = (uint32_t)(2 * H + 2 * scale_pitch_bytes(H));
+  int R = 8;
+  while (R > 1 && (uint32_t)R * unit > kStageTarget) R /= 2;
+  a.R = R;
+  const uint32_t dn_stage = (uint32_t)(kRowBlock * (I + scale_pitch_bytes(I)));
+  a.stage_bytes = std::max((uint32_t)R * unit, dn_stage);
+  const int64_t ring_bytes = (int64_t)g_smem_optin - align128(a.act_bytes) - 256;
+  a.stages = (int)std::min<int64_t>(kMaxStages, ring_bytes / a.stage_bytes);
+  if (a.stages < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = align128(a.act_bytes) + (size_t)a.stages * a.stage_bytes;
+  KernelTimer tm(h, FW_KERNEL_DECODE_EXPERTS, s);
+  cudaError_t err = launch(a, (unsigned)grid, smem, s, true);
+  if (err == cudaErrorNotSupported || err == cudaErrorInvalidValue) {
+    cudaGetLastError();  // the combination of attributes was refused: launch without PDL
+    err = launch(a, (unsigned)grid, smem, s, false);
   }
   return err;
 }

@@ -37,12 +37,14 @@ __host__ __device__ inline int64_t gu_row_up(int64_t i) { return gu_row_gate(i) 
 
 // Device-side routing metadata (one small struct per handle, device memory).
 struct Meta {
+  unsigned long long gbar;  // decode grid-wide barrier: CTAs arrived (reset by the router)
   int32_t n_unique;     // experts with at least one row, shared included
   uint32_t ticket;      // last-CTA detection in the router (self-resetting)
   int32_t status;       // kStatus* bits
   int32_t T;            // T of the last route
   int32_t n_mtiles;     // prefill: number of (expert, 128-row) tiles
-  int32_t pad[3];
+  int32_t pad;
+  int32_t diag[4];      // first failed wait: (site, block, stage, detail); site 0 = none
 };
 
 // Host-side event pool of the optional per-kernel timing.
@@ -73,10 +75,10 @@ struct Handle {
   int num_sms;
   int last_T;         // T of the last fw_moe_route, -1 before any
   // ---- repacked weights (device)
-  int8_t* q_gu;       // [EU][2I][H] codes, gate/up interleaved per 64-row group
+  int8_t* q_gu;       // [EU][2I][H] codes + 128 (offset binary), gate/up interleaved per 64-row group
   uint8_t* s_gu;      // [EU][2I][pitch(H)] binary16 scales, row-major (padded rows)
   uint16_t* st_gu;    // [EU][H/32][2I] binary16 scales, transposed
-  int8_t* q_d;        // [EU][H][I]
+  int8_t* q_d;        // [EU][H][I] codes + 128
   uint8_t* s_d;       // [EU][H][pitch(I)]
   uint16_t* st_d;     // [EU][I/32][H]
   float* wr;          // [E][H]
@@ -135,6 +137,9 @@ inline cudaError_t allow_max_dynamic_smem(K kernel) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin - (int)fa.sharedSizeBytes);
   return e;
 }
+
+// Record the text of a failed call for fw_moe_last_error; returns st.
+fw_status set_error(fw_status st, const char* text);
 
 // ---------------------------------------------------------------- launchers
 cudaError_t configure_route_kernels();
@@ -243,12 +248,11 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   return r;
 }
 
-// Four int8 codes packed in a word -> four exact floats, without a conversion
-// instruction: byte b of (w ^ 0x80808080) is q_b + 128; placing it in the low
-// mantissa byte of 2^23 gives the float 2^23 + q_b + 128 exactly, and
-// subtracting 2^23 + 128 leaves q_b.
-__device__ __forceinline__ void i8x4_to_f32(uint32_t w, float& a, float& b, float& c, float& d) {
-  const uint32_t u = w ^ 0x80808080u;
+// Four offset-binary codes (q + 128) packed in a word -> four exact floats q,
+// without a conversion instruction: placing byte b in the low mantissa byte of
+// 2^23 gives the float 2^23 + q_b + 128 exactly, and subtracting 2^23 + 128
+// leaves q_b.
+__device__ __forceinline__ void u8x4_to_f32(uint32_t u, float& a, float& b, float& c, float& d) {
   const float bias = 8388736.0f;  // 2^23 + 128
   a = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7650)) - bias;
   b = __uint_as_float(__byte_perm(u, 0x4B000000u, 0x7651)) - bias;
@@ -271,6 +275,21 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 __device__ __forceinline__ void report(Meta* m, int bits) { atomicOr(&m->status, bits); }
+
+// Sites of bounded waits, recorded with the first timeout (see Meta::diag).
+enum WaitSite {
+  kSiteGuX = 1, kSiteGuFull = 2, kSiteGuEmpty = 3, kSiteDnH = 4, kSiteDnFull = 5, kSiteDnEmpty = 6,
+  kSiteGemm = 7, kSiteGrid = 8
+};
+
+__device__ __forceinline__ void report_wait(Meta* m, int site, int64_t stage, int detail) {
+  if (atomicCAS(&m->diag[0], 0, site) == 0) {
+    m->diag[1] = blockIdx.x;
+    m->diag[2] = (int32_t)stage;
+    m->diag[3] = detail;
+  }
+  atomicOr(&m->status, kStatusTimeout);
+}
 
 }  // namespace dev
 }  // namespace fw

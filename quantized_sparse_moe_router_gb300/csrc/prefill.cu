@@ -175,7 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
     if (mbar_wait(bar, parity)) return true;
-    if (atomicExch(&s_abort, 1) == 0) report(const_cast<Meta*>(a.meta), kStatusTimeout);
+    if (atomicExch(&s_abort, 1) == 0) report_wait(const_cast<Meta*>(a.meta), kSiteGemm, warp, (int)parity);
     return false;
   };
 
@@ -252,10 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint4 qv = *reinterpret_cast<const uint4*>(q + r * BK + c * 16);
           const float d = half_bits_to_f32(sc[(c >> 1) * BN + r]);
           float f[16];
-          i8x4_to_f32(qv.x, f[0], f[1], f[2], f[3]);
-          i8x4_to_f32(qv.y, f[4], f[5], f[6], f[7]);
-          i8x4_to_f32(qv.z, f[8], f[9], f[10], f[11]);
-          i8x4_to_f32(qv.w, f[12], f[13], f[14], f[15]);
+          u8x4_to_f32(qv.x, f[0], f[1], f[2], f[3]);
+          u8x4_to_f32(qv.y, f[4], f[5], f[6], f[7]);
+          u8x4_to_f32(qv.z, f[8], f[9], f[10], f[11]);
+          u8x4_to_f32(qv.w, f[12], f[13], f[14], f[15]);
           uint4 lo, hi;
           lo.x = pack_bf16x2(f[0] * d, f[1] * d);
           lo.y = pack_bf16x2(f[2] * d, f[3] * d);

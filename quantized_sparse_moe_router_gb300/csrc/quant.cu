@@ -66,6 +66,8 @@ __device__ __forceinline__ int64_t plane_row(const PlaneView& p, int64_t r) {
 }
 
 // One thread per block of one expert range: GGUF block -> code plane + both scale planes.
+// The code planes hold q + 128 (offset binary: q XOR 0x80), which the kernels
+// turn into floats with one byte permute and one subtraction.
 __global__ void repack_kernel(PlaneView p, int expert0, int64_t nblocks, const uint8_t* __restrict__ src) {
   int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (blk >= nblocks) return;
@@ -77,7 +79,7 @@ __global__ void repack_kernel(PlaneView p, int expert0, int64_t nblocks, const u
   const uint16_t* in = reinterpret_cast<const uint16_t*>(src + blk * kQBlockBytes);
   uint32_t words[8];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) words[i] = (uint32_t)in[1 + 2 * i] | ((uint32_t)in[2 + 2 * i] << 16);
+  for (int i = 0; i < 8; ++i) words[i] = ((uint32_t)in[1 + 2 * i] | ((uint32_t)in[2 + 2 * i] << 16)) ^ 0x80808080u;
   const int64_t prow = e * p.prows + plane_row(p, r);
   uint4* qd = reinterpret_cast<uint4*>(p.q + prow * p.K + b * kQBlock);
   qd[0] = make_uint4(words[0], words[1], words[2], words[3]);
@@ -95,6 +97,8 @@ __global__ void export_kernel(PlaneView p, int expert, int64_t nblocks, uint8_t*
   const uint4* qs = reinterpret_cast<const uint4*>(p.q + prow * p.K + b * kQBlock);
   uint4 a = qs[0], c = qs[1];
   uint32_t words[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+  for (int i = 0; i < 8; ++i) words[i] ^= 0x80808080u;  // back from offset binary
   uint16_t* out = reinterpret_cast<uint16_t*>(dst + blk * kQBlockBytes);
   out[0] = reinterpret_cast<const uint16_t*>(p.s + prow * scale_pitch_bytes(p.K))[b];
 #pragma unroll

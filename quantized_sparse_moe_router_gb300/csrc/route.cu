@@ -53,6 +53,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
   const int e = blockIdx.x;
   const int T = a.T, H = a.H;
   pdl_launch_dependents();  // the expert kernels wait for this grid's completion before reading
+  if (blockIdx.x == 0 && tid == 0) a.meta->gbar = 0;  // fresh grid barrier for this call's expert kernel
   {
     float acc[kMaxDecodeT];
 #pragma unroll

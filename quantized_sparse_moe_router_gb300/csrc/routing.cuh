@@ -62,118 +62,192 @@ __device__ __forceinline__ float warp_gate(float my_z, int k, int lane) {
   return ex / sum;
 }
 
-// Exclusive scan of n ints in shared memory by the whole block of NT threads.
-// Returns the total.
-template <int NT>
-__device__ int block_exclusive_scan(int* v, int n, int* warp_tot) {
-  constexpr int NW = NT / 32;
-  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int per = (n + NT - 1) / NT;
-  const int b = tid * per, e = min(n, b + per);
+// Bitonic sort, within one warp, of 32*EPL (logit, id) pairs into "comes
+// first" order: descending logit, equal logits by ascending id. Lane l holds
+// positions l*EPL .. l*EPL+EPL-1.
+template <int EPL>
+__device__ __forceinline__ void warp_sort_desc(float (&z)[EPL], int (&id)[EPL], int lane) {
+  constexpr int N = 32 * EPL;
+#pragma unroll
+  for (int size = 2; size <= N; size <<= 1) {
+#pragma unroll
+    for (int stride = size / 2; stride > 0; stride >>= 1) {
+      if (stride >= EPL) {
+        const int pl = stride / EPL;
+        const bool lower = (lane & pl) == 0;
+#pragma unroll
+        for (int m = 0; m < EPL; ++m) {
+          const float oz = __shfl_xor_sync(0xFFFFFFFFu, z[m], pl);
+          const int oid = __shfl_xor_sync(0xFFFFFFFFu, id[m], pl);
+          const bool up = ((((lane & ~pl) * EPL) + m) & size) == 0;
+          const bool mine_first = z[m] > oz || (z[m] == oz && id[m] < oid);
+          const bool keep = (lower == up) ? mine_first : !mine_first;
+          if (!keep) {
+            z[m] = oz;
+            id[m] = oid;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int m = 0; m < EPL; ++m) {
+          const int mm = m ^ stride;
+          if (mm > m) {
+            const bool up = (((lane * EPL) + m) & size) == 0;
+            const bool m_first = z[m] > z[mm] || (z[m] == z[mm] && id[m] < id[mm]);
+            if (m_first != up) {
+              const float tz = z[m];
+              z[m] = z[mm];
+              z[mm] = tz;
+              const int ti = id[m];
+              id[m] = id[mm];
+              id[mm] = ti;
+            }
+          }
+        }
+      }
+    }
+  }
+}
+
+// One warp: the top-k of logits z[0..E) (E <= 32*EPL), ties to the lower id,
+// in descending order; lane j < k ends with (id_j, gate_j).
+template <int EPL>
+__device__ __forceinline__ void warp_select_sorted(const float* zrow, int E, int k, int lane, int* out_id,
+                                                   float* out_gate) {
+  float z[EPL];
+  int id[EPL];
+#pragma unroll
+  for (int m = 0; m < EPL; ++m) {
+    const int e = lane * EPL + m;
+    z[m] = e < E ? __ldcg(zrow + e) : -INFINITY;
+    id[m] = e < E ? e : 0x40000000 + e;  // padding sorts last
+  }
+  warp_sort_desc<EPL>(z, id, lane);
+  int my_id = -1;
+  float my_z = -INFINITY;
+#pragma unroll
+  for (int m = 0; m < EPL; ++m) {
+    const float vz = __shfl_sync(0xFFFFFFFFu, z[m], lane / EPL);
+    const int vi = __shfl_sync(0xFFFFFFFFu, id[m], lane / EPL);
+    if (lane % EPL == m) {
+      my_z = vz;
+      my_id = vi;
+    }
+  }
+  *out_id = my_id;
+  *out_gate = warp_gate(my_z, k, lane);
+}
+
+__device__ __forceinline__ void warp_select_any(const float* zrow, int E, int k, int lane, int* id, float* g) {
+  if (E <= 32)
+    warp_select_sorted<1>(zrow, E, k, lane, id, g);
+  else if (E <= 64)
+    warp_select_sorted<2>(zrow, E, k, lane, id, g);
+  else if (E <= 128)
+    warp_select_sorted<4>(zrow, E, k, lane, id, g);
+  else
+    warp_select_sorted<8>(zrow, E, k, lane, id, g);
+}
+
+// One warp: exclusive scan of n <= 32*9 ints in place; returns the total.
+__device__ __forceinline__ int warp_exclusive_scan(int* v, int n, int lane) {
+  const int per = (n + 31) / 32;
+  const int b = lane * per, e = min(n, b + per);
   int s = 0;
   for (int i = b; i < e; ++i) s += v[i];
   int incl = s;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
     if (lane >= o) incl += t;
   }
-  if (lane == 31) warp_tot[w] = incl;
-  __syncthreads();
-  int wbase = 0, total = 0;
-#pragma unroll
-  for (int i = 0; i < NW; ++i) {
-    if (i < w) wbase += warp_tot[i];
-    total += warp_tot[i];
-  }
-  int run = wbase + incl - s;
+  int run = incl - s;
   for (int i = b; i < e; ++i) {
-    int c = v[i];
+    const int c = v[i];
     v[i] = run;
     run += c;
   }
-  __syncthreads();
-  return total;
+  return __shfl_sync(0xFFFFFFFFu, incl, 31);
 }
 
 // The routing of a decode batch in shared memory.
 struct SmemRouting {
   int ids[kMaxDecodeT * kMaxK];
   float gates[kMaxDecodeT * kMaxK];
-  int cnt[kMaxE + 2];     // per expert, then exclusive offsets (cnt[EU] = rows)
-  int c2[kMaxE + 2];      // per-expert counts
+  int cnt[kMaxE + 2];     // per-expert counts (cnt[E] = T for the shared expert)
+  int off[kMaxE + 2];     // exclusive offsets (off[EU] = rows)
   uint32_t mask[kMaxE + 1];
   int nz[kMaxE + 2];      // nonzero flags, then their exclusive scan
   int4 u[kMaxE + 1];      // (expert, first row, rows, 0) of experts with rows, ascending
   int tok[kMaxRowsDecode];
   float rg[kMaxRowsDecode];
   int slot[kMaxRowsDecode];  // grouped row -> slot id (perm)
-  int wtot[32];
   int n_unique;
   int rows;
 };
 
-// Whole block (NT threads, NT >= 32 * min(T, NT/32)): selection for T tokens
-// from logits [T][E] (global, written by an earlier kernel), gates, and the
-// grouping. Ends with a __syncthreads; every field above is then valid.
+// Whole block (NT threads, at least min(T, NT/32) warps): selection for T <= 16
+// tokens from logits [T][E] (global, written by an earlier kernel; one warp per
+// token, bitonic top-k), gates, and the grouping. Four block barriers; ends
+// with one, after which every field is valid.
 template <int NT>
 __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, SmemRouting& r) {
   constexpr int NW = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int EU = E + S;
   for (int t = warp; t < T; t += NW) {
-    float zl[kMaxEPerLane];
-#pragma unroll
-    for (int m = 0; m < kMaxEPerLane; ++m) {
-      int ee = lane + 32 * m;
-      zl[m] = ee < E ? __ldcg(logits + t * E + ee) : -INFINITY;
-    }
     int id;
-    float zv;
-    warp_topk(zl, E, k, lane, &id, &zv);
-    float g = warp_gate(zv, k, lane);
+    float g;
+    warp_select_any(logits + t * E, E, k, lane, &id, &g);
     if (lane < k) {
       r.ids[t * k + lane] = id;
       r.gates[t * k + lane] = g;
     }
   }
-  const int EU = E + S;
-  for (int i = tid; i < EU + 1; i += NT) r.cnt[i] = 0;
-  for (int i = tid; i < EU; i += NT) r.mask[i] = 0;
+  for (int i = tid; i < EU + 1; i += NT) {
+    r.cnt[i] = 0;
+    if (i < EU) r.mask[i] = 0;
+  }
   __syncthreads();
   for (int p = tid; p < T * k; p += NT) {
-    int ee = r.ids[p];
+    const int ee = r.ids[p];
     atomicAdd(&r.cnt[ee], 1);
     atomicOr(&r.mask[ee], 1u << (p / k));
   }
   if (S && tid == 0) r.cnt[E] = T;
   __syncthreads();
-  for (int i = tid; i < EU; i += NT) {
-    r.c2[i] = r.cnt[i];
-    r.nz[i] = r.cnt[i] > 0;
+  if (warp == 0) {
+    for (int i = lane; i < EU + 1; i += 32) {
+      r.off[i] = i < EU ? r.cnt[i] : 0;
+      r.nz[i] = i < EU ? (r.cnt[i] > 0) : 0;
+    }
+    __syncwarp();
+    const int rows = warp_exclusive_scan(r.off, EU + 1, lane);
+    __syncwarp();
+    const int n_unique = warp_exclusive_scan(r.nz, EU, lane);
+    __syncwarp();
+    for (int i = lane; i < EU; i += 32)
+      if (r.cnt[i] > 0) r.u[r.nz[i]] = make_int4(i, r.off[i], r.cnt[i], 0);
+    if (lane == 0) {
+      r.n_unique = n_unique;
+      r.rows = rows;
+    }
   }
   __syncthreads();
-  const int rows = block_exclusive_scan<NT>(r.cnt, EU + 1, r.wtot);
   for (int p = tid; p < T * k; p += NT) {
-    int t = p / k, ee = r.ids[p];
-    int pos = r.cnt[ee] + __popc(r.mask[ee] & ((1u << t) - 1u));
+    const int t = p / k, ee = r.ids[p];
+    const int pos = r.off[ee] + __popc(r.mask[ee] & ((1u << t) - 1u));
     r.tok[pos] = t;
     r.rg[pos] = r.gates[p];
     r.slot[pos] = p;
   }
   if (S)
     for (int t = tid; t < T; t += NT) {
-      int pos = r.cnt[E] + t;
+      const int pos = r.off[E] + t;
       r.tok[pos] = t;
       r.rg[pos] = 1.0f;
       r.slot[pos] = T * k + t;
     }
-  const int n_unique = block_exclusive_scan<NT>(r.nz, EU, r.wtot);
-  for (int i = tid; i < EU; i += NT)
-    if (r.c2[i] > 0) r.u[r.nz[i]] = make_int4(i, r.cnt[i], r.c2[i], 0);
-  if (tid == 0) {
-    r.n_unique = n_unique;
-    r.rows = rows;
-  }
   __syncthreads();
 }
 
@@ -202,8 +276,8 @@ __device__ void publish_routing(const SmemRouting& r, int T, int E, int k, int S
     o.ids[p] = r.ids[p];
     o.gates[p] = r.gates[p];
   }
-  for (int i = tid; i < EU; i += NT) o.counts[i] = r.c2[i];
-  for (int i = tid; i < EU + 1; i += NT) o.offsets[i] = r.cnt[i];
+  for (int i = tid; i < EU; i += NT) o.counts[i] = r.cnt[i];
+  for (int i = tid; i < EU + 1; i += NT) o.offsets[i] = r.off[i];
   for (int pos = tid; pos < r.rows; pos += NT) {
     o.perm[pos] = r.slot[pos];
     o.inv[r.slot[pos]] = pos;

@@ -19,7 +19,7 @@ from synth import KIND_DOWN, KIND_GATE, KIND_UP
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
-GATE_TOL = 2e-6
+GATE_TOL = 1e-5  # fp32 logits over H <= 8192 terms: gate error well below 1e-5 (1e-2 x output tolerance)
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -40,7 +40,7 @@ def check(wl, x, res, ol, sample=None):
     ids, gates, out, (off, perm, inv) = res
     ids_ref, gates_ref = ol.route(x)
     assert np.array_equal(ids, ids_ref)
-    assert np.abs(gates - gates_ref).max() <= 2e-6
+    assert np.abs(gates - gates_ref).max() <= 1e-5  # fp32 logits over H <= 8192 terms
     o_ref, p_ref, i_ref = oracle.permutation(ids_ref, wl.E)
     assert np.array_equal(off, o_ref) and np.array_equal(perm, p_ref) and np.array_equal(inv, i_ref)
     rows = np.arange(x.shape[0]) if sample is None else np.asarray(sample)
