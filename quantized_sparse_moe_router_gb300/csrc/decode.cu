@@ -9,7 +9,7 @@
 // asynchronous copies into a shared-memory ring fed by one producer warp, and
 // dequantised in registers by sixteen consumer warps.
 //
-// One persistent CTA per SM, launched cooperatively (all CTAs resident):
+// One persistent CTA per SM (all resident at once, see launch()):
 //   0. after the router's grid completes (programmatic dependent launch), each
 //      CTA rebuilds the batch's routing from the logits in shared memory
 //      (bitonic top-k per token; deterministic, so every CTA agrees); CTA 0
@@ -60,6 +60,7 @@ struct DecodeArgs {
   int h_smem;            // h staged in shared memory (fp32)
   uint32_t act_bytes;    // shared-memory area for x, then for h
 };
+// (smem layouts of x and h: see x16_from_f32_t)
 
 // ------------------------------------------------------------- packed fp32
 typedef unsigned long long f2;
@@ -110,13 +111,17 @@ __device__ __forceinline__ float dot16(const uint4 q, const f2 (&x)[8]) {
   return f2_hsum(f2_add(a, b));
 }
 
-__device__ __forceinline__ void x16_from_f32(const float* p, f2 (&x)[8]) {
-  const float4* q = reinterpret_cast<const float4*>(p);
+// Shared-memory vectors (x, h) are stored "segment-transposed" so that lane l
+// reading its 16-element segment l touches consecutive 16-byte words in each
+// of its loads (no bank conflicts): fp32 element e = 16 seg + 4 i + j of a
+// length-K vector sits at i * K/4 + 4 seg + j; bf16 element e = 16 seg + 8 i + j
+// at i * K/2 + 8 seg + j.
+__device__ __forceinline__ void x16_from_f32_t(const float* v, int K, int seg, f2 (&x)[8]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float4 v = q[i];
-    x[2 * i] = f2_pack(v.x, v.y);
-    x[2 * i + 1] = f2_pack(v.z, v.w);
+    const float4 w = *reinterpret_cast<const float4*>(v + i * (K / 4) + seg * 4);
+    x[2 * i] = f2_pack(w.x, w.y);
+    x[2 * i + 1] = f2_pack(w.z, w.w);
   }
 }
 
@@ -126,11 +131,13 @@ __device__ __forceinline__ void x16_from_bf16(uint4 a, uint4 b, f2 (&x)[8]) {
   for (int i = 0; i < 8; ++i) x[i] = f2_pack_bits(w[i] << 16, w[i] & 0xFFFF0000u);
 }
 
+// h written by other CTAs during this kernel: coherent (L2) loads, not the
+// read-only path.
 __device__ __forceinline__ void x16_from_f32_global(const float* p, f2 (&x)[8]) {
   const float4* q = reinterpret_cast<const float4*>(p);
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float4 v = __ldg(q + i);
+    const float4 v = __ldcg(q + i);
     x[2 * i] = f2_pack(v.x, v.y);
     x[2 * i + 1] = f2_pack(v.z, v.w);
   }
@@ -153,7 +160,7 @@ __host__ __device__ inline uint32_t align128(uint32_t v) { return (v + 127) / 12
 // ------------------------------------------------------------- the kernel
 __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
-  __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages], actbar;
+  __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
   __shared__ SmemRouting r;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = a.H, I = a.I, T = a.T, R = a.R;
@@ -164,7 +171,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kCW);
     }
-    mbar_init(&actbar, 1);
     fence_mbar_init();
   }
   pdl_wait();  // the router's logits (and its reset of the grid barrier)
@@ -222,22 +228,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   } else {
     // ------------------------------------------------------ consumers
     bool ok = true;
-    // x for this batch: fp32 or bf16 in shared memory, else read from global
+    // x for this batch, segment-transposed: fp32 or bf16 in shared memory, else read from global
     if (a.x_mode == kXSmemF32) {
       float* xs = reinterpret_cast<float*>(smem);
-      for (int i = tid; i < T * H / 8; i += kCW * 32) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
+      for (int c = tid; c < T * H / 8; c += kCW * 32) {  // c: 8 bf16 = half a segment
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x) + c);
+        const int t = c / (H / 8), cc = c % (H / 8), seg = cc >> 1, half = cc & 1;
         float4 lo4, hi4;
         bf16x2_to_f32(v.x, lo4.x, lo4.y);
         bf16x2_to_f32(v.y, lo4.z, lo4.w);
         bf16x2_to_f32(v.z, hi4.x, hi4.y);
         bf16x2_to_f32(v.w, hi4.z, hi4.w);
-        reinterpret_cast<float4*>(xs)[2 * i] = lo4;
-        reinterpret_cast<float4*>(xs)[2 * i + 1] = hi4;
+        float* base = xs + (size_t)t * H + seg * 4;
+        *reinterpret_cast<float4*>(base + (2 * half) * (H / 4)) = lo4;
+        *reinterpret_cast<float4*>(base + (2 * half + 1) * (H / 4)) = hi4;
       }
     } else if (a.x_mode == kXSmemBf16) {
-      for (int i = tid; i < T * H / 8; i += kCW * 32)
-        reinterpret_cast<uint4*>(smem)[i] = __ldg(reinterpret_cast<const uint4*>(a.x) + i);
+      __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);
+      for (int c = tid; c < T * H / 8; c += kCW * 32) {
+        const int t = c / (H / 8), cc = c % (H / 8), seg = cc >> 1, half = cc & 1;
+        *reinterpret_cast<uint4*>(xs + (size_t)t * H + half * (H / 2) + seg * 8) =
+            __ldg(reinterpret_cast<const uint4*>(a.x) + c);
+      }
     }
     consumer_sync();
 
@@ -270,14 +282,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
           for (int seg = lane; seg < nseg_h; seg += 32) {
             f2 xv[8];
             if (a.x_mode == kXSmemF32) {
-              x16_from_f32(reinterpret_cast<const float*>(smem) + (size_t)t * H + seg * 16, xv);
+              x16_from_f32_t(reinterpret_cast<const float*>(smem) + (size_t)t * H, H, seg, xv);
+            } else if (a.x_mode == kXSmemBf16) {
+              const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(smem) + (size_t)t * H;
+              x16_from_bf16(*reinterpret_cast<const uint4*>(xb + seg * 8),
+                            *reinterpret_cast<const uint4*>(xb + H / 2 + seg * 8), xv);
             } else {
-              const uint4* xp = a.x_mode == kXSmemBf16
-                                    ? reinterpret_cast<const uint4*>(smem + ((size_t)t * H + seg * 16) * 2)
-                                    : reinterpret_cast<const uint4*>(a.x + (size_t)t * H + seg * 16);
-              const uint4 x0 = a.x_mode == kXSmemBf16 ? xp[0] : __ldg(xp);
-              const uint4 x1 = a.x_mode == kXSmemBf16 ? xp[1] : __ldg(xp + 1);
-              x16_from_bf16(x0, x1, xv);
+              const uint4* xp = reinterpret_cast<const uint4*>(a.x + (size_t)t * H + seg * 16);
+              x16_from_bf16(__ldg(xp), __ldg(xp + 1), xv);
             }
             const uint4 qg = *reinterpret_cast<const uint4*>(qg_row + seg * 16);
             const uint4 qu = *reinterpret_cast<const uint4*>(qu_row + seg * 16);
@@ -293,30 +305,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       if (lane == 0) mbar_arrive(&empty[st]);
     }
 
-    // ---- phase 2: every CTA's h is written before any CTA reads it
+    // ---- phase 2: every CTA's h is written before any CTA reads it. The
+    // arrival is a release (ordering this CTA's h stores, which the consumer
+    // barrier ordered before it), the poll an acquire.
     consumer_sync();
     if (tid == 0) {
-      __threadfence();
-      atomicAdd(reinterpret_cast<unsigned long long*>(&a.meta->gbar), 1ull);
-      const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire_u64(reinterpret_cast<const unsigned long long*>(&a.meta->gbar)) < gridDim.x) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          report_wait(a.meta, kSiteGrid, 0, gridDim.x);
-          break;
+      unsigned long long* gb = reinterpret_cast<unsigned long long*>(&a.meta->gbar);
+      asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(gb) : "memory");
+      if (ld_acquire_u64(gb) < gridDim.x) {
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_u64(gb) < gridDim.x) {
+          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            report_wait(a.meta, kSiteGrid, 0, gridDim.x);
+            break;
+          }
         }
-        __nanosleep(64);
-      }
-      if (a.h_smem) {  // x is no longer read: the area now takes h
-        fence_proxy_async_smem();
-        const uint32_t hb = (uint32_t)r.rows * I * 4;
-        mbar_arrive_expect_tx(&actbar, hb);
-        bulk_g2s(smem, a.hbuf, hb, &actbar);
       }
     }
     consumer_sync();
-    if (a.h_smem && ok && !mbar_wait(&actbar, 0)) {
-      report_wait(a.meta, kSiteDnH, 0, r.rows);
-      ok = false;
+    if (a.h_smem) {  // x is no longer read: the area now takes h, segment-transposed
+      float* hs = reinterpret_cast<float*>(smem);
+      const int q4 = I / 4;
+      for (int c = tid; c < r.rows * q4; c += kCW * 32) {  // c: 4 floats
+        const int pos = c / q4, cc = c % q4, seg = cc >> 2, i = cc & 3;
+        *reinterpret_cast<float4*>(hs + (size_t)pos * I + i * (I / 4) + seg * 4) =
+            __ldcg(reinterpret_cast<const float4*>(a.hbuf) + c);
+      }
+      consumer_sync();
     }
 
     // ---- phase 3: down + combine. Warp w owns row w of every 16-row block.
@@ -347,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
           for (int seg = lane; seg < nseg_i; seg += 32) {
             f2 hv[8];
             if (a.h_smem)
-              x16_from_f32(hrow + seg * 16, hv);
+              x16_from_f32_t(hrow, I, seg, hv);
             else
               x16_from_f32_global(hrow + seg * 16, hv);
             const uint4 qq = *reinterpret_cast<const uint4*>(qrow + seg * 16);
@@ -373,19 +388,21 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   __syncthreads();
 }
 
-cudaError_t launch(const DecodeArgs& a, unsigned grid, size_t smem, cudaStream_t s, bool pdl) {
+// The grid-wide barrier needs every CTA resident: the grid is one CTA per SM
+// and each CTA takes most of an SM's shared memory, so once earlier work has
+// drained all of them are; if something else holds SMs past the wait limit
+// the call reports FW_ETIMEOUT instead of hanging.
+cudaError_t launch(const DecodeArgs& a, unsigned grid, size_t smem, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeCooperative;  // the grid-wide barrier needs every CTA resident
-  attr[0].val.cooperative = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 2 : 1;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_experts_kernel, a);
 }
 
@@ -447,14 +464,11 @@ cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfl
   const int64_t ring_bytes = (int64_t)g_smem_optin - align128(a.act_bytes) - 256;
   a.stages = (int)std::min<int64_t>(kMaxStages, ring_bytes / a.stage_bytes);
   if (a.stages < 2) return cudaErrorInvalidConfiguration;
-  const size_t smem = align128(a.act_bytes) + (size_t)a.stages * a.stage_bytes;
+  // at least half the SM's shared memory, so that no two CTAs share an SM
+  const size_t smem = std::max<size_t>(align128(a.act_bytes) + (size_t)a.stages * a.stage_bytes,
+                                       (size_t)g_smem_optin / 2 + 1024);
   KernelTimer tm(h, FW_KERNEL_DECODE_EXPERTS, s);
-  cudaError_t err = launch(a, (unsigned)grid, smem, s, true);
-  if (err == cudaErrorNotSupported || err == cudaErrorInvalidValue) {
-    cudaGetLastError();  // the combination of attributes was refused: launch without PDL
-    err = launch(a, (unsigned)grid, smem, s, false);
-  }
-  return err;
+  return launch(a, (unsigned)grid, smem, s);
 }
 
 }  // namespace fw

@@ -62,15 +62,40 @@ __device__ __forceinline__ float warp_gate(float my_z, int k, int lane) {
   return ex / sum;
 }
 
+// Compare-exchange of the register pairs (m, m ^ S) of one lane inside a
+// bitonic stage of block size `size` (S < EPL: both elements are in this lane).
+template <int EPL, int S>
+__device__ __forceinline__ void bitonic_local(float (&z)[EPL], int (&id)[EPL], int lane, int size) {
+  if constexpr (S < EPL) {
+#pragma unroll
+    for (int m = 0; m < EPL; ++m) {
+      const int mm = m ^ S;
+      if (mm > m) {
+        const bool up = (((lane * EPL) + m) & size) == 0;
+        const bool m_first = z[m] > z[mm] || (z[m] == z[mm] && id[m] < id[mm]);
+        if (m_first != up) {
+          const float tz = z[m];
+          z[m] = z[mm];
+          z[mm] = tz;
+          const int ti = id[m];
+          id[m] = id[mm];
+          id[mm] = ti;
+        }
+      }
+    }
+  }
+}
+
 // Bitonic sort, within one warp, of 32*EPL (logit, id) pairs into "comes
 // first" order: descending logit, equal logits by ascending id. Lane l holds
-// positions l*EPL .. l*EPL+EPL-1.
+// positions l*EPL .. l*EPL+EPL-1. The stage loops stay rolled: this runs once
+// per CTA, where instruction fetch, not arithmetic, is the cost.
 template <int EPL>
 __device__ __forceinline__ void warp_sort_desc(float (&z)[EPL], int (&id)[EPL], int lane) {
   constexpr int N = 32 * EPL;
-#pragma unroll
+#pragma unroll 1
   for (int size = 2; size <= N; size <<= 1) {
-#pragma unroll
+#pragma unroll 1
     for (int stride = size / 2; stride > 0; stride >>= 1) {
       if (stride >= EPL) {
         const int pl = stride / EPL;
@@ -87,23 +112,12 @@ __device__ __forceinline__ void warp_sort_desc(float (&z)[EPL], int (&id)[EPL], 
             id[m] = oid;
           }
         }
+      } else if (stride == 4) {
+        bitonic_local<EPL, 4>(z, id, lane, size);
+      } else if (stride == 2) {
+        bitonic_local<EPL, 2>(z, id, lane, size);
       } else {
-#pragma unroll
-        for (int m = 0; m < EPL; ++m) {
-          const int mm = m ^ stride;
-          if (mm > m) {
-            const bool up = (((lane * EPL) + m) & size) == 0;
-            const bool m_first = z[m] > z[mm] || (z[m] == z[mm] && id[m] < id[mm]);
-            if (m_first != up) {
-              const float tz = z[m];
-              z[m] = z[mm];
-              z[mm] = tz;
-              const int ti = id[m];
-              id[m] = id[mm];
-              id[mm] = ti;
-            }
-          }
-        }
+        bitonic_local<EPL, 1>(z, id, lane, size);
       }
     }
   }
@@ -139,11 +153,7 @@ __device__ __forceinline__ void warp_select_sorted(const float* zrow, int E, int
 }
 
 __device__ __forceinline__ void warp_select_any(const float* zrow, int E, int k, int lane, int* id, float* g) {
-  if (E <= 32)
-    warp_select_sorted<1>(zrow, E, k, lane, id, g);
-  else if (E <= 64)
-    warp_select_sorted<2>(zrow, E, k, lane, id, g);
-  else if (E <= 128)
+  if (E <= 128)
     warp_select_sorted<4>(zrow, E, k, lane, id, g);
   else
     warp_select_sorted<8>(zrow, E, k, lane, id, g);
