@@ -305,7 +305,7 @@ def run_fw(args, rank, world, local_rank):
         ids_h = torch.empty((T, k), dtype=torch.int32).pin_memory()
         out_h = torch.empty((T, w.H), dtype=torch.bfloat16).pin_memory()
         e2e_steps = max(1, min(args.steps, 3))
-        for r in range(4):
+        for r in range(min(4, N_X_ROWS)):
             layers[0].forward_host(xh[r], ids_h, out_h)
         barrier()
         t_s = time.perf_counter()

@@ -12,15 +12,17 @@
 // One persistent CTA per SM (all resident at once, see launch()):
 //   0. after the router's grid completes (programmatic dependent launch), each
 //      CTA rebuilds the batch's routing from the logits in shared memory
-//      (bitonic top-k per token; deterministic, so every CTA agrees); CTA 0
-//      publishes it;
+//      (top-k by rank; deterministic, so every CTA agrees); CTA 0 publishes
+//      it;
 //   1. gate/up: the CTA's slice of the (touched expert, i) units; for each of
 //      the expert's tokens h = SiLU(g) * u -> hbuf (fp32, grouped row order);
 //   2. grid-wide barrier (every h written) -- meanwhile the producer keeps
 //      streaming this CTA's W_down rows into the ring;
-//   3. down + combine: the CTA's block of output rows, every touched expert in
-//      ascending id (shared last); lane t accumulates gate * (W_down h) for
-//      token t and writes out[t] (bf16): fixed order, no atomics.
+//   3. down + combine: the CTA's output rows in blocks of 16, per block every
+//      touched expert in ascending id (shared last); each lane keeps partial
+//      sums of gate * (W_down h) per token across the experts, one warp
+//      reduction per (row, token) at the end of the block; out[t] (bf16) in a
+//      fixed order, no atomics.
 #include <algorithm>
 
 #include "routing.cuh"
@@ -35,8 +37,8 @@ constexpr int kThreads = (kCW + 1) * 32;   // + one producer warp
 constexpr int kProducer = kCW;
 constexpr int kMaxStages = 16;
 constexpr int kRowBlock = 16;              // output rows per W_down stage
-constexpr int kMaxRowBlocks = 4;           // row blocks a CTA may own
 constexpr uint32_t kConsumerBarrier = 1;   // named barrier of the 16 consumer warps
+constexpr int64_t kL2PrefetchMax = 40ll << 20;  // W_down bytes per call prefetched into L2 (L2 is 129 MB)
 
 enum XMode { kXGlobal = 0, kXSmemF32 = 1, kXSmemBf16 = 2 };
 
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   const int64_t lo = n_units * blockIdx.x / gridDim.x, hi = n_units * (blockIdx.x + 1) / gridDim.x;
   const int64_t b0 = lo / R;
   const int64_t n_gu = hi > lo ? (hi + R - 1) / R - b0 : 0;
-  // down stages: output rows [o0, o1), blocks of 16 rows, every touched expert (block fastest)
+  // down stages: output rows [o0, o1), blocks of 16 rows; per block every touched expert
   const int o0 = (int)((int64_t)H * blockIdx.x / gridDim.x), o1 = (int)((int64_t)H * (blockIdx.x + 1) / gridDim.x);
   const int n_blk = (o1 - o0 + kRowBlock - 1) / kRowBlock;
   const int64_t n_dn = (int64_t)nU * n_blk;
@@ -192,8 +194,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   if (warp == kProducer) {
     // ------------------------------------------------------ producer
     if (lane == 0) {
+      // Once the ring is full of gate/up stages, ask L2 for all of this CTA's
+      // W_down rows, so that they stream from HBM alongside gate/up instead
+      // of after it -- when the call's W_down fits comfortably in L2.
+      const bool pf = (int64_t)nU * H * (I + pitch_i) <= kL2PrefetchMax;
+      const int64_t pf_at = std::min<int64_t>(n_gu, a.stages);
       int64_t j = 0;
       for (; j < n_all; ++j) {
+        if (pf && j == pf_at)
+          for (int u = 0; u < nU; ++u) {
+            const int64_t row = (int64_t)r.u[u].x * H + o0;
+            prefetch_l2(a.q_d + row * I, (uint32_t)(o1 - o0) * I);
+            prefetch_l2(a.s_d + row * pitch_i, (uint32_t)(o1 - o0) * pitch_i);
+          }
         const int st = (int)(j % a.stages);
         if (j >= a.stages && !mbar_wait(&empty[st], (uint32_t)(((j / a.stages) - 1) & 1))) {
           report_wait(a.meta, kSiteGuEmpty, j, (int)n_all);
@@ -212,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
           bulk_g2s(sb + (size_t)2 * R * H, a.s_gu + rg * pitch_h, sbb, &full[st]);
           bulk_g2s(sb + (size_t)2 * R * H + (size_t)R * pitch_h, a.s_gu + ru * pitch_h, sbb, &full[st]);
         } else {
-          const int64_t jd = j - n_gu;
-          const int e = r.u[jd / n_blk].x, blk = (int)(jd % n_blk);
+          const int64_t jd = j - n_gu;  // block-major: all experts of block 0, then block 1, ...
+          const int e = r.u[jd % nU].x, blk = (int)(jd / nU);
           const int r0 = o0 + blk * kRowBlock, nr = ::min(kRowBlock + 0, o1 - r0);
           const int64_t row = (int64_t)e * H + r0;
           mbar_arrive_expect_tx(&full[st], (uint32_t)nr * (I + pitch_i));
@@ -334,12 +347,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       consumer_sync();
     }
 
-    // ---- phase 3: down + combine. Warp w owns row w of every 16-row block.
+    // ---- phase 3: down + combine. Warp w owns row w of every 16-row block;
+    // per block it visits every touched expert (ascending id, shared last)
+    // keeping per-lane partial sums per token, and reduces across the warp
+    // once, at the end of the block.
     const float* hsrc = a.h_smem ? reinterpret_cast<const float*>(smem) : a.hbuf;
     const int nseg_i = I / 16;
-    float acc[kMaxRowBlocks];
+    float part[kMaxDecodeT];
 #pragma unroll
-    for (int b = 0; b < kMaxRowBlocks; ++b) acc[b] = 0.f;
+    for (int t = 0; t < kMaxDecodeT; ++t) part[t] = 0.f;
     for (int64_t jd = 0; jd < n_dn && ok; ++jd) {
       const int64_t j = n_gu + jd;
       const int st = (int)(j % a.stages);
@@ -348,9 +364,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
         ok = false;
         break;
       }
-      const int4 ui = r.u[jd / n_blk];
-      const int blk = (int)(jd % n_blk);
-      const int nr = ::min(kRowBlock + 0, o1 - (o0 + blk * kRowBlock));
+      const int u = (int)(jd % nU), blk = (int)(jd / nU);
+      const int4 ui = r.u[u];
+      const int r0 = o0 + blk * kRowBlock;
+      const int nr = ::min(kRowBlock + 0, o1 - r0);
       if (warp < nr) {
         const uint8_t* sb = ring + (size_t)st * a.stage_bytes;
         const uint8_t* qrow = sb + (size_t)warp * I;
@@ -368,20 +385,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
             const uint4 qq = *reinterpret_cast<const uint4*>(qrow + seg * 16);
             d = fmaf(half_bits_to_f32(sc[seg >> 1]), dot16(qq, hv), d);
           }
-          d = warp_sum(d);
+          const float g = r.rg[pos];
+          if (T == 1) {
+            part[0] = fmaf(g, d, part[0]);
+          } else {
+            const int t = r.tok[pos];
 #pragma unroll
-          for (int b = 0; b < kMaxRowBlocks; ++b)
-            if (b == blk && lane == r.tok[pos]) acc[b] = fmaf(r.rg[pos], d, acc[b]);
+            for (int tt = 0; tt < kMaxDecodeT; ++tt)
+              if (tt == t) part[tt] = fmaf(g, d, part[tt]);
+          }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
-    }
-    if (ok && lane < T) {
+      if (u == nU - 1) {  // block done: one reduction per token, lane t writes token t
+        if (warp < nr) {
+          float mine = 0.f;
 #pragma unroll
-      for (int b = 0; b < kMaxRowBlocks; ++b) {
-        const int row = o0 + b * kRowBlock + warp;
-        if (b < n_blk && row < o1) a.out[(int64_t)lane * H + row] = __float2bfloat16_rn(acc[b]);
+          for (int tt = 0; tt < kMaxDecodeT; ++tt) {
+            if (tt < T) {
+              const float v = warp_sum(part[tt]);
+              if (lane == tt) mine = v;
+            }
+            part[tt] = 0.f;
+          }
+          if (lane < T) a.out[(int64_t)lane * H + r0 + warp] = __float2bfloat16_rn(mine);
+        }
       }
     }
   }
@@ -430,7 +459,6 @@ cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfl
   const int H = h->cfg.H, I = h->cfg.I, k = h->cfg.k, S = h->S;
   const int rows = T * (k + S);
   const int grid = h->num_sms;
-  if ((H + grid - 1) / grid > kRowBlock * kMaxRowBlocks) return cudaErrorNotSupported;
   DecodeArgs a;
   a.q_gu = reinterpret_cast<const uint8_t*>(h->q_gu);
   a.s_gu = h->s_gu;

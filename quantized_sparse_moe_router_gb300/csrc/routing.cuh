@@ -62,132 +62,15 @@ __device__ __forceinline__ float warp_gate(float my_z, int k, int lane) {
   return ex / sum;
 }
 
-// Compare-exchange of the register pairs (m, m ^ S) of one lane inside a
-// bitonic stage of block size `size` (S < EPL: both elements are in this lane).
-template <int EPL, int S>
-__device__ __forceinline__ void bitonic_local(float (&z)[EPL], int (&id)[EPL], int lane, int size) {
-  if constexpr (S < EPL) {
-#pragma unroll
-    for (int m = 0; m < EPL; ++m) {
-      const int mm = m ^ S;
-      if (mm > m) {
-        const bool up = (((lane * EPL) + m) & size) == 0;
-        const bool m_first = z[m] > z[mm] || (z[m] == z[mm] && id[m] < id[mm]);
-        if (m_first != up) {
-          const float tz = z[m];
-          z[m] = z[mm];
-          z[mm] = tz;
-          const int ti = id[m];
-          id[m] = id[mm];
-          id[mm] = ti;
-        }
-      }
-    }
-  }
-}
-
-// Bitonic sort, within one warp, of 32*EPL (logit, id) pairs into "comes
-// first" order: descending logit, equal logits by ascending id. Lane l holds
-// positions l*EPL .. l*EPL+EPL-1. The stage loops stay rolled: this runs once
-// per CTA, where instruction fetch, not arithmetic, is the cost.
-template <int EPL>
-__device__ __forceinline__ void warp_sort_desc(float (&z)[EPL], int (&id)[EPL], int lane) {
-  constexpr int N = 32 * EPL;
-#pragma unroll 1
-  for (int size = 2; size <= N; size <<= 1) {
-#pragma unroll 1
-    for (int stride = size / 2; stride > 0; stride >>= 1) {
-      if (stride >= EPL) {
-        const int pl = stride / EPL;
-        const bool lower = (lane & pl) == 0;
-#pragma unroll
-        for (int m = 0; m < EPL; ++m) {
-          const float oz = __shfl_xor_sync(0xFFFFFFFFu, z[m], pl);
-          const int oid = __shfl_xor_sync(0xFFFFFFFFu, id[m], pl);
-          const bool up = ((((lane & ~pl) * EPL) + m) & size) == 0;
-          const bool mine_first = z[m] > oz || (z[m] == oz && id[m] < oid);
-          const bool keep = (lower == up) ? mine_first : !mine_first;
-          if (!keep) {
-            z[m] = oz;
-            id[m] = oid;
-          }
-        }
-      } else if (stride == 4) {
-        bitonic_local<EPL, 4>(z, id, lane, size);
-      } else if (stride == 2) {
-        bitonic_local<EPL, 2>(z, id, lane, size);
-      } else {
-        bitonic_local<EPL, 1>(z, id, lane, size);
-      }
-    }
-  }
-}
-
-// One warp: the top-k of logits z[0..E) (E <= 32*EPL), ties to the lower id,
-// in descending order; lane j < k ends with (id_j, gate_j).
-template <int EPL>
-__device__ __forceinline__ void warp_select_sorted(const float* zrow, int E, int k, int lane, int* out_id,
-                                                   float* out_gate) {
-  float z[EPL];
-  int id[EPL];
-#pragma unroll
-  for (int m = 0; m < EPL; ++m) {
-    const int e = lane * EPL + m;
-    z[m] = e < E ? __ldcg(zrow + e) : -INFINITY;
-    id[m] = e < E ? e : 0x40000000 + e;  // padding sorts last
-  }
-  warp_sort_desc<EPL>(z, id, lane);
-  int my_id = -1;
-  float my_z = -INFINITY;
-#pragma unroll
-  for (int m = 0; m < EPL; ++m) {
-    const float vz = __shfl_sync(0xFFFFFFFFu, z[m], lane / EPL);
-    const int vi = __shfl_sync(0xFFFFFFFFu, id[m], lane / EPL);
-    if (lane % EPL == m) {
-      my_z = vz;
-      my_id = vi;
-    }
-  }
-  *out_id = my_id;
-  *out_gate = warp_gate(my_z, k, lane);
-}
-
-__device__ __forceinline__ void warp_select_any(const float* zrow, int E, int k, int lane, int* id, float* g) {
-  if (E <= 128)
-    warp_select_sorted<4>(zrow, E, k, lane, id, g);
-  else
-    warp_select_sorted<8>(zrow, E, k, lane, id, g);
-}
-
-// One warp: exclusive scan of n <= 32*9 ints in place; returns the total.
-__device__ __forceinline__ int warp_exclusive_scan(int* v, int n, int lane) {
-  const int per = (n + 31) / 32;
-  const int b = lane * per, e = min(n, b + per);
-  int s = 0;
-  for (int i = b; i < e; ++i) s += v[i];
-  int incl = s;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int t = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-    if (lane >= o) incl += t;
-  }
-  int run = incl - s;
-  for (int i = b; i < e; ++i) {
-    const int c = v[i];
-    v[i] = run;
-    run += c;
-  }
-  return __shfl_sync(0xFFFFFFFFu, incl, 31);
-}
-
 // The routing of a decode batch in shared memory.
 struct SmemRouting {
+  float z[kMaxDecodeT * kMaxE];  // the batch's logits
+  float zsel[kMaxDecodeT * kMaxK];  // selected logits, in rank order
   int ids[kMaxDecodeT * kMaxK];
   float gates[kMaxDecodeT * kMaxK];
   int cnt[kMaxE + 2];     // per-expert counts (cnt[E] = T for the shared expert)
   int off[kMaxE + 2];     // exclusive offsets (off[EU] = rows)
-  uint32_t mask[kMaxE + 1];
-  int nz[kMaxE + 2];      // nonzero flags, then their exclusive scan
+  uint32_t mask[kMaxE + 1];  // per expert: bit t set when token t selected it
   int4 u[kMaxE + 1];      // (expert, first row, rows, 0) of experts with rows, ascending
   int tok[kMaxRowsDecode];
   float rg[kMaxRowsDecode];
@@ -196,29 +79,62 @@ struct SmemRouting {
   int rows;
 };
 
-// Whole block (NT threads, at least min(T, NT/32) warps): selection for T <= 16
-// tokens from logits [T][E] (global, written by an earlier kernel; one warp per
-// token, bitonic top-k), gates, and the grouping. Four block barriers; ends
-// with one, after which every field is valid.
+// Whole block (NT threads): selection for T <= 16 tokens from logits [T][E]
+// (global, written by an earlier kernel), gates, and the grouping. Selection
+// is by rank: every (token, expert) pair counts the logits that come before
+// it (larger, or equal with a lower id), split over a group of s lanes; ranks
+// below k are the top-k in order. Each step is short and latency-bound (a few
+// hundred cycles): four block barriers, the last of which leaves every field
+// valid.
 template <int NT>
 __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, SmemRouting& r) {
+  static_assert(NT % 32 == 0, "whole warps");
   constexpr int NW = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int EU = E + S;
-  for (int t = warp; t < T; t += NW) {
-    int id;
-    float g;
-    warp_select_any(logits + t * E, E, k, lane, &id, &g);
-    if (lane < k) {
-      r.ids[t * k + lane] = id;
-      r.gates[t * k + lane] = g;
-    }
-  }
-  for (int i = tid; i < EU + 1; i += NT) {
+  for (int i = tid; i < T * E; i += NT) r.z[i] = __ldcg(logits + i);
+  for (int i = tid; i < EU; i += NT) {
     r.cnt[i] = 0;
-    if (i < EU) r.mask[i] = 0;
+    r.mask[i] = 0;
   }
   __syncthreads();
+
+  // ranks: s lanes per pair (s a power of two, as many as the block allows);
+  // lane c of a group compares f = c, c + s, ... (same-c lanes read the same
+  // word, distinct c consecutive words: no bank conflicts)
+  const int P = T * E;
+  int s = 32;
+  while (s > 1 && P * s > NT) s >>= 1;
+  const int gpw = 32 / s, c = lane & (s - 1);
+  for (int b = warp * gpw; b < P; b += NW * gpw) {  // warp-uniform trip count
+    const int p = b + lane / s;
+    int rank = 0, t = 0, e = 0;
+    float z = 0.f;
+    if (p < P) {
+      t = p / E;
+      e = p - t * E;
+      const float* zt = r.z + t * E;
+      z = zt[e];
+#pragma unroll 4
+      for (int f = c; f < E; f += s) {
+        const float zf = zt[f];
+        rank += (zf > z) | ((zf == z) & (f < e));
+      }
+    }
+    for (int o = 1; o < s; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+    if (p < P && c == 0 && rank < k) {
+      r.ids[t * k + rank] = e;
+      r.zsel[t * k + rank] = z;
+    }
+  }
+  __syncthreads();
+
+  // gates (one warp per token) and per-expert counts / token masks
+  for (int t = warp; t < T; t += NW) {
+    const float zj = lane < k ? r.zsel[t * k + lane] : 0.f;
+    const float g = warp_gate(zj, k, lane);
+    if (lane < k) r.gates[t * k + lane] = g;
+  }
   for (int p = tid; p < T * k; p += NT) {
     const int ee = r.ids[p];
     atomicAdd(&r.cnt[ee], 1);
@@ -226,24 +142,50 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
   }
   if (S && tid == 0) r.cnt[E] = T;
   __syncthreads();
+
+  // one warp: offsets and the table of touched experts. Lane l owns the
+  // consecutive experts [l * per, l * per + per), held in registers; both
+  // scans (rows and touched experts) in one pass of shuffles.
   if (warp == 0) {
-    for (int i = lane; i < EU + 1; i += 32) {
-      r.off[i] = i < EU ? r.cnt[i] : 0;
-      r.nz[i] = i < EU ? (r.cnt[i] > 0) : 0;
+    constexpr int kPer = (kMaxE + 1 + 31) / 32;
+    const int per = (EU + 31) / 32, b0 = lane * per;
+    int cn[kPer];
+    int sc = 0, sn = 0;
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      const int i = b0 + m;
+      cn[m] = (m < per && i < EU) ? r.cnt[i] : 0;
+      sc += cn[m];
+      sn += cn[m] > 0;
     }
-    __syncwarp();
-    const int rows = warp_exclusive_scan(r.off, EU + 1, lane);
-    __syncwarp();
-    const int n_unique = warp_exclusive_scan(r.nz, EU, lane);
-    __syncwarp();
-    for (int i = lane; i < EU; i += 32)
-      if (r.cnt[i] > 0) r.u[r.nz[i]] = make_int4(i, r.off[i], r.cnt[i], 0);
-    if (lane == 0) {
-      r.n_unique = n_unique;
-      r.rows = rows;
+    int ic = sc, in = sn;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int uc = __shfl_up_sync(0xFFFFFFFFu, ic, o), un = __shfl_up_sync(0xFFFFFFFFu, in, o);
+      if (lane >= o) {
+        ic += uc;
+        in += un;
+      }
+    }
+    int rc = ic - sc, rn = in - sn;
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      const int i = b0 + m;
+      if (m < per && i < EU) {
+        r.off[i] = rc;
+        if (cn[m] > 0) r.u[rn++] = make_int4(i, rc, cn[m], 0);
+        rc += cn[m];
+      }
+    }
+    if (lane == 31) {
+      r.off[EU] = ic;
+      r.rows = ic;
+      r.n_unique = in;
     }
   }
   __syncthreads();
+
+  // grouped positions: within an expert, ascending token
   for (int p = tid; p < T * k; p += NT) {
     const int t = p / k, ee = r.ids[p];
     const int pos = r.off[ee] + __popc(r.mask[ee] & ((1u << t) - 1u));
