@@ -66,7 +66,7 @@ struct Allocator {
 };
 
 void free_handle_memory(Handle* h) {
-  void* ptrs[] = {h->q_gu, h->s_gu, h->st_gu, h->q_d, h->s_d, h->st_d, h->wr, h->bias, h->ids, h->gates,
+  void* ptrs[] = {h->q_gu, h->st_gu, h->q_d, h->st_d, h->wr, h->bias, h->ids, h->gates,
                   h->logits, h->counts, h->offsets, h->perm, h->inv, h->row_token, h->row_gate, h->uinfo,
                   h->hist, h->minfo, h->xperm, h->hbuf, h->yp, h->meta, h->x_dev, h->out_dev, h->ids_dev};
   for (void* p : ptrs)
@@ -150,11 +150,9 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
     void** p;
     size_t bytes;
   } req[] = {
-      {(void**)&h->q_gu, (size_t)(EU * 2 * I * H)},
-      {(void**)&h->s_gu, (size_t)(EU * 2 * I * scale_pitch_bytes(H))},
+      {(void**)&h->q_gu, (size_t)(EU * 2 * I * row_bytes(H))},
       {(void**)&h->st_gu, (size_t)(EU * (H / 32) * 2 * I * 2)},
-      {(void**)&h->q_d, (size_t)(EU * H * I)},
-      {(void**)&h->s_d, (size_t)(EU * H * scale_pitch_bytes(I))},
+      {(void**)&h->q_d, (size_t)(EU * H * row_bytes(I))},
       {(void**)&h->st_d, (size_t)(EU * (I / 32) * H * 2)},
       {(void**)&h->wr, (size_t)(E * H * 4)},
       {(void**)&h->bias, (size_t)(E * 4)},
@@ -193,9 +191,9 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
     e = w->router_bias ? cudaMemcpyAsync(h->bias, w->router_bias, E * 4, cudaMemcpyDeviceToDevice, s)
                        : cudaMemsetAsync(h->bias, 0, E * 4, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(h->meta, 0, sizeof(Meta), s);
-  // pad bytes of the scale planes are never read, but keep them defined
-  if (e == cudaSuccess) e = cudaMemsetAsync(h->s_gu, 0, EU * 2 * I * scale_pitch_bytes(H), s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(h->s_d, 0, EU * H * scale_pitch_bytes(I), s);
+  // the scale pads of the code planes are never used, but keep them defined
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->q_gu, 0, EU * 2 * I * row_bytes(H), s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(h->q_d, 0, EU * H * row_bytes(I), s);
   if (e == cudaSuccess) e = launch_repack(h, 0, 0, (int)E, w->w_gate, s);
   if (e == cudaSuccess) e = launch_repack(h, 1, 0, (int)E, w->w_up, s);
   if (e == cudaSuccess) e = launch_repack(h, 2, 0, (int)E, w->w_down, s);

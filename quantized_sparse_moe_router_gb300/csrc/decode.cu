@@ -43,10 +43,8 @@ constexpr int64_t kL2PrefetchMax = 40ll << 20;  // W_down bytes per call prefetc
 enum XMode { kXGlobal = 0, kXSmemF32 = 1, kXSmemBf16 = 2 };
 
 struct DecodeArgs {
-  const uint8_t* q_gu;   // codes + 128
-  const uint8_t* s_gu;   // row-major binary16 scales, padded rows
-  const uint8_t* q_d;
-  const uint8_t* s_d;
+  const uint8_t* q_gu;   // rows of row_bytes(H): codes + 128, then binary16 scales
+  const uint8_t* q_d;    // rows of row_bytes(I)
   const __nv_bfloat16* x;
   const float* logits;
   float* hbuf;           // [rows][I] fp32
@@ -55,7 +53,7 @@ struct DecodeArgs {
   Meta* meta;
   int H, I, E, k, S, T;
   int publish;
-  int R;                 // gate/up units per stage (divides 64)
+  int R;                 // gate/up units per stage (a multiple of kGUGroup dividing 32)
   uint32_t stage_bytes;  // ring slot size (max of a gate/up and a down stage)
   int stages;
   int x_mode;
@@ -166,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   __shared__ SmemRouting r;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = a.H, I = a.I, T = a.T, R = a.R;
-  const uint32_t pitch_h = (uint32_t)scale_pitch_bytes(H), pitch_i = (uint32_t)scale_pitch_bytes(I);
+  const uint32_t rb_h = (uint32_t)row_bytes(H), rb_i = (uint32_t)row_bytes(I);
   uint8_t* ring = smem + align128(a.act_bytes);
   if (tid == 0) {
     for (int s = 0; s < a.stages; ++s) {
@@ -181,8 +179,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
 
   const int nU = r.n_unique;
   // gate/up stages: units [lo, hi) of the nU x I unit space, R consecutive per stage
-  const int64_t n_units = (int64_t)nU * I;
-  const int64_t lo = n_units * blockIdx.x / gridDim.x, hi = n_units * (blockIdx.x + 1) / gridDim.x;
+  // (a CTA's range starts and ends on a kGUGroup boundary: every stage is
+  // then one run of consecutive interleaved rows, fetched with one copy)
+  const int64_t n_grp = (int64_t)nU * I / kGUGroup;
+  const int64_t lo = n_grp * blockIdx.x / gridDim.x * kGUGroup, hi = n_grp * (blockIdx.x + 1) / gridDim.x * kGUGroup;
   const int64_t b0 = lo / R;
   const int64_t n_gu = hi > lo ? (hi + R - 1) / R - b0 : 0;
   // down stages: output rows [o0, o1), blocks of 16 rows; per block every touched expert
@@ -197,15 +197,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       // Once the ring is full of gate/up stages, ask L2 for all of this CTA's
       // W_down rows, so that they stream from HBM alongside gate/up instead
       // of after it -- when the call's W_down fits comfortably in L2.
-      const bool pf = (int64_t)nU * H * (I + pitch_i) <= kL2PrefetchMax;
+      const bool pf = (int64_t)nU * H * rb_i <= kL2PrefetchMax;
       const int64_t pf_at = std::min<int64_t>(n_gu, a.stages);
       int64_t j = 0;
       for (; j < n_all; ++j) {
         if (pf && j == pf_at)
           for (int u = 0; u < nU; ++u) {
             const int64_t row = (int64_t)r.u[u].x * H + o0;
-            prefetch_l2(a.q_d + row * I, (uint32_t)(o1 - o0) * I);
-            prefetch_l2(a.s_d + row * pitch_i, (uint32_t)(o1 - o0) * pitch_i);
+            prefetch_l2(a.q_d + row * rb_i, (uint32_t)(o1 - o0) * rb_i);
           }
         const int st = (int)(j % a.stages);
         if (j >= a.stages && !mbar_wait(&empty[st], (uint32_t)(((j / a.stages) - 1) & 1))) {
@@ -215,23 +214,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
         uint8_t* sb = ring + (size_t)st * a.stage_bytes;
         if (j < n_gu) {
           const int64_t u0 = std::max<int64_t>(lo, (b0 + j) * R), u1 = std::min<int64_t>(hi, (b0 + j + 1) * R);
-          const int n = (int)(u1 - u0);
           const int e = r.u[u0 / I].x, i0 = (int)(u0 % I);
-          const int64_t rg = (int64_t)e * 2 * I + gu_row_gate(i0), ru = (int64_t)e * 2 * I + gu_row_up(i0);
-          const uint32_t qb = (uint32_t)n * H, sbb = (uint32_t)n * pitch_h;
-          mbar_arrive_expect_tx(&full[st], 2 * qb + 2 * sbb);
-          bulk_g2s(sb, a.q_gu + rg * H, qb, &full[st]);
-          bulk_g2s(sb + (size_t)R * H, a.q_gu + ru * H, qb, &full[st]);
-          bulk_g2s(sb + (size_t)2 * R * H, a.s_gu + rg * pitch_h, sbb, &full[st]);
-          bulk_g2s(sb + (size_t)2 * R * H + (size_t)R * pitch_h, a.s_gu + ru * pitch_h, sbb, &full[st]);
+          const uint32_t bytes = (uint32_t)(u1 - u0) * 2 * rb_h;
+          mbar_arrive_expect_tx(&full[st], bytes);
+          bulk_g2s(sb, a.q_gu + ((int64_t)e * 2 * I + 2 * i0) * rb_h, bytes, &full[st]);
         } else {
           const int64_t jd = j - n_gu;  // block-major: all experts of block 0, then block 1, ...
           const int e = r.u[jd % nU].x, blk = (int)(jd / nU);
           const int r0 = o0 + blk * kRowBlock, nr = ::min(kRowBlock + 0, o1 - r0);
           const int64_t row = (int64_t)e * H + r0;
-          mbar_arrive_expect_tx(&full[st], (uint32_t)nr * (I + pitch_i));
-          bulk_g2s(sb, a.q_d + row * I, (uint32_t)nr * I, &full[st]);
-          bulk_g2s(sb + (size_t)kRowBlock * I, a.s_d + row * pitch_i, (uint32_t)nr * pitch_i, &full[st]);
+          mbar_arrive_expect_tx(&full[st], (uint32_t)nr * rb_i);
+          bulk_g2s(sb, a.q_d + row * rb_i, (uint32_t)nr * rb_i, &full[st]);
         }
       }
       // every copy issued has landed before the CTA may leave
@@ -280,12 +273,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       const int64_t u0 = std::max<int64_t>(lo, (b0 + j) * R), u1 = std::min<int64_t>(hi, (b0 + j + 1) * R);
       const uint8_t* sb = ring + (size_t)st * a.stage_bytes;
       for (int64_t g = u0 + ((warp - (u0 - lo)) % kCW + kCW) % kCW; g < u1; g += kCW) {
-        const size_t off = (size_t)(g - u0);
-        const uint8_t* qg_row = sb + off * H;
-        const uint8_t* qu_row = sb + (size_t)R * H + off * H;
-        const uint16_t* sg = reinterpret_cast<const uint16_t*>(sb + (size_t)2 * R * H + off * pitch_h);
-        const uint16_t* su =
-            reinterpret_cast<const uint16_t*>(sb + (size_t)2 * R * H + (size_t)R * pitch_h + off * pitch_h);
+        // the stage holds rows 2 i0 .. 2 i1 of the expert: per group, kGUGroup
+        // gate rows then their up rows; u0 is group-aligned
+        const int off = (int)(g - u0);
+        const uint8_t* qg_row = sb + (size_t)((off / kGUGroup) * 2 * kGUGroup + off % kGUGroup) * rb_h;
+        const uint8_t* qu_row = qg_row + (size_t)kGUGroup * rb_h;
+        const uint16_t* sg = reinterpret_cast<const uint16_t*>(qg_row + H);
+        const uint16_t* su = reinterpret_cast<const uint16_t*>(qu_row + H);
         const int4 ui = r.u[g / I];
         const int i = (int)(g % I);
         for (int rr = 0; rr < ui.z; ++rr) {
@@ -370,8 +364,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       const int nr = ::min(kRowBlock + 0, o1 - r0);
       if (warp < nr) {
         const uint8_t* sb = ring + (size_t)st * a.stage_bytes;
-        const uint8_t* qrow = sb + (size_t)warp * I;
-        const uint16_t* sc = reinterpret_cast<const uint16_t*>(sb + (size_t)kRowBlock * I + (size_t)warp * pitch_i);
+        const uint8_t* qrow = sb + (size_t)warp * rb_i;
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(qrow + I);
         for (int m = 0; m < ui.z; ++m) {
           const int pos = ui.y + m;
           const float* hrow = hsrc + (size_t)pos * I;
@@ -437,7 +431,7 @@ cudaError_t launch(const DecodeArgs& a, unsigned grid, size_t smem, cudaStream_t
 
 int g_smem_optin = 0;
 constexpr uint32_t kActMax = 80 * 1024;     // x or h in shared memory up to this size
-constexpr uint32_t kStageTarget = 24 * 1024;
+constexpr uint32_t kStageTarget = 36 * 1024;  // one bulk copy per stage: fewer, larger copies stream faster
 
 }  // namespace
 
@@ -460,10 +454,8 @@ cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfl
   const int rows = T * (k + S);
   const int grid = h->num_sms;
   DecodeArgs a;
-  a.q_gu = reinterpret_cast<const uint8_t*>(h->q_gu);
-  a.s_gu = h->s_gu;
-  a.q_d = reinterpret_cast<const uint8_t*>(h->q_d);
-  a.s_d = h->s_d;
+  a.q_gu = h->q_gu;
+  a.q_d = h->q_d;
   a.x = x;
   a.logits = h->logits;
   a.hbuf = static_cast<float*>(h->hbuf);
@@ -483,11 +475,11 @@ cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfl
   a.h_smem = hb <= kActMax;
   const uint32_t xb = a.x_mode == kXSmemF32 ? x32 : (a.x_mode == kXSmemBf16 ? x16 : 0);
   a.act_bytes = std::max(xb, a.h_smem ? hb : 0u);
-  const uint32_t unit = (uint32_t)(2 * H + 2 * scale_pitch_bytes(H));
-  int R = 8;
-  while (R > 1 && (uint32_t)R * unit > kStageTarget) R /= 2;
+  const uint32_t unit = (uint32_t)(2 * row_bytes(H));
+  int R = 32;
+  while (R > kGUGroup && (uint32_t)R * unit > kStageTarget) R /= 2;
   a.R = R;
-  const uint32_t dn_stage = (uint32_t)(kRowBlock * (I + scale_pitch_bytes(I)));
+  const uint32_t dn_stage = (uint32_t)(kRowBlock * row_bytes(I));
   a.stage_bytes = std::max((uint32_t)R * unit, dn_stage);
   const int64_t ring_bytes = (int64_t)g_smem_optin - align128(a.act_bytes) - 256;
   a.stages = (int)std::min<int64_t>(kMaxStages, ring_bytes / a.stage_bytes);

@@ -17,7 +17,7 @@ constexpr uint32_t kHandleMagic = 0x4D6F4531u;  // "1EoM"
 constexpr uint32_t kHandleFreed = 0xDEADF00Du;
 constexpr int kQBlock = 32;        // Q8_0 block length
 constexpr int kQBlockBytes = 34;   // fp16 scale + 32 int8
-constexpr int kGUGroup = 64;       // gate/up rows are interleaved in groups of 64
+constexpr int kGUGroup = 2;        // gate/up rows are interleaved in groups of 2
 constexpr int kMaxK = 16;          // experts per token
 constexpr int kMaxDecodeT = 16;    // decode path token limit (one lane per token in the combine)
 constexpr int kRouteTileM = 32;    // tokens per CTA in the tiled router
@@ -26,12 +26,17 @@ constexpr int kRouteTileM = 32;    // tokens per CTA in the tiled router
 constexpr int kStatusTimeout = 1;
 constexpr int kStatusBadIndex = 2;
 
-// Scale rows are padded to a multiple of 16 bytes so each row can be fetched
-// with one bulk copy.
+// Scale rows are padded to a multiple of 16 bytes.
 __host__ __device__ inline int64_t scale_pitch_bytes(int64_t K) { return ((K / kQBlock) * 2 + 15) / 16 * 16; }
 
-// Row of gate/up matrix row i in the interleaved [2I, H] code plane:
-// groups of 64 gate rows followed by the 64 up rows of the same i range.
+// One row of a code plane: its K codes (offset binary), then its K/32 binary16
+// scales padded to 16 bytes, so that any run of consecutive rows -- codes and
+// scales -- is one contiguous, 16-byte aligned range.
+__host__ __device__ inline int64_t row_bytes(int64_t K) { return K + scale_pitch_bytes(K); }
+
+// Row of gate/up matrix row i in the interleaved [2I] plane: groups of
+// kGUGroup gate rows followed by the up rows of the same i, so the units
+// i0..i1 (kGUGroup-aligned) are the consecutive rows 2 i0 .. 2 i1.
 __host__ __device__ inline int64_t gu_row_gate(int64_t i) { return (i / kGUGroup) * 2 * kGUGroup + (i % kGUGroup); }
 __host__ __device__ inline int64_t gu_row_up(int64_t i) { return gu_row_gate(i) + kGUGroup; }
 
@@ -59,9 +64,9 @@ struct Timing {
 struct PrefillMaps {
   CUtensorMap a_x;    // xperm [rows_max][H] bf16, box 64 x 128, 128B swizzle
   CUtensorMap a_h;    // hbuf  [rows_max][I] bf16, box 64 x 128, 128B swizzle
-  CUtensorMap q_gu;   // code plane [EU*2I][H] u8, box 64 x 256
+  CUtensorMap q_gu;   // code plane [EU*2I][H] u8 (row stride row_bytes(H)), box 64 x 256
   CUtensorMap s_gu;   // scale plane [EU*H/32][2I] u16, box 256 x 2
-  CUtensorMap q_d;    // [EU*H][I] u8
+  CUtensorMap q_d;    // [EU*H][I] u8 (row stride row_bytes(I))
   CUtensorMap s_d;    // [EU*I/32][H] u16
 };
 
@@ -75,11 +80,10 @@ struct Handle {
   int num_sms;
   int last_T;         // T of the last fw_moe_route, -1 before any
   // ---- repacked weights (device)
-  int8_t* q_gu;       // [EU][2I][H] codes + 128 (offset binary), gate/up interleaved per 64-row group
-  uint8_t* s_gu;      // [EU][2I][pitch(H)] binary16 scales, row-major (padded rows)
-  uint16_t* st_gu;    // [EU][H/32][2I] binary16 scales, transposed
-  int8_t* q_d;        // [EU][H][I] codes + 128
-  uint8_t* s_d;       // [EU][H][pitch(I)]
+  uint8_t* q_gu;      // [EU][2I] rows of row_bytes(H): codes + 128 (offset binary), then scales;
+                      // gate/up interleaved per kGUGroup rows
+  uint16_t* st_gu;    // [EU][H/32][2I] binary16 scales, transposed (prefill)
+  uint8_t* q_d;       // [EU][H] rows of row_bytes(I)
   uint16_t* st_d;     // [EU][I/32][H]
   float* wr;          // [E][H]
   float* bias;        // [E] (zeros when none)

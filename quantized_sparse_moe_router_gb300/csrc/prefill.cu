@@ -291,27 +291,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = m < mi.z;
       const int64_t row = (int64_t)mi.y + m;
       if (EPI == kEpiSwiGLU) {
-        // columns of the 256-row weight tile: [64 gate][64 up][64 gate][64 up]
+        // columns of the 256-row weight tile: groups of kGUGroup gate rows,
+        // then the up rows of the same i; 32 columns give 16 consecutive i
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          float v[32];
+          tmem_ld32(taddr + c0, v);
+          const int i0 = (n0 + c0) / 2;
+          if (valid && i0 < a.out_cols) {
+            uint32_t hw[8];
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-#pragma unroll
-          for (int c0 = 0; c0 < 64; c0 += 32) {
-            float g[32], u[32];
-            tmem_ld32(taddr + half * 128 + c0, g);
-            tmem_ld32(taddr + half * 128 + 64 + c0, u);
-            const int i0 = n0 / 2 + half * 64 + c0;
-            if (valid && i0 < a.out_cols) {
-              uint4* dst = reinterpret_cast<uint4*>(a.outp + row * a.out_cols + i0);
-#pragma unroll
-              for (int q = 0; q < 4; ++q) {
-                uint4 v;
-                v.x = pack_bf16x2(silu(g[8 * q + 0]) * u[8 * q + 0], silu(g[8 * q + 1]) * u[8 * q + 1]);
-                v.y = pack_bf16x2(silu(g[8 * q + 2]) * u[8 * q + 2], silu(g[8 * q + 3]) * u[8 * q + 3]);
-                v.z = pack_bf16x2(silu(g[8 * q + 4]) * u[8 * q + 4], silu(g[8 * q + 5]) * u[8 * q + 5]);
-                v.w = pack_bf16x2(silu(g[8 * q + 6]) * u[8 * q + 6], silu(g[8 * q + 7]) * u[8 * q + 7]);
-                dst[q] = v;
-              }
+            for (int j = 0; j < 16; j += 2) {
+              const int q0 = (j / kGUGroup) * 2 * kGUGroup + j % kGUGroup;
+              const int q1 = ((j + 1) / kGUGroup) * 2 * kGUGroup + (j + 1) % kGUGroup;
+              hw[j / 2] = pack_bf16x2(silu(v[q0]) * v[q0 + kGUGroup], silu(v[q1]) * v[q1 + kGUGroup]);
             }
+            uint4* dst = reinterpret_cast<uint4*>(a.outp + row * a.out_cols + i0);
+            dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+            dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
           }
         }
       } else {
@@ -441,13 +438,13 @@ cudaError_t prepare_prefill(Handle* h) {
     e = encode_2d(&m->a_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->hbuf, I, R, I * 2, BK, BM,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
   if (e == cudaSuccess)
-    e = encode_2d(&m->q_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->q_gu, H, EU * 2 * I, H, BK, BN,
+    e = encode_2d(&m->q_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->q_gu, H, EU * 2 * I, row_bytes(H), BK, BN,
                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (e == cudaSuccess)
     e = encode_2d(&m->s_gu, CU_TENSOR_MAP_DATA_TYPE_UINT16, h->st_gu, 2 * I, EU * (H / 32), 2 * I * 2, BN, 2,
                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (e == cudaSuccess)
-    e = encode_2d(&m->q_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->q_d, I, EU * H, I, BK, BN, CU_TENSOR_MAP_SWIZZLE_NONE,
+    e = encode_2d(&m->q_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->q_d, I, EU * H, row_bytes(I), BK, BN, CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (e == cudaSuccess)
     e = encode_2d(&m->s_d, CU_TENSOR_MAP_DATA_TYPE_UINT16, h->st_d, H, EU * (I / 32), H * 2, BN, 2,

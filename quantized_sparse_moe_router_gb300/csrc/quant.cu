@@ -52,8 +52,7 @@ __global__ void quantize_q8_0_kernel(const float* __restrict__ w, int64_t nblock
 }
 
 struct PlaneView {
-  int8_t* q;       // code plane of this matrix kind, expert 0
-  uint8_t* s;      // row-major scale plane (padded rows)
+  uint8_t* q;      // code plane of this matrix kind, expert 0 (rows: codes, then scales)
   uint16_t* st;    // transposed scale plane
   int64_t rows;    // rows of one expert's matrix (I for gate/up, H for down)
   int64_t prows;   // rows of one expert in the plane (2I for gate/up, H for down)
@@ -81,10 +80,11 @@ __global__ void repack_kernel(PlaneView p, int expert0, int64_t nblocks, const u
 #pragma unroll
   for (int i = 0; i < 8; ++i) words[i] = ((uint32_t)in[1 + 2 * i] | ((uint32_t)in[2 + 2 * i] << 16)) ^ 0x80808080u;
   const int64_t prow = e * p.prows + plane_row(p, r);
-  uint4* qd = reinterpret_cast<uint4*>(p.q + prow * p.K + b * kQBlock);
+  uint8_t* row = p.q + prow * row_bytes(p.K);
+  uint4* qd = reinterpret_cast<uint4*>(row + b * kQBlock);
   qd[0] = make_uint4(words[0], words[1], words[2], words[3]);
   qd[1] = make_uint4(words[4], words[5], words[6], words[7]);
-  reinterpret_cast<uint16_t*>(p.s + prow * scale_pitch_bytes(p.K))[b] = in[0];
+  reinterpret_cast<uint16_t*>(row + p.K)[b] = in[0];
   p.st[(e * nb + b) * p.prows + plane_row(p, r)] = in[0];
 }
 
@@ -94,13 +94,14 @@ __global__ void export_kernel(PlaneView p, int expert, int64_t nblocks, uint8_t*
   const int64_t nb = p.K / kQBlock;
   const int64_t r = blk / nb, b = blk % nb;
   const int64_t prow = (int64_t)expert * p.prows + plane_row(p, r);
-  const uint4* qs = reinterpret_cast<const uint4*>(p.q + prow * p.K + b * kQBlock);
+  const uint8_t* row = p.q + prow * row_bytes(p.K);
+  const uint4* qs = reinterpret_cast<const uint4*>(row + b * kQBlock);
   uint4 a = qs[0], c = qs[1];
   uint32_t words[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
 #pragma unroll
   for (int i = 0; i < 8; ++i) words[i] ^= 0x80808080u;  // back from offset binary
   uint16_t* out = reinterpret_cast<uint16_t*>(dst + blk * kQBlockBytes);
-  out[0] = reinterpret_cast<const uint16_t*>(p.s + prow * scale_pitch_bytes(p.K))[b];
+  out[0] = reinterpret_cast<const uint16_t*>(row + p.K)[b];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     out[1 + 2 * i] = (uint16_t)(words[i] & 0xFFFF);
@@ -114,14 +115,12 @@ PlaneView view_of(const Handle* h, int which) {
   p.which = which;
   if (which == 2) {
     p.q = h->q_d;
-    p.s = h->s_d;
     p.st = h->st_d;
     p.rows = H;
     p.prows = H;
     p.K = I;
   } else {
     p.q = h->q_gu;
-    p.s = h->s_gu;
     p.st = h->st_gu;
     p.rows = I;
     p.prows = 2 * I;

@@ -117,71 +117,90 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
 
 // ------------------------------------------------------ prefill router
 // Tiled fp32 router: each CTA owns 32 tokens and all E (<= 256) experts; the
-// K loop stages 32-wide slices of x and Wr in shared memory; every thread keeps
-// 4 tokens x ceil(E/32) experts of accumulators. Then one warp per 4 tokens
-// selects, and the CTA writes its per-expert counts.
+// 32 tokens x all experts per CTA (256 threads: warp w owns tokens 4w..4w+3,
+// lane l experts l + 32m). The K loop runs over 32-wide slices of x (bf16 ->
+// fp32) and Wr, double-buffered in shared memory: the next slice's global
+// loads are in registers while the current one is multiplied, so one barrier
+// per slice. Rows are padded to 36 floats, which makes each lane's 128-bit
+// read of its expert row conflict-free; the token reads are broadcasts. Then
+// one warp per 4 tokens selects, and the CTA writes its per-expert counts.
 constexpr int kKC = 32;
+constexpr int kKP = kKC + 4;  // padded row (floats)
 
 template <int EM>
 __global__ void __launch_bounds__(256) route_tiles_kernel(RouteArgs a, int32_t* hist) {
-  extern __shared__ float smem[];
-  float* xs = smem;                       // [32][kKC + 1]
-  float* ws = xs + kRouteTileM * (kKC + 1);  // [EM*32][kKC + 1], later z [32][EM*32 + 1]
+  extern __shared__ __align__(16) float smem[];
+  float* xs = smem;                             // [2][32][kKP]
+  float* ws = xs + 2 * kRouteTileM * kKP;       // [2][EM*32][kKP]; later z [32][EM*32 + 1]
   __shared__ int s_cnt[kMaxE];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int ty = tid >> 5, tx = tid & 31;
+  const int ty = warp, tx = lane;
   const int T = a.T, H = a.H, E = a.E, k = a.k;
   const int t0 = blockIdx.x * kRouteTileM;
+  constexpr int kWPer = EM * 32 * (kKC / 4) / 256;  // float4 of the Wr slice per thread (= EM)
   float acc[4][EM];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
 #pragma unroll
     for (int m = 0; m < EM; ++m) acc[i][m] = 0.0f;
 
-  for (int h0 = 0; h0 < H; h0 += kKC) {
-    // x slice: 32 tokens x 32 values, 4 per thread (bf16 -> f32)
-    {
-      int r = tid >> 3, c = (tid & 7) * 4;
-      int t = t0 + r;
-      float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
-      if (t < T) {
-        uint2 xv = __ldg(reinterpret_cast<const uint2*>(a.x + (int64_t)t * H + h0 + c));
-        bf16x2_to_f32(xv.x, v0, v1);
-        bf16x2_to_f32(xv.y, v2, v3);
-      }
-      float* d = xs + r * (kKC + 1) + c;
-      d[0] = v0;
-      d[1] = v1;
-      d[2] = v2;
-      d[3] = v3;
-    }
-    // Wr slice: EM*32 rows x 32 values
-    for (int idx = tid; idx < EM * 32 * (kKC / 4); idx += 256) {
-      int r = idx / (kKC / 4), c = (idx % (kKC / 4)) * 4;
-      float4 w = r < E ? __ldg(reinterpret_cast<const float4*>(a.wr + (int64_t)r * H + h0 + c))
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
-      float* d = ws + r * (kKC + 1) + c;
-      d[0] = w.x;
-      d[1] = w.y;
-      d[2] = w.z;
-      d[3] = w.w;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int kk = 0; kk < kKC; ++kk) {
-      float xv[4], wv[EM];
+  // this thread's share of a slice: x row xr, columns xc..xc+3; Wr rows wr_q
+  const int xr = tid >> 3, xc = (tid & 7) * 4;
+  const bool xok = t0 + xr < T;
+  const __nv_bfloat16* xsrc = a.x + (int64_t)(t0 + xr) * H + xc;
+  uint2 xreg;
+  float4 wreg[kWPer];
+  auto load = [&](int h0) {
+    xreg = xok ? __ldg(reinterpret_cast<const uint2*>(xsrc + h0)) : make_uint2(0u, 0u);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) xv[i] = xs[(ty * 4 + i) * (kKC + 1) + kk];
+    for (int q = 0; q < kWPer; ++q) {
+      const int idx = tid + 256 * q, r = idx >> 3, c = (idx & 7) * 4;
+      wreg[q] = r < E ? __ldg(reinterpret_cast<const float4*>(a.wr + (int64_t)r * H + h0 + c))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  auto store = [&](int b) {
+    float4 xv;
+    bf16x2_to_f32(xreg.x, xv.x, xv.y);
+    bf16x2_to_f32(xreg.y, xv.z, xv.w);
+    *reinterpret_cast<float4*>(xs + (b * kRouteTileM + xr) * kKP + xc) = xv;
 #pragma unroll
-      for (int m = 0; m < EM; ++m) wv[m] = ws[(tx + 32 * m) * (kKC + 1) + kk];
+    for (int q = 0; q < kWPer; ++q) {
+      const int idx = tid + 256 * q, r = idx >> 3, c = (idx & 7) * 4;
+      *reinterpret_cast<float4*>(ws + (b * EM * 32 + r) * kKP + c) = wreg[q];
+    }
+  };
+
+  const int nS = H / kKC;
+  load(0);
+  store(0);
+  __syncthreads();
+  for (int sl = 0; sl < nS; ++sl) {
+    const int b = sl & 1;
+    if (sl + 1 < nS) load((sl + 1) * kKC);
+    const float* xb = xs + (b * kRouteTileM + ty * 4) * kKP;
+    const float* wb = ws + (b * EM * 32 + tx) * kKP;
+#pragma unroll
+    for (int kk = 0; kk < kKC; kk += 4) {
+      float4 xv[4], wv[EM];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) xv[i] = *reinterpret_cast<const float4*>(xb + i * kKP + kk);
+#pragma unroll
+      for (int m = 0; m < EM; ++m) wv[m] = *reinterpret_cast<const float4*>(wb + m * 32 * kKP + kk);
 #pragma unroll
       for (int i = 0; i < 4; ++i)
 #pragma unroll
-        for (int m = 0; m < EM; ++m) acc[i][m] = fmaf(xv[i], wv[m], acc[i][m]);
+        for (int m = 0; m < EM; ++m) {
+          acc[i][m] = fmaf(xv[i].x, wv[m].x, acc[i][m]);
+          acc[i][m] = fmaf(xv[i].y, wv[m].y, acc[i][m]);
+          acc[i][m] = fmaf(xv[i].z, wv[m].z, acc[i][m]);
+          acc[i][m] = fmaf(xv[i].w, wv[m].w, acc[i][m]);
+        }
     }
+    if (sl + 1 < nS) store(b ^ 1);  // the other buffer: last read before the previous barrier
     __syncthreads();
   }
-  // logits to shared memory (z[token][expert])
+  // logits to shared memory (z[token][expert]); the slices are no longer read
   float* zs = ws;
   const int zp = EM * 32 + 1;
 #pragma unroll
@@ -341,8 +360,8 @@ RouteArgs route_args(Handle* h, const __nv_bfloat16* x, int T, int32_t* ids_out,
 
 template <int EM>
 cudaError_t launch_tiles(RouteArgs a, int32_t* hist, int n_tiles, cudaStream_t s) {
-  size_t smem = sizeof(float) * (kRouteTileM * (kKC + 1) + (size_t)EM * 32 * (kKC + 1));
-  size_t zsmem = sizeof(float) * (kRouteTileM * (kKC + 1) + (size_t)kRouteTileM * (EM * 32 + 1));
+  size_t smem = sizeof(float) * (2 * kRouteTileM * kKP + 2 * (size_t)EM * 32 * kKP);
+  size_t zsmem = sizeof(float) * (2 * kRouteTileM * kKP + (size_t)kRouteTileM * (EM * 32 + 1));
   if (zsmem > smem) smem = zsmem;
   route_tiles_kernel<EM><<<n_tiles, 256, smem, s>>>(a, hist);
   return cudaGetLastError();
