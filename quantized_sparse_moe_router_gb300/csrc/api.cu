@@ -144,7 +144,7 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
 
   Allocator A;
   const int64_t n_route_tiles = (Tm + kRouteTileM - 1) / kRouteTileM;
-  const int64_t n_mtiles_max = h->rows_max / 128 + EU + 1;
+  const int64_t n_mtiles_max = h->rows_max / kTokTile + EU + 1;
   const size_t hbuf_bytes = (size_t)h->rows_max * I * sizeof(float);
   struct {
     void** p;

@@ -21,6 +21,7 @@ constexpr int kGUGroup = 2;        // gate/up rows are interleaved in groups of 
 constexpr int kMaxK = 16;          // experts per token
 constexpr int kMaxDecodeT = 16;    // decode path token limit (one lane per token in the combine)
 constexpr int kRouteTileM = 32;    // tokens per CTA in the tiled router
+constexpr int kTokTile = 192;      // prefill GEMM token tile (rows of one expert)
 
 // Status bits written by kernels into the handle's device status word.
 constexpr int kStatusTimeout = 1;
@@ -62,10 +63,10 @@ struct Timing {
 
 // TMA descriptors of the prefill GEMMs (host copies, passed by value).
 struct PrefillMaps {
-  CUtensorMap a_x;    // xperm [rows_max][H] bf16, box 64 x 128, 128B swizzle
-  CUtensorMap a_h;    // hbuf  [rows_max][I] bf16, box 64 x 128, 128B swizzle
-  CUtensorMap q_gu;   // code plane [EU*2I][H] u8 (row stride row_bytes(H)), box 64 x 256
-  CUtensorMap s_gu;   // scale plane [EU*H/32][2I] u16, box 256 x 2
+  CUtensorMap a_x;    // xperm [rows_max][H] bf16, box 64 x 64, 128B swizzle
+  CUtensorMap a_h;    // hbuf  [rows_max][I] bf16, box 64 x 64, 128B swizzle
+  CUtensorMap q_gu;   // code plane [EU*2I][H] u8 (row stride row_bytes(H)), box 64 x 128, 64B swizzle
+  CUtensorMap s_gu;   // scale plane [EU*H/32][2I] u16, box 128 x 2
   CUtensorMap q_d;    // [EU*H][I] u8 (row stride row_bytes(I))
   CUtensorMap s_d;    // [EU*I/32][H] u16
 };
@@ -100,7 +101,7 @@ struct Handle {
   float* row_gate;    // [rows_max]
   int4* uinfo;        // [EU] (expert, first grouped row, rows, 0) of the experts with rows, ascending id
   int32_t* hist;      // [ceil(T_max/32)][EU] per-tile counts, then per-tile bases
-  int4* minfo;        // [rows_max/128 + EU] prefill 128-row tiles: (expert, first row, valid rows, 0)
+  int4* minfo;        // [rows_max/kTokTile + EU] prefill token tiles: (expert, first row, valid rows, 0)
   __nv_bfloat16* xperm; // [rows_max][H] x gathered into grouped order (prefill)
   void* hbuf;         // [rows_max][I] fp32 (decode) or bf16 (prefill)
   __nv_bfloat16* yp;  // [rows_max][H] bf16 (prefill)
@@ -219,13 +220,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// The same with a suspend-time hint: the thread sleeps in the barrier until the
+// phase completes (or the hint runs out) instead of re-polling, so waiting
+// warps take no issue slots from the working ones.
+constexpr uint32_t kSuspendHintNs = 100000;
+
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(kSuspendHintNs)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait for the phase with the given parity to complete. false = gave up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
-  uint64_t t0 = globaltimer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+  const uint64_t t0 = globaltimer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity)) return true;
+    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
 

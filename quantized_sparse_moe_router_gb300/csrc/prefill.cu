@@ -1,6 +1,6 @@
 // Prefill path (T > decode_T_max): the experts as grouped GEMMs on the
-// tcgen05 tensor cores, with the Q8_0 weights dequantised to bf16 in shared
-// memory.
+// tcgen05 tensor cores, with the Q8_0 weights dequantised to bf16 straight
+// into tensor memory.
 //
 // The pages' runtime has a tensor-core GEMM that dequantises stored Q8_0 in
 // place against bf16 activations (Flyweight README, §Image generation,
@@ -10,15 +10,23 @@
 // way into the MMA, with fp32 accumulation in tensor memory.
 //
 //   gather:   xperm[pos] = x[token of grouped row pos]           (bf16 rows)
-//   GEMM 1:   per (expert, 128-row tile, 256-column tile of the interleaved
-//             gate/up rows): acc = X_tile . deq(W_gu)^T; epilogue
-//             h = SiLU(gate) * up -> hbuf (bf16, grouped order)
-//   GEMM 2:   per (expert, 128-row tile, 256 output columns):
-//             Yp = gate_of_row * (h . deq(W_down)^T)  -> yp (bf16)
+//   GEMM 1:   per (token tile of one expert, 128 interleaved gate/up rows):
+//             D = deq(W_gu rows) . X_tile^T; epilogue h = SiLU(gate) * up
+//             -> hbuf (bf16, grouped order)
+//   GEMM 2:   per (token tile, 128 output features):
+//             Yp = gate_of_row * (deq(W_down rows) . h_tile^T) -> yp (bf16)
 //   combine:  out[t] = sum_j Yp[inv[t*k + j]] (+ shared row), fixed order
 //
+// The weights are the MMA's A operand (M = 128 rows, read from tensor
+// memory, written there by the dequantising warps with tcgen05.st); the
+// tokens are B (N = the tile's rows rounded up to 16, at most 192; K-major
+// bf16 in shared memory, 128-byte swizzle, loaded by TMA). So the bf16
+// weights never pass through shared memory, and a partial token tile costs
+// only the MMA columns it uses.
+//
 // One persistent CTA per SM, 14 warps: 0-3 epilogue (TMEM lane quarters),
-// 4 TMA producer, 5 MMA issuer (and TMEM owner), 6-13 dequantisers.
+// 4 TMA producer, 5 MMA issuer (and TMEM owner), 6-13 dequantisers (two per
+// lane quarter, one Q8_0 block of the stage's 64 K each).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -30,27 +38,33 @@ namespace {
 
 using namespace dev;
 
-constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int kStages = 3;
+constexpr int BM = 128, BK = 64;
+constexpr int BN = kTokTile;                // tokens per tile (N <= 192)
+constexpr int kXBox = 64;                   // token rows per TMA box
+constexpr int kStages = 4;
 constexpr int kEpiWarps = 4, kProducerWarp = 4, kMmaWarp = 5, kDeqWarp0 = 6, kDeqWarps = 8;
 constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 448
-constexpr uint32_t kABytes = BM * BK * 2;    // 16 KB bf16 A tile
-constexpr uint32_t kBBytes = BN * BK * 2;    // 32 KB bf16 B tile
-constexpr uint32_t kQBytes = BN * BK;        // 16 KB int8 codes
-constexpr uint32_t kSBytes = BN * 2 * 2;     // 1 KB: 2 scale blocks x 256 rows
-constexpr uint32_t kSmemBytes = kStages * (kABytes + kBBytes + kQBytes + kSBytes) + 1024;
-constexpr uint32_t kTmemCols = 512;          // two 128 x 256 fp32 accumulators
+constexpr uint32_t kXBytes = BN * BK * 2;   // 24 KB bf16 token tile
+constexpr uint32_t kQBytes = BM * BK;       // 8 KB int8 codes
+constexpr uint32_t kSBytes = BM * 2 * 2;    // 512 B: 2 scale blocks x 128 rows
+constexpr uint32_t kSmemBytes = kStages * (kXBytes + kQBytes + kSBytes) + 1024;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCols = BN;           // one fp32 accumulator: 128 lanes x 192 columns
+constexpr uint32_t kACol0 = 2 * kAccCols;   // A stages after the two accumulators
+constexpr uint32_t kACols = BK / 2;         // 64 bf16 per row = 32 columns per stage
+static_assert(kACol0 + kStages * kACols <= kTmemCols, "tensor memory budget");
+static_assert(BN % kXBox == 0 && BN % 16 == 0 && BN <= 256, "token tile");
 
 enum Epi { kEpiSwiGLU = 0, kEpiDownScale = 1 };
 
 struct GemmArgs {
-  const int4* minfo;      // per 128-row tile: (expert, first row, valid rows, 0)
+  const int4* minfo;      // per token tile: (expert, first grouped row, valid rows, 0)
   const Meta* meta;
   const float* row_gate;  // kEpiDownScale
   __nv_bfloat16* outp;    // hbuf (SwiGLU, [rows][I]) or yp ([rows][H])
   int K;                  // reduction length (H or I)
   int prows;              // weight rows per expert in the code plane (2I or H)
-  int n_ntiles;           // ceil(prows / 256)
+  int n_mb;               // ceil(prows / 128)
   int out_cols;           // I (SwiGLU) or H
 };
 
@@ -81,12 +95,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
+// D (tensor memory) [+]= A (tensor memory, lane = row) x B (shared memory descriptor)
+__device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -114,9 +129,41 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 16 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      : "memory");
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// ------------------------------------------------------------- packed fp32
+typedef unsigned long long f2;
+__device__ __forceinline__ f2 f2_pack(float a, float b) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ f2 f2_pack_bits(uint32_t a, uint32_t b) {
+  f2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(a), "r"(b));
+  return r;
+}
+// (q_lo + c, q_hi + c) * d, both exact, rounded once to a bf16 pair (low half = first)
+__device__ __forceinline__ uint32_t deq_pair_bf16(uint32_t bits_lo, uint32_t bits_hi, f2 bias, f2 dd) {
+  f2 m = f2_pack_bits(bits_lo, bits_hi), q, w;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(q) : "l"(m), "l"(bias));
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(w) : "l"(q), "l"(dd));
+  uint32_t r;
+  asm("{\n\t.reg .f32 a, b;\n\tmov.b64 {a, b}, %1;\n\tcvt.rn.bf16x2.f32 %0, b, a;\n\t}" : "=r"(r) : "l"(w));
+  return r;
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
@@ -124,11 +171,10 @@ __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 // ------------------------------------------------------------- the GEMM
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_q,
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_s, GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t a_full[kStages], q_full[kStages], b_full[kStages];
-  __shared__ __align__(8) uint64_t ab_empty[kStages], q_empty[kStages];
+  __shared__ __align__(8) uint64_t full[kStages], a_full[kStages], empty[kStages];
   __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], mma_done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -136,18 +182,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* base = smem_raw + pad;
-  uint8_t* sA = base;
-  uint8_t* sB = sA + kStages * kABytes;
-  uint8_t* sQ = sB + kStages * kBBytes;
-  uint8_t* sS = sQ + kStages * kQBytes;
+  uint8_t* sX = base;                            // [kStages][192 rows][128 B], 128B swizzle
+  uint8_t* sQ = sX + kStages * kXBytes;          // [kStages][128 rows][64 B], 64B swizzle
+  uint8_t* sS = sQ + kStages * kQBytes;          // [kStages][2][128] binary16
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(&a_full[i], 1);
-      mbar_init(&q_full[i], 1);
-      mbar_init(&b_full[i], kDeqWarps);
-      mbar_init(&ab_empty[i], 1);
-      mbar_init(&q_empty[i], kDeqWarps);
+      mbar_init(&full[i], 1);
+      mbar_init(&a_full[i], kDeqWarps);
+      mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -168,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = s_tmem;
 
-  const int n_tiles = a.meta->n_mtiles * a.n_ntiles;
+  const int n_tiles = a.meta->n_mtiles * a.n_mb;
   const int KT = a.K / BK;
   const int nb = a.K / 32;  // scale blocks per weight row
   bool ok = true;
@@ -184,47 +227,47 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       uint32_t it = 0;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const int4 mi = a.minfo[tile / a.n_ntiles];
-        const int n0 = (tile % a.n_ntiles) * BN;
+        const int4 mi = a.minfo[tile / a.n_mb];
+        const int m0 = (tile % a.n_mb) * BM;
+        const int nx = (mi.z + kXBox - 1) / kXBox;
         for (int kb = 0; kb < KT && ok; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
-          if (!(ok = wait(&ab_empty[s], ph ^ 1))) break;
-          if (!(ok = wait(&q_empty[s], ph ^ 1))) break;
-          mbar_arrive_expect_tx(&a_full[s], kABytes);
-          tma_load_2d(sA + s * kABytes, &map_a, kb * BK, mi.y, &a_full[s]);
-          mbar_arrive_expect_tx(&q_full[s], kQBytes + kSBytes);
-          tma_load_2d(sQ + s * kQBytes, &map_q, kb * BK, mi.x * a.prows + n0, &q_full[s]);
-          tma_load_2d(sS + s * kSBytes, &map_s, n0, mi.x * nb + kb * 2, &q_full[s]);
+          if (!(ok = wait(&empty[s], ph ^ 1))) break;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)nx * kXBox * BK * 2 + kQBytes + kSBytes);
+          for (int x = 0; x < nx; ++x)
+            tma_load_2d(sX + s * kXBytes + x * kXBox * 128, &map_b, kb * BK, mi.y + x * kXBox, &full[s]);
+          tma_load_2d(sQ + s * kQBytes, &map_q, kb * BK, mi.x * a.prows + m0, &full[s]);
+          tma_load_2d(sS + s * kSBytes, &map_s, m0, mi.x * nb + kb * 2, &full[s]);
         }
       }
       // copies still in flight after an abort land before the CTA leaves
-      for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j) {
-        mbar_wait(&a_full[j % kStages], (j / kStages) & 1);
-        mbar_wait(&q_full[j % kStages], (j / kStages) & 1);
-      }
+      for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1);
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(BM, BN);
       uint32_t it = 0, tc = 0;
       for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
+        const int4 mi = a.minfo[tile / a.n_mb];
+        const int n_mma = (mi.z + 15) / 16 * 16;
+        const uint32_t idesc = idesc_bf16(BM, n_mma);
         const int b = tc & 1;
         if (!(ok = wait(&acc_empty[b], ((tc >> 1) & 1) ^ 1))) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + b * BN;
+        const uint32_t d_tmem = tmem_base + b * kAccCols;
         for (int kb = 0; kb < KT; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
+          if (!(ok = wait(&full[s], ph))) break;
           if (!(ok = wait(&a_full[s], ph))) break;
-          if (!(ok = wait(&b_full[s], ph))) break;
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + s * kABytes), b0 = smem_u32(sB + s * kBBytes);
+          const uint32_t b0 = smem_u32(sX + s * kXBytes);
+          const uint32_t a0 = tmem_base + kACol0 + s * kACols;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
-            mma_bf16(d_tmem, sw128_desc(a0 + k * 32), sw128_desc(b0 + k * 32), idesc, (kb | k) != 0);
-          mma_commit(&ab_empty[s]);
+            mma_tmem_a(d_tmem, a0 + k * 8, sw128_desc(b0 + k * 32), idesc, (kb | k) != 0);
+          mma_commit(&empty[s]);
         }
         if (ok) mma_commit(&acc_full[b]);
       }
@@ -233,101 +276,86 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait(&mma_done, 0);
     }
   } else if (warp >= kDeqWarp0) {
-    // ------------------------------------------------ dequantisers: int8 x scale -> bf16, swizzled
-    const int dt = threadIdx.x - kDeqWarp0 * 32;  // 0..255
+    // ------------------------------------------------ dequantisers: int8 x scale -> bf16 -> TMEM (A)
+    const int quarter = warp & 3, half = (warp - kDeqWarp0) >> 2;
+    const int r = quarter * 32 + lane;  // weight row of the tile = TMEM lane
+    const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+    const f2 bias = f2_pack(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
     uint32_t it = 0;
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
       for (int kb = 0; kb < KT && ok; ++kb, ++it) {
         const int s = it % kStages;
         const uint32_t ph = (it / kStages) & 1;
-        if (!(ok = wait(&q_full[s], ph))) break;
-        if (!(ok = wait(&ab_empty[s], ph ^ 1))) break;
-        const uint8_t* q = sQ + s * kQBytes;
-        const uint16_t* sc = reinterpret_cast<const uint16_t*>(sS + s * kSBytes);
-        uint8_t* bt = sB + s * kBBytes;
+        // full[s] also means the MMAs that last read A stage s have completed
+        // (the producer waited for them before refilling the stage)
+        if (!(ok = wait(&full[s], ph))) break;
+        // this thread's block: row r, codes [32 half, 32 half + 32) of the stage,
+        // 16-byte chunks 2 half and 2 half + 1, stored with the 64-byte swizzle
+        const uint8_t* qrow = sQ + s * kQBytes + r * 64;
+        const int sw = (r >> 1) & 3;
+        const uint4 c0 = *reinterpret_cast<const uint4*>(qrow + (((2 * half) ^ sw) << 4));
+        const uint4 c1 = *reinterpret_cast<const uint4*>(qrow + (((2 * half + 1) ^ sw) << 4));
+        const float d = half_bits_to_f32(reinterpret_cast<const uint16_t*>(sS + s * kSBytes)[half * BM + r]);
+        const f2 dd = f2_pack(d, d);
+        const uint32_t w8[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        uint32_t out[16];
 #pragma unroll
-        for (int i = 0; i < (BN * BK / 16) / 256; ++i) {
-          const int item = dt + 256 * i;
-          const int r = item >> 2, c = item & 3;
-          const uint4 qv = *reinterpret_cast<const uint4*>(q + r * BK + c * 16);
-          const float d = half_bits_to_f32(sc[(c >> 1) * BN + r]);
-          float f[16];
-          u8x4_to_f32(qv.x, f[0], f[1], f[2], f[3]);
-          u8x4_to_f32(qv.y, f[4], f[5], f[6], f[7]);
-          u8x4_to_f32(qv.z, f[8], f[9], f[10], f[11]);
-          u8x4_to_f32(qv.w, f[12], f[13], f[14], f[15]);
-          uint4 lo, hi;
-          lo.x = pack_bf16x2(f[0] * d, f[1] * d);
-          lo.y = pack_bf16x2(f[2] * d, f[3] * d);
-          lo.z = pack_bf16x2(f[4] * d, f[5] * d);
-          lo.w = pack_bf16x2(f[6] * d, f[7] * d);
-          hi.x = pack_bf16x2(f[8] * d, f[9] * d);
-          hi.y = pack_bf16x2(f[10] * d, f[11] * d);
-          hi.z = pack_bf16x2(f[12] * d, f[13] * d);
-          hi.w = pack_bf16x2(f[14] * d, f[15] * d);
-          const int sw = r & 7;
-          *reinterpret_cast<uint4*>(bt + r * 128 + (((2 * c) ^ sw) << 4)) = lo;
-          *reinterpret_cast<uint4*>(bt + r * 128 + (((2 * c + 1) ^ sw) << 4)) = hi;
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t w = w8[i];
+          out[2 * i] = deq_pair_bf16(__byte_perm(w, 0x4B000000u, 0x7650), __byte_perm(w, 0x4B000000u, 0x7651), bias,
+                                     dd);
+          out[2 * i + 1] = deq_pair_bf16(__byte_perm(w, 0x4B000000u, 0x7652), __byte_perm(w, 0x4B000000u, 0x7653),
+                                         bias, dd);
         }
-        fence_proxy_async_smem();  // the generic-proxy stores must be visible to the tensor cores
+        tmem_st16(tmem_base + lane_addr + kACol0 + s * kACols + half * 16, out);
+        asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+        tc_fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&b_full[s]);
-          mbar_arrive(&q_empty[s]);
-        }
+        if (lane == 0) mbar_arrive(&a_full[s]);
       }
     }
   } else {
     // ------------------------------------------------ epilogue: TMEM -> registers -> global
-    const int m = warp * 32 + lane;  // row of the tile = TMEM lane
     uint32_t tc = 0;
     for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
-      const int4 mi = a.minfo[tile / a.n_ntiles];
-      const int n0 = (tile % a.n_ntiles) * BN;
+      const int4 mi = a.minfo[tile / a.n_mb];
+      const int m0 = (tile % a.n_mb) * BM;
       const int b = tc & 1;
       if (!(ok = wait(&acc_full[b], (tc >> 1) & 1))) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + b * BN + ((uint32_t)(warp * 32) << 16);
-      const bool valid = m < mi.z;
-      const int64_t row = (int64_t)mi.y + m;
-      if (EPI == kEpiSwiGLU) {
-        // columns of the 256-row weight tile: groups of kGUGroup gate rows,
-        // then the up rows of the same i; 32 columns give 16 consecutive i
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          float v[32];
-          tmem_ld32(taddr + c0, v);
-          const int i0 = (n0 + c0) / 2;
-          if (valid && i0 < a.out_cols) {
-            uint32_t hw[8];
+      const uint32_t taddr = tmem_base + b * kAccCols + ((uint32_t)(warp * 32) << 16);
+      const int prow = m0 + warp * 32 + lane;  // weight row (interleaved gate/up for SwiGLU)
+      for (int c0 = 0; c0 < mi.z; c0 += 32) {
+        float v[32];
+        tmem_ld32(taddr + c0, v);
+        if (EPI == kEpiSwiGLU) {
+          // lanes 4g, 4g+1 hold the gate rows of i = 2(prow/4) + {0,1}, lanes
+          // 4g+2, 4g+3 the matching up rows. Partners (lane ^ 2) swap halves:
+          // a gate lane computes tokens 0..15 of the chunk, an up lane 16..31,
+          // so every lane makes 16 distinct outputs.
+          const bool gate_lane = (lane & 2) == 0;
+          const int i = (prow >> 2) * 2 + (lane & 1);
+          const int jt = gate_lane ? 0 : 16;
 #pragma unroll
-            for (int j = 0; j < 16; j += 2) {
-              const int q0 = (j / kGUGroup) * 2 * kGUGroup + j % kGUGroup;
-              const int q1 = ((j + 1) / kGUGroup) * 2 * kGUGroup + (j + 1) % kGUGroup;
-              hw[j / 2] = pack_bf16x2(silu(v[q0]) * v[q0 + kGUGroup], silu(v[q1]) * v[q1 + kGUGroup]);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(a.outp + row * a.out_cols + i0);
-            dst[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-            dst[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+          for (int j = 0; j < 16; ++j) {
+            const float mine = gate_lane ? v[j] : v[16 + j];
+            const float other = __shfl_xor_sync(0xFFFFFFFFu, gate_lane ? v[16 + j] : v[j], 2);
+            const float g = gate_lane ? mine : other, u = gate_lane ? other : mine;
+            const float hv = g * __frcp_rn(1.0f + __expf(-g)) * u;
+            const float hn = __shfl_xor_sync(0xFFFFFFFFu, hv, 1);
+            const int c = c0 + jt + j;
+            if ((lane & 1) == 0 && c < mi.z && i < a.out_cols)
+              *reinterpret_cast<uint32_t*>(a.outp + (int64_t)(mi.y + c) * a.out_cols + i) = pack_bf16x2(hv, hn);
           }
-        }
-      } else {
-        const float gate = valid ? a.row_gate[row] : 0.f;
-#pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
-          float v[32];
-          tmem_ld32(taddr + c0, v);
-          if (valid && n0 + c0 < a.out_cols) {
-            uint4* dst = reinterpret_cast<uint4*>(a.outp + row * a.out_cols + n0 + c0);
+        } else {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 w;
-              w.x = pack_bf16x2(gate * v[8 * q + 0], gate * v[8 * q + 1]);
-              w.y = pack_bf16x2(gate * v[8 * q + 2], gate * v[8 * q + 3]);
-              w.z = pack_bf16x2(gate * v[8 * q + 4], gate * v[8 * q + 5]);
-              w.w = pack_bf16x2(gate * v[8 * q + 6], gate * v[8 * q + 7]);
-              dst[q] = w;
-            }
+          for (int j = 0; j < 32; ++j) {
+            const bool valid = c0 + j < mi.z;
+            const float g = valid ? __ldg(a.row_gate + mi.y + c0 + j) : 0.f;
+            const float y = g * v[j];
+            const float yn = __shfl_down_sync(0xFFFFFFFFu, y, 1);
+            if ((lane & 1) == 0 && valid && prow < a.out_cols)
+              *reinterpret_cast<uint32_t*>(a.outp + (int64_t)(mi.y + c0 + j) * a.out_cols + prow) = pack_bf16x2(y, yn);
           }
         }
       }
@@ -432,22 +460,22 @@ cudaError_t prepare_prefill(Handle* h) {
   const uint64_t H = h->cfg.H, I = h->cfg.I, EU = h->EU, R = h->rows_max;
   PrefillMaps* m = new PrefillMaps();
   h->maps = m;
-  cudaError_t e = encode_2d(&m->a_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->xperm, H, R, H * 2, BK, BM,
+  cudaError_t e = encode_2d(&m->a_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->xperm, H, R, H * 2, BK, kXBox,
                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
   if (e == cudaSuccess)
-    e = encode_2d(&m->a_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->hbuf, I, R, I * 2, BK, BM,
+    e = encode_2d(&m->a_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->hbuf, I, R, I * 2, BK, kXBox,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
   if (e == cudaSuccess)
-    e = encode_2d(&m->q_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->q_gu, H, EU * 2 * I, row_bytes(H), BK, BN,
+    e = encode_2d(&m->q_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->q_gu, H, EU * 2 * I, row_bytes(H), BK, BM,
+                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (e == cudaSuccess)
+    e = encode_2d(&m->s_gu, CU_TENSOR_MAP_DATA_TYPE_UINT16, h->st_gu, 2 * I, EU * (H / 32), 2 * I * 2, BM, 2,
                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (e == cudaSuccess)
-    e = encode_2d(&m->s_gu, CU_TENSOR_MAP_DATA_TYPE_UINT16, h->st_gu, 2 * I, EU * (H / 32), 2 * I * 2, BN, 2,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+    e = encode_2d(&m->q_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->q_d, I, EU * H, row_bytes(I), BK, BM,
+                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (e == cudaSuccess)
-    e = encode_2d(&m->q_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->q_d, I, EU * H, row_bytes(I), BK, BN, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-  if (e == cudaSuccess)
-    e = encode_2d(&m->s_d, CU_TENSOR_MAP_DATA_TYPE_UINT16, h->st_d, H, EU * (I / 32), H * 2, BN, 2,
+    e = encode_2d(&m->s_d, CU_TENSOR_MAP_DATA_TYPE_UINT16, h->st_d, H, EU * (I / 32), H * 2, BM, 2,
                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   return e;
 }
@@ -470,7 +498,7 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
     g.outp = static_cast<__nv_bfloat16*>(h->hbuf);
     g.K = H;
     g.prows = 2 * I;
-    g.n_ntiles = (2 * I + BN - 1) / BN;
+    g.n_mb = (2 * I + BM - 1) / BM;
     g.out_cols = I;
     KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP, s);
     grouped_gemm_kernel<kEpiSwiGLU><<<h->num_sms, kThreads, kSmemBytes, s>>>(h->maps->a_x, h->maps->q_gu,
@@ -480,7 +508,7 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
     g.outp = h->yp;
     g.K = I;
     g.prows = H;
-    g.n_ntiles = (H + BN - 1) / BN;
+    g.n_mb = (H + BM - 1) / BM;
     g.out_cols = H;
     KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN, s);
     grouped_gemm_kernel<kEpiDownScale><<<h->num_sms, kThreads, kSmemBytes, s>>>(h->maps->a_h, h->maps->q_d,

@@ -236,64 +236,99 @@ __global__ void __launch_bounds__(256) route_tiles_kernel(RouteArgs a, int32_t* 
 
 // One CTA: per-expert totals over the tiles, offsets (shared expert last),
 // per-tile absolute bases (in place of the tile counts), the list of experts
-// with rows, and the list of 128-row tiles per expert for the prefill GEMMs.
+// with rows, and the list of token tiles (kTokTile rows) per expert for the
+// prefill GEMMs.
+// The per-expert walks over the tiles batch their loads 16 deep; the three
+// scans over the experts run in one warp, in registers.
+constexpr int kScanBatch = 16;
+
 __global__ void __launch_bounds__(256) route_scan_kernel(RouteArgs a, int32_t* hist, int n_tiles,
                                                          int4* minfo) {
+  __shared__ int s_cnt[kMaxE + 2];
   __shared__ int s_off[kMaxE + 2];
   __shared__ int s_nz[kMaxE + 2];
   __shared__ int s_nt[kMaxE + 2];
-  const int E = a.E, EU = E + a.S, T = a.T, tid = threadIdx.x;
-  for (int e = tid; e < EU + 1; e += 256) s_off[e] = 0;
-  __syncthreads();
+  const int E = a.E, EU = E + a.S, T = a.T, tid = threadIdx.x, lane = tid & 31;
   for (int e = tid; e < E; e += 256) {
     int run = 0;
-    for (int c = 0; c < n_tiles; ++c) {
-      int v = hist[(int64_t)c * E + e];
-      hist[(int64_t)c * E + e] = run;
-      run += v;
+    for (int c0 = 0; c0 < n_tiles; c0 += kScanBatch) {
+      int v[kScanBatch];
+#pragma unroll
+      for (int u = 0; u < kScanBatch; ++u) v[u] = c0 + u < n_tiles ? hist[(int64_t)(c0 + u) * E + e] : 0;
+#pragma unroll
+      for (int u = 0; u < kScanBatch; ++u) run += v[u];
     }
-    s_off[e] = run;
+    s_cnt[e] = run;
   }
-  if (a.S && tid == 0) s_off[E] = T;
+  if (a.S && tid == 0) s_cnt[E] = T;
   __syncthreads();
-  for (int e = tid; e < EU; e += 256) {
-    a.counts[e] = s_off[e];
-    s_nz[e] = s_off[e] > 0;
-    s_nt[e] = (s_off[e] + 127) / 128;
-  }
-  if (tid == 0) {
-    // tiny serial scans (EU <= 257) kept simple: one thread
-    int run = 0, nz = 0, nt = 0;
-    for (int e = 0; e < EU; ++e) {
-      int c = s_off[e];
-      s_off[e] = run;
-      run += c;
-      int z = s_nz[e];
-      s_nz[e] = nz;
-      nz += z;
-      int t = s_nt[e];
-      s_nt[e] = nt;
-      nt += t;
+  if (tid < 32) {
+    constexpr int kPer = (kMaxE + 1 + 31) / 32;
+    const int per = (EU + 31) / 32, b0 = lane * per;
+    int cn[kPer];
+    int sc = 0, sn = 0, st = 0;
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      const int i = b0 + m;
+      cn[m] = (m < per && i < EU) ? s_cnt[i] : 0;
+      sc += cn[m];
+      sn += cn[m] > 0;
+      st += (cn[m] + kTokTile - 1) / kTokTile;
     }
-    s_off[EU] = run;
-    s_nz[EU] = nz;
-    s_nt[EU] = nt;
-    a.meta->n_unique = nz;
-    a.meta->n_mtiles = nt;
-    a.meta->T = T;
+    int ic = sc, in = sn, it = st;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int uc = __shfl_up_sync(0xFFFFFFFFu, ic, o), un = __shfl_up_sync(0xFFFFFFFFu, in, o),
+                ut = __shfl_up_sync(0xFFFFFFFFu, it, o);
+      if (lane >= o) {
+        ic += uc;
+        in += un;
+        it += ut;
+      }
+    }
+    int rc = ic - sc, rn = in - sn, rt = it - st;
+#pragma unroll
+    for (int m = 0; m < kPer; ++m) {
+      const int i = b0 + m;
+      if (m < per && i < EU) {
+        s_off[i] = rc;
+        s_nz[i] = rn;
+        s_nt[i] = rt;
+        rc += cn[m];
+        rn += cn[m] > 0;
+        rt += (cn[m] + kTokTile - 1) / kTokTile;
+      }
+    }
+    if (lane == 31) {
+      s_off[EU] = ic;
+      a.meta->n_unique = in;
+      a.meta->n_mtiles = it;
+      a.meta->T = T;
+    }
   }
   __syncthreads();
   for (int e = tid; e < EU + 1; e += 256) a.offsets[e] = s_off[e];
   for (int e = tid; e < EU; e += 256) {
-    int cnt = a.counts[e];
+    const int cnt = s_cnt[e];
+    a.counts[e] = cnt;
     if (cnt > 0) a.uinfo[s_nz[e]] = make_int4(e, s_off[e], cnt, 0);
-    int nt = (cnt + 127) / 128;
-    for (int i = 0; i < nt; ++i) minfo[s_nt[e] + i] = make_int4(e, s_off[e] + 128 * i, min(128, cnt - 128 * i), 0);
+    const int nt = (cnt + kTokTile - 1) / kTokTile;
+    for (int i = 0; i < nt; ++i)
+      minfo[s_nt[e] + i] = make_int4(e, s_off[e] + kTokTile * i, min(kTokTile, cnt - kTokTile * i), 0);
   }
-  __syncthreads();
   for (int e = tid; e < E; e += 256) {
-    int base = s_off[e];
-    for (int c = 0; c < n_tiles; ++c) hist[(int64_t)c * E + e] += base;
+    int run = s_off[e];
+    for (int c0 = 0; c0 < n_tiles; c0 += kScanBatch) {
+      int v[kScanBatch];
+#pragma unroll
+      for (int u = 0; u < kScanBatch; ++u) v[u] = c0 + u < n_tiles ? hist[(int64_t)(c0 + u) * E + e] : 0;
+#pragma unroll
+      for (int u = 0; u < kScanBatch; ++u)
+        if (c0 + u < n_tiles) {
+          hist[(int64_t)(c0 + u) * E + e] = run;
+          run += v[u];
+        }
+    }
   }
 }
 
