@@ -36,7 +36,8 @@ constexpr int kCW = 16;                    // consumer warps
 constexpr int kThreads = (kCW + 1) * 32;   // + one producer warp
 constexpr int kProducer = kCW;
 constexpr int kMaxStages = 16;
-constexpr int kRowBlock = 16;              // output rows per W_down stage
+constexpr int kRowBlock = 16;              // output rows per W_down block
+constexpr int kMaxPer = 4;                 // experts' blocks per W_down stage
 constexpr uint32_t kConsumerBarrier = 1;   // named barrier of the 16 consumer warps
 constexpr int64_t kL2PrefetchMax = 40ll << 20;  // W_down bytes per call prefetched into L2 (L2 is 129 MB)
 
@@ -54,6 +55,7 @@ struct DecodeArgs {
   int H, I, E, k, S, T;
   int publish;
   int R;                 // gate/up units per stage (a multiple of kGUGroup dividing 32)
+  int n_per;             // experts per W_down stage (each a block of <= 16 rows), <= kMaxPer
   uint32_t stage_bytes;  // ring slot size (max of a gate/up and a down stage)
   int stages;
   int x_mode;
@@ -187,8 +189,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   const int64_t n_gu = hi > lo ? (hi + R - 1) / R - b0 : 0;
   // down stages: output rows [o0, o1), blocks of 16 rows; per block every touched expert
   const int o0 = (int)((int64_t)H * blockIdx.x / gridDim.x), o1 = (int)((int64_t)H * (blockIdx.x + 1) / gridDim.x);
+  // (a down stage holds the same 16-row block of up to n_per experts, so that
+  // a warp's dot products for those experts overlap)
   const int n_blk = (o1 - o0 + kRowBlock - 1) / kRowBlock;
-  const int64_t n_dn = (int64_t)nU * n_blk;
+  const int n_ge = (nU + a.n_per - 1) / a.n_per;
+  const int64_t n_dn = (int64_t)n_ge * n_blk;
   const int64_t n_all = n_gu + n_dn;
 
   if (warp == kProducer) {
@@ -219,12 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
           mbar_arrive_expect_tx(&full[st], bytes);
           bulk_g2s(sb, a.q_gu + ((int64_t)e * 2 * I + 2 * i0) * rb_h, bytes, &full[st]);
         } else {
-          const int64_t jd = j - n_gu;  // block-major: all experts of block 0, then block 1, ...
-          const int e = r.u[jd % nU].x, blk = (int)(jd / nU);
+          const int64_t jd = j - n_gu;  // block-major: all expert groups of block 0, then block 1, ...
+          const int blk = (int)(jd / n_ge), e0 = (int)(jd % n_ge) * a.n_per, e1 = ::min(nU, e0 + a.n_per);
           const int r0 = o0 + blk * kRowBlock, nr = ::min(kRowBlock + 0, o1 - r0);
-          const int64_t row = (int64_t)e * H + r0;
-          mbar_arrive_expect_tx(&full[st], (uint32_t)nr * rb_i);
-          bulk_g2s(sb, a.q_d + row * rb_i, (uint32_t)nr * rb_i, &full[st]);
+          mbar_arrive_expect_tx(&full[st], (uint32_t)(e1 - e0) * nr * rb_i);
+          for (int u = e0; u < e1; ++u)
+            bulk_g2s(sb + (size_t)(u - e0) * kRowBlock * rb_i, a.q_d + ((int64_t)r.u[u].x * H + r0) * rb_i,
+                     (uint32_t)nr * rb_i, &full[st]);
         }
       }
       // every copy issued has landed before the CTA may leave
@@ -282,30 +288,62 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
         const uint16_t* su = reinterpret_cast<const uint16_t*>(qu_row + H);
         const int4 ui = r.u[g / I];
         const int i = (int)(g % I);
-        for (int rr = 0; rr < ui.z; ++rr) {
-          const int pos = ui.y + rr;
-          const int t = r.tok[pos];
-          float accg = 0.f, accu = 0.f;
-          for (int seg = lane; seg < nseg_h; seg += 32) {
-            f2 xv[8];
-            if (a.x_mode == kXSmemF32) {
-              x16_from_f32_t(reinterpret_cast<const float*>(smem) + (size_t)t * H, H, seg, xv);
-            } else if (a.x_mode == kXSmemBf16) {
-              const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(smem) + (size_t)t * H;
-              x16_from_bf16(*reinterpret_cast<const uint4*>(xb + seg * 8),
-                            *reinterpret_cast<const uint4*>(xb + H / 2 + seg * 8), xv);
-            } else {
-              const uint4* xp = reinterpret_cast<const uint4*>(a.x + (size_t)t * H + seg * 16);
-              x16_from_bf16(__ldg(xp), __ldg(xp + 1), xv);
-            }
-            const uint4 qg = *reinterpret_cast<const uint4*>(qg_row + seg * 16);
-            const uint4 qu = *reinterpret_cast<const uint4*>(qu_row + seg * 16);
-            accg = fmaf(half_bits_to_f32(sg[seg >> 1]), dot16(qg, xv), accg);
-            accu = fmaf(half_bits_to_f32(su[seg >> 1]), dot16(qu, xv), accu);
+        auto load_x = [&](int t, int seg, f2(&xv)[8]) {
+          if (a.x_mode == kXSmemF32) {
+            x16_from_f32_t(reinterpret_cast<const float*>(smem) + (size_t)t * H, H, seg, xv);
+          } else if (a.x_mode == kXSmemBf16) {
+            const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(smem) + (size_t)t * H;
+            x16_from_bf16(*reinterpret_cast<const uint4*>(xb + seg * 8), *reinterpret_cast<const uint4*>(xb + H / 2 + seg * 8),
+                          xv);
+          } else {
+            const uint4* xp = reinterpret_cast<const uint4*>(a.x + (size_t)t * H + seg * 16);
+            x16_from_bf16(__ldg(xp), __ldg(xp + 1), xv);
           }
-          accg = warp_sum(accg);
-          accu = warp_sum(accu);
-          if (lane == 0) a.hbuf[(int64_t)pos * I + i] = silu(accg) * accu;
+        };
+        if (T == 1) {
+          // one row: two segments per pass, independent accumulators
+          float ag0 = 0.f, au0 = 0.f, ag1 = 0.f, au1 = 0.f;
+          int seg = lane;
+          for (; seg + 32 < nseg_h; seg += 64) {
+            f2 x0[8], x1[8];
+            load_x(0, seg, x0);
+            load_x(0, seg + 32, x1);
+            const uint4 g0 = *reinterpret_cast<const uint4*>(qg_row + seg * 16);
+            const uint4 v0 = *reinterpret_cast<const uint4*>(qu_row + seg * 16);
+            const uint4 g1 = *reinterpret_cast<const uint4*>(qg_row + (seg + 32) * 16);
+            const uint4 v1 = *reinterpret_cast<const uint4*>(qu_row + (seg + 32) * 16);
+            ag0 = fmaf(half_bits_to_f32(sg[seg >> 1]), dot16(g0, x0), ag0);
+            au0 = fmaf(half_bits_to_f32(su[seg >> 1]), dot16(v0, x0), au0);
+            ag1 = fmaf(half_bits_to_f32(sg[(seg + 32) >> 1]), dot16(g1, x1), ag1);
+            au1 = fmaf(half_bits_to_f32(su[(seg + 32) >> 1]), dot16(v1, x1), au1);
+          }
+          if (seg < nseg_h) {
+            f2 x0[8];
+            load_x(0, seg, x0);
+            const uint4 g0 = *reinterpret_cast<const uint4*>(qg_row + seg * 16);
+            const uint4 v0 = *reinterpret_cast<const uint4*>(qu_row + seg * 16);
+            ag0 = fmaf(half_bits_to_f32(sg[seg >> 1]), dot16(g0, x0), ag0);
+            au0 = fmaf(half_bits_to_f32(su[seg >> 1]), dot16(v0, x0), au0);
+          }
+          const float accg = warp_sum(ag0 + ag1), accu = warp_sum(au0 + au1);
+          if (lane == 0) a.hbuf[(int64_t)ui.y * I + i] = silu(accg) * accu;
+        } else {
+          for (int rr = 0; rr < ui.z; ++rr) {
+            const int pos = ui.y + rr;
+            const int t = r.tok[pos];
+            float accg = 0.f, accu = 0.f;
+            for (int seg = lane; seg < nseg_h; seg += 32) {
+              f2 xv[8];
+              load_x(t, seg, xv);
+              const uint4 qg = *reinterpret_cast<const uint4*>(qg_row + seg * 16);
+              const uint4 qu = *reinterpret_cast<const uint4*>(qu_row + seg * 16);
+              accg = fmaf(half_bits_to_f32(sg[seg >> 1]), dot16(qg, xv), accg);
+              accu = fmaf(half_bits_to_f32(su[seg >> 1]), dot16(qu, xv), accu);
+            }
+            accg = warp_sum(accg);
+            accu = warp_sum(accu);
+            if (lane == 0) a.hbuf[(int64_t)pos * I + i] = silu(accg) * accu;
+          }
         }
       }
       __syncwarp();
@@ -344,7 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
     // ---- phase 3: down + combine. Warp w owns row w of every 16-row block;
     // per block it visits every touched expert (ascending id, shared last)
     // keeping per-lane partial sums per token, and reduces across the warp
-    // once, at the end of the block.
+    // once, at the end of the block. The experts of a stage are processed
+    // together (independent dot products in flight).
     const float* hsrc = a.h_smem ? reinterpret_cast<const float*>(smem) : a.hbuf;
     const int nseg_i = I / 16;
     float part[kMaxDecodeT];
@@ -358,41 +397,73 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
         ok = false;
         break;
       }
-      const int u = (int)(jd % nU), blk = (int)(jd / nU);
-      const int4 ui = r.u[u];
+      const int ge = (int)(jd % n_ge), blk = (int)(jd / n_ge);
+      const int e0 = ge * a.n_per, ne = ::min(nU, e0 + a.n_per) - e0;
       const int r0 = o0 + blk * kRowBlock;
       const int nr = ::min(kRowBlock + 0, o1 - r0);
       if (warp < nr) {
-        const uint8_t* sb = ring + (size_t)st * a.stage_bytes;
-        const uint8_t* qrow = sb + (size_t)warp * rb_i;
-        const uint16_t* sc = reinterpret_cast<const uint16_t*>(qrow + I);
-        for (int m = 0; m < ui.z; ++m) {
-          const int pos = ui.y + m;
-          const float* hrow = hsrc + (size_t)pos * I;
-          float d = 0.f;
-          for (int seg = lane; seg < nseg_i; seg += 32) {
-            f2 hv[8];
-            if (a.h_smem)
-              x16_from_f32_t(hrow, I, seg, hv);
-            else
-              x16_from_f32_global(hrow + seg * 16, hv);
-            const uint4 qq = *reinterpret_cast<const uint4*>(qrow + seg * 16);
-            d = fmaf(half_bits_to_f32(sc[seg >> 1]), dot16(qq, hv), d);
-          }
-          const float g = r.rg[pos];
-          if (T == 1) {
-            part[0] = fmaf(g, d, part[0]);
-          } else {
-            const int t = r.tok[pos];
+        const uint8_t* sb = ring + (size_t)st * a.stage_bytes + (size_t)warp * rb_i;
+        if (T == 1) {
+          // one row per expert: the stage's experts' dot products interleaved
+          float dacc[kMaxPer];
+          const float* hrow[kMaxPer];
 #pragma unroll
-            for (int tt = 0; tt < kMaxDecodeT; ++tt)
-              if (tt == t) part[tt] = fmaf(g, d, part[tt]);
+          for (int el = 0; el < kMaxPer; ++el) {
+            dacc[el] = 0.f;
+            hrow[el] = hsrc + (size_t)(el < ne ? r.u[e0 + el].y : 0) * I;
+          }
+          for (int seg = lane; seg < nseg_i; seg += 32) {
+#pragma unroll
+            for (int el = 0; el < kMaxPer; ++el) {
+              if (el < ne) {
+                const uint8_t* qrow = sb + (size_t)el * kRowBlock * rb_i;
+                f2 hv[8];
+                if (a.h_smem)
+                  x16_from_f32_t(hrow[el], I, seg, hv);
+                else
+                  x16_from_f32_global(hrow[el] + seg * 16, hv);
+                const uint4 qq = *reinterpret_cast<const uint4*>(qrow + seg * 16);
+                const uint16_t* sc = reinterpret_cast<const uint16_t*>(qrow + I);
+                dacc[el] = fmaf(half_bits_to_f32(sc[seg >> 1]), dot16(qq, hv), dacc[el]);
+              }
+            }
+          }
+#pragma unroll
+          for (int el = 0; el < kMaxPer; ++el)
+            if (el < ne) {
+              const int pos = r.u[e0 + el].y;
+              part[0] = fmaf(r.gates[r.slot[pos]], dacc[el], part[0]);
+            }
+        } else {
+          for (int el = 0; el < ne; ++el) {
+            const int4 ui = r.u[e0 + el];
+            const uint8_t* qrow = sb + (size_t)el * kRowBlock * rb_i;
+            const uint16_t* sc = reinterpret_cast<const uint16_t*>(qrow + I);
+            for (int m = 0; m < ui.z; ++m) {
+              const int pos = ui.y + m;
+              const float* hr = hsrc + (size_t)pos * I;
+              float d = 0.f;
+              for (int seg = lane; seg < nseg_i; seg += 32) {
+                f2 hv[8];
+                if (a.h_smem)
+                  x16_from_f32_t(hr, I, seg, hv);
+                else
+                  x16_from_f32_global(hr + seg * 16, hv);
+                const uint4 qq = *reinterpret_cast<const uint4*>(qrow + seg * 16);
+                d = fmaf(half_bits_to_f32(sc[seg >> 1]), dot16(qq, hv), d);
+              }
+              const float g = r.gates[r.slot[pos]];
+              const int t = r.tok[pos];
+#pragma unroll
+              for (int tt = 0; tt < kMaxDecodeT; ++tt)
+                if (tt == t) part[tt] = fmaf(g, d, part[tt]);
+            }
           }
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
-      if (u == nU - 1) {  // block done: one reduction per token, lane t writes token t
+      if (ge == n_ge - 1) {  // block done: one reduction per token, lane t writes token t
         if (warp < nr) {
           float mine = 0.f;
 #pragma unroll
@@ -479,8 +550,9 @@ cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfl
   int R = 32;
   while (R > kGUGroup && (uint32_t)R * unit > kStageTarget) R /= 2;
   a.R = R;
-  const uint32_t dn_stage = (uint32_t)(kRowBlock * row_bytes(I));
-  a.stage_bytes = std::max((uint32_t)R * unit, dn_stage);
+  const uint32_t dn_block = (uint32_t)(kRowBlock * row_bytes(I));
+  a.n_per = (int)std::max<uint32_t>(1, std::min<uint32_t>(kMaxPer, (uint32_t)R * unit / dn_block));
+  a.stage_bytes = std::max((uint32_t)R * unit, (uint32_t)a.n_per * dn_block);
   const int64_t ring_bytes = (int64_t)g_smem_optin - align128(a.act_bytes) - 256;
   a.stages = (int)std::min<int64_t>(kMaxStages, ring_bytes / a.stage_bytes);
   if (a.stages < 2) return cudaErrorInvalidConfiguration;

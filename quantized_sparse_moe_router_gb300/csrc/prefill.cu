@@ -41,9 +41,11 @@ using namespace dev;
 constexpr int BM = 128, BK = 64;
 constexpr int BN = kTokTile;                // tokens per tile (N <= 192)
 constexpr int kXBox = 64;                   // token rows per TMA box
-constexpr int kStages = 4;
+constexpr int kStages = 6;                  // shared-memory stages (TMA -> dequant / MMA)
+constexpr int kAStages = 4;                 // tensor-memory A stages (dequant -> MMA)
 constexpr int kEpiWarps = 4, kProducerWarp = 4, kMmaWarp = 5, kDeqWarp0 = 6, kDeqWarps = 8;
 constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 448
+constexpr int kClusterSize = 2;             // CTA pairs share (multicast) each token tile
 constexpr uint32_t kXBytes = BN * BK * 2;   // 24 KB bf16 token tile
 constexpr uint32_t kQBytes = BM * BK;       // 8 KB int8 codes
 constexpr uint32_t kSBytes = BM * 2 * 2;    // 512 B: 2 scale blocks x 128 rows
@@ -52,7 +54,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCols = BN;           // one fp32 accumulator: 128 lanes x 192 columns
 constexpr uint32_t kACol0 = 2 * kAccCols;   // A stages after the two accumulators
 constexpr uint32_t kACols = BK / 2;         // 64 bf16 per row = 32 columns per stage
-static_assert(kACol0 + kStages * kACols <= kTmemCols, "tensor memory budget");
+static_assert(kACol0 + kAStages * kACols <= kTmemCols, "tensor memory budget");
 static_assert(BN % kXBox == 0 && BN % 16 == 0 && BN <= 256, "token tile");
 
 enum Epi { kEpiSwiGLU = 0, kEpiDownScale = 1 };
@@ -105,6 +107,37 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
+// The same box delivered to this CTA and its cluster peer (same shared-memory
+// offsets), completion counted on each CTA's barrier at bar's offset.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
+                                               uint16_t cta_mask) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
+      "{%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(cta_mask)
+      : "memory");
+}
+
+// Arrive on the barrier at bar's offset in every CTA of cta_mask once this
+// thread's earlier MMAs have completed.
+__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+          smem_u32(bar)),
+      "h"(cta_mask)
+      : "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -129,13 +162,15 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-// 16 consecutive 32-bit columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+// 32 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
-          taddr),
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
       "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
-      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+      "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]),
+      "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]),
+      "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
 
@@ -166,15 +201,13 @@ __device__ __forceinline__ uint32_t deq_pair_bf16(uint32_t bits_lo, uint32_t bit
   return r;
 }
 
-__device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
-
 // ------------------------------------------------------------- the GEMM
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_s, GemmArgs a) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full[kStages], a_full[kStages], empty[kStages];
+  __shared__ __align__(8) uint64_t full[kStages], empty[kStages], a_full[kAStages], a_empty[kAStages];
   __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], mma_done;
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
@@ -189,8 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&a_full[i], kDeqWarps);
-      mbar_init(&empty[i], 1);
+      mbar_init(&empty[i], kClusterSize);  // both CTAs' MMAs read the multicast token tile
+    }
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(&a_full[i], kDeqWarps / 2);  // one group of four warps per stage
+      mbar_init(&a_empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
@@ -208,10 +244,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // the peer's barriers are initialised before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem_base = s_tmem;
+  const uint32_t crank = cluster_ctarank();
+  const uint16_t kPair = (1u << kClusterSize) - 1u;
 
-  const int n_tiles = a.meta->n_mtiles * a.n_mb;
+  // tiles per cluster: (token tile, pair of 128-row blocks), CTA rank r takes
+  // block 2 p + r (a block past the matrix runs but stores nothing)
+  const int n_mb2 = (a.n_mb + kClusterSize - 1) / kClusterSize;
+  const int n_tiles = a.meta->n_mtiles * n_mb2;
+  const int cid = blockIdx.x / kClusterSize, ncl = gridDim.x / kClusterSize;
   const int KT = a.K / BK;
   const int nb = a.K / 32;  // scale blocks per weight row
   bool ok = true;
@@ -226,17 +269,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const int4 mi = a.minfo[tile / a.n_mb];
-        const int m0 = (tile % a.n_mb) * BM;
+      for (int tile = cid; tile < n_tiles && ok; tile += ncl) {
+        const int4 mi = a.minfo[tile / n_mb2];
+        const int m0 = ((tile % n_mb2) * kClusterSize + (int)crank) * BM;
         const int nx = (mi.z + kXBox - 1) / kXBox;
         for (int kb = 0; kb < KT && ok; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
           if (!(ok = wait(&empty[s], ph ^ 1))) break;
           mbar_arrive_expect_tx(&full[s], (uint32_t)nx * kXBox * BK * 2 + kQBytes + kSBytes);
-          for (int x = 0; x < nx; ++x)
-            tma_load_2d(sX + s * kXBytes + x * kXBox * 128, &map_b, kb * BK, mi.y + x * kXBox, &full[s]);
+          for (int x = (int)crank; x < nx; x += kClusterSize)  // half the boxes each, to both CTAs
+            tma_load_2d_mc(sX + s * kXBytes + x * kXBox * 128, &map_b, kb * BK, mi.y + x * kXBox, &full[s], kPair);
           tma_load_2d(sQ + s * kQBytes, &map_q, kb * BK, mi.x * a.prows + m0, &full[s]);
           tma_load_2d(sS + s * kSBytes, &map_s, m0, mi.x * nb + kb * 2, &full[s]);
         }
@@ -248,8 +291,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t it = 0, tc = 0;
-      for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
-        const int4 mi = a.minfo[tile / a.n_mb];
+      for (int tile = cid; tile < n_tiles && ok; tile += ncl, ++tc) {
+        const int4 mi = a.minfo[tile / n_mb2];
         const int n_mma = (mi.z + 15) / 16 * 16;
         const uint32_t idesc = idesc_bf16(BM, n_mma);
         const int b = tc & 1;
@@ -257,17 +300,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + b * kAccCols;
         for (int kb = 0; kb < KT; ++kb, ++it) {
-          const int s = it % kStages;
-          const uint32_t ph = (it / kStages) & 1;
-          if (!(ok = wait(&full[s], ph))) break;
-          if (!(ok = wait(&a_full[s], ph))) break;
+          const int s = it % kStages, sa = it % kAStages;
+          if (!(ok = wait(&full[s], (it / kStages) & 1))) break;
+          if (!(ok = wait(&a_full[sa], (it / kAStages) & 1))) break;
           tc_fence_after();
           const uint32_t b0 = smem_u32(sX + s * kXBytes);
-          const uint32_t a0 = tmem_base + kACol0 + s * kACols;
+          const uint32_t a0 = tmem_base + kACol0 + sa * kACols;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)
             mma_tmem_a(d_tmem, a0 + k * 8, sw128_desc(b0 + k * 32), idesc, (kb | k) != 0);
-          mma_commit(&empty[s]);
+          mma_commit_mc(&empty[s], kPair);
+          mma_commit(&a_empty[sa]);
         }
         if (ok) mma_commit(&acc_full[b]);
       }
@@ -277,49 +320,55 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kDeqWarp0) {
     // ------------------------------------------------ dequantisers: int8 x scale -> bf16 -> TMEM (A)
-    const int quarter = warp & 3, half = (warp - kDeqWarp0) >> 2;
+    // Two groups of four warps (one per TMEM lane quarter) take alternate
+    // stages, so the conversion of one stage overlaps the next; a thread
+    // converts the 64 codes (two Q8_0 blocks) of its row.
+    const int quarter = warp & 3, group = (warp - kDeqWarp0) >> 2;
     const int r = quarter * 32 + lane;  // weight row of the tile = TMEM lane
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
     const f2 bias = f2_pack(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+    const int sw = (r >> 1) & 3;                        // 64-byte swizzle of this row
     uint32_t it = 0;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+    for (int tile = cid; tile < n_tiles && ok; tile += ncl) {
       for (int kb = 0; kb < KT && ok; ++kb, ++it) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
-        // full[s] also means the MMAs that last read A stage s have completed
-        // (the producer waited for them before refilling the stage)
-        if (!(ok = wait(&full[s], ph))) break;
-        // this thread's block: row r, codes [32 half, 32 half + 32) of the stage,
-        // 16-byte chunks 2 half and 2 half + 1, stored with the 64-byte swizzle
+        if ((int)(it & 1) != group) continue;
+        const int s = it % kStages, sa = it % kAStages;
+        if (!(ok = wait(&full[s], (it / kStages) & 1))) break;
+        // the MMAs that last read A stage sa have completed
+        if (!(ok = wait(&a_empty[sa], ((it / kAStages) & 1) ^ 1))) break;
         const uint8_t* qrow = sQ + s * kQBytes + r * 64;
-        const int sw = (r >> 1) & 3;
-        const uint4 c0 = *reinterpret_cast<const uint4*>(qrow + (((2 * half) ^ sw) << 4));
-        const uint4 c1 = *reinterpret_cast<const uint4*>(qrow + (((2 * half + 1) ^ sw) << 4));
-        const float d = half_bits_to_f32(reinterpret_cast<const uint16_t*>(sS + s * kSBytes)[half * BM + r]);
-        const f2 dd = f2_pack(d, d);
-        const uint32_t w8[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-        uint32_t out[16];
+        uint4 c[4];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const uint32_t w = w8[i];
-          out[2 * i] = deq_pair_bf16(__byte_perm(w, 0x4B000000u, 0x7650), __byte_perm(w, 0x4B000000u, 0x7651), bias,
-                                     dd);
-          out[2 * i + 1] = deq_pair_bf16(__byte_perm(w, 0x4B000000u, 0x7652), __byte_perm(w, 0x4B000000u, 0x7653),
-                                         bias, dd);
+        for (int q = 0; q < 4; ++q) c[q] = *reinterpret_cast<const uint4*>(qrow + ((q ^ sw) << 4));
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(sS + s * kSBytes);
+        const float d0 = half_bits_to_f32(sc[r]), d1 = half_bits_to_f32(sc[BM + r]);
+        uint32_t out[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const f2 dd = q < 2 ? f2_pack(d0, d0) : f2_pack(d1, d1);
+          const uint32_t w4[4] = {c[q].x, c[q].y, c[q].z, c[q].w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint32_t w = w4[i];
+            out[8 * q + 2 * i] = deq_pair_bf16(__byte_perm(w, 0x4B000000u, 0x7650), __byte_perm(w, 0x4B000000u, 0x7651),
+                                               bias, dd);
+            out[8 * q + 2 * i + 1] = deq_pair_bf16(__byte_perm(w, 0x4B000000u, 0x7652),
+                                                   __byte_perm(w, 0x4B000000u, 0x7653), bias, dd);
+          }
         }
-        tmem_st16(tmem_base + lane_addr + kACol0 + s * kACols + half * 16, out);
+        tmem_st32(tmem_base + lane_addr + kACol0 + sa * kACols, out);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&a_full[s]);
+        if (lane == 0) mbar_arrive(&a_full[sa]);
       }
     }
   } else {
     // ------------------------------------------------ epilogue: TMEM -> registers -> global
     uint32_t tc = 0;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x, ++tc) {
-      const int4 mi = a.minfo[tile / a.n_mb];
-      const int m0 = (tile % a.n_mb) * BM;
+    for (int tile = cid; tile < n_tiles && ok; tile += ncl, ++tc) {
+      const int4 mi = a.minfo[tile / n_mb2];
+      const int m0 = ((tile % n_mb2) * kClusterSize + (int)crank) * BM;
       const int b = tc & 1;
       if (!(ok = wait(&acc_full[b], (tc >> 1) & 1))) break;
       tc_fence_after();
@@ -367,6 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // no multicast copy or commit of the peer still targets this CTA
   tc_fence_after();
   if (warp == kMmaWarp)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
@@ -441,6 +491,34 @@ unsigned grid_for(int64_t n, int threads, int cap) {
   return (unsigned)(g < 1 ? 1 : g);
 }
 
+
+
+int g_max_clusters = 0;  // CTA pairs of the GEMM resident at once
+
+template <int EPI>
+cudaLaunchConfig_t gemm_config(unsigned grid, cudaStream_t s, cudaLaunchAttribute* attr) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kClusterSize;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cfg;
+}
+
+template <int EPI>
+cudaError_t launch_gemm(const CUtensorMap& mb, const CUtensorMap& mq, const CUtensorMap& ms, const GemmArgs& g,
+                        unsigned grid, cudaStream_t s) {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = gemm_config<EPI>(grid, s, attr);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<EPI>, mb, mq, ms, g);
+}
+
 }  // namespace
 
 cudaError_t configure_prefill_kernels() {
@@ -453,6 +531,13 @@ cudaError_t configure_prefill_kernels() {
   }
   cudaError_t e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiSwiGLU>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDownScale>);
+  if (e == cudaSuccess && g_max_clusters == 0) {
+    cudaLaunchAttribute attr[1];
+    cudaLaunchConfig_t cfg = gemm_config<kEpiSwiGLU>(kClusterSize, 0, attr);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<kEpiSwiGLU>, &cfg);
+    if (e == cudaSuccess) g_max_clusters = n > 0 ? n : 1;
+  }
   return e;
 }
 
@@ -490,6 +575,7 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
     gather_rows_kernel<<<grid_for((int64_t)rows * (H / 8), 256, h->num_sms * 8), 256, 0, s>>>(x, h->row_token, rows,
                                                                                             H, h->xperm);
   }
+  const unsigned grid = (unsigned)std::min(h->num_sms / kClusterSize, g_max_clusters) * kClusterSize;
   GemmArgs g;
   g.minfo = h->minfo;
   g.meta = h->meta;
@@ -501,8 +587,7 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
     g.n_mb = (2 * I + BM - 1) / BM;
     g.out_cols = I;
     KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP, s);
-    grouped_gemm_kernel<kEpiSwiGLU><<<h->num_sms, kThreads, kSmemBytes, s>>>(h->maps->a_x, h->maps->q_gu,
-                                                                             h->maps->s_gu, g);
+    err = launch_gemm<kEpiSwiGLU>(h->maps->a_x, h->maps->q_gu, h->maps->s_gu, g, grid, s);
   }
   {
     g.outp = h->yp;
@@ -511,16 +596,15 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
     g.n_mb = (H + BM - 1) / BM;
     g.out_cols = H;
     KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN, s);
-    grouped_gemm_kernel<kEpiDownScale><<<h->num_sms, kThreads, kSmemBytes, s>>>(h->maps->a_h, h->maps->q_d,
-                                                                                h->maps->s_d, g);
+    if (err == cudaSuccess) err = launch_gemm<kEpiDownScale>(h->maps->a_h, h->maps->q_d, h->maps->s_d, g, grid, s);
   }
+  if (err != cudaSuccess) return err;
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_COMBINE, s);
     combine_kernel<<<grid_for((int64_t)T * (H / 8), 256, h->num_sms * 8), 256, 0, s>>>(h->yp, h->inv, T, k, S, H,
                                                                                      out);
   }
-  err = cudaGetLastError();
-  return err;
+  return cudaGetLastError();
 }
 
 }  // namespace fw

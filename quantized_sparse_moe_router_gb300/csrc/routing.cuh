@@ -67,86 +67,101 @@ struct SmemRouting {
   float z[kMaxDecodeT * kMaxE];  // the batch's logits
   float zsel[kMaxDecodeT * kMaxK];  // selected logits, in rank order
   int ids[kMaxDecodeT * kMaxK];
-  float gates[kMaxDecodeT * kMaxK];
+  float gates[kMaxDecodeT * (kMaxK + 1)];  // by slot; slot T k + t is token t's shared expert (1)
   int cnt[kMaxE + 2];     // per-expert counts (cnt[E] = T for the shared expert)
   int off[kMaxE + 2];     // exclusive offsets (off[EU] = rows)
   uint32_t mask[kMaxE + 1];  // per expert: bit t set when token t selected it
   int4 u[kMaxE + 1];      // (expert, first row, rows, 0) of experts with rows, ascending
   int tok[kMaxRowsDecode];
-  float rg[kMaxRowsDecode];
-  int slot[kMaxRowsDecode];  // grouped row -> slot id (perm)
+  int slot[kMaxRowsDecode];  // grouped row -> slot id (perm); its gate is gates[slot]
   int n_unique;
   int rows;
 };
 
 // Whole block (NT threads): selection for T <= 16 tokens from logits [T][E]
-// (global, written by an earlier kernel), gates, and the grouping. Selection
-// is by rank: every (token, expert) pair counts the logits that come before
-// it (larger, or equal with a lower id), split over a group of s lanes; ranks
-// below k are the top-k in order. Each step is short and latency-bound (a few
-// hundred cycles): four block barriers, the last of which leaves every field
-// valid.
+// (global, written by an earlier kernel), gates, and the grouping. Three
+// block barriers; after the last one every field is valid.
+//
+// Selection: when T E is small (at least 4 lanes per pair), by rank -- every
+// (token, expert) pair counts, split over a group of lanes, the logits that
+// come before it (larger, or equal with a lower id); ranks below k are the
+// top-k in order. Otherwise one warp per token takes the k largest in turn
+// (warp_topk). Then warp 0 alone groups the pairs (counts, offsets, the
+// table of touched experts, positions) while other warps make the gates.
 template <int NT>
 __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, SmemRouting& r) {
-  static_assert(NT % 32 == 0, "whole warps");
+  static_assert(NT % 32 == 0 && NT >= 64, "whole warps, at least two");
   constexpr int NW = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int EU = E + S;
-  for (int i = tid; i < T * E; i += NT) r.z[i] = __ldcg(logits + i);
+  const int P = T * E;
+  const bool by_rank = 4 * P <= NT;
+  if (by_rank)
+    for (int i = tid; i < P; i += NT) r.z[i] = __ldcg(logits + i);
   for (int i = tid; i < EU; i += NT) {
     r.cnt[i] = 0;
     r.mask[i] = 0;
   }
   __syncthreads();
 
-  // ranks: s lanes per pair (s a power of two, as many as the block allows);
-  // lane c of a group compares f = c, c + s, ... (same-c lanes read the same
-  // word, distinct c consecutive words: no bank conflicts)
-  const int P = T * E;
-  int s = 32;
-  while (s > 1 && P * s > NT) s >>= 1;
-  const int gpw = 32 / s, c = lane & (s - 1);
-  for (int b = warp * gpw; b < P; b += NW * gpw) {  // warp-uniform trip count
-    const int p = b + lane / s;
-    int rank = 0, t = 0, e = 0;
-    float z = 0.f;
-    if (p < P) {
-      t = p / E;
-      e = p - t * E;
-      const float* zt = r.z + t * E;
-      z = zt[e];
+  if (by_rank) {
+    // s lanes per pair (a power of two, as many as the block allows); lane c
+    // of a group compares f = c, c + s, ... (same-c lanes read the same word,
+    // distinct c consecutive words: no bank conflicts)
+    int s = 32;
+    while (s > 1 && P * s > NT) s >>= 1;
+    const int gpw = 32 / s, c = lane & (s - 1);
+    for (int b = warp * gpw; b < P; b += NW * gpw) {  // warp-uniform trip count
+      const int p = b + lane / s;
+      int rank = 0, t = 0, e = 0;
+      float z = 0.f;
+      if (p < P) {
+        t = p / E;
+        e = p - t * E;
+        const float* zt = r.z + t * E;
+        z = zt[e];
 #pragma unroll 4
-      for (int f = c; f < E; f += s) {
-        const float zf = zt[f];
-        rank += (zf > z) | ((zf == z) & (f < e));
+        for (int f = c; f < E; f += s) {
+          const float zf = zt[f];
+          rank += (zf > z) | ((zf == z) & (f < e));
+        }
+      }
+      for (int o = 1; o < s; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+      if (p < P && c == 0 && rank < k) {
+        r.ids[t * k + rank] = e;
+        r.zsel[t * k + rank] = z;
       }
     }
-    for (int o = 1; o < s; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
-    if (p < P && c == 0 && rank < k) {
-      r.ids[t * k + rank] = e;
-      r.zsel[t * k + rank] = z;
+  } else {
+    for (int t = warp; t < T; t += NW) {
+      float zl[kMaxEPerLane];
+#pragma unroll
+      for (int m = 0; m < kMaxEPerLane; ++m) {
+        const int e = lane + 32 * m;
+        zl[m] = e < E ? __ldcg(logits + t * E + e) : -INFINITY;
+      }
+      int id;
+      float zv;
+      warp_topk(zl, E, k, lane, &id, &zv);
+      const float g = warp_gate(zv, k, lane);
+      if (lane < k) {
+        r.ids[t * k + lane] = id;
+        r.gates[t * k + lane] = g;
+      }
     }
   }
   __syncthreads();
 
-  // gates (one warp per token) and per-expert counts / token masks
-  for (int t = warp; t < T; t += NW) {
-    const float zj = lane < k ? r.zsel[t * k + lane] : 0.f;
-    const float g = warp_gate(zj, k, lane);
-    if (lane < k) r.gates[t * k + lane] = g;
-  }
-  for (int p = tid; p < T * k; p += NT) {
-    const int ee = r.ids[p];
-    atomicAdd(&r.cnt[ee], 1);
-    atomicOr(&r.mask[ee], 1u << (p / k));
-  }
-  if (S && tid == 0) r.cnt[E] = T;
-  __syncthreads();
-
-  // one warp: offsets and the table of touched experts. Lane l owns the
-  // consecutive experts [l * per, l * per + per), held in registers; both
-  // scans (rows and touched experts) in one pass of shuffles.
   if (warp == 0) {
+    for (int p = lane; p < T * k; p += 32) {
+      const int ee = r.ids[p];
+      atomicAdd(&r.cnt[ee], 1);
+      atomicOr(&r.mask[ee], 1u << (p / k));
+    }
+    if (S && lane == 0) r.cnt[E] = T;
+    __syncwarp();
+    // lane l owns the consecutive experts [l per, l per + per), in registers;
+    // both scans (rows and touched experts) in one pass of shuffles
     constexpr int kPer = (kMaxE + 1 + 31) / 32;
     const int per = (EU + 31) / 32, b0 = lane * per;
     int cn[kPer];
@@ -182,24 +197,28 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
       r.rows = ic;
       r.n_unique = in;
     }
-  }
-  __syncthreads();
-
-  // grouped positions: within an expert, ascending token
-  for (int p = tid; p < T * k; p += NT) {
-    const int t = p / k, ee = r.ids[p];
-    const int pos = r.off[ee] + __popc(r.mask[ee] & ((1u << t) - 1u));
-    r.tok[pos] = t;
-    r.rg[pos] = r.gates[p];
-    r.slot[pos] = p;
-  }
-  if (S)
-    for (int t = tid; t < T; t += NT) {
-      const int pos = r.off[E] + t;
+    __syncwarp();
+    // grouped positions: within an expert, ascending token
+    for (int p = lane; p < T * k; p += 32) {
+      const int t = p / k, ee = r.ids[p];
+      const int pos = r.off[ee] + __popc(r.mask[ee] & ((1u << t) - 1u));
       r.tok[pos] = t;
-      r.rg[pos] = 1.0f;
-      r.slot[pos] = T * k + t;
+      r.slot[pos] = p;
     }
+    if (S)
+      for (int t = lane; t < T; t += 32) {
+        const int pos = r.off[E] + t;
+        r.tok[pos] = t;
+        r.slot[pos] = T * k + t;
+        r.gates[T * k + t] = 1.0f;
+      }
+  } else if (by_rank) {
+    for (int t = warp - 1; t < T; t += NW - 1) {
+      const float zj = lane < k ? r.zsel[t * k + lane] : 0.f;
+      const float g = warp_gate(zj, k, lane);
+      if (lane < k) r.gates[t * k + lane] = g;
+    }
+  }
   __syncthreads();
 }
 
@@ -234,7 +253,7 @@ __device__ void publish_routing(const SmemRouting& r, int T, int E, int k, int S
     o.perm[pos] = r.slot[pos];
     o.inv[r.slot[pos]] = pos;
     o.row_token[pos] = r.tok[pos];
-    o.row_gate[pos] = r.rg[pos];
+    o.row_gate[pos] = r.gates[r.slot[pos]];
   }
   for (int i = tid; i < r.n_unique; i += NT) o.uinfo[i] = r.u[i];
   if (tid == 0) {
