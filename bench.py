@@ -18,8 +18,10 @@ bounded sample of the same workload (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -75,6 +77,39 @@ def load_peaks():
             d = json.load(f)
         return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained", d["bf16_tflops"]), "measured"
     return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# Source files each timed kernel is built from: a profile summary under
+# profiles/ records their hash, and its DRAM traffic is reported only while
+# the kernel is unchanged since the counters were taken.
+KERNEL_SOURCES = {
+    "decode_experts": ("decode.cu", "routing.cuh", "internal.cuh"),
+    "prefill_gateup": ("prefill.cu", "internal.cuh"),
+}
+
+
+def kernel_source_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "quantized_sparse_moe_router_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch (read + write) of `kernel` from the committed ncu
+    summary profiles/<kernel>_<workload>.md, or None when there is none or it
+    was taken on other source."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if kernel not in KERNEL_SOURCES or not os.path.exists(path):
+        return None
+    with open(path) as f:
+        txt = f.read()
+    m = re.search(r"^traffic_bytes_per_launch:\s*([0-9.]+)\s*$", txt, re.M)
+    h = re.search(r"^source_sha256:\s*([0-9a-f]{64})\s*$", txt, re.M)
+    if not m or not h or h.group(1) != kernel_source_hash(kernel):
+        return None
+    return float(m.group(1))
 
 
 # ------------------------------------------------------------------ clocks
@@ -277,7 +312,7 @@ def run_fw(args, rank, world, local_rank):
         dom_ms, dom_n = prof[dom]
         achieved = dom_bytes / (dom_ms / 1e3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                    "frac": round(achieved / hbm, 4), "traffic": None, "kernel": dom,
+                    "frac": round(achieved / hbm, 4), "traffic": measured_traffic(dom, w.name), "kernel": dom,
                     "avg_launch_us": round(dom_ms / dom_n * 1e3, 3),
                     "algorithmic_bytes_per_launch": round(dom_bytes / dom_n),
                     "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"}
@@ -287,7 +322,7 @@ def run_fw(args, rank, world, local_rank):
         fl = work["flops"] * 2 / 3
         achieved = fl / (dom_ms / 1e3) / 1e12
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16_burst, "unit": "TFLOP/s",
-                    "frac": round(achieved / bf16_burst, 4), "traffic": None, "kernel": dom,
+                    "frac": round(achieved / bf16_burst, 4), "traffic": measured_traffic(dom, w.name), "kernel": dom,
                     "peak_source": f"{peak_src} bf16_tflops (cuBLAS burst)"}
     step_bytes = work["bytes"] / args.steps
     whole = {"algorithmic_GBps": round(step_bytes / (ms / args.steps / 1e3) / 1e9, 1),

@@ -160,12 +160,17 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
 __host__ __device__ inline uint32_t align128(uint32_t v) { return (v + 127) / 128 * 128; }
 
 // ------------------------------------------------------------- the kernel
+// kOne: the single-token instantiation (T = 1, x in shared memory as fp32):
+// its hot code is the T = 1 paths only, which keeps it small for the
+// instruction cache.
+template <bool kOne>
 __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
   __shared__ SmemRouting r;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = a.H, I = a.I, T = a.T, R = a.R;
+  const int H = a.H, I = a.I, T = kOne ? 1 : a.T, R = a.R;
+  const int x_mode = kOne ? (int)kXSmemF32 : a.x_mode;
   const uint32_t rb_h = (uint32_t)row_bytes(H), rb_i = (uint32_t)row_bytes(I);
   uint8_t* ring = smem + align128(a.act_bytes);
   if (tid == 0) {
@@ -241,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
     // ------------------------------------------------------ consumers
     bool ok = true;
     // x for this batch, segment-transposed: fp32 or bf16 in shared memory, else read from global
-    if (a.x_mode == kXSmemF32) {
+    if (x_mode == kXSmemF32) {
       float* xs = reinterpret_cast<float*>(smem);
       for (int c = tid; c < T * H / 8; c += kCW * 32) {  // c: 8 bf16 = half a segment
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x) + c);
@@ -255,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
         *reinterpret_cast<float4*>(base + (2 * half) * (H / 4)) = lo4;
         *reinterpret_cast<float4*>(base + (2 * half + 1) * (H / 4)) = hi4;
       }
-    } else if (a.x_mode == kXSmemBf16) {
+    } else if (x_mode == kXSmemBf16) {
       __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);
       for (int c = tid; c < T * H / 8; c += kCW * 32) {
         const int t = c / (H / 8), cc = c % (H / 8), seg = cc >> 1, half = cc & 1;
@@ -289,9 +294,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
         const int4 ui = r.u[g / I];
         const int i = (int)(g % I);
         auto load_x = [&](int t, int seg, f2(&xv)[8]) {
-          if (a.x_mode == kXSmemF32) {
+          if (x_mode == kXSmemF32) {
             x16_from_f32_t(reinterpret_cast<const float*>(smem) + (size_t)t * H, H, seg, xv);
-          } else if (a.x_mode == kXSmemBf16) {
+          } else if (x_mode == kXSmemBf16) {
             const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(smem) + (size_t)t * H;
             x16_from_bf16(*reinterpret_cast<const uint4*>(xb + seg * 8), *reinterpret_cast<const uint4*>(xb + H / 2 + seg * 8),
                           xv);
@@ -497,7 +502,8 @@ cudaError_t launch(const DecodeArgs& a, unsigned grid, size_t smem, cudaStream_t
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_experts_kernel, a);
+  return a.T == 1 && a.x_mode == kXSmemF32 ? cudaLaunchKernelEx(&cfg, decode_experts_kernel<true>, a)
+                                           : cudaLaunchKernelEx(&cfg, decode_experts_kernel<false>, a);
 }
 
 int g_smem_optin = 0;
@@ -511,11 +517,13 @@ cudaError_t configure_decode_kernels() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   cudaFuncAttributes fa;
-  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, decode_experts_kernel);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, decode_experts_kernel<false>);
   if (e == cudaSuccess) {
     g_smem_optin -= (int)fa.sharedSizeBytes;
-    e = cudaFuncSetAttribute(decode_experts_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_optin);
+    e = cudaFuncSetAttribute(decode_experts_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_optin);
   }
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_experts_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_optin);
   return e;
 }
 

@@ -238,12 +238,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 }
 
 // Bounded wait for the phase with the given parity to complete. false = gave up.
+// A short wait polls; past about a microsecond the thread also sleeps between
+// polls, so that warps parked on a barrier for long leave the issue slots to
+// the working ones.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
+  const long long c0 = clock64();
   const uint64_t t0 = globaltimer_ns();
-  for (;;) {
+  for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait_sleep(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    if (clock64() - c0 > 2048) __nanosleep(64);
+    if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
 }
 

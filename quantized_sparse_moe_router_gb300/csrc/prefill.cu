@@ -40,7 +40,7 @@ using namespace dev;
 
 constexpr int BM = 128, BK = 64;
 constexpr int BN = kTokTile;                // tokens per tile (N <= 192)
-constexpr int kXBox = 64;                   // token rows per TMA box
+constexpr int kXBox = 96;                   // token rows per TMA box (one per CTA of the pair)
 constexpr int kStages = 6;                  // shared-memory stages (TMA -> dequant / MMA)
 constexpr int kAStages = 4;                 // tensor-memory A stages (dequant -> MMA)
 constexpr int kEpiWarps = 4, kProducerWarp = 4, kMmaWarp = 5, kDeqWarp0 = 6, kDeqWarps = 8;
@@ -55,7 +55,8 @@ constexpr uint32_t kAccCols = BN;           // one fp32 accumulator: 128 lanes x
 constexpr uint32_t kACol0 = 2 * kAccCols;   // A stages after the two accumulators
 constexpr uint32_t kACols = BK / 2;         // 64 bf16 per row = 32 columns per stage
 static_assert(kACol0 + kAStages * kACols <= kTmemCols, "tensor memory budget");
-static_assert(BN % kXBox == 0 && BN % 16 == 0 && BN <= 256, "token tile");
+static_assert(BN % kXBox == 0 && BN % 16 == 0 && BN <= 256 && kXBox % 8 == 0, "token tile");
+static_assert(kStages % 2 == 0 && kAStages % 2 == 0, "the two dequantising groups own alternate stages");
 
 enum Epi { kEpiSwiGLU = 0, kEpiDownScale = 1 };
 
@@ -269,10 +270,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0;
+      int4 mi_next = cid < n_tiles ? a.minfo[cid / n_mb2] : make_int4(0, 0, 0, 0);
       for (int tile = cid; tile < n_tiles && ok; tile += ncl) {
-        const int4 mi = a.minfo[tile / n_mb2];
+        const int4 mi = mi_next;
         const int m0 = ((tile % n_mb2) * kClusterSize + (int)crank) * BM;
         const int nx = (mi.z + kXBox - 1) / kXBox;
+        if (tile + ncl < n_tiles) mi_next = a.minfo[(tile + ncl) / n_mb2];  // in flight during this tile
         for (int kb = 0; kb < KT && ok; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
@@ -291,8 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       uint32_t it = 0, tc = 0;
+      int4 mi_next = cid < n_tiles ? a.minfo[cid / n_mb2] : make_int4(0, 0, 0, 0);
       for (int tile = cid; tile < n_tiles && ok; tile += ncl, ++tc) {
-        const int4 mi = a.minfo[tile / n_mb2];
+        const int4 mi = mi_next;
+        if (tile + ncl < n_tiles) mi_next = a.minfo[(tile + ncl) / n_mb2];
         const int n_mma = (mi.z + 15) / 16 * 16;
         const uint32_t idesc = idesc_bf16(BM, n_mma);
         const int b = tc & 1;
@@ -366,8 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------ epilogue: TMEM -> registers -> global
     uint32_t tc = 0;
+    int4 mi_next = cid < n_tiles ? a.minfo[cid / n_mb2] : make_int4(0, 0, 0, 0);
     for (int tile = cid; tile < n_tiles && ok; tile += ncl, ++tc) {
-      const int4 mi = a.minfo[tile / n_mb2];
+      const int4 mi = mi_next;
+      if (tile + ncl < n_tiles) mi_next = a.minfo[(tile + ncl) / n_mb2];
       const int m0 = ((tile % n_mb2) * kClusterSize + (int)crank) * BM;
       const int b = tc & 1;
       if (!(ok = wait(&acc_full[b], (tc >> 1) & 1))) break;
