@@ -37,7 +37,7 @@ constexpr int kThreads = (kCW + 1) * 32;   // + one producer warp
 constexpr int kProducer = kCW;
 constexpr int kMaxStages = 16;
 constexpr int kRowBlock = 16;              // output rows per W_down block
-constexpr int kMaxPer = 4;                 // experts' blocks per W_down stage
+constexpr int kMaxPer = 2;                 // experts' blocks per W_down stage
 constexpr uint32_t kConsumerBarrier = 1;   // named barrier of the 16 consumer warps
 constexpr int64_t kL2PrefetchMax = 40ll << 20;  // W_down bytes per call prefetched into L2 (L2 is 129 MB)
 

@@ -240,9 +240,9 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // Bounded wait for the phase with the given parity to complete. false = gave up.
 // A short wait polls; past about a microsecond the thread also sleeps between
 // polls, so that warps parked on a barrier for long leave the issue slots to
-// the working ones.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  if (mbar_try_wait(bar, parity)) return true;
+// the working ones. Only the first poll is inlined at each call site (code
+// size: these kernels are sensitive to instruction-cache misses).
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t* bar, uint32_t parity) {
   const long long c0 = clock64();
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t i = 1;; ++i) {
@@ -250,6 +250,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if (clock64() - c0 > 2048) __nanosleep(64);
     if ((i & 63u) == 0 && globaltimer_ns() - t0 > kWaitLimitNs) return false;
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity);
 }
 
 // One bulk asynchronous copy global -> shared (16-byte aligned, size % 16 == 0),
@@ -315,7 +320,7 @@ enum WaitSite {
   kSiteGemm = 7, kSiteGrid = 8
 };
 
-__device__ __forceinline__ void report_wait(Meta* m, int site, int64_t stage, int detail) {
+static __device__ __noinline__ void report_wait(Meta* m, int site, int64_t stage, int detail) {
   if (atomicCAS(&m->diag[0], 0, site) == 0) {
     m->diag[1] = blockIdx.x;
     m->diag[2] = (int32_t)stage;
