@@ -66,7 +66,7 @@ struct Allocator {
 };
 
 void free_handle_memory(Handle* h) {
-  void* ptrs[] = {h->q_gu, h->st_gu, h->q_d, h->st_d, h->wr, h->bias, h->ids, h->gates,
+  void* ptrs[] = {h->q_gu, h->st_gu, h->q_d, h->st_d, h->wr3, h->wr, h->bias, h->ids, h->gates,
                   h->logits, h->counts, h->offsets, h->perm, h->inv, h->row_token, h->row_gate, h->uinfo,
                   h->hist, h->minfo, h->xperm, h->hbuf, h->yp, h->meta, h->x_dev, h->out_dev, h->ids_dev};
   for (void* p : ptrs)
@@ -156,6 +156,7 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
       {(void**)&h->st_d, (size_t)(EU * (I / 32) * H * 2)},
       {(void**)&h->wr, (size_t)(E * H * 4)},
       {(void**)&h->bias, (size_t)(E * 4)},
+      {(void**)&h->wr3, (size_t)(Tm > decode_limit(h) ? 3 * E * H * 2 : 256)},
       {(void**)&h->ids, (size_t)(Tm * k * 4)},
       {(void**)&h->gates, (size_t)(Tm * k * 4)},
       {(void**)&h->logits, (size_t)(std::min<int64_t>(Tm, kMaxDecodeT) * E * 4)},
@@ -206,6 +207,7 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
     // rows past the valid ones of a tile are read (and masked); keep them finite
     e = cudaMemsetAsync(h->xperm, 0, (size_t)h->rows_max * H * 2, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->hbuf, 0, hbuf_bytes, s);
+    if (e == cudaSuccess) e = launch_split_router(h, s);
     if (e == cudaSuccess) e = prepare_prefill(h);
   }
   if (e == cudaSuccess) e = cudaStreamSynchronize(s);

@@ -38,6 +38,7 @@ constexpr int kProducer = kCW;
 constexpr int kMaxStages = 16;
 constexpr int kRowBlock = 16;              // output rows per W_down block
 constexpr int kMaxPer = 2;                 // experts' blocks per W_down stage
+constexpr int kStaticChunks = 2;           // gate/up chunks per CTA assigned without a ticket
 constexpr uint32_t kConsumerBarrier = 1;   // named barrier of the 16 consumer warps
 constexpr int64_t kL2PrefetchMax = 40ll << 20;  // W_down bytes per call prefetched into L2 (L2 is 129 MB)
 
@@ -168,6 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
   __shared__ SmemRouting r;
+  __shared__ int2 stage_units[kMaxStages];  // gate/up units [x, y) held by each ring stage (x < 0: no more)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = a.H, I = a.I, T = kOne ? 1 : a.T, R = a.R;
   const int x_mode = kOne ? (int)kXSmemF32 : a.x_mode;
@@ -185,13 +187,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   if (a.publish && blockIdx.x == 0) publish_routing<kThreads>(r, T, a.E, a.k, a.S, a.ro);
 
   const int nU = r.n_unique;
-  // gate/up stages: units [lo, hi) of the nU x I unit space, R consecutive per stage
-  // (a CTA's range starts and ends on a kGUGroup boundary: every stage is
-  // then one run of consecutive interleaved rows, fetched with one copy)
-  const int64_t n_grp = (int64_t)nU * I / kGUGroup;
+  // gate/up work, in stages of at most R consecutive units of the nU x I unit
+  // space (never across an expert, since R divides I: a stage is one run of
+  // consecutive interleaved rows of one expert, one copy).
+  //  * one token: the units are split evenly, each CTA a contiguous range
+  //    starting and ending on a kGUGroup boundary (every unit costs the same);
+  //  * several tokens: the cost of a unit is its expert's token count, so
+  //    R-unit chunks are handed out -- CTA b's first kStaticChunks are b,
+  //    b + grid, ..., the rest come from a ticket counter.
+  const int64_t n_units = (int64_t)nU * I;
+  const int64_t n_grp = n_units / kGUGroup;
   const int64_t lo = n_grp * blockIdx.x / gridDim.x * kGUGroup, hi = n_grp * (blockIdx.x + 1) / gridDim.x * kGUGroup;
-  const int64_t b0 = lo / R;
-  const int64_t n_gu = hi > lo ? (hi + R - 1) / R - b0 : 0;
   // down stages: output rows [o0, o1), blocks of 16 rows; per block every touched expert
   const int o0 = (int)((int64_t)H * blockIdx.x / gridDim.x), o1 = (int)((int64_t)H * (blockIdx.x + 1) / gridDim.x);
   // (a down stage holds the same 16-row block of up to n_per experts, so that
@@ -199,7 +205,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   const int n_blk = (o1 - o0 + kRowBlock - 1) / kRowBlock;
   const int n_ge = (nU + a.n_per - 1) / a.n_per;
   const int64_t n_dn = (int64_t)n_ge * n_blk;
-  const int64_t n_all = n_gu + n_dn;
 
   if (warp == kProducer) {
     // ------------------------------------------------------ producer
@@ -207,35 +212,65 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       // Once the ring is full of gate/up stages, ask L2 for all of this CTA's
       // W_down rows, so that they stream from HBM alongside gate/up instead
       // of after it -- when the call's W_down fits comfortably in L2.
-      const bool pf = (int64_t)nU * H * rb_i <= kL2PrefetchMax;
-      const int64_t pf_at = std::min<int64_t>(n_gu, a.stages);
-      int64_t j = 0;
-      for (; j < n_all; ++j) {
-        if (pf && j == pf_at)
+      bool pf = (int64_t)nU * H * rb_i <= kL2PrefetchMax;
+      // (several tokens) chunk of the current stage and of the next two: the
+      // ticket for the second is requested two stages ahead, so its round
+      // trip overlaps copies
+      int64_t j = 0, c = blockIdx.x, q0 = (int64_t)blockIdx.x + gridDim.x, q1 = 0;
+      if (!kOne) q1 = (int64_t)atomicAdd(&a.meta->chunk_ctr, 1u) + (int64_t)kStaticChunks * gridDim.x;
+      int64_t su = lo;  // (one token) next unit of the CTA's range
+      bool gu = true;   // still issuing gate/up stages
+      for (int64_t jd = 0; gu || jd < n_dn; ++j) {
+        if (pf && j == a.stages) {  // the ring is full: the TMA unit has time for it
+          pf = false;
           for (int u = 0; u < nU; ++u) {
             const int64_t row = (int64_t)r.u[u].x * H + o0;
             prefetch_l2(a.q_d + row * rb_i, (uint32_t)(o1 - o0) * rb_i);
           }
+        }
         const int st = (int)(j % a.stages);
         if (j >= a.stages && !mbar_wait(&empty[st], (uint32_t)(((j / a.stages) - 1) & 1))) {
-          report_wait(a.meta, kSiteGuEmpty, j, (int)n_all);
+          report_wait(a.meta, kSiteGuEmpty, j, (int)n_dn);
           break;
         }
         uint8_t* sb = ring + (size_t)st * a.stage_bytes;
-        if (j < n_gu) {
-          const int64_t u0 = std::max<int64_t>(lo, (b0 + j) * R), u1 = std::min<int64_t>(hi, (b0 + j + 1) * R);
+        if (gu) {
+          int64_t u0, u1;
+          if (kOne) {
+            u0 = su;
+            u1 = std::min<int64_t>(hi, (su / R + 1) * R);
+            su = u1;
+          } else {
+            u0 = c * R;
+            u1 = u0 + R;
+            c = q0;
+            q0 = q1;
+            q1 = (int64_t)atomicAdd(&a.meta->chunk_ctr, 1u) + (int64_t)kStaticChunks * gridDim.x;
+          }
+          if (u0 >= (kOne ? hi : n_units)) {
+            gu = false;
+            if (kOne) {  // the consumers know the count: go straight to the down stages
+              --j;
+              continue;
+            }
+            stage_units[st] = make_int2(-1, -1);  // ticketed work: an empty stage tells the consumers
+            mbar_arrive(&full[st]);
+            continue;
+          }
+          stage_units[st] = make_int2((int)u0, (int)u1);
           const int e = r.u[u0 / I].x, i0 = (int)(u0 % I);
           const uint32_t bytes = (uint32_t)(u1 - u0) * 2 * rb_h;
           mbar_arrive_expect_tx(&full[st], bytes);
           bulk_g2s(sb, a.q_gu + ((int64_t)e * 2 * I + 2 * i0) * rb_h, bytes, &full[st]);
         } else {
-          const int64_t jd = j - n_gu;  // block-major: all expert groups of block 0, then block 1, ...
+          // block-major: all expert groups of block 0, then block 1, ...
           const int blk = (int)(jd / n_ge), e0 = (int)(jd % n_ge) * a.n_per, e1 = ::min(nU, e0 + a.n_per);
           const int r0 = o0 + blk * kRowBlock, nr = ::min(kRowBlock + 0, o1 - r0);
           mbar_arrive_expect_tx(&full[st], (uint32_t)(e1 - e0) * nr * rb_i);
           for (int u = e0; u < e1; ++u)
             bulk_g2s(sb + (size_t)(u - e0) * kRowBlock * rb_i, a.q_d + ((int64_t)r.u[u].x * H + r0) * rb_i,
                      (uint32_t)nr * rb_i, &full[st]);
+          ++jd;
         }
       }
       // every copy issued has landed before the CTA may leave
@@ -272,18 +307,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
 
     // ---- phase 1: gate/up. Every consumer warp passes every stage in order
     // (no wait is ever more than one phase ahead of its barrier) and computes
-    // the units g of the stage with (g - lo) % 16 == warp.
+    // its units of the stage's chunk, until the empty stage.
     const int nseg_h = H / 16;
-    for (int64_t j = 0; j < n_gu && ok; ++j) {
+    // stages of gate/up work this CTA took (ticketed work: then one empty stage)
+    int64_t n_gu = kOne ? (hi > lo ? (hi + R - 1) / R - lo / R : 0) : 0;
+    for (int64_t j = 0; ok && (!kOne || j < n_gu); ++j) {
       const int st = (int)(j % a.stages);
       if (!mbar_wait(&full[st], (uint32_t)((j / a.stages) & 1))) {
         report_wait(a.meta, kSiteGuFull, j, warp);
         ok = false;
         break;
       }
-      const int64_t u0 = std::max<int64_t>(lo, (b0 + j) * R), u1 = std::min<int64_t>(hi, (b0 + j + 1) * R);
+      const int2 su = stage_units[st];
+      if (su.x < 0) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        n_gu = j + 1;
+        break;
+      }
+      const int64_t u0 = su.x, u1 = su.y;
       const uint8_t* sb = ring + (size_t)st * a.stage_bytes;
-      for (int64_t g = u0 + ((warp - (u0 - lo)) % kCW + kCW) % kCW; g < u1; g += kCW) {
+      // units alternate over the warps from stage to stage: unit q of stage j
+      // goes to warp (j R + q) mod 16
+      for (int64_t g = u0 + ((warp - j * R) % kCW + kCW) % kCW; g < u1; g += kCW) {
         // the stage holds rows 2 i0 .. 2 i1 of the expert: per group, kGUGroup
         // gate rows then their up rows; u0 is group-aligned
         const int off = (int)(g - u0);

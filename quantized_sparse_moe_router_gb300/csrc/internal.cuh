@@ -49,7 +49,7 @@ struct Meta {
   int32_t status;       // kStatus* bits
   int32_t T;            // T of the last route
   int32_t n_mtiles;     // prefill: number of (expert, 128-row) tiles
-  int32_t pad;
+  uint32_t chunk_ctr;   // decode gate/up chunk tickets handed out (reset by the router)
   int32_t diag[4];      // first failed wait: (site, block, stage, detail); site 0 = none
 };
 
@@ -69,6 +69,7 @@ struct PrefillMaps {
   CUtensorMap s_gu;   // scale plane [EU*H/32][2I] u16, box 128 x 2
   CUtensorMap q_d;    // [EU*H][I] u8 (row stride row_bytes(I))
   CUtensorMap s_d;    // [EU*I/32][H] u16
+  CUtensorMap w3;     // router planes [3E][H] bf16, box 64 x E, 128B swizzle (E <= 128)
 };
 
 struct Handle {
@@ -88,6 +89,7 @@ struct Handle {
   uint16_t* st_d;     // [EU][I/32][H]
   float* wr;          // [E][H]
   float* bias;        // [E] (zeros when none)
+  __nv_bfloat16* wr3; // [3][E][H] bf16 planes summing exactly to wr (prefill router), or null
   // ---- workspace (device), sized for T_max
   int64_t rows_max;   // T_max * (k + S)
   int32_t* ids;       // [T_max][k]
@@ -167,6 +169,12 @@ cudaError_t launch_route_prefill(Handle* h, const __nv_bfloat16* x, int T, int32
 cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfloat16* out, bool publish,
                               int32_t* ids_out, float* gates_out, cudaStream_t s);
 cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bfloat16* out, cudaStream_t s);
+// The prefill router on the tensor cores (E <= 128 and planes present):
+// ids, gates and the per-32-token expert counts in h->hist. false = not taken.
+bool route_prefill_mma_available(const Handle* h);
+cudaError_t launch_route_prefill_mma(Handle* h, const __nv_bfloat16* x, int T, int32_t* ids_out, float* gates_out,
+                                     cudaStream_t s);
+cudaError_t launch_split_router(Handle* h, cudaStream_t s);
 cudaError_t launch_get_permutation(const Handle* h, int T, int32_t* offsets, int32_t* perm, int32_t* inv,
                                    cudaStream_t s);
 

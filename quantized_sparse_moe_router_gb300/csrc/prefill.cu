@@ -108,6 +108,16 @@ __device__ __forceinline__ void mma_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 
+// D (tensor memory) [+]= A (shared memory descriptor) x B (shared memory descriptor)
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                       uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // The same box delivered to this CTA and its cluster peer (same shared-memory
 // offsets), completion counted on each CTA's barrier at bar's offset.
 __device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
@@ -430,6 +440,182 @@ __global__ void __launch_bounds__(kThreads, 1)
                  : "memory");
 }
 
+
+// ------------------------------------------------------------- router on the tensor cores
+// Logits z = x W_r^T + b for 128 tokens per CTA, then the top-k, the gates and
+// the per-32-token expert counts the scan kernel takes (the same outputs as
+// the tiled fp32 router). W_r is split once into three bf16 planes whose sum
+// is exactly W_r (each holds the next 8 significant bits); x is bf16. So every
+// product is exact, and the three MMAs of a K step add them into one fp32
+// accumulator in tensor memory.
+constexpr int kRM = 128, kRK = 64, kRStages = 3;
+constexpr int kRThreads = 192;  // warp 0 TMA, warp 1 MMA (TMEM owner), warps 2-5 epilogue (lane quarters 2,3,0,1)
+constexpr int kRMaxE = 128;
+
+struct RouteMmaArgs {
+  const float* bias;
+  int T, H, E, k;
+  int32_t* ids;
+  float* gates;
+  int32_t* ids_out;
+  float* gates_out;
+  int32_t* hist;  // [ceil(T/32)][E]
+  Meta* meta;
+};
+
+__global__ void __launch_bounds__(kRThreads, 1)
+    route_mma_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
+                     RouteMmaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full[kRStages], empty[kRStages], acc_full;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_cnt[4][kRMaxE];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = a.E, k = a.k, t0 = blockIdx.x * kRM;
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* sX = smem_raw + pad;                 // [kRStages][128 tokens][128 B]
+  uint8_t* sW = sX + kRStages * kRM * kRK * 2;  // [kRStages][3 planes][E rows][128 B]
+  const uint32_t wstage = 3u * E * kRK * 2;
+  for (int i = threadIdx.x; i < 4 * kRMaxE; i += kRThreads) (&s_cnt[0][0])[i] = 0;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kRStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(&acc_full, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(kRMaxE)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const int KT = a.H / kRK;
+  bool ok = true;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int kb = 0; kb < KT && ok; ++kb) {
+        const int s = kb % kRStages;
+        if (!(ok = mbar_wait(&empty[s], ((kb / kRStages) & 1) ^ 1))) {
+          report_wait(a.meta, kSiteGemm, kb, 0);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], (uint32_t)kRM * kRK * 2 + wstage);
+        tma_load_2d(sX + s * kRM * kRK * 2, &map_x, kb * kRK, t0, &full[s]);
+        for (int p = 0; p < 3; ++p)
+          tma_load_2d(sW + s * wstage + p * E * kRK * 2, &map_w, kb * kRK, p * E, &full[s]);
+      }
+      for (int j = ::max(0, KT - kRStages); j < KT; ++j) mbar_wait(&full[j % kRStages], (j / kRStages) & 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kRM, E);
+      for (int kb = 0; kb < KT && ok; ++kb) {
+        const int s = kb % kRStages;
+        if (!(ok = mbar_wait(&full[s], (kb / kRStages) & 1))) {
+          report_wait(a.meta, kSiteGemm, kb, 1);
+          break;
+        }
+        tc_fence_after();
+        const uint32_t x0 = smem_u32(sX + s * kRM * kRK * 2), w0 = smem_u32(sW + s * wstage);
+#pragma unroll
+        for (int kk = 0; kk < kRK / 16; ++kk)
+#pragma unroll
+          for (int p = 2; p >= 0; --p)  // smallest plane first
+            mma_ss(tmem, sw128_desc(x0 + kk * 32), sw128_desc(w0 + p * E * kRK * 2 + kk * 32), idesc,
+                   (kb | kk | (2 - p)) != 0);
+        mma_commit(&empty[s]);
+      }
+      mma_commit(&acc_full);  // (also when aborted: the epilogue then reads what is there)
+    }
+  } else {
+    // epilogue: thread = token row (TMEM lane); top-k kept sorted in registers
+    const int q = warp & 3, row = q * 32 + lane, t = t0 + row;
+    if (!mbar_wait(&acc_full, 0)) report_wait(a.meta, kSiteGemm, 0, 2);
+    tc_fence_after();
+    float tv[kMaxK];
+    int ti[kMaxK];
+#pragma unroll
+    for (int j = 0; j < kMaxK; ++j) {
+      tv[j] = -INFINITY;
+      ti[j] = j;  // valid ids even if nothing is inserted
+    }
+    for (int c0 = 0; c0 < E; c0 += 32) {
+      float v[32];
+      tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const int e = c0 + j;
+        if (e < E) {
+          // ascending e: a strictly larger logit moves ahead, an equal one stays
+          // behind (ties to the lower id); only the first k slots are used
+          float cv = v[j] + __ldg(a.bias + e);
+          if (cv > tv[kMaxK - 1]) {
+            int ci = e;
+#pragma unroll
+            for (int m = 0; m < kMaxK; ++m) {
+              if (cv > tv[m]) {
+                const float fv = tv[m];
+                const int fi = ti[m];
+                tv[m] = cv;
+                ti[m] = ci;
+                cv = fv;
+                ci = fi;
+              }
+            }
+          }
+        }
+      }
+    }
+    if (t < a.T) {
+      float ex[kMaxK], sum = 0.f;
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j) {
+        ex[j] = j < k ? expf(tv[j] - tv[0]) : 0.f;
+        sum += ex[j];
+      }
+#pragma unroll
+      for (int j = 0; j < kMaxK; ++j)
+        if (j < k) {
+          const float g = ex[j] / sum;
+          a.ids[t * k + j] = ti[j];
+          a.gates[t * k + j] = g;
+          a.ids_out[t * k + j] = ti[j];
+          if (a.gates_out) a.gates_out[t * k + j] = g;
+          atomicAdd(&s_cnt[q][ti[j]], 1);
+        }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  for (int i = threadIdx.x; i < 4 * E; i += kRThreads) {
+    const int q = i / E, e = i % E, tile = blockIdx.x * 4 + q;
+    if (tile * 32 < a.T) a.hist[(int64_t)tile * E + e] = s_cnt[q][e];
+  }
+  if (warp == 1)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kRMaxE) : "memory");
+}
+
+// W_r (fp32) -> three bf16 planes hi, mid, lo with hi + mid + lo == W_r exactly.
+__global__ void split_router_kernel(const float* __restrict__ wr, int64_t n, __nv_bfloat16* __restrict__ w3) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  const float w = wr[i];
+  const __nv_bfloat16 hi = __float2bfloat16_rn(w);
+  const float r1 = w - __bfloat162float(hi);
+  const __nv_bfloat16 mid = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(mid);
+  w3[i] = hi;
+  w3[n + i] = mid;
+  w3[2 * n + i] = __float2bfloat16_rn(r2);
+}
+
 // ------------------------------------------------------------- gather, combine
 // xperm[pos] = x[row_token[pos]], 16 bytes per thread.
 __global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_token,
@@ -538,6 +724,7 @@ cudaError_t configure_prefill_kernels() {
   }
   cudaError_t e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiSwiGLU>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDownScale>);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(route_mma_kernel);
   if (e == cudaSuccess && g_max_clusters == 0) {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = gemm_config<kEpiSwiGLU>(kClusterSize, 0, attr);
@@ -569,7 +756,44 @@ cudaError_t prepare_prefill(Handle* h) {
   if (e == cudaSuccess)
     e = encode_2d(&m->s_d, CU_TENSOR_MAP_DATA_TYPE_UINT16, h->st_d, H, EU * (I / 32), H * 2, BM, 2,
                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+  if (e == cudaSuccess && h->wr3)
+    e = encode_2d(&m->w3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->wr3, H, 3 * (uint64_t)h->cfg.E, H * 2, kRK,
+                  (uint32_t)h->cfg.E, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   return e;
+}
+
+bool route_prefill_mma_available(const Handle* h) {
+  return h->maps && h->wr3 && h->cfg.E <= kRMaxE && h->cfg.E % 16 == 0 && h->cfg.E >= 16;
+}
+
+cudaError_t launch_split_router(Handle* h, cudaStream_t s) {
+  const int64_t n = (int64_t)h->cfg.E * h->cfg.H;
+  split_router_kernel<<<grid_for(n, 256, 1 << 20), 256, 0, s>>>(h->wr, n, h->wr3);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_prefill_mma(Handle* h, const __nv_bfloat16* x, int T, int32_t* ids_out, float* gates_out,
+                                     cudaStream_t s) {
+  const int H = h->cfg.H, E = h->cfg.E;
+  CUtensorMap map_x;  // x is the caller's buffer: its map is made per call
+  cudaError_t e = encode_2d(&map_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<__nv_bfloat16*>(x), H, T, H * 2,
+                            kRK, kRM, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+  if (e != cudaSuccess) return e;
+  RouteMmaArgs a;
+  a.bias = h->bias;
+  a.T = T;
+  a.H = H;
+  a.E = E;
+  a.k = h->cfg.k;
+  a.ids = h->ids;
+  a.gates = h->gates;
+  a.ids_out = ids_out;
+  a.gates_out = gates_out;
+  a.hist = h->hist;
+  a.meta = h->meta;
+  const size_t smem = (size_t)kRStages * (kRM * kRK * 2 + 3 * E * kRK * 2) + 1024;
+  route_mma_kernel<<<(T + kRM - 1) / kRM, kRThreads, smem, s>>>(map_x, h->maps->w3, a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bfloat16* out, cudaStream_t s) {

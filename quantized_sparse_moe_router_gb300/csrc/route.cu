@@ -53,7 +53,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
   const int e = blockIdx.x;
   const int T = a.T, H = a.H;
   pdl_launch_dependents();  // the expert kernels wait for this grid's completion before reading
-  if (blockIdx.x == 0 && tid == 0) a.meta->gbar = 0;  // fresh grid barrier for this call's expert kernel
+  if (blockIdx.x == 0 && tid == 0) {  // fresh grid barrier and chunk tickets for this call's expert kernel
+    a.meta->gbar = 0;
+    a.meta->chunk_ctr = 0;
+  }
   {
     float acc[kMaxDecodeT];
 #pragma unroll
@@ -430,7 +433,10 @@ cudaError_t launch_route_prefill(Handle* h, const __nv_bfloat16* x, int T, int32
   const int n_tiles = (T + kRouteTileM - 1) / kRouteTileM;
   const int EM = (h->cfg.E + 31) / 32;
   cudaError_t err;
-  {
+  if (route_prefill_mma_available(h)) {
+    KernelTimer tm(h, FW_KERNEL_ROUTE_TILES, s);
+    err = launch_route_prefill_mma(h, x, T, ids_out, gates_out, s);
+  } else {
   KernelTimer tm(h, FW_KERNEL_ROUTE_TILES, s);
   switch (EM) {
     case 1: err = launch_tiles<1>(a, h->hist, n_tiles, s); break;

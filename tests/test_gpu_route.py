@@ -15,6 +15,12 @@ from layer_inputs import DeviceLayer, OracleLayer, hidden_with_margins, to_devic
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
+# Gates from fp32-accurate logits: the decode router sums fp32 FMAs; the
+# prefill router adds exact bf16-plane products in a tensor-core fp32
+# accumulator, whose truncating accumulation over H/16 x 3 steps moves logits
+# by ~2e-5 relative -- far below the 1e-3 logit margin of the inputs, and
+# within this bound on the gates (the one used across the suite).
+GATE_TOL = 1e-5
 
 
 def route_and_check(wl, x, dl, ol, layer):
@@ -24,7 +30,7 @@ def route_and_check(wl, x, dl, ol, layer):
     torch.cuda.synchronize()
     ids_ref, gates_ref = ol.route(x)
     assert np.array_equal(ids.cpu().numpy(), ids_ref)
-    assert np.abs(gates.cpu().numpy() - gates_ref).max() <= 2e-6
+    assert np.abs(gates.cpu().numpy() - gates_ref).max() <= GATE_TOL
     off, perm, inv = layer.permutation(T)
     o_ref, p_ref, i_ref = oracle.permutation(ids_ref, wl.E)
     assert np.array_equal(off.cpu().numpy(), o_ref)
