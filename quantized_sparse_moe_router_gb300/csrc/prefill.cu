@@ -463,6 +463,28 @@ struct RouteMmaArgs {
   Meta* meta;
 };
 
+// Insert (v, e) into the descending list (tv, ti) of length KS, behind any
+// equal value (ids arrive in ascending order, so ties keep the lower id).
+// Branch-free: every slot compares against the old list, so the KS selects
+// are independent of one another.
+template <int KS>
+__device__ __forceinline__ void topk_insert(float (&tv)[KS], int (&ti)[KS], float v, int e) {
+  bool c[KS];
+#pragma unroll
+  for (int m = 0; m < KS; ++m) c[m] = v > tv[m];
+#pragma unroll
+  for (int m = KS - 1; m > 0; --m) {
+    const float nv = c[m - 1] ? tv[m - 1] : (c[m] ? v : tv[m]);
+    const int ni = c[m - 1] ? ti[m - 1] : (c[m] ? e : ti[m]);
+    tv[m] = nv;
+    ti[m] = ni;
+  }
+  tv[0] = c[0] ? v : tv[0];
+  ti[0] = c[0] ? e : ti[0];
+}
+
+// KS: length of the per-token list, the smallest of 8 and 16 that holds k.
+template <int KS>
 __global__ void __launch_bounds__(kRThreads, 1)
     route_mma_kernel(const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_w,
                      RouteMmaArgs a) {
@@ -470,6 +492,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   __shared__ __align__(8) uint64_t full[kRStages], empty[kRStages], acc_full;
   __shared__ uint32_t s_tmem;
   __shared__ int s_cnt[4][kRMaxE];
+  __shared__ float s_bias[kRMaxE];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E, k = a.k, t0 = blockIdx.x * kRM;
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -477,6 +500,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   uint8_t* sW = sX + kRStages * kRM * kRK * 2;  // [kRStages][3 planes][E rows][128 B]
   const uint32_t wstage = 3u * E * kRK * 2;
   for (int i = threadIdx.x; i < 4 * kRMaxE; i += kRThreads) (&s_cnt[0][0])[i] = 0;
+  for (int i = threadIdx.x; i < E; i += kRThreads) s_bias[i] = a.bias[i];
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRStages; ++i) {
       mbar_init(&full[i], 1);
@@ -496,20 +520,24 @@ __global__ void __launch_bounds__(kRThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   const int KT = a.H / kRK;
+  // each CTA starts its K loop at its own offset, so the CTAs do not all ask
+  // the same L2 lines for the same W_r tile at the same time
+  const int kb0 = (int)(((int64_t)blockIdx.x * KT) / gridDim.x);
   bool ok = true;
 
   if (warp == 0) {
     if (lane == 0) {
       for (int kb = 0; kb < KT && ok; ++kb) {
         const int s = kb % kRStages;
+        const int kk = kb + kb0 < KT ? kb + kb0 : kb + kb0 - KT;
         if (!(ok = mbar_wait(&empty[s], ((kb / kRStages) & 1) ^ 1))) {
           report_wait(a.meta, kSiteGemm, kb, 0);
           break;
         }
         mbar_arrive_expect_tx(&full[s], (uint32_t)kRM * kRK * 2 + wstage);
-        tma_load_2d(sX + s * kRM * kRK * 2, &map_x, kb * kRK, t0, &full[s]);
+        tma_load_2d(sX + s * kRM * kRK * 2, &map_x, kk * kRK, t0, &full[s]);
         for (int p = 0; p < 3; ++p)
-          tma_load_2d(sW + s * wstage + p * E * kRK * 2, &map_w, kb * kRK, p * E, &full[s]);
+          tma_load_2d(sW + s * wstage + p * E * kRK * 2, &map_w, kk * kRK, p * E, &full[s]);
       }
       for (int j = ::max(0, KT - kRStages); j < KT; ++j) mbar_wait(&full[j % kRStages], (j / kRStages) & 1);
     }
@@ -539,49 +567,33 @@ __global__ void __launch_bounds__(kRThreads, 1)
     const int q = warp & 3, row = q * 32 + lane, t = t0 + row;
     if (!mbar_wait(&acc_full, 0)) report_wait(a.meta, kSiteGemm, 0, 2);
     tc_fence_after();
-    float tv[kMaxK];
-    int ti[kMaxK];
+    float tv[KS];
+    int ti[KS];
 #pragma unroll
-    for (int j = 0; j < kMaxK; ++j) {
+    for (int j = 0; j < KS; ++j) {
       tv[j] = -INFINITY;
       ti[j] = j;  // valid ids even if nothing is inserted
     }
-    for (int c0 = 0; c0 < E; c0 += 32) {
+    for (int c0 = 0; c0 < E; c0 += 32) {  // E is a multiple of 16, so only the last chunk is partial
       float v[32];
       tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
+      if (c0 + 32 <= E) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const int e = c0 + j;
-        if (e < E) {
-          // ascending e: a strictly larger logit moves ahead, an equal one stays
-          // behind (ties to the lower id); only the first k slots are used
-          float cv = v[j] + __ldg(a.bias + e);
-          if (cv > tv[kMaxK - 1]) {
-            int ci = e;
+        for (int j = 0; j < 32; ++j) topk_insert<KS>(tv, ti, v[j] + s_bias[c0 + j], c0 + j);
+      } else {
 #pragma unroll
-            for (int m = 0; m < kMaxK; ++m) {
-              if (cv > tv[m]) {
-                const float fv = tv[m];
-                const int fi = ti[m];
-                tv[m] = cv;
-                ti[m] = ci;
-                cv = fv;
-                ci = fi;
-              }
-            }
-          }
-        }
+        for (int j = 0; j < 16; ++j) topk_insert<KS>(tv, ti, v[j] + s_bias[c0 + j], c0 + j);
       }
     }
     if (t < a.T) {
-      float ex[kMaxK], sum = 0.f;
+      float ex[KS], sum = 0.f;
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
+      for (int j = 0; j < KS; ++j) {
         ex[j] = j < k ? expf(tv[j] - tv[0]) : 0.f;
         sum += ex[j];
       }
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
+      for (int j = 0; j < KS; ++j)
         if (j < k) {
           const float g = ex[j] / sum;
           a.ids[t * k + j] = ti[j];
@@ -724,7 +736,8 @@ cudaError_t configure_prefill_kernels() {
   }
   cudaError_t e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiSwiGLU>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDownScale>);
-  if (e == cudaSuccess) e = allow_max_dynamic_smem(route_mma_kernel);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(route_mma_kernel<8>);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(route_mma_kernel<16>);
   if (e == cudaSuccess && g_max_clusters == 0) {
     cudaLaunchAttribute attr[1];
     cudaLaunchConfig_t cfg = gemm_config<kEpiSwiGLU>(kClusterSize, 0, attr);
@@ -792,7 +805,11 @@ cudaError_t launch_route_prefill_mma(Handle* h, const __nv_bfloat16* x, int T, i
   a.hist = h->hist;
   a.meta = h->meta;
   const size_t smem = (size_t)kRStages * (kRM * kRK * 2 + 3 * E * kRK * 2) + 1024;
-  route_mma_kernel<<<(T + kRM - 1) / kRM, kRThreads, smem, s>>>(map_x, h->maps->w3, a);
+  const unsigned grid = (unsigned)((T + kRM - 1) / kRM);
+  if (a.k <= 8)
+    route_mma_kernel<8><<<grid, kRThreads, smem, s>>>(map_x, h->maps->w3, a);
+  else
+    route_mma_kernel<16><<<grid, kRThreads, smem, s>>>(map_x, h->maps->w3, a);
   return cudaGetLastError();
 }
 

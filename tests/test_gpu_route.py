@@ -41,7 +41,7 @@ def route_and_check(wl, x, dl, ol, layer):
 
 
 @pytest.mark.parametrize("T", [17, 33, 129, 1000])
-@pytest.mark.parametrize("E, k", [(8, 2), (64, 8), (256, 8), (40, 5)])
+@pytest.mark.parametrize("E, k", [(8, 2), (64, 8), (256, 8), (40, 5), (48, 12), (128, 16)])
 def test_tiled_router_small(T, E, k):
     wl = synth.WORKLOADS["tiny"].with_(E=E, k=k, T=T, sigma_router=0.1)
     dl = DeviceLayer(wl, 0, DEV)
@@ -65,14 +65,15 @@ def test_router_prefill_full_size_zipf():
     layer.close()
 
 
-def test_router_ties_tiled():
-    wl = synth.WORKLOADS["tiny"].with_(E=64, k=8, T=100)
-    dl = DeviceLayer(wl, 0, DEV, Wr=np.zeros((64, wl.H), np.float32))
+@pytest.mark.parametrize("E, k", [(64, 8), (48, 12)])
+def test_router_ties_tiled(E, k):
+    wl = synth.WORKLOADS["tiny"].with_(E=E, k=k, T=100)
+    dl = DeviceLayer(wl, 0, DEV, Wr=np.zeros((E, wl.H), np.float32))
     layer = dl.make(T_max=100)
     x = synth.hidden_bf16_bits(wl, 0)
     ids, _ = layer.route(to_device_bf16(x, DEV))
-    assert ids.cpu().numpy().tolist() == [list(range(8))] * 100
+    assert ids.cpu().numpy().tolist() == [list(range(k))] * 100
     off, perm, inv = layer.permutation(100)
-    o_ref, p_ref, _ = oracle.permutation(np.tile(np.arange(8, dtype=np.int32), (100, 1)), 64)
+    o_ref, p_ref, _ = oracle.permutation(np.tile(np.arange(k, dtype=np.int32), (100, 1)), E)
     assert np.array_equal(off.cpu().numpy(), o_ref) and np.array_equal(perm.cpu().numpy(), p_ref)
     layer.close()
