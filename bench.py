@@ -47,6 +47,8 @@ def parse():
     p.add_argument("--workload", default="dec1", choices=sorted(synth.WORKLOADS))
     p.add_argument("--impl", default="fw", choices=["fw", "reference"])
     p.add_argument("--layers", type=int, default=0, help="override the workload's layer count")
+    p.add_argument("--experts", type=int, default=0,
+                   help="override E (a smaller case for profiling: at T = 1 the expert work per call is the same)")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
@@ -215,6 +217,8 @@ def run_fw(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     w = synth.WORKLOADS[args.workload]
+    if args.experts:
+        w = w.with_(E=args.experts)
     n_layers = args.layers or w.layers
     layers = build_layers(w, n_layers, dev)
     N_X_ROWS = n_x_rows(w)

@@ -182,6 +182,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
     }
     fence_mbar_init();
   }
+  if (warp != kProducer) {
+    // x was written before the router kernel started (that launch waits for
+    // the whole stream), so it is staged while the router still runs.
+    // segment-transposed, fp32 or bf16 in shared memory (else read from global)
+    if (x_mode == kXSmemF32) {
+      float* xs = reinterpret_cast<float*>(smem);
+      for (int c = tid; c < T * H / 8; c += kCW * 32) {  // c: 8 bf16 = half a segment
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x) + c);
+        const int t = c / (H / 8), cc = c % (H / 8), seg = cc >> 1, half = cc & 1;
+        float4 lo4, hi4;
+        bf16x2_to_f32(v.x, lo4.x, lo4.y);
+        bf16x2_to_f32(v.y, lo4.z, lo4.w);
+        bf16x2_to_f32(v.z, hi4.x, hi4.y);
+        bf16x2_to_f32(v.w, hi4.z, hi4.w);
+        float* base = xs + (size_t)t * H + seg * 4;
+        *reinterpret_cast<float4*>(base + (2 * half) * (H / 4)) = lo4;
+        *reinterpret_cast<float4*>(base + (2 * half + 1) * (H / 4)) = hi4;
+      }
+    } else if (x_mode == kXSmemBf16) {
+      __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);
+      for (int c = tid; c < T * H / 8; c += kCW * 32) {
+        const int t = c / (H / 8), cc = c % (H / 8), seg = cc >> 1, half = cc & 1;
+        *reinterpret_cast<uint4*>(xs + (size_t)t * H + half * (H / 2) + seg * 8) =
+            __ldg(reinterpret_cast<const uint4*>(a.x) + c);
+      }
+    }
+  }
   pdl_wait();  // the router's logits (and its reset of the grid barrier)
   route_in_smem<kThreads>(a.logits, T, a.E, a.k, a.S, r);
   if (a.publish && blockIdx.x == 0) publish_routing<kThreads>(r, T, a.E, a.k, a.S, a.ro);
@@ -279,31 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
     }
   } else {
     // ------------------------------------------------------ consumers
-    bool ok = true;
-    // x for this batch, segment-transposed: fp32 or bf16 in shared memory, else read from global
-    if (x_mode == kXSmemF32) {
-      float* xs = reinterpret_cast<float*>(smem);
-      for (int c = tid; c < T * H / 8; c += kCW * 32) {  // c: 8 bf16 = half a segment
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x) + c);
-        const int t = c / (H / 8), cc = c % (H / 8), seg = cc >> 1, half = cc & 1;
-        float4 lo4, hi4;
-        bf16x2_to_f32(v.x, lo4.x, lo4.y);
-        bf16x2_to_f32(v.y, lo4.z, lo4.w);
-        bf16x2_to_f32(v.z, hi4.x, hi4.y);
-        bf16x2_to_f32(v.w, hi4.z, hi4.w);
-        float* base = xs + (size_t)t * H + seg * 4;
-        *reinterpret_cast<float4*>(base + (2 * half) * (H / 4)) = lo4;
-        *reinterpret_cast<float4*>(base + (2 * half + 1) * (H / 4)) = hi4;
-      }
-    } else if (x_mode == kXSmemBf16) {
-      __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);
-      for (int c = tid; c < T * H / 8; c += kCW * 32) {
-        const int t = c / (H / 8), cc = c % (H / 8), seg = cc >> 1, half = cc & 1;
-        *reinterpret_cast<uint4*>(xs + (size_t)t * H + half * (H / 2) + seg * 8) =
-            __ldg(reinterpret_cast<const uint4*>(a.x) + c);
-      }
-    }
-    consumer_sync();
+    bool ok = true;  // (x is visible: route_in_smem ends with a CTA barrier)
 
     // ---- phase 1: gate/up. Every consumer warp passes every stage in order
     // (no wait is ever more than one phase ahead of its barrier) and computes

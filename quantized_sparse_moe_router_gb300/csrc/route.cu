@@ -408,7 +408,12 @@ cudaError_t launch_tiles(RouteArgs a, int32_t* hist, int n_tiles, cudaStream_t s
 }  // namespace
 
 cudaError_t configure_route_kernels() {
-  cudaError_t e = allow_max_dynamic_smem(route_tiles_kernel<1>);
+  // The decode router runs on the SMs that the expert kernel (all of shared
+  // memory) takes next: with the same carve-out an SM need not be
+  // reconfigured between the two.
+  cudaError_t e = cudaFuncSetAttribute(route_decode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(route_tiles_kernel<1>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_tiles_kernel<2>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_tiles_kernel<3>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_tiles_kernel<4>);
