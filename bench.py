@@ -321,8 +321,9 @@ def run_fw(args, rank, world, local_rank):
                     "algorithmic_bytes_per_launch": round(dom_bytes / dom_n),
                     "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"}
     else:
-        dom = "prefill_gateup"
+        dom = "prefill_gateup"  # both launches: the large-tile and the small-tile GEMM
         dom_ms, dom_n = prof.get(dom, (float("nan"), 1))
+        dom_ms += prof.get("prefill_gateup_small", (0.0, 0))[0]
         fl = work["flops"] * 2 / 3
         achieved = fl / (dom_ms / 1e3) / 1e12
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16_burst, "unit": "TFLOP/s",

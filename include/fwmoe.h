@@ -134,6 +134,8 @@ enum {
   FW_KERNEL_PREFILL_DOWN = 7,    /* prefill down grouped GEMM (tcgen05) x gate */
   FW_KERNEL_PREFILL_COMBINE = 8, /* prefill un-permute and sum */
   FW_KERNEL_PREFILL_GATHER = 9, /* prefill: x rows gathered into grouped order */
+  FW_KERNEL_PREFILL_GATEUP_SMALL = 10, /* prefill gate/up GEMM over the tiles of at most 64 rows */
+  FW_KERNEL_PREFILL_DOWN_SMALL = 11,   /* prefill down GEMM over the tiles of at most 64 rows */
   FW_KERNEL_KINDS = 16
 };
 

@@ -53,7 +53,8 @@ EXPORTED = ("fw_moe_init", "fw_moe_route", "fw_moe_ffn", "fw_moe_forward", "fw_m
             "fw_q8_0_quantize", "fw_moe_profile_begin", "fw_moe_profile_end", "fw_moe_route_noalloc")
 
 KERNEL_KINDS = ("route_decode", "route_tiles", "route_scan", "route_scatter", "decode_experts", "reserved",
-                "prefill_gateup", "prefill_down", "prefill_combine", "prefill_gather")
+                "prefill_gateup", "prefill_down", "prefill_combine", "prefill_gather", "prefill_gateup_small",
+                "prefill_down_small")
 
 
 def lib():

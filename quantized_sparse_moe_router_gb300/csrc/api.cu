@@ -68,7 +68,7 @@ struct Allocator {
 void free_handle_memory(Handle* h) {
   void* ptrs[] = {h->q_gu, h->st_gu, h->q_d, h->st_d, h->wr3, h->wr, h->bias, h->ids, h->gates,
                   h->logits, h->counts, h->offsets, h->perm, h->inv, h->row_token, h->row_gate, h->uinfo,
-                  h->hist, h->minfo, h->xperm, h->hbuf, h->yp, h->meta, h->x_dev, h->out_dev, h->ids_dev};
+                  h->hist, h->minfo, h->minfo_s, h->xperm, h->hbuf, h->yp, h->meta, h->x_dev, h->out_dev, h->ids_dev};
   for (void* p : ptrs)
     if (p) cudaFree(p);
 }
@@ -169,6 +169,7 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
       {(void**)&h->uinfo, (size_t)(EU * 16)},
       {(void**)&h->hist, (size_t)(n_route_tiles * EU * 4)},
       {(void**)&h->minfo, (size_t)(n_mtiles_max * 16)},
+      {(void**)&h->minfo_s, (size_t)(EU * 16)},
       {(void**)&h->xperm, (size_t)(Tm > decode_limit(h) ? h->rows_max * H * 2 : 256)},
       {(void**)&h->hbuf, hbuf_bytes},
       {(void**)&h->yp, (size_t)(Tm > decode_limit(h) ? h->rows_max * H * 2 : 256)},

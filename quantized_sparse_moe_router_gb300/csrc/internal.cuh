@@ -22,6 +22,7 @@ constexpr int kMaxK = 16;          // experts per token
 constexpr int kMaxDecodeT = 16;    // decode path token limit (one lane per token in the combine)
 constexpr int kRouteTileM = 32;    // tokens per CTA in the tiled router
 constexpr int kTokTile = 192;      // prefill GEMM token tile (rows of one expert)
+constexpr int kSmallTile = 64;     // tiles of at most this many rows go to the small-tile GEMM
 
 // Status bits written by kernels into the handle's device status word.
 constexpr int kStatusTimeout = 1;
@@ -48,7 +49,8 @@ struct Meta {
   uint32_t ticket;      // last-CTA detection in the router (self-resetting)
   int32_t status;       // kStatus* bits
   int32_t T;            // T of the last route
-  int32_t n_mtiles;     // prefill: number of (expert, 128-row) tiles
+  int32_t n_mtiles;     // prefill: token tiles of more than kSmallTile rows (minfo)
+  int32_t n_stiles;     // prefill: token tiles of at most kSmallTile rows (minfo_s)
   uint32_t chunk_ctr;   // decode gate/up chunk tickets handed out (reset by the router)
   int32_t diag[4];      // first failed wait: (site, block, stage, detail); site 0 = none
 };
@@ -63,8 +65,10 @@ struct Timing {
 
 // TMA descriptors of the prefill GEMMs (host copies, passed by value).
 struct PrefillMaps {
-  CUtensorMap a_x;    // xperm [rows_max][H] bf16, box 64 x 64, 128B swizzle
-  CUtensorMap a_h;    // hbuf  [rows_max][I] bf16, box 64 x 64, 128B swizzle
+  CUtensorMap a_x;    // xperm [rows_max][H] bf16, box 64 x 96, 128B swizzle
+  CUtensorMap a_h;    // hbuf  [rows_max][I] bf16, box 64 x 96, 128B swizzle
+  CUtensorMap a_xs;   // the same, box 64 x 64 (small-tile GEMM)
+  CUtensorMap a_hs;
   CUtensorMap q_gu;   // code plane [EU*2I][H] u8 (row stride row_bytes(H)), box 64 x 128, 64B swizzle
   CUtensorMap s_gu;   // scale plane [EU*H/32][2I] u16, box 128 x 2
   CUtensorMap q_d;    // [EU*H][I] u8 (row stride row_bytes(I))
@@ -104,6 +108,7 @@ struct Handle {
   int4* uinfo;        // [EU] (expert, first grouped row, rows, 0) of the experts with rows, ascending id
   int32_t* hist;      // [ceil(T_max/32)][EU] per-tile counts, then per-tile bases
   int4* minfo;        // [rows_max/kTokTile + EU] prefill token tiles: (expert, first row, valid rows, 0)
+  int4* minfo_s;      // [EU] the tiles of at most kSmallTile rows (an expert's only or last tile)
   __nv_bfloat16* xperm; // [rows_max][H] x gathered into grouped order (prefill)
   void* hbuf;         // [rows_max][I] fp32 (decode) or bf16 (prefill)
   __nv_bfloat16* yp;  // [rows_max][H] bf16 (prefill)

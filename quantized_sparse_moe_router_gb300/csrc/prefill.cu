@@ -39,29 +39,44 @@ namespace {
 using namespace dev;
 
 constexpr int BM = 128, BK = 64;
-constexpr int BN = kTokTile;                // tokens per tile (N <= 192)
-constexpr int kXBox = 96;                   // token rows per TMA box (one per CTA of the pair)
-constexpr int kStages = 6;                  // shared-memory stages (TMA -> dequant / MMA)
 constexpr int kAStages = 4;                 // tensor-memory A stages (dequant -> MMA)
 constexpr int kEpiWarps = 4, kProducerWarp = 4, kMmaWarp = 5, kDeqWarp0 = 6, kDeqWarps = 8;
 constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 448
 constexpr int kClusterSize = 2;             // CTA pairs share (multicast) each token tile
-constexpr uint32_t kXBytes = BN * BK * 2;   // 24 KB bf16 token tile
-constexpr uint32_t kQBytes = BM * BK;       // 8 KB int8 codes
-constexpr uint32_t kSBytes = BM * 2 * 2;    // 512 B: 2 scale blocks x 128 rows
-constexpr uint32_t kSmemBytes = kStages * (kXBytes + kQBytes + kSBytes) + 1024;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kAccCols = BN;           // one fp32 accumulator: 128 lanes x 192 columns
-constexpr uint32_t kACol0 = 2 * kAccCols;   // A stages after the two accumulators
-constexpr uint32_t kACols = BK / 2;         // 64 bf16 per row = 32 columns per stage
-static_assert(kACol0 + kAStages * kACols <= kTmemCols, "tensor memory budget");
-static_assert(BN % kXBox == 0 && BN % 16 == 0 && BN <= 256 && kXBox % 8 == 0, "token tile");
-static_assert(kStages % 2 == 0 && kAStages % 2 == 0, "the two dequantising groups own alternate stages");
+constexpr uint32_t kSmemLimit = 227 * 1024; // dynamic shared memory a CTA may have
+
+// The two shapes of the grouped GEMM. MB = 1: token tiles of up to 192 rows
+// against one 128-row weight block per CTA. MB = 2: tiles of at most 64 rows
+// (an expert's only or last tile) against two weight blocks per CTA, so that
+// a stage carries 16 KB of codes for 8 KB of tokens -- such tiles stream
+// weights more than they multiply, and this keeps twice the code bytes in
+// flight per SM.
+template <int MB_>
+struct Shape {
+  static constexpr int MB = MB_;                                 // 128-row weight blocks per CTA
+  static constexpr int BN = MB_ == 1 ? kTokTile : kSmallTile;    // tokens per tile (MMA N <= BN)
+  static constexpr int XBox = MB_ == 1 ? BN / 2 : BN;            // token rows per TMA box
+  static constexpr uint32_t XBytes = BN * BK * 2;                // bf16 token tile slot
+  static constexpr uint32_t QBytes = MB * BM * BK;               // int8 codes
+  static constexpr uint32_t SBytes = MB * BM * 2 * 2;            // 2 scale blocks x 128 rows per block
+  static constexpr uint32_t StageBytes = XBytes + QBytes + SBytes;
+  static constexpr int Stages = (int)((kSmemLimit - 2048) / StageBytes) & ~1;
+  static constexpr uint32_t SmemBytes = Stages * StageBytes + 1024;
+  static constexpr uint32_t AccCols = MB * BN;                   // one accumulator buffer (MB blocks)
+  static constexpr uint32_t ACol0 = 2 * AccCols;                 // A stages after the two buffers
+  static constexpr uint32_t ACols = MB * BK / 2;                 // one A stage: 64 bf16 per row per block
+  static_assert(ACol0 + kAStages * ACols <= kTmemCols, "tensor memory budget");
+  static_assert(BN % XBox == 0 && BN % 16 == 0 && BN <= 256 && XBox % 8 == 0, "token tile");
+  static_assert(Stages >= 4 && Stages % 2 == 0 && kAStages % 2 == 0,
+                "the two dequantising groups own alternate stages");
+};
 
 enum Epi { kEpiSwiGLU = 0, kEpiDownScale = 1 };
 
 struct GemmArgs {
   const int4* minfo;      // per token tile: (expert, first grouped row, valid rows, 0)
+  const int32_t* n_mtiles; // number of tiles in minfo (written by the scan kernel)
   const Meta* meta;
   const float* row_gate;  // kEpiDownScale
   __nv_bfloat16* outp;    // hbuf (SwiGLU, [rows][I]) or yp ([rows][H])
@@ -213,10 +228,12 @@ __device__ __forceinline__ uint32_t deq_pair_bf16(uint32_t bits_lo, uint32_t bit
 }
 
 // ------------------------------------------------------------- the GEMM
-template <int EPI>
+template <int EPI, int MB>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_q,
                         const __grid_constant__ CUtensorMap map_s, GemmArgs a) {
+  using G = Shape<MB>;
+  constexpr int kStages = G::Stages;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], a_full[kAStages], a_empty[kAStages];
   __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], mma_done;
@@ -226,9 +243,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* base = smem_raw + pad;
-  uint8_t* sX = base;                            // [kStages][192 rows][128 B], 128B swizzle
-  uint8_t* sQ = sX + kStages * kXBytes;          // [kStages][128 rows][64 B], 64B swizzle
-  uint8_t* sS = sQ + kStages * kQBytes;          // [kStages][2][128] binary16
+  uint8_t* sX = base;                            // [kStages][BN rows][128 B], 128B swizzle
+  uint8_t* sQ = sX + kStages * G::XBytes;        // [kStages][MB][128 rows][64 B], 64B swizzle
+  uint8_t* sS = sQ + kStages * G::QBytes;        // [kStages][MB][2][128] binary16
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -261,10 +278,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t crank = cluster_ctarank();
   const uint16_t kPair = (1u << kClusterSize) - 1u;
 
-  // tiles per cluster: (token tile, pair of 128-row blocks), CTA rank r takes
-  // block 2 p + r (a block past the matrix runs but stores nothing)
-  const int n_mb2 = (a.n_mb + kClusterSize - 1) / kClusterSize;
-  const int n_tiles = a.meta->n_mtiles * n_mb2;
+  // tiles per cluster: (token tile, pair of MB-block groups), CTA rank r takes
+  // group 2 p + r (a block past the matrix runs but stores nothing)
+  const int n_mbg = (a.n_mb + MB - 1) / MB;
+  const int n_mb2 = (n_mbg + kClusterSize - 1) / kClusterSize;
+  const int n_tiles = *a.n_mtiles * n_mb2;
   const int cid = blockIdx.x / kClusterSize, ncl = gridDim.x / kClusterSize;
   const int KT = a.K / BK;
   const int nb = a.K / 32;  // scale blocks per weight row
@@ -283,18 +301,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       int4 mi_next = cid < n_tiles ? a.minfo[cid / n_mb2] : make_int4(0, 0, 0, 0);
       for (int tile = cid; tile < n_tiles && ok; tile += ncl) {
         const int4 mi = mi_next;
-        const int m0 = ((tile % n_mb2) * kClusterSize + (int)crank) * BM;
-        const int nx = (mi.z + kXBox - 1) / kXBox;
+        const int m0 = ((tile % n_mb2) * kClusterSize + (int)crank) * MB * BM;
+        const int nx = (mi.z + G::XBox - 1) / G::XBox;
         if (tile + ncl < n_tiles) mi_next = a.minfo[(tile + ncl) / n_mb2];  // in flight during this tile
         for (int kb = 0; kb < KT && ok; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
           if (!(ok = wait(&empty[s], ph ^ 1))) break;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)nx * kXBox * BK * 2 + kQBytes + kSBytes);
-          for (int x = (int)crank; x < nx; x += kClusterSize)  // half the boxes each, to both CTAs
-            tma_load_2d_mc(sX + s * kXBytes + x * kXBox * 128, &map_b, kb * BK, mi.y + x * kXBox, &full[s], kPair);
-          tma_load_2d(sQ + s * kQBytes, &map_q, kb * BK, mi.x * a.prows + m0, &full[s]);
-          tma_load_2d(sS + s * kSBytes, &map_s, m0, mi.x * nb + kb * 2, &full[s]);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)nx * G::XBox * BK * 2 + G::QBytes + G::SBytes);
+          for (int x = (int)crank; x < nx; x += kClusterSize)  // the boxes shared out, each to both CTAs
+            tma_load_2d_mc(sX + s * G::XBytes + x * G::XBox * 128, &map_b, kb * BK, mi.y + x * G::XBox, &full[s],
+                           kPair);
+#pragma unroll
+          for (int b = 0; b < MB; ++b) {
+            tma_load_2d(sQ + s * G::QBytes + b * BM * BK, &map_q, kb * BK, mi.x * a.prows + m0 + b * BM, &full[s]);
+            tma_load_2d(sS + s * G::SBytes + b * BM * 4, &map_s, m0 + b * BM, mi.x * nb + kb * 2, &full[s]);
+          }
         }
       }
       // copies still in flight after an abort land before the CTA leaves
@@ -313,17 +335,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int b = tc & 1;
         if (!(ok = wait(&acc_empty[b], ((tc >> 1) & 1) ^ 1))) break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + b * kAccCols;
+        const uint32_t d_tmem = tmem_base + b * G::AccCols;
         for (int kb = 0; kb < KT; ++kb, ++it) {
           const int s = it % kStages, sa = it % kAStages;
           if (!(ok = wait(&full[s], (it / kStages) & 1))) break;
           if (!(ok = wait(&a_full[sa], (it / kAStages) & 1))) break;
           tc_fence_after();
-          const uint32_t b0 = smem_u32(sX + s * kXBytes);
-          const uint32_t a0 = tmem_base + kACol0 + sa * kACols;
+          const uint32_t b0 = smem_u32(sX + s * G::XBytes);
+          const uint32_t a0 = tmem_base + G::ACol0 + sa * G::ACols;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k)
-            mma_tmem_a(d_tmem, a0 + k * 8, sw128_desc(b0 + k * 32), idesc, (kb | k) != 0);
+          for (int mb = 0; mb < MB; ++mb)
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k)
+              mma_tmem_a(d_tmem + mb * G::BN, a0 + mb * (BK / 2) + k * 8, sw128_desc(b0 + k * 32), idesc,
+                         (kb | k) != 0);
           mma_commit_mc(&empty[s], kPair);
           mma_commit(&a_empty[sa]);
         }
@@ -351,27 +376,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait(&full[s], (it / kStages) & 1))) break;
         // the MMAs that last read A stage sa have completed
         if (!(ok = wait(&a_empty[sa], ((it / kAStages) & 1) ^ 1))) break;
-        const uint8_t* qrow = sQ + s * kQBytes + r * 64;
-        uint4 c[4];
+#pragma unroll 1
+        for (int mb = 0; mb < MB; ++mb) {  // row r of each of the CTA's weight blocks
+          const uint8_t* qrow = sQ + s * G::QBytes + mb * BM * BK + r * 64;
+          uint4 c[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) c[q] = *reinterpret_cast<const uint4*>(qrow + ((q ^ sw) << 4));
-        const uint16_t* sc = reinterpret_cast<const uint16_t*>(sS + s * kSBytes);
-        const float d0 = half_bits_to_f32(sc[r]), d1 = half_bits_to_f32(sc[BM + r]);
-        uint32_t out[32];
+          for (int q = 0; q < 4; ++q) c[q] = *reinterpret_cast<const uint4*>(qrow + ((q ^ sw) << 4));
+          const uint16_t* sc = reinterpret_cast<const uint16_t*>(sS + s * G::SBytes + mb * BM * 4);
+          const float d0 = half_bits_to_f32(sc[r]), d1 = half_bits_to_f32(sc[BM + r]);
+          uint32_t out[32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const f2 dd = q < 2 ? f2_pack(d0, d0) : f2_pack(d1, d1);
-          const uint32_t w4[4] = {c[q].x, c[q].y, c[q].z, c[q].w};
+          for (int q = 0; q < 4; ++q) {
+            const f2 dd = q < 2 ? f2_pack(d0, d0) : f2_pack(d1, d1);
+            const uint32_t w4[4] = {c[q].x, c[q].y, c[q].z, c[q].w};
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint32_t w = w4[i];
-            out[8 * q + 2 * i] = deq_pair_bf16(__byte_perm(w, 0x4B000000u, 0x7650), __byte_perm(w, 0x4B000000u, 0x7651),
-                                               bias, dd);
-            out[8 * q + 2 * i + 1] = deq_pair_bf16(__byte_perm(w, 0x4B000000u, 0x7652),
-                                                   __byte_perm(w, 0x4B000000u, 0x7653), bias, dd);
+            for (int i = 0; i < 4; ++i) {
+              const uint32_t w = w4[i];
+              out[8 * q + 2 * i] = deq_pair_bf16(__byte_perm(w, 0x4B000000u, 0x7650), __byte_perm(w, 0x4B000000u, 0x7651),
+                                                 bias, dd);
+              out[8 * q + 2 * i + 1] = deq_pair_bf16(__byte_perm(w, 0x4B000000u, 0x7652),
+                                                     __byte_perm(w, 0x4B000000u, 0x7653), bias, dd);
+            }
           }
+          tmem_st32(tmem_base + lane_addr + G::ACol0 + sa * G::ACols + mb * (BK / 2), out);
         }
-        tmem_st32(tmem_base + lane_addr + kACol0 + sa * kACols, out);
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
         tc_fence_before();
         __syncwarp();
@@ -385,43 +413,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int tile = cid; tile < n_tiles && ok; tile += ncl, ++tc) {
       const int4 mi = mi_next;
       if (tile + ncl < n_tiles) mi_next = a.minfo[(tile + ncl) / n_mb2];
-      const int m0 = ((tile % n_mb2) * kClusterSize + (int)crank) * BM;
+      const int m0 = ((tile % n_mb2) * kClusterSize + (int)crank) * MB * BM;
       const int b = tc & 1;
       if (!(ok = wait(&acc_full[b], (tc >> 1) & 1))) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + b * kAccCols + ((uint32_t)(warp * 32) << 16);
-      const int prow = m0 + warp * 32 + lane;  // weight row (interleaved gate/up for SwiGLU)
-      for (int c0 = 0; c0 < mi.z; c0 += 32) {
-        float v[32];
-        tmem_ld32(taddr + c0, v);
-        if (EPI == kEpiSwiGLU) {
-          // lanes 4g, 4g+1 hold the gate rows of i = 2(prow/4) + {0,1}, lanes
-          // 4g+2, 4g+3 the matching up rows. Partners (lane ^ 2) swap halves:
-          // a gate lane computes tokens 0..15 of the chunk, an up lane 16..31,
-          // so every lane makes 16 distinct outputs.
-          const bool gate_lane = (lane & 2) == 0;
-          const int i = (prow >> 2) * 2 + (lane & 1);
-          const int jt = gate_lane ? 0 : 16;
+#pragma unroll 1
+      for (int mb = 0; mb < MB; ++mb) {
+        const uint32_t taddr = tmem_base + b * G::AccCols + mb * G::BN + ((uint32_t)(warp * 32) << 16);
+        const int prow = m0 + mb * BM + warp * 32 + lane;  // weight row (interleaved gate/up for SwiGLU)
+        for (int c0 = 0; c0 < mi.z; c0 += 32) {
+          float v[32];
+          tmem_ld32(taddr + c0, v);
+          if (EPI == kEpiSwiGLU) {
+            // lanes 4g, 4g+1 hold the gate rows of i = 2(prow/4) + {0,1}, lanes
+            // 4g+2, 4g+3 the matching up rows. Partners (lane ^ 2) swap halves:
+            // a gate lane computes tokens 0..15 of the chunk, an up lane 16..31,
+            // so every lane makes 16 distinct outputs.
+            const bool gate_lane = (lane & 2) == 0;
+            const int i = (prow >> 2) * 2 + (lane & 1);
+            const int jt = gate_lane ? 0 : 16;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float mine = gate_lane ? v[j] : v[16 + j];
-            const float other = __shfl_xor_sync(0xFFFFFFFFu, gate_lane ? v[16 + j] : v[j], 2);
-            const float g = gate_lane ? mine : other, u = gate_lane ? other : mine;
-            const float hv = g * __frcp_rn(1.0f + __expf(-g)) * u;
-            const float hn = __shfl_xor_sync(0xFFFFFFFFu, hv, 1);
-            const int c = c0 + jt + j;
-            if ((lane & 1) == 0 && c < mi.z && i < a.out_cols)
-              *reinterpret_cast<uint32_t*>(a.outp + (int64_t)(mi.y + c) * a.out_cols + i) = pack_bf16x2(hv, hn);
-          }
-        } else {
+            for (int j = 0; j < 16; ++j) {
+              const float mine = gate_lane ? v[j] : v[16 + j];
+              const float other = __shfl_xor_sync(0xFFFFFFFFu, gate_lane ? v[16 + j] : v[j], 2);
+              const float g = gate_lane ? mine : other, u = gate_lane ? other : mine;
+              const float hv = g * __frcp_rn(1.0f + __expf(-g)) * u;
+              const float hn = __shfl_xor_sync(0xFFFFFFFFu, hv, 1);
+              const int c = c0 + jt + j;
+              if ((lane & 1) == 0 && c < mi.z && i < a.out_cols)
+                *reinterpret_cast<uint32_t*>(a.outp + (int64_t)(mi.y + c) * a.out_cols + i) = pack_bf16x2(hv, hn);
+            }
+          } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const bool valid = c0 + j < mi.z;
-            const float g = valid ? __ldg(a.row_gate + mi.y + c0 + j) : 0.f;
-            const float y = g * v[j];
-            const float yn = __shfl_down_sync(0xFFFFFFFFu, y, 1);
-            if ((lane & 1) == 0 && valid && prow < a.out_cols)
-              *reinterpret_cast<uint32_t*>(a.outp + (int64_t)(mi.y + c0 + j) * a.out_cols + prow) = pack_bf16x2(y, yn);
+            for (int j = 0; j < 32; ++j) {
+              const bool valid = c0 + j < mi.z;
+              const float g = valid ? __ldg(a.row_gate + mi.y + c0 + j) : 0.f;
+              const float y = g * v[j];
+              const float yn = __shfl_down_sync(0xFFFFFFFFu, y, 1);
+              if ((lane & 1) == 0 && valid && prow < a.out_cols)
+                *reinterpret_cast<uint32_t*>(a.outp + (int64_t)(mi.y + c0 + j) * a.out_cols + prow) = pack_bf16x2(y, yn);
+            }
           }
         }
       }
@@ -698,14 +729,14 @@ unsigned grid_for(int64_t n, int threads, int cap) {
 
 
 
-int g_max_clusters = 0;  // CTA pairs of the GEMM resident at once
+int g_max_clusters[3] = {0, 0, 0};  // CTA pairs of the GEMM resident at once, by MB
 
-template <int EPI>
+template <int MB>
 cudaLaunchConfig_t gemm_config(unsigned grid, cudaStream_t s, cudaLaunchAttribute* attr) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.dynamicSmemBytes = Shape<MB>::SmemBytes;
   cfg.stream = s;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = kClusterSize;
@@ -716,12 +747,24 @@ cudaLaunchConfig_t gemm_config(unsigned grid, cudaStream_t s, cudaLaunchAttribut
   return cfg;
 }
 
-template <int EPI>
+template <int EPI, int MB>
 cudaError_t launch_gemm(const CUtensorMap& mb, const CUtensorMap& mq, const CUtensorMap& ms, const GemmArgs& g,
-                        unsigned grid, cudaStream_t s) {
+                        int num_sms, cudaStream_t s) {
+  const unsigned grid = (unsigned)std::min(num_sms / kClusterSize, g_max_clusters[MB]) * kClusterSize;
   cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = gemm_config<EPI>(grid, s, attr);
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<EPI>, mb, mq, ms, g);
+  cudaLaunchConfig_t cfg = gemm_config<MB>(grid, s, attr);
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<EPI, MB>, mb, mq, ms, g);
+}
+
+template <int MB>
+cudaError_t max_clusters() {
+  if (g_max_clusters[MB]) return cudaSuccess;
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg = gemm_config<MB>(kClusterSize, 0, attr);
+  int n = 0;
+  cudaError_t e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<kEpiSwiGLU, MB>, &cfg);
+  if (e == cudaSuccess) g_max_clusters[MB] = n > 0 ? n : 1;
+  return e;
 }
 
 }  // namespace
@@ -734,17 +777,14 @@ cudaError_t configure_prefill_kernels() {
     if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  cudaError_t e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiSwiGLU>);
-  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDownScale>);
+  cudaError_t e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiSwiGLU, 1>);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDownScale, 1>);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiSwiGLU, 2>);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDownScale, 2>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_mma_kernel<8>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_mma_kernel<16>);
-  if (e == cudaSuccess && g_max_clusters == 0) {
-    cudaLaunchAttribute attr[1];
-    cudaLaunchConfig_t cfg = gemm_config<kEpiSwiGLU>(kClusterSize, 0, attr);
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<kEpiSwiGLU>, &cfg);
-    if (e == cudaSuccess) g_max_clusters = n > 0 ? n : 1;
-  }
+  if (e == cudaSuccess) e = max_clusters<1>();
+  if (e == cudaSuccess) e = max_clusters<2>();
   return e;
 }
 
@@ -752,10 +792,16 @@ cudaError_t prepare_prefill(Handle* h) {
   const uint64_t H = h->cfg.H, I = h->cfg.I, EU = h->EU, R = h->rows_max;
   PrefillMaps* m = new PrefillMaps();
   h->maps = m;
-  cudaError_t e = encode_2d(&m->a_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->xperm, H, R, H * 2, BK, kXBox,
+  cudaError_t e = encode_2d(&m->a_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->xperm, H, R, H * 2, BK, Shape<1>::XBox,
                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
   if (e == cudaSuccess)
-    e = encode_2d(&m->a_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->hbuf, I, R, I * 2, BK, kXBox,
+    e = encode_2d(&m->a_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->hbuf, I, R, I * 2, BK, Shape<1>::XBox,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+  if (e == cudaSuccess)
+    e = encode_2d(&m->a_xs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->xperm, H, R, H * 2, BK, Shape<2>::XBox,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+  if (e == cudaSuccess)
+    e = encode_2d(&m->a_hs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->hbuf, I, R, I * 2, BK, Shape<2>::XBox,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
   if (e == cudaSuccess)
     e = encode_2d(&m->q_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->q_gu, H, EU * 2 * I, row_bytes(H), BK, BM,
@@ -823,9 +869,10 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
     gather_rows_kernel<<<grid_for((int64_t)rows * (H / 8), 256, h->num_sms * 8), 256, 0, s>>>(x, h->row_token, rows,
                                                                                             H, h->xperm);
   }
-  const unsigned grid = (unsigned)std::min(h->num_sms / kClusterSize, g_max_clusters) * kClusterSize;
-  GemmArgs g;
+  // each projection: the tiles of more than kSmallTile rows, then the small ones
+  GemmArgs g, gs;
   g.minfo = h->minfo;
+  g.n_mtiles = &h->meta->n_mtiles;
   g.meta = h->meta;
   g.row_gate = h->row_gate;
   {
@@ -834,8 +881,16 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
     g.prows = 2 * I;
     g.n_mb = (2 * I + BM - 1) / BM;
     g.out_cols = I;
-    KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP, s);
-    err = launch_gemm<kEpiSwiGLU>(h->maps->a_x, h->maps->q_gu, h->maps->s_gu, g, grid, s);
+    gs = g;
+    gs.minfo = h->minfo_s;
+    gs.n_mtiles = &h->meta->n_stiles;
+    {
+      KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP, s);
+      err = launch_gemm<kEpiSwiGLU, 1>(h->maps->a_x, h->maps->q_gu, h->maps->s_gu, g, h->num_sms, s);
+    }
+    KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP_SMALL, s);
+    if (err == cudaSuccess)
+      err = launch_gemm<kEpiSwiGLU, 2>(h->maps->a_xs, h->maps->q_gu, h->maps->s_gu, gs, h->num_sms, s);
   }
   {
     g.outp = h->yp;
@@ -843,8 +898,17 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
     g.prows = H;
     g.n_mb = (H + BM - 1) / BM;
     g.out_cols = H;
-    KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN, s);
-    if (err == cudaSuccess) err = launch_gemm<kEpiDownScale>(h->maps->a_h, h->maps->q_d, h->maps->s_d, g, grid, s);
+    gs = g;
+    gs.minfo = h->minfo_s;
+    gs.n_mtiles = &h->meta->n_stiles;
+    {
+      KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN, s);
+      if (err == cudaSuccess)
+        err = launch_gemm<kEpiDownScale, 1>(h->maps->a_h, h->maps->q_d, h->maps->s_d, g, h->num_sms, s);
+    }
+    KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN_SMALL, s);
+    if (err == cudaSuccess)
+      err = launch_gemm<kEpiDownScale, 2>(h->maps->a_hs, h->maps->q_d, h->maps->s_d, gs, h->num_sms, s);
   }
   if (err != cudaSuccess) return err;
   {

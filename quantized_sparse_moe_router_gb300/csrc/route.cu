@@ -245,12 +245,24 @@ __global__ void __launch_bounds__(256) route_tiles_kernel(RouteArgs a, int32_t* 
 // scans over the experts run in one warp, in registers.
 constexpr int kScanBatch = 16;
 
+// An expert's token tiles: full kTokTile-row tiles, then the rest -- which
+// goes to the small-tile list when it has at most kSmallTile rows.
+__device__ __forceinline__ int big_tiles(int c) {
+  const int r = c % kTokTile;
+  return c / kTokTile + (r > kSmallTile ? 1 : 0);
+}
+__device__ __forceinline__ int small_tiles(int c) {
+  const int r = c % kTokTile;
+  return r > 0 && r <= kSmallTile ? 1 : 0;
+}
+
 __global__ void __launch_bounds__(256) route_scan_kernel(RouteArgs a, int32_t* hist, int n_tiles,
-                                                         int4* minfo) {
+                                                         int4* minfo, int4* minfo_s) {
   __shared__ int s_cnt[kMaxE + 2];
   __shared__ int s_off[kMaxE + 2];
   __shared__ int s_nz[kMaxE + 2];
   __shared__ int s_nt[kMaxE + 2];
+  __shared__ int s_ns[kMaxE + 2];
   const int E = a.E, EU = E + a.S, T = a.T, tid = threadIdx.x, lane = tid & 31;
   for (int e = tid; e < E; e += 256) {
     int run = 0;
@@ -269,27 +281,29 @@ __global__ void __launch_bounds__(256) route_scan_kernel(RouteArgs a, int32_t* h
     constexpr int kPer = (kMaxE + 1 + 31) / 32;
     const int per = (EU + 31) / 32, b0 = lane * per;
     int cn[kPer];
-    int sc = 0, sn = 0, st = 0;
+    int sc = 0, sn = 0, st = 0, ss = 0;
 #pragma unroll
     for (int m = 0; m < kPer; ++m) {
       const int i = b0 + m;
       cn[m] = (m < per && i < EU) ? s_cnt[i] : 0;
       sc += cn[m];
       sn += cn[m] > 0;
-      st += (cn[m] + kTokTile - 1) / kTokTile;
+      st += big_tiles(cn[m]);
+      ss += small_tiles(cn[m]);
     }
-    int ic = sc, in = sn, it = st;
+    int ic = sc, in = sn, it = st, is = ss;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int uc = __shfl_up_sync(0xFFFFFFFFu, ic, o), un = __shfl_up_sync(0xFFFFFFFFu, in, o),
-                ut = __shfl_up_sync(0xFFFFFFFFu, it, o);
+                ut = __shfl_up_sync(0xFFFFFFFFu, it, o), us = __shfl_up_sync(0xFFFFFFFFu, is, o);
       if (lane >= o) {
         ic += uc;
         in += un;
         it += ut;
+        is += us;
       }
     }
-    int rc = ic - sc, rn = in - sn, rt = it - st;
+    int rc = ic - sc, rn = in - sn, rt = it - st, rs = is - ss;
 #pragma unroll
     for (int m = 0; m < kPer; ++m) {
       const int i = b0 + m;
@@ -297,15 +311,18 @@ __global__ void __launch_bounds__(256) route_scan_kernel(RouteArgs a, int32_t* h
         s_off[i] = rc;
         s_nz[i] = rn;
         s_nt[i] = rt;
+        s_ns[i] = rs;
         rc += cn[m];
         rn += cn[m] > 0;
-        rt += (cn[m] + kTokTile - 1) / kTokTile;
+        rt += big_tiles(cn[m]);
+        rs += small_tiles(cn[m]);
       }
     }
     if (lane == 31) {
       s_off[EU] = ic;
       a.meta->n_unique = in;
       a.meta->n_mtiles = it;
+      a.meta->n_stiles = is;
       a.meta->T = T;
     }
   }
@@ -315,9 +332,13 @@ __global__ void __launch_bounds__(256) route_scan_kernel(RouteArgs a, int32_t* h
     const int cnt = s_cnt[e];
     a.counts[e] = cnt;
     if (cnt > 0) a.uinfo[s_nz[e]] = make_int4(e, s_off[e], cnt, 0);
-    const int nt = (cnt + kTokTile - 1) / kTokTile;
+    const int nt = big_tiles(cnt);
     for (int i = 0; i < nt; ++i)
       minfo[s_nt[e] + i] = make_int4(e, s_off[e] + kTokTile * i, min(kTokTile, cnt - kTokTile * i), 0);
+    if (small_tiles(cnt)) {
+      const int r0 = cnt / kTokTile * kTokTile;
+      minfo_s[s_ns[e]] = make_int4(e, s_off[e] + r0, cnt - r0, 0);
+    }
   }
   for (int e = tid; e < E; e += 256) {
     int run = s_off[e];
@@ -457,7 +478,7 @@ cudaError_t launch_route_prefill(Handle* h, const __nv_bfloat16* x, int T, int32
   if (err != cudaSuccess) return err;
   {
     KernelTimer tm(h, FW_KERNEL_ROUTE_SCAN, s);
-    route_scan_kernel<<<1, 256, 0, s>>>(a, h->hist, n_tiles, h->minfo);
+    route_scan_kernel<<<1, 256, 0, s>>>(a, h->hist, n_tiles, h->minfo, h->minfo_s);
   }
   {
     KernelTimer tm(h, FW_KERNEL_ROUTE_SCATTER, s);

@@ -58,6 +58,8 @@ CASES = [
     ("tiny", dict(T=200, S=1)),                         # shared expert rows
     ("tiny", dict(T=64, I=192)),                        # I % 128 == 64: half-empty last gate/up tile
     ("tiny", dict(T=40, H=320, E=8, k=3)),              # H % 256 != 0: partial last down tile
+    ("tiny", dict(T=1000, k=2)),                        # 192-row tiles and small last tiles (both GEMM shapes)
+    ("tiny", dict(T=700, k=2, I=192, S=1)),             # large remainders (> 64 rows), shared expert, odd blocks
 ]
 
 
