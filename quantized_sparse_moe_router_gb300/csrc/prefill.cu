@@ -41,7 +41,8 @@ using namespace dev;
 constexpr int BM = 128, BK = 64;
 constexpr int kAStages = 4;                 // tensor-memory A stages (dequant -> MMA)
 constexpr int kEpiWarps = 4, kProducerWarp = 4, kMmaWarp = 5, kDeqWarp0 = 6, kDeqWarps = 8;
-constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;  // 448
+constexpr int kMmaWarp2 = kDeqWarp0 + kDeqWarps;        // the second MMA issuer (two-block shape)
+constexpr int kThreads = (kMmaWarp2 + 1) * 32;          // 480
 constexpr int kClusterSize = 2;             // CTA pairs share (multicast) each token tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSmemLimit = 227 * 1024; // dynamic shared memory a CTA may have
@@ -234,6 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap map_s, GemmArgs a) {
   using G = Shape<MB>;
   constexpr int kStages = G::Stages;
+  constexpr int kIssuers = MB;  // MMA-issuing threads: one per weight block
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], a_full[kAStages], a_empty[kAStages];
   __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], mma_done;
@@ -250,17 +252,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kClusterSize);  // both CTAs' MMAs read the multicast token tile
+      mbar_init(&empty[i], kClusterSize * kIssuers);  // both CTAs' MMAs read the multicast token tile
     }
     for (int i = 0; i < kAStages; ++i) {
       mbar_init(&a_full[i], kDeqWarps / 2);  // one group of four warps per stage
-      mbar_init(&a_empty[i], 1);
+      mbar_init(&a_empty[i], kIssuers);
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_full[i], kIssuers);
       mbar_init(&acc_empty[i], kEpiWarps);
     }
-    mbar_init(&mma_done, 1);
+    mbar_init(&mma_done, kIssuers);
     s_abort = 0;
     fence_mbar_init();
   }
@@ -322,9 +324,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // copies still in flight after an abort land before the CTA leaves
       for (uint32_t j = it > kStages ? it - kStages : 0; j < it; ++j) mbar_wait(&full[j % kStages], (j / kStages) & 1);
     }
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------ MMA issuer
-    if (lane == 0) {
+  } else if (warp == kMmaWarp || warp == kMmaWarp2) {
+    // ------------------------------------------------ MMA issuers
+    // One thread issues tcgen05.mma at only about one per 75-110 cycles
+    // whatever N is, which the small tiles' N <= 64 cannot afford: with two
+    // weight blocks each block has its own issuing warp (both wait for the
+    // same stages; the barriers the MMAs release count both commits).
+    if (lane == 0 && (warp == kMmaWarp || kIssuers == 2)) {
+      const int q = warp == kMmaWarp ? 0 : 1;
       uint32_t it = 0, tc = 0;
       int4 mi_next = cid < n_tiles ? a.minfo[cid / n_mb2] : make_int4(0, 0, 0, 0);
       for (int tile = cid; tile < n_tiles && ok; tile += ncl, ++tc) {
@@ -344,21 +351,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t b0 = smem_u32(sX + s * G::XBytes);
           const uint32_t a0 = tmem_base + G::ACol0 + sa * G::ACols;
 #pragma unroll
-          for (int mb = 0; mb < MB; ++mb)
-#pragma unroll
-            for (int k = 0; k < BK / 16; ++k)
-              mma_tmem_a(d_tmem + mb * G::BN, a0 + mb * (BK / 2) + k * 8, sw128_desc(b0 + k * 32), idesc,
-                         (kb | k) != 0);
+          for (int k = 0; k < BK / 16; ++k)  // block q
+            mma_tmem_a(d_tmem + q * G::BN, a0 + q * (BK / 2) + k * 8, sw128_desc(b0 + k * 32), idesc, (kb | k) != 0);
           mma_commit_mc(&empty[s], kPair);
           mma_commit(&a_empty[sa]);
         }
         if (ok) mma_commit(&acc_full[b]);
       }
-      // every MMA this thread issued has finished before TMEM is released
+      // every MMA either issuer issued has finished before TMEM is released
       mma_commit(&mma_done);
       mbar_wait(&mma_done, 0);
     }
-  } else if (warp >= kDeqWarp0) {
+  } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps) {
     // ------------------------------------------------ dequantisers: int8 x scale -> bf16 -> TMEM (A)
     // Two groups of four warps (one per TMEM lane quarter) take alternate
     // stages, so the conversion of one stage overlaps the next; a thread
