@@ -326,10 +326,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp || warp == kMmaWarp2) {
     // ------------------------------------------------ MMA issuers
-    // One thread issues tcgen05.mma at only about one per 75-110 cycles
-    // whatever N is, which the small tiles' N <= 64 cannot afford: with two
-    // weight blocks each block has its own issuing warp (both wait for the
-    // same stages; the barriers the MMAs release count both commits).
+    // At the small tiles' N <= 64 one thread's MMAs and commits keep the
+    // tensor pipe busy less than half of the time, two issuing threads reach
+    // its peak: with two weight blocks each block has its own issuing warp
+    // (both wait for the same stages; the barriers the MMAs release count
+    // both commits).
     if (lane == 0 && (warp == kMmaWarp || kIssuers == 2)) {
       const int q = warp == kMmaWarp ? 0 : 1;
       uint32_t it = 0, tc = 0;
