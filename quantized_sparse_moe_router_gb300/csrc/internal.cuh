@@ -73,7 +73,7 @@ struct PrefillMaps {
   CUtensorMap s_gu;   // scale plane [EU*H/32][2I] u16, box 128 x 2
   CUtensorMap q_d;    // [EU*H][I] u8 (row stride row_bytes(I))
   CUtensorMap s_d;    // [EU*I/32][H] u16
-  CUtensorMap w3;     // router planes [3E][H] bf16, box 64 x E, 128B swizzle (E <= 128)
+  CUtensorMap w3;     // router planes [3E][H] bf16, box 64 x min(E, 128), 128B swizzle (E <= 256)
 };
 
 struct Handle {

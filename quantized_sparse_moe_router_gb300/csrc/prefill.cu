@@ -486,7 +486,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // accumulator in tensor memory.
 constexpr int kRM = 128, kRK = 64, kRStages = 3;
 constexpr int kRThreads = 192;  // warp 0 TMA, warp 1 MMA (TMEM owner), warps 2-5 epilogue (lane quarters 2,3,0,1)
-constexpr int kRMaxE = 128;
+constexpr int kRMaxE = 256;
+constexpr int kRPassE = 128;    // experts per pass over x (E > 128: two passes, N = 128 each)
 
 struct RouteMmaArgs {
   const float* bias;
@@ -533,8 +534,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
   const int E = a.E, k = a.k, t0 = blockIdx.x * kRM;
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* sX = smem_raw + pad;                 // [kRStages][128 tokens][128 B]
-  uint8_t* sW = sX + kRStages * kRM * kRK * 2;  // [kRStages][3 planes][E rows][128 B]
-  const uint32_t wstage = 3u * E * kRK * 2;
+  const int BR = E < kRPassE ? E : kRPassE;      // W_r rows per pass
+  const int n_pass = (E + kRPassE - 1) / kRPassE;
+  uint8_t* sW = sX + kRStages * kRM * kRK * 2;  // [kRStages][3 planes][BR rows][128 B]
+  const uint32_t wstage = 3u * BR * kRK * 2;
   for (int i = threadIdx.x; i < 4 * kRMaxE; i += kRThreads) (&s_cnt[0][0])[i] = 0;
   for (int i = threadIdx.x; i < E; i += kRThreads) s_bias[i] = a.bias[i];
   if (threadIdx.x == 0) {
@@ -556,6 +559,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   tc_fence_after();
   const uint32_t tmem = s_tmem;
   const int KT = a.H / kRK;
+  const int NI = n_pass * KT;  // pipeline iterations: (pass, K step)
   // each CTA starts its K loop at its own offset, so the CTAs do not all ask
   // the same L2 lines for the same W_r tile at the same time
   const int kb0 = (int)(((int64_t)blockIdx.x * KT) / gridDim.x);
@@ -563,36 +567,38 @@ __global__ void __launch_bounds__(kRThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      for (int kb = 0; kb < KT && ok; ++kb) {
-        const int s = kb % kRStages;
+      for (int i = 0; i < NI && ok; ++i) {
+        const int s = i % kRStages, ps = i / KT, kb = i % KT;
         const int kk = kb + kb0 < KT ? kb + kb0 : kb + kb0 - KT;
-        if (!(ok = mbar_wait(&empty[s], ((kb / kRStages) & 1) ^ 1))) {
-          report_wait(a.meta, kSiteGemm, kb, 0);
+        if (!(ok = mbar_wait(&empty[s], ((i / kRStages) & 1) ^ 1))) {
+          report_wait(a.meta, kSiteGemm, i, 0);
           break;
         }
         mbar_arrive_expect_tx(&full[s], (uint32_t)kRM * kRK * 2 + wstage);
         tma_load_2d(sX + s * kRM * kRK * 2, &map_x, kk * kRK, t0, &full[s]);
         for (int p = 0; p < 3; ++p)
-          tma_load_2d(sW + s * wstage + p * E * kRK * 2, &map_w, kk * kRK, p * E, &full[s]);
+          tma_load_2d(sW + s * wstage + p * BR * kRK * 2, &map_w, kk * kRK, p * E + ps * kRPassE, &full[s]);
       }
-      for (int j = ::max(0, KT - kRStages); j < KT; ++j) mbar_wait(&full[j % kRStages], (j / kRStages) & 1);
+      for (int j = ::max(0, NI - kRStages); j < NI; ++j) mbar_wait(&full[j % kRStages], (j / kRStages) & 1);
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(kRM, E);
-      for (int kb = 0; kb < KT && ok; ++kb) {
-        const int s = kb % kRStages;
-        if (!(ok = mbar_wait(&full[s], (kb / kRStages) & 1))) {
-          report_wait(a.meta, kSiteGemm, kb, 1);
+      for (int i = 0; i < NI && ok; ++i) {
+        const int s = i % kRStages, ps = i / KT, kb = i % KT;
+        const int np = E - ps * kRPassE < kRPassE ? E - ps * kRPassE : kRPassE;  // this pass's experts
+        const uint32_t idesc = idesc_bf16(kRM, np);
+        if (!(ok = mbar_wait(&full[s], (i / kRStages) & 1))) {
+          report_wait(a.meta, kSiteGemm, i, 1);
           break;
         }
         tc_fence_after();
         const uint32_t x0 = smem_u32(sX + s * kRM * kRK * 2), w0 = smem_u32(sW + s * wstage);
+        const uint32_t d = tmem + ps * kRPassE;  // the pass's accumulator columns
 #pragma unroll
         for (int kk = 0; kk < kRK / 16; ++kk)
 #pragma unroll
           for (int p = 2; p >= 0; --p)  // smallest plane first
-            mma_ss(tmem, sw128_desc(x0 + kk * 32), sw128_desc(w0 + p * E * kRK * 2 + kk * 32), idesc,
+            mma_ss(d, sw128_desc(x0 + kk * 32), sw128_desc(w0 + p * BR * kRK * 2 + kk * 32), idesc,
                    (kb | kk | (2 - p)) != 0);
         mma_commit(&empty[s]);
       }
@@ -822,7 +828,7 @@ cudaError_t prepare_prefill(Handle* h) {
                   CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (e == cudaSuccess && h->wr3)
     e = encode_2d(&m->w3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->wr3, H, 3 * (uint64_t)h->cfg.E, H * 2, kRK,
-                  (uint32_t)h->cfg.E, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
+                  (uint32_t)std::min(h->cfg.E, kRPassE), CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   return e;
 }
 
@@ -855,7 +861,7 @@ cudaError_t launch_route_prefill_mma(Handle* h, const __nv_bfloat16* x, int T, i
   a.gates_out = gates_out;
   a.hist = h->hist;
   a.meta = h->meta;
-  const size_t smem = (size_t)kRStages * (kRM * kRK * 2 + 3 * E * kRK * 2) + 1024;
+  const size_t smem = (size_t)kRStages * (kRM * kRK * 2 + 3 * std::min(E, kRPassE) * kRK * 2) + 1024;
   const unsigned grid = (unsigned)((T + kRM - 1) / kRM);
   if (a.k <= 8)
     route_mma_kernel<8><<<grid, kRThreads, smem, s>>>(map_x, h->maps->w3, a);

@@ -256,23 +256,40 @@ __device__ __forceinline__ int small_tiles(int c) {
   return r > 0 && r <= kSmallTile ? 1 : 0;
 }
 
-__global__ void __launch_bounds__(256) route_scan_kernel(RouteArgs a, int32_t* hist, int n_tiles,
-                                                         int4* minfo, int4* minfo_s) {
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads) route_scan_kernel(RouteArgs a, int32_t* hist, int n_tiles,
+                                                                  int4* minfo, int4* minfo_s) {
   __shared__ int s_cnt[kMaxE + 2];
   __shared__ int s_off[kMaxE + 2];
   __shared__ int s_nz[kMaxE + 2];
   __shared__ int s_nt[kMaxE + 2];
   __shared__ int s_ns[kMaxE + 2];
+  __shared__ int s_part[kScanThreads];  // [part][expert]: the part's count (pass 1)
   const int E = a.E, EU = E + a.S, T = a.T, tid = threadIdx.x, lane = tid & 31;
-  for (int e = tid; e < E; e += 256) {
+  // thread (part, expert): the experts' per-tile counts are summed by P
+  // threads each over consecutive tile ranges (a few batched loads instead
+  // of n_tiles / 16 round trips)
+  int ep = 32;
+  while (ep < E) ep *= 2;
+  const int P = kScanThreads / ep, part = tid / ep, e_me = tid % ep;
+  const int per = (n_tiles + P - 1) / P, c_lo = ::min(n_tiles, part * per), c_hi = ::min(n_tiles, c_lo + per);
+  {
     int run = 0;
-    for (int c0 = 0; c0 < n_tiles; c0 += kScanBatch) {
-      int v[kScanBatch];
+    if (e_me < E)
+      for (int c0 = c_lo; c0 < c_hi; c0 += kScanBatch) {
+        int v[kScanBatch];
 #pragma unroll
-      for (int u = 0; u < kScanBatch; ++u) v[u] = c0 + u < n_tiles ? hist[(int64_t)(c0 + u) * E + e] : 0;
+        for (int u = 0; u < kScanBatch; ++u) v[u] = c0 + u < c_hi ? hist[(int64_t)(c0 + u) * E + e_me] : 0;
 #pragma unroll
-      for (int u = 0; u < kScanBatch; ++u) run += v[u];
-    }
+        for (int u = 0; u < kScanBatch; ++u) run += v[u];
+      }
+    s_part[tid] = run;
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += kScanThreads) {
+    int run = 0;
+    for (int q = 0; q < P; ++q) run += s_part[q * ep + e];
     s_cnt[e] = run;
   }
   if (a.S && tid == 0) s_cnt[E] = T;
@@ -327,8 +344,8 @@ __global__ void __launch_bounds__(256) route_scan_kernel(RouteArgs a, int32_t* h
     }
   }
   __syncthreads();
-  for (int e = tid; e < EU + 1; e += 256) a.offsets[e] = s_off[e];
-  for (int e = tid; e < EU; e += 256) {
+  for (int e = tid; e < EU + 1; e += kScanThreads) a.offsets[e] = s_off[e];
+  for (int e = tid; e < EU; e += kScanThreads) {
     const int cnt = s_cnt[e];
     a.counts[e] = cnt;
     if (cnt > 0) a.uinfo[s_nz[e]] = make_int4(e, s_off[e], cnt, 0);
@@ -340,16 +357,18 @@ __global__ void __launch_bounds__(256) route_scan_kernel(RouteArgs a, int32_t* h
       minfo_s[s_ns[e]] = make_int4(e, s_off[e] + r0, cnt - r0, 0);
     }
   }
-  for (int e = tid; e < E; e += 256) {
-    int run = s_off[e];
-    for (int c0 = 0; c0 < n_tiles; c0 += kScanBatch) {
+  // per-tile bases: thread (part, expert) starts after the parts before it
+  if (e_me < E) {
+    int run = s_off[e_me];
+    for (int q = 0; q < part; ++q) run += s_part[q * ep + e_me];
+    for (int c0 = c_lo; c0 < c_hi; c0 += kScanBatch) {
       int v[kScanBatch];
 #pragma unroll
-      for (int u = 0; u < kScanBatch; ++u) v[u] = c0 + u < n_tiles ? hist[(int64_t)(c0 + u) * E + e] : 0;
+      for (int u = 0; u < kScanBatch; ++u) v[u] = c0 + u < c_hi ? hist[(int64_t)(c0 + u) * E + e_me] : 0;
 #pragma unroll
       for (int u = 0; u < kScanBatch; ++u)
-        if (c0 + u < n_tiles) {
-          hist[(int64_t)(c0 + u) * E + e] = run;
+        if (c0 + u < c_hi) {
+          hist[(int64_t)(c0 + u) * E + e_me] = run;
           run += v[u];
         }
     }
@@ -478,7 +497,7 @@ cudaError_t launch_route_prefill(Handle* h, const __nv_bfloat16* x, int T, int32
   if (err != cudaSuccess) return err;
   {
     KernelTimer tm(h, FW_KERNEL_ROUTE_SCAN, s);
-    route_scan_kernel<<<1, 256, 0, s>>>(a, h->hist, n_tiles, h->minfo, h->minfo_s);
+    route_scan_kernel<<<1, kScanThreads, 0, s>>>(a, h->hist, n_tiles, h->minfo, h->minfo_s);
   }
   {
     KernelTimer tm(h, FW_KERNEL_ROUTE_SCATTER, s);

@@ -1,7 +1,7 @@
 """GPU parity of the quantiser, the repack, the routers and the decode path
 (T <= 16) against the fp64 oracle, through the C ABI.
 
-Bar: expert ids, offsets, perm and inv bit-exact; gates within 1e-5; outputs
+Bar: expert ids, offsets, perm and inv bit-exact; gates within GATE_TOL; outputs
 max |gpu - oracle| <= 1e-2 * max|oracle| + 1e-3 (the GPU's bf16 widened
 exactly to fp64)."""
 import numpy as np
@@ -14,12 +14,11 @@ if not torch.cuda.is_available():
 import oracle
 import quantized_sparse_moe_router_gb300 as fw
 import synth
-from layer_inputs import DeviceLayer, OracleLayer, hidden_with_margins, to_device_bf16, tolerance
+from layer_inputs import GATE_TOL, DeviceLayer, OracleLayer, hidden_with_margins, to_device_bf16, tolerance
 from synth import KIND_DOWN, KIND_GATE, KIND_UP
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
-GATE_TOL = 1e-5  # fp32 logits over H <= 8192 terms: gate error well below 1e-5 (1e-2 x output tolerance)
 
 
 @pytest.fixture(scope="module", autouse=True)

@@ -11,16 +11,14 @@ if not torch.cuda.is_available():
 import oracle
 import quantized_sparse_moe_router_gb300 as fw
 import synth
-from layer_inputs import DeviceLayer, OracleLayer, hidden_with_margins, to_device_bf16
+from layer_inputs import GATE_TOL, DeviceLayer, OracleLayer, hidden_with_margins, to_device_bf16
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
 # Gates from fp32-accurate logits: the decode router sums fp32 FMAs; the
 # prefill router adds exact bf16-plane products in a tensor-core fp32
-# accumulator, whose truncating accumulation over H/16 x 3 steps moves logits
-# by ~2e-5 relative -- far below the 1e-3 logit margin of the inputs, and
-# within this bound on the gates (the one used across the suite).
-GATE_TOL = 1e-5
+# accumulator over H/16 x 3 steps. Either stays far below the 1e-3 logit
+# margin of the inputs (ids bit-exact); GATE_TOL is the suite's gate bound.
 
 
 def route_and_check(wl, x, dl, ol, layer):
@@ -41,7 +39,7 @@ def route_and_check(wl, x, dl, ol, layer):
 
 
 @pytest.mark.parametrize("T", [17, 33, 129, 1000])
-@pytest.mark.parametrize("E, k", [(8, 2), (64, 8), (256, 8), (40, 5), (48, 12), (128, 16)])
+@pytest.mark.parametrize("E, k", [(8, 2), (64, 8), (256, 8), (40, 5), (48, 12), (128, 16), (192, 6)])
 def test_tiled_router_small(T, E, k):
     wl = synth.WORKLOADS["tiny"].with_(E=E, k=k, T=T, sigma_router=0.1)
     dl = DeviceLayer(wl, 0, DEV)

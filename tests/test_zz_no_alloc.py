@@ -13,11 +13,10 @@ if not torch.cuda.is_available():
 
 import quantized_sparse_moe_router_gb300 as fw
 import synth
-from layer_inputs import DeviceLayer, OracleLayer, hidden_with_margins, to_device_bf16
+from layer_inputs import GATE_TOL, DeviceLayer, OracleLayer, hidden_with_margins, to_device_bf16
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
-GATE_TOL = 1e-5  # fp32 logits over H <= 8192 terms: gate error well below 1e-5 (1e-2 x output tolerance)
 
 
 @pytest.mark.parametrize("name, over", [("tiny", dict(T=4)), ("dec16", {}), ("tiny", dict(T=16, E=256, k=8))])
