@@ -210,7 +210,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
     }
   }
   pdl_wait();  // the router's logits (and its reset of the grid barrier)
-  route_in_smem<kThreads>(a.logits, T, a.E, a.k, a.S, r);
+  if (kOne)
+    route_one_in_smem<kThreads>(a.logits, a.E, a.k, a.S, r);
+  else
+    route_in_smem<kThreads>(a.logits, T, a.E, a.k, a.S, r);
   if (a.publish && blockIdx.x == 0) publish_routing<kThreads>(r, T, a.E, a.k, a.S, a.ro);
 
   const int nU = r.n_unique;

@@ -222,6 +222,81 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
   __syncthreads();
 }
 
+// The same for one token (T = 1), with less work and code: the k selected
+// experts each get one grouped row, so the grouping is a sort of k ids; the
+// counts and offsets for all experts (read only when CTA 0 publishes) come
+// from comparisons with the k ids.
+template <int NT>
+__device__ void route_one_in_smem(const float* logits, int E, int k, int S, SmemRouting& r) {
+  constexpr int NW = NT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  for (int i = tid; i < E; i += NT) r.z[i] = __ldcg(logits + i);
+  __syncthreads();
+  {
+    int s = 32;  // lanes per expert, as many as the block allows
+    while (s > 1 && E * s > NT) s >>= 1;
+    const int gpw = 32 / s, c = lane & (s - 1);
+    for (int b = warp * gpw; b < E; b += NW * gpw) {  // warp-uniform trip count
+      const int e = b + lane / s;
+      int rank = 0;
+      float z = 0.f;
+      if (e < E) {
+        z = r.z[e];
+#pragma unroll 4
+        for (int f = c; f < E; f += s) {
+          const float zf = r.z[f];
+          rank += (zf > z) | ((zf == z) & (f < e));
+        }
+      }
+      for (int o = 1; o < s; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+      if (e < E && c == 0 && rank < k) {
+        r.ids[rank] = e;
+        r.zsel[rank] = z;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // lane j < k: the expert of rank j, its row among the k ids in ascending order
+    const int e = lane < k ? r.ids[lane] : 0x7FFFFFFF;
+    int pos = 0;
+    for (int m = 0; m < k; ++m) pos += __shfl_sync(0xFFFFFFFFu, e, m) < e;
+    const float g = warp_gate(lane < k ? r.zsel[lane] : 0.f, k, lane);
+    if (lane < k) {
+      r.gates[lane] = g;
+      r.u[pos] = make_int4(e, pos, 1, 0);
+      r.tok[pos] = 0;
+      r.slot[pos] = lane;
+    }
+    if (lane == 0) {
+      if (S) {
+        r.u[k] = make_int4(E, k, 1, 0);
+        r.tok[k] = 0;
+        r.slot[k] = k;
+        r.gates[k] = 1.0f;
+      }
+      r.n_unique = k + S;
+      r.rows = k + S;
+    }
+  } else {
+    for (int i = tid - 32; i <= E + S; i += NT - 32) {  // offsets [EU + 1], counts [EU]
+      int before = 0, hit = 0;
+      for (int m = 0; m < k; ++m) {
+        const int em = r.ids[m];
+        before += em < i;
+        hit += em == i;
+      }
+      if (i >= E) {  // the shared expert's row comes after the k routed ones
+        before = k + (i > E ? 1 : 0);
+        hit = i == E ? 1 : 0;
+      }
+      r.off[i] = before;
+      if (i < E + S) r.cnt[i] = hit;
+    }
+  }
+  __syncthreads();
+}
+
 // Publish a routing computed by route_in_smem (whole block).
 struct RoutingOut {
   int32_t* ids_out;    // caller [T][k]
