@@ -225,16 +225,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   //  * several tokens: the cost of a unit is its expert's token count, so
   //    R-unit chunks are handed out -- CTA b's first kStaticChunks are b,
   //    b + grid, ..., the rest come from a ticket counter.
-  const int64_t n_units = (int64_t)nU * I;
+  // (32-bit indices throughout the loops: a 64-bit division is a long
+  // software routine, and these run once per stage in every warp)
+  const int n_units = nU * I;
   const int64_t n_grp = n_units / kGUGroup;
-  const int64_t lo = n_grp * blockIdx.x / gridDim.x * kGUGroup, hi = n_grp * (blockIdx.x + 1) / gridDim.x * kGUGroup;
+  const int lo = (int)(n_grp * blockIdx.x / gridDim.x) * kGUGroup;
+  const int hi = (int)(n_grp * (blockIdx.x + 1) / gridDim.x) * kGUGroup;
   // down stages: output rows [o0, o1), blocks of 16 rows; per block every touched expert
   const int o0 = (int)((int64_t)H * blockIdx.x / gridDim.x), o1 = (int)((int64_t)H * (blockIdx.x + 1) / gridDim.x);
   // (a down stage holds the same 16-row block of up to n_per experts, so that
   // a warp's dot products for those experts overlap)
   const int n_blk = (o1 - o0 + kRowBlock - 1) / kRowBlock;
   const int n_ge = (nU + a.n_per - 1) / a.n_per;
-  const int64_t n_dn = (int64_t)n_ge * n_blk;
+  const int n_dn = n_ge * n_blk;
 
   if (warp == kProducer) {
     // ------------------------------------------------------ producer
@@ -246,11 +249,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       // (several tokens) chunk of the current stage and of the next two: the
       // ticket for the second is requested two stages ahead, so its round
       // trip overlaps copies
-      int64_t j = 0, c = blockIdx.x, q0 = (int64_t)blockIdx.x + gridDim.x, q1 = 0;
-      if (!kOne) q1 = (int64_t)atomicAdd(&a.meta->chunk_ctr, 1u) + (int64_t)kStaticChunks * gridDim.x;
-      int64_t su = lo;  // (one token) next unit of the CTA's range
+      int j = 0, c = blockIdx.x, q0 = blockIdx.x + gridDim.x, q1 = 0;
+      if (!kOne) q1 = (int)atomicAdd(&a.meta->chunk_ctr, 1u) + kStaticChunks * (int)gridDim.x;
+      int su = lo;      // (one token) next unit of the CTA's range
       bool gu = true;   // still issuing gate/up stages
-      for (int64_t jd = 0; gu || jd < n_dn; ++j) {
+      int st = 0;       // j % stages
+      uint32_t ph = 0;  // (j / stages) & 1
+      int ge = 0, blk = 0;  // down stage jd: expert group, row block
+      for (int jd = 0; gu || jd < n_dn;) {
         if (pf && j == a.stages) {  // the ring is full: the TMA unit has time for it
           pf = false;
           for (int u = 0; u < nU; ++u) {
@@ -258,53 +264,59 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
             prefetch_l2(a.q_d + row * rb_i, (uint32_t)(o1 - o0) * rb_i);
           }
         }
-        const int st = (int)(j % a.stages);
-        if (j >= a.stages && !mbar_wait(&empty[st], (uint32_t)(((j / a.stages) - 1) & 1))) {
-          report_wait(a.meta, kSiteGuEmpty, j, (int)n_dn);
+        if (j >= a.stages && !mbar_wait(&empty[st], ph ^ 1u)) {
+          report_wait(a.meta, kSiteGuEmpty, j, n_dn);
           break;
         }
         uint8_t* sb = ring + (size_t)st * a.stage_bytes;
         if (gu) {
-          int64_t u0, u1;
+          int u0, u1;
           if (kOne) {
             u0 = su;
-            u1 = std::min<int64_t>(hi, (su / R + 1) * R);
+            u1 = ::min(hi, (su / R + 1) * R);
             su = u1;
           } else {
             u0 = c * R;
             u1 = u0 + R;
             c = q0;
             q0 = q1;
-            q1 = (int64_t)atomicAdd(&a.meta->chunk_ctr, 1u) + (int64_t)kStaticChunks * gridDim.x;
+            q1 = (int)atomicAdd(&a.meta->chunk_ctr, 1u) + kStaticChunks * (int)gridDim.x;
           }
           if (u0 >= (kOne ? hi : n_units)) {
             gu = false;
-            if (kOne) {  // the consumers know the count: go straight to the down stages
-              --j;
-              continue;
-            }
+            if (kOne) continue;  // the consumers know the count: this slot goes to the down stages
             stage_units[st] = make_int2(-1, -1);  // ticketed work: an empty stage tells the consumers
             mbar_arrive(&full[st]);
-            continue;
+          } else {
+            stage_units[st] = make_int2(u0, u1);
+            const int eu = u0 / I;  // a stage never spans two experts (R divides I)
+            const int e = r.u[eu].x, i0 = u0 - eu * I;
+            const uint32_t bytes = (uint32_t)(u1 - u0) * 2 * rb_h;
+            mbar_arrive_expect_tx(&full[st], bytes);
+            bulk_g2s(sb, a.q_gu + ((int64_t)e * 2 * I + 2 * i0) * rb_h, bytes, &full[st]);
           }
-          stage_units[st] = make_int2((int)u0, (int)u1);
-          const int e = r.u[u0 / I].x, i0 = (int)(u0 % I);
-          const uint32_t bytes = (uint32_t)(u1 - u0) * 2 * rb_h;
-          mbar_arrive_expect_tx(&full[st], bytes);
-          bulk_g2s(sb, a.q_gu + ((int64_t)e * 2 * I + 2 * i0) * rb_h, bytes, &full[st]);
         } else {
           // block-major: all expert groups of block 0, then block 1, ...
-          const int blk = (int)(jd / n_ge), e0 = (int)(jd % n_ge) * a.n_per, e1 = ::min(nU, e0 + a.n_per);
+          const int e0 = ge * a.n_per, e1 = ::min(nU, e0 + a.n_per);
           const int r0 = o0 + blk * kRowBlock, nr = ::min(kRowBlock + 0, o1 - r0);
           mbar_arrive_expect_tx(&full[st], (uint32_t)(e1 - e0) * nr * rb_i);
           for (int u = e0; u < e1; ++u)
             bulk_g2s(sb + (size_t)(u - e0) * kRowBlock * rb_i, a.q_d + ((int64_t)r.u[u].x * H + r0) * rb_i,
                      (uint32_t)nr * rb_i, &full[st]);
           ++jd;
+          if (++ge == n_ge) {
+            ge = 0;
+            ++blk;
+          }
+        }
+        ++j;
+        if (++st == a.stages) {
+          st = 0;
+          ph ^= 1u;
         }
       }
       // every copy issued has landed before the CTA may leave
-      for (int64_t q = std::max<int64_t>(0, j - a.stages); q < j; ++q)
+      for (int q = ::max(0, j - a.stages); q < j; ++q)
         mbar_wait(&full[q % a.stages], (uint32_t)((q / a.stages) & 1));
     }
   } else {
@@ -316,10 +328,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
     // its units of the stage's chunk, until the empty stage.
     const int nseg_h = H / 16;
     // stages of gate/up work this CTA took (ticketed work: then one empty stage)
-    int64_t n_gu = kOne ? (hi > lo ? (hi + R - 1) / R - lo / R : 0) : 0;
-    for (int64_t j = 0; ok && (!kOne || j < n_gu); ++j) {
-      const int st = (int)(j % a.stages);
-      if (!mbar_wait(&full[st], (uint32_t)((j / a.stages) & 1))) {
+    int n_gu = kOne ? (hi > lo ? (hi + R - 1) / R - lo / R : 0) : 0;
+    int st = 0;       // j % stages
+    uint32_t ph = 0;  // (j / stages) & 1
+    for (int j = 0; ok && (!kOne || j < n_gu); ++j) {
+      if (!mbar_wait(&full[st], ph)) {
         report_wait(a.meta, kSiteGuFull, j, warp);
         ok = false;
         break;
@@ -331,11 +344,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
         n_gu = j + 1;
         break;
       }
-      const int64_t u0 = su.x, u1 = su.y;
+      const int u0 = su.x, u1 = su.y;
       const uint8_t* sb = ring + (size_t)st * a.stage_bytes;
+      const int eu = u0 / I;  // the stage's expert (a stage never spans two)
+      const int4 ui = r.u[eu];
       // units alternate over the warps from stage to stage: unit q of stage j
       // goes to warp (j R + q) mod 16
-      for (int64_t g = u0 + ((warp - j * R) % kCW + kCW) % kCW; g < u1; g += kCW) {
+      for (int g = u0 + ((warp - j * R) % kCW + kCW) % kCW; g < u1; g += kCW) {
         // the stage holds rows 2 i0 .. 2 i1 of the expert: per group, kGUGroup
         // gate rows then their up rows; u0 is group-aligned
         const int off = (int)(g - u0);
@@ -343,8 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
         const uint8_t* qu_row = qg_row + (size_t)kGUGroup * rb_h;
         const uint16_t* sg = reinterpret_cast<const uint16_t*>(qg_row + H);
         const uint16_t* su = reinterpret_cast<const uint16_t*>(qu_row + H);
-        const int4 ui = r.u[g / I];
-        const int i = (int)(g % I);
+        const int i = g - eu * I;
         auto load_x = [&](int t, int seg, f2(&xv)[8]) {
           if (x_mode == kXSmemF32) {
             x16_from_f32_t(reinterpret_cast<const float*>(smem) + (size_t)t * H, H, seg, xv);
@@ -405,6 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
+      if (++st == a.stages) {
+        st = 0;
+        ph ^= 1u;
+      }
     }
 
     // ---- phase 2: every CTA's h is written before any CTA reads it. The
@@ -446,15 +464,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
     float part[kMaxDecodeT];
 #pragma unroll
     for (int t = 0; t < kMaxDecodeT; ++t) part[t] = 0.f;
-    for (int64_t jd = 0; jd < n_dn && ok; ++jd) {
-      const int64_t j = n_gu + jd;
-      const int st = (int)(j % a.stages);
-      if (!mbar_wait(&full[st], (uint32_t)((j / a.stages) & 1))) {
-        report_wait(a.meta, kSiteDnFull, j, warp);
+    st = n_gu % a.stages;  // ring position of stage n_gu + jd
+    ph = (uint32_t)(n_gu / a.stages) & 1u;
+    int ge = 0, blk = 0;  // expert group and row block of down stage jd
+    for (int jd = 0; jd < n_dn && ok; ++jd) {
+      if (!mbar_wait(&full[st], ph)) {
+        report_wait(a.meta, kSiteDnFull, n_gu + jd, warp);
         ok = false;
         break;
       }
-      const int ge = (int)(jd % n_ge), blk = (int)(jd / n_ge);
       const int e0 = ge * a.n_per, ne = ::min(nU, e0 + a.n_per) - e0;
       const int r0 = o0 + blk * kRowBlock;
       const int nr = ::min(kRowBlock + 0, o1 - r0);
@@ -533,6 +551,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
           }
           if (lane < T) a.out[(int64_t)lane * H + r0 + warp] = __float2bfloat16_rn(mine);
         }
+      }
+      if (++ge == n_ge) {
+        ge = 0;
+        ++blk;
+      }
+      if (++st == a.stages) {
+        st = 0;
+        ph ^= 1u;
       }
     }
   }
