@@ -671,48 +671,54 @@ __global__ void split_router_kernel(const float* __restrict__ wr, int64_t n, __n
 }
 
 // ------------------------------------------------------------- gather, combine
-// xperm[pos] = x[row_token[pos]], 16 bytes per thread.
-__global__ void gather_rows_kernel(const __nv_bfloat16* __restrict__ x, const int32_t* __restrict__ row_token,
-                                   int rows, int H, __nv_bfloat16* __restrict__ xperm) {
-  const int chunks = H / 8;
-  const int64_t n = (int64_t)rows * chunks;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t pos = i / chunks;
-    const int c = (int)(i % chunks);
-    const uint4 v = __ldg(reinterpret_cast<const uint4*>(x + (int64_t)row_token[pos] * H) + c);
-    reinterpret_cast<uint4*>(xperm + pos * H)[c] = v;
+// One warp per row, 16 bytes per lane per step (no per-element division).
+constexpr int kRowThreads = 256;
+
+// xperm[pos] = x[row_token[pos]].
+__global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
+                                                                  const int32_t* __restrict__ row_token, int rows,
+                                                                  int H, __nv_bfloat16* __restrict__ xperm) {
+  const int chunks = H / 8, lane = threadIdx.x & 31;
+  const int nw = gridDim.x * (kRowThreads / 32);
+  for (int pos = blockIdx.x * (kRowThreads / 32) + (threadIdx.x >> 5); pos < rows; pos += nw) {
+    const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)row_token[pos] * H);
+    uint4* dst = reinterpret_cast<uint4*>(xperm + (int64_t)pos * H);
+    for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
   }
 }
 
 // out[t] = sum over the token's slots j (ascending) of Yp[inv[t*k + j]], then
-// the shared expert's row; fp32 sum, one bf16 rounding.
-__global__ void combine_kernel(const __nv_bfloat16* __restrict__ yp, const int32_t* __restrict__ inv, int T, int k,
-                               int S, int H, __nv_bfloat16* __restrict__ out) {
+// the shared expert's row; fp32 sum, one bf16 rounding. One CTA per token,
+// a thread per 16-byte chunk (all of a chunk's k + S row loads in flight).
+__global__ void __launch_bounds__(kRowThreads) combine_kernel(const __nv_bfloat16* __restrict__ yp,
+                                                              const int32_t* __restrict__ inv, int T, int k, int S,
+                                                              int H, __nv_bfloat16* __restrict__ out) {
   const int chunks = H / 8;
-  const int64_t n = (int64_t)T * chunks;
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
-    const int t = (int)(i / chunks), c = (int)(i % chunks);
-    float acc[8];
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    for (int c = threadIdx.x; c < chunks; c += kRowThreads) {
+      float acc[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-    for (int j = 0; j < k + S; ++j) {
-      const int slot = j < k ? t * k + j : T * k + t;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(yp + (int64_t)inv[slot] * H) + c);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+#pragma unroll 4
+      for (int j = 0; j < k + S; ++j) {
+        const int slot = j < k ? t * k + j : T * k + t;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(yp + (int64_t)inv[slot] * H) + c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float lo, hi;
-        bf16x2_to_f32(w[q], lo, hi);
-        acc[2 * q] += lo;
-        acc[2 * q + 1] += hi;
+        for (int q = 0; q < 4; ++q) {
+          float lo, hi;
+          bf16x2_to_f32(w[q], lo, hi);
+          acc[2 * q] += lo;
+          acc[2 * q + 1] += hi;
+        }
       }
+      uint4 o;
+      o.x = pack_bf16x2(acc[0], acc[1]);
+      o.y = pack_bf16x2(acc[2], acc[3]);
+      o.z = pack_bf16x2(acc[4], acc[5]);
+      o.w = pack_bf16x2(acc[6], acc[7]);
+      reinterpret_cast<uint4*>(out + (int64_t)t * H)[c] = o;
     }
-    uint4 o;
-    o.x = pack_bf16x2(acc[0], acc[1]);
-    o.y = pack_bf16x2(acc[2], acc[3]);
-    o.z = pack_bf16x2(acc[4], acc[5]);
-    o.w = pack_bf16x2(acc[6], acc[7]);
-    reinterpret_cast<uint4*>(out + (int64_t)t * H)[c] = o;
   }
 }
 
@@ -877,8 +883,8 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
   cudaError_t err;
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_GATHER, s);
-    gather_rows_kernel<<<grid_for((int64_t)rows * (H / 8), 256, h->num_sms * 8), 256, 0, s>>>(x, h->row_token, rows,
-                                                                                            H, h->xperm);
+    gather_rows_kernel<<<grid_for(rows, kRowThreads / 32, h->num_sms * 8), kRowThreads, 0, s>>>(x, h->row_token,
+                                                                                               rows, H, h->xperm);
   }
   // each projection: the tiles of more than kSmallTile rows, then the small ones
   GemmArgs g, gs;
@@ -924,8 +930,7 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
   if (err != cudaSuccess) return err;
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_COMBINE, s);
-    combine_kernel<<<grid_for((int64_t)T * (H / 8), 256, h->num_sms * 8), 256, 0, s>>>(h->yp, h->inv, T, k, S, H,
-                                                                                     out);
+    combine_kernel<<<(unsigned)std::min(T, h->num_sms * 16), kRowThreads, 0, s>>>(h->yp, h->inv, T, k, S, H, out);
   }
   return cudaGetLastError();
 }
