@@ -291,7 +291,8 @@ def run_fw(args, rank, world, local_rank):
     # ---- per-kernel timing pass (events around every kernel; same K steps)
     ids_log = []
     for L in layers:
-        fw.fw_moe_profile_begin(L.handle, 8 * N_X_ROWS * max(args.steps, 1))
+        # room for every launch: 2 kernels per decode call, at most 12 per prefill call
+        fw.fw_moe_profile_begin(L.handle, (2 if T <= 16 else 12) * N_X_ROWS * max(args.steps, 1))
     ids_all = torch.empty((args.steps, N_X_ROWS, n_layers, T, k), dtype=torch.int32, device=dev)
     for s_ in range(args.steps):
         for r in range(N_X_ROWS):
@@ -307,27 +308,34 @@ def run_fw(args, rank, world, local_rank):
             a[1] += cnt
     ids_np = ids_all.cpu().numpy().reshape(-1, T, k)
     work = algorithmic(w, ids_np)
-    launches_per_call = sum(c for _, c in prof.values()) / (args.steps * calls_per_step)
+    n_calls = args.steps * calls_per_step
+    launches_per_call = sum(c for _, c in prof.values()) / n_calls
+
+    def avg_launch_ms(name):  # mean duration of one launch of this kind
+        tot, cnt = prof.get(name, (0.0, 0))
+        return tot / cnt if cnt else 0.0
+
     hbm, bf16_burst, bf16_sus, peak_src = load_peaks()
     decode = T <= 16
     if decode:
-        dom = "decode_experts"  # gate/up + down + combine in one kernel
-        dom_bytes = work["gu_bytes"] + work["d_bytes"]
-        dom_ms, dom_n = prof[dom]
-        achieved = dom_bytes / (dom_ms / 1e3) / 1e9
+        dom = "decode_experts"  # gate/up + down + combine in one kernel (one launch per call)
+        dom_bytes = (work["gu_bytes"] + work["d_bytes"]) / n_calls
+        t_ms = avg_launch_ms(dom)
+        achieved = dom_bytes / (t_ms / 1e3) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                     "frac": round(achieved / hbm, 4), "traffic": measured_traffic(dom, w.name), "kernel": dom,
-                    "avg_launch_us": round(dom_ms / dom_n * 1e3, 3),
-                    "algorithmic_bytes_per_launch": round(dom_bytes / dom_n),
+                    "avg_launch_us": round(t_ms * 1e3, 3),
+                    "algorithmic_bytes_per_launch": round(dom_bytes),
                     "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"}
     else:
-        dom = "prefill_gateup"  # both launches: the large-tile and the small-tile GEMM
-        dom_ms, dom_n = prof.get(dom, (float("nan"), 1))
-        dom_ms += prof.get("prefill_gateup_small", (0.0, 0))[0]
-        fl = work["flops"] * 2 / 3
-        achieved = fl / (dom_ms / 1e3) / 1e12
+        # the gate/up "launch": the pair of GEMM launches of one call (192-row tiles, then the small tiles)
+        dom = "prefill_gateup"
+        t_ms = avg_launch_ms(dom) + avg_launch_ms("prefill_gateup_small")
+        fl = work["flops"] * 2 / 3 / n_calls
+        achieved = fl / (t_ms / 1e3) / 1e12
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16_burst, "unit": "TFLOP/s",
                     "frac": round(achieved / bf16_burst, 4), "traffic": measured_traffic(dom, w.name), "kernel": dom,
+                    "avg_launch_us": round(t_ms * 1e3, 3), "algorithmic_flops_per_launch": round(fl),
                     "peak_source": f"{peak_src} bf16_tflops (cuBLAS burst)"}
     step_bytes = work["bytes"] / args.steps
     whole = {"algorithmic_GBps": round(step_bytes / (ms / args.steps / 1e3) / 1e9, 1),
