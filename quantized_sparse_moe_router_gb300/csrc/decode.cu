@@ -38,6 +38,7 @@ constexpr int kProducer = kCW;
 constexpr int kMaxStages = 16;
 constexpr int kRowBlock = 16;              // output rows per W_down block
 constexpr int kMaxPer = 2;                 // experts' blocks per W_down stage
+constexpr int kMaxRowsOne = 128;           // output rows per CTA of the one-token instantiation
 constexpr int kStaticChunks = 2;           // gate/up chunks per CTA assigned without a ticket
 constexpr uint32_t kConsumerBarrier = 1;   // named barrier of the 16 consumer warps
 constexpr int64_t kL2PrefetchMax = 40ll << 20;  // W_down bytes per call prefetched into L2 (L2 is 129 MB)
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
   __shared__ SmemRouting r;
   __shared__ int2 stage_units[kMaxStages];  // gate/up units [x, y) held by each ring stage (x < 0: no more)
+  __shared__ float s_half[2][kMaxRowsOne];   // (one token) the two halves of each output row
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = a.H, I = a.I, T = kOne ? 1 : a.T, R = a.R;
   const int x_mode = kOne ? (int)kXSmemF32 : a.x_mode;
@@ -476,40 +478,55 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       const int e0 = ge * a.n_per, ne = ::min(nU, e0 + a.n_per) - e0;
       const int r0 = o0 + blk * kRowBlock;
       const int nr = ::min(kRowBlock + 0, o1 - r0);
-      if (warp < nr) {
-        const uint8_t* sb = ring + (size_t)st * a.stage_bytes + (size_t)warp * rb_i;
-        if (T == 1) {
-          // one row per expert: the stage's experts' dot products interleaved
-          float dacc[kMaxPer];
+      if (kOne) {
+        // one token: warp w takes rows ra = w & 7 and ra + 8 of the block and
+        // the segments of parity w >> 3, so an h segment is loaded once for
+        // two rows; the two halves of a row are added after the loop
+        const int ra = warp & 7, hf = warp >> 3;
+        if (ra < nr) {
+          const bool has_b = ra + 8 < nr;
+          const uint8_t* sa = ring + (size_t)st * a.stage_bytes + (size_t)ra * rb_i;
+          float da[kMaxPer], db[kMaxPer];
           const float* hrow[kMaxPer];
 #pragma unroll
           for (int el = 0; el < kMaxPer; ++el) {
-            dacc[el] = 0.f;
+            da[el] = 0.f;
+            db[el] = 0.f;
             hrow[el] = hsrc + (size_t)(el < ne ? r.u[e0 + el].y : 0) * I;
           }
-          for (int seg = lane; seg < nseg_i; seg += 32) {
+          for (int seg = 2 * lane + hf; seg < nseg_i; seg += 64) {
 #pragma unroll
             for (int el = 0; el < kMaxPer; ++el) {
               if (el < ne) {
-                const uint8_t* qrow = sb + (size_t)el * kRowBlock * rb_i;
+                const uint8_t* qa = sa + (size_t)el * kRowBlock * rb_i;
                 f2 hv[8];
                 if (a.h_smem)
                   x16_from_f32_t(hrow[el], I, seg, hv);
                 else
                   x16_from_f32_global(hrow[el] + seg * 16, hv);
-                const uint4 qq = *reinterpret_cast<const uint4*>(qrow + seg * 16);
-                const uint16_t* sc = reinterpret_cast<const uint16_t*>(qrow + I);
-                dacc[el] = fmaf(half_bits_to_f32(sc[seg >> 1]), dot16(qq, hv), dacc[el]);
+                const uint4 qq = *reinterpret_cast<const uint4*>(qa + seg * 16);
+                da[el] = fmaf(half_bits_to_f32(reinterpret_cast<const uint16_t*>(qa + I)[seg >> 1]), dot16(qq, hv),
+                              da[el]);
+                if (has_b) {
+                  const uint8_t* qb = qa + (size_t)8 * rb_i;
+                  const uint4 qr = *reinterpret_cast<const uint4*>(qb + seg * 16);
+                  db[el] = fmaf(half_bits_to_f32(reinterpret_cast<const uint16_t*>(qb + I)[seg >> 1]), dot16(qr, hv),
+                                db[el]);
+                }
               }
             }
           }
 #pragma unroll
           for (int el = 0; el < kMaxPer; ++el)
             if (el < ne) {
-              const int pos = r.u[e0 + el].y;
-              part[0] = fmaf(r.gates[r.slot[pos]], dacc[el], part[0]);
+              const float g = r.gates[r.slot[r.u[e0 + el].y]];
+              part[0] = fmaf(g, da[el], part[0]);
+              part[1] = fmaf(g, db[el], part[1]);
             }
-        } else {
+        }
+      } else if (warp < nr) {
+        const uint8_t* sb = ring + (size_t)st * a.stage_bytes + (size_t)warp * rb_i;
+        if (T == 1) {        } else {
           for (int el = 0; el < ne; ++el) {
             const int4 ui = r.u[e0 + el];
             const uint8_t* qrow = sb + (size_t)el * kRowBlock * rb_i;
@@ -538,7 +555,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
-      if (ge == n_ge - 1) {  // block done: one reduction per token, lane t writes token t
+      if (ge == n_ge - 1 && kOne) {  // block done: this warp's halves of its two rows
+        const float va = warp_sum(part[0]), vb = warp_sum(part[1]);
+        const int ra = warp & 7, hf = warp >> 3, rr = blk * kRowBlock + ra;
+        if (lane == 0 && ra < nr) s_half[hf][rr] = va;
+        if (lane == 0 && ra + 8 < nr) s_half[hf][rr + 8] = vb;
+        part[0] = 0.f;
+        part[1] = 0.f;
+      } else if (ge == n_ge - 1) {  // block done: one reduction per token, lane t writes token t
         if (warp < nr) {
           float mine = 0.f;
 #pragma unroll
@@ -561,6 +585,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
         ph ^= 1u;
       }
     }
+    if (kOne) {  // every consumer warp gets here (a timed-out wait ends the loop, not the warp)
+      consumer_sync();
+      for (int i = tid; i < o1 - o0; i += kCW * 32) a.out[o0 + i] = __float2bfloat16_rn(s_half[0][i] + s_half[1][i]);
+    }
   }
   __syncthreads();
 }
@@ -580,8 +608,9 @@ cudaError_t launch(const DecodeArgs& a, unsigned grid, size_t smem, cudaStream_t
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return a.T == 1 && a.x_mode == kXSmemF32 ? cudaLaunchKernelEx(&cfg, decode_experts_kernel<true>, a)
-                                           : cudaLaunchKernelEx(&cfg, decode_experts_kernel<false>, a);
+  const bool one = a.T == 1 && a.x_mode == kXSmemF32 && (a.H + (int)grid - 1) / (int)grid <= kMaxRowsOne;
+  return one ? cudaLaunchKernelEx(&cfg, decode_experts_kernel<true>, a)
+             : cudaLaunchKernelEx(&cfg, decode_experts_kernel<false>, a);
 }
 
 int g_smem_optin = 0;
@@ -594,10 +623,13 @@ cudaError_t configure_decode_kernels() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  cudaFuncAttributes fa;
+  // the dynamic budget is what the larger static footprint of the two
+  // instantiations leaves (the one-token one also holds the row halves)
+  cudaFuncAttributes fa, fb;
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, decode_experts_kernel<false>);
+  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fb, decode_experts_kernel<true>);
   if (e == cudaSuccess) {
-    g_smem_optin -= (int)fa.sharedSizeBytes;
+    g_smem_optin -= (int)std::max(fa.sharedSizeBytes, fb.sharedSizeBytes);
     e = cudaFuncSetAttribute(decode_experts_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_optin);
   }
   if (e == cudaSuccess)
