@@ -90,12 +90,28 @@ KERNEL_SOURCES = {
 }
 
 
-def kernel_source_hash(kernel: str) -> str:
+def code_only(text: str) -> str:
+    """A CUDA source without its comments, trailing blanks and empty lines: a
+    change of comments alone leaves the measured code, and so the hash, as it
+    was."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
+def source_hash(texts) -> str:
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(ROOT, "quantized_sparse_moe_router_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    for t in texts:
+        h.update(code_only(t).encode())
     return h.hexdigest()
+
+
+def kernel_source_hash(kernel: str) -> str:
+    texts = []
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "quantized_sparse_moe_router_gb300", "csrc", f)) as fh:
+            texts.append(fh.read())
+    return source_hash(texts)
 
 
 def measured_traffic(kernel: str, workload: str):

@@ -19,14 +19,18 @@
 //
 // The weights are the MMA's A operand (M = 128 rows, read from tensor
 // memory, written there by the dequantising warps with tcgen05.st); the
-// tokens are B (N = the tile's rows rounded up to 16, at most 192; K-major
-// bf16 in shared memory, 128-byte swizzle, loaded by TMA). So the bf16
-// weights never pass through shared memory, and a partial token tile costs
-// only the MMA columns it uses.
+// tokens are B (N = the tile's rows rounded up to 16; K-major bf16 in shared
+// memory, 128-byte swizzle, loaded by TMA). So the bf16 weights never pass
+// through shared memory, and a partial token tile costs only the MMA columns
+// it uses. Two shapes of the kernel: token tiles of up to 192 rows against
+// one 128-row weight block per CTA, and the tiles of at most 64 rows (an
+// expert's only or last tile) against two blocks per CTA.
 //
-// One persistent CTA per SM, 14 warps: 0-3 epilogue (TMEM lane quarters),
-// 4 TMA producer, 5 MMA issuer (and TMEM owner), 6-13 dequantisers (two per
-// lane quarter, one Q8_0 block of the stage's 64 K each).
+// One persistent CTA per SM (pairs share each token tile by TMA multicast),
+// 15 warps: 0-3 epilogue (TMEM lane quarters), 4 TMA producer, 5 MMA issuer
+// (and TMEM owner), 6-13 dequantisers (two groups of four, one per lane
+// quarter, taking alternate stages; a thread converts the 64 codes of its
+// weight row in the stage), 14 the second MMA issuer of the two-block shape.
 #include <cudaTypedefs.h>
 
 #include <algorithm>

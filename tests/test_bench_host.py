@@ -33,13 +33,16 @@ def test_measured_traffic_requires_matching_source(tmp_path, monkeypatch):
     src = tmp_path / "quantized_sparse_moe_router_gb300" / "csrc"
     src.mkdir(parents=True)
     for f in bench.KERNEL_SOURCES["decode_experts"]:
-        (src / f).write_text("// " + f + "\n")
+        (src / f).write_text("// " + f + "\nint x_" + f.replace(".", "_") + " = 1;\n")
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     digest = bench.kernel_source_hash("decode_experts")
     (prof / "decode_experts_dec1.md").write_text(
         f"# summary\n\ntraffic_bytes_per_launch: 40203008\nsource_sha256: {digest}\n")
     assert bench.measured_traffic("decode_experts", "dec1") == 40203008.0
-    (src / "decode.cu").write_text("// changed\n")  # kernel edited after the capture
+    # comments and blank lines do not change the measured code
+    (src / "decode.cu").write_text("/* new\n   comment */\n\nint x_decode_cu = 1;   // same code\n")
+    assert bench.measured_traffic("decode_experts", "dec1") == 40203008.0
+    (src / "decode.cu").write_text("int x_decode_cu = 2;\n")  # kernel edited after the capture
     assert bench.measured_traffic("decode_experts", "dec1") is None
     assert bench.measured_traffic("decode_experts", "dec16") is None  # no summary for that workload
 
