@@ -87,3 +87,26 @@ def test_binding_fails_loudly_without_the_library(tmp_path, monkeypatch):
     monkeypatch.setattr(fw, "_lib", None)
     with pytest.raises(ImportError):
         fw.lib()
+
+
+def test_noalloc_router_rejects_bad_arguments_before_any_device_call():
+    """fw_moe_route_noalloc checks sizes, pointers and alignment on the host
+    (no CUDA call happens for these), and T = 0 is a no-op."""
+    L = fw.lib()
+    ok = dict(x=4096, T=1, H=2048, w=4096, b=None, E=128, k=8, ids=4096, g=4096)
+
+    def call(**over):
+        a = dict(ok, **over)
+        return L.fw_moe_route_noalloc(a["x"], a["T"], a["H"], a["w"], a["b"], a["E"], a["k"], a["ids"], a["g"], None)
+
+    assert call(T=17) == fw.FW_EINVAL and "T must be" in fw.fw_moe_last_error()
+    assert call(T=-1) == fw.FW_EINVAL
+    assert call(E=257) == fw.FW_EINVAL and call(E=0) == fw.FW_EINVAL
+    assert call(k=0) == fw.FW_EINVAL and call(k=17, E=64) == fw.FW_EINVAL and call(k=9, E=8) == fw.FW_EINVAL
+    assert call(H=6) == fw.FW_EINVAL and call(H=0) == fw.FW_EINVAL
+    assert call(x=None) == fw.FW_EINVAL and call(w=None) == fw.FW_EINVAL and call(ids=None) == fw.FW_EINVAL
+    assert call(x=4100) == fw.FW_EINVAL            # x needs 8-byte alignment
+    assert call(w=4104) == fw.FW_EINVAL            # router_w needs 16-byte alignment
+    assert call(ids=4098) == fw.FW_EINVAL and call(g=4098) == fw.FW_EINVAL and call(b=4098) == fw.FW_EINVAL
+    assert "alignment" in fw.fw_moe_last_error()
+    assert call(T=0, x=None, w=None, ids=None) == fw.FW_OK  # nothing to route
