@@ -1,19 +1,28 @@
 #!/usr/bin/env python
-"""Throughput of the routed Q8_0 MoE feed-forward step on one GB300 (or N replicas).
+"""Throughput of the routed Q8_0 MoE feed-forward step on one GB300.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload dec1] [--impl fw|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl fw|reference]
 
-Default workload: decode batch-1 (H=2048, I=768, E=128, top-8, T=1) over 48
-independently generated layers cycled so the working set (32.6 GB of repacked
-Q8_0 experts) is far larger than L2. One step = every one of 64 synthetic
-hidden rows through all 48 layers in turn (3072 route+ffn calls; 64/T batches
-for T > 1), all on one stream. value = tokens x layer-calls per second, i.e. the token throughput of
-one MoE layer, summed over ranks. The path does not shard: N GPUs run N
-independent replicas (weak scaling) and the only collective is the timing's
-max over ranks.
+With no --workload, every workload of the layer shapes is timed in one run and
+the headline line is the largest one, large2048 (H=7168, I=2048, 256 routed
+experts top-8 + 1 shared, T=2048 tokens per call, 2 layers of 12.7 GB cycled);
+the others (tiny, dec1, dec16, pre4096, large1) are reported under
+"per_config", each with its own roofline. --workload NAME times one workload
+as the headline.
 
---impl reference times the fp64 oracle on the host cores instead, on a
-bounded sample of the same workload (rank 0 only).
+A step of a workload is one pass of the whole hot path (route, experts,
+combine) over every layer of the workload for each of its hidden batches
+(64 rows for T = 1, fewer batches for larger T), all on one stream, captured
+once as a CUDA graph and replayed. value = tokens x layer-calls per second.
+Every workload cycles more layers than L2 holds (no flush needed). Timing: CUDA
+events around K graph replays, repeated 5 times, median.
+
+The path does not shard: this build runs on one GPU (its prefill GEMM shares
+token tiles between paired SMs by TMA multicast within the GPU), so --gpus N
+with N > 1 reports that it is unavailable instead of running.
+
+--impl reference times the fp64 oracle on the host cores instead (rank 0),
+on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -34,26 +43,36 @@ sys.path.insert(0, ROOT)
 
 import synth  # noqa: E402
 
+HEADLINE = "large2048"
+ALL_WORKLOADS = ("tiny", "dec1", "dec16", "pre4096", "large1", "large2048")
+REPEATS = 5
+# Workloads that run on another workload's layers (same shapes; the weights
+# are made once): multi-slot decode on the batch-1 decode layers, and the
+# large MoE's decode run on its prefill layers.
+SHARED_LAYERS = {"dec16": "dec1", "large1": "large2048"}
+
+
 def n_x_rows(w):
     """Distinct hidden batches cycled per step: 64 rows at T=1, fewer for larger T."""
     return max(1, 64 // w.T)
 
 
-def parse():
+def parse(argv=None):
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=30)
+    p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=3)
-    p.add_argument("--workload", default="dec1", choices=sorted(synth.WORKLOADS))
+    p.add_argument("--workload", default=None, choices=sorted(synth.WORKLOADS))
     p.add_argument("--impl", default="fw", choices=["fw", "reference"])
     p.add_argument("--layers", type=int, default=0, help="override the workload's layer count")
     p.add_argument("--experts", type=int, default=0,
                    help="override E (a smaller case for profiling: at T = 1 the expert work per call is the same)")
+    p.add_argument("--repeats", type=int, default=REPEATS)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="host time budget of the oracle baseline (and of the whole reference arm)")
-    return p.parse_args()
+    return p.parse_args(argv)
 
 
 def max_over_ranks(x: float, world: int, device=None) -> float:
@@ -172,7 +191,8 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- layers
-def build_layers(w, n_layers, device):
+def build_layers(w, n_layers, device, T_max):
+    """n_layers seeded layers of workload w's shapes, quantised to Q8_0 on the GPU."""
     import torch
     import quantized_sparse_moe_router_gb300 as fw
     layers = []
@@ -193,7 +213,7 @@ def build_layers(w, n_layers, device):
                    "w_gate": q[0][:E], "w_up": q[1][:E], "w_down": q[2][:E]}
         if S:
             weights.update(shared_gate=q[0][E], shared_up=q[1][E], shared_down=q[2][E])
-        layers.append(fw.MoELayer(H, I, E, w.k, n_shared=S, T_max=w.T, weights=weights))
+        layers.append(fw.MoELayer(H, I, E, w.k, n_shared=S, T_max=T_max, weights=weights))
         del q, Wr, weights
     del tmp
     torch.cuda.synchronize()
@@ -225,33 +245,32 @@ def algorithmic(w, ids_list):
     return tot
 
 
+def work_bytes_layer(w):
+    return (w.E + w.S) * 3 * w.I * w.H * (1 + 4 / 32)
+
+
 # ------------------------------------------------------------ fw arm
-def run_fw(args, rank, world, local_rank):
+def time_workload(w, layers, args, world, dev, e2e: bool):
+    """Time one workload on its layers: graph of one step, REPEATS x K replays,
+    median; a per-kernel event pass; e2e through the host-buffer entry point."""
     import torch
     import quantized_sparse_moe_router_gb300 as fw
-    fw.build()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    w = synth.WORKLOADS[args.workload]
-    if args.experts:
-        w = w.with_(E=args.experts)
-    n_layers = args.layers or w.layers
-    layers = build_layers(w, n_layers, dev)
-    N_X_ROWS = n_x_rows(w)
-    xs_host = hidden_rows(w, N_X_ROWS)
+    n_layers = len(layers)
+    NX = n_x_rows(w)
+    xs_host = hidden_rows(w, NX)
     xs = [torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16) for x in xs_host]
     T, k = w.T, w.k
     ids = torch.empty((T, k), dtype=torch.int32, device=dev)
     out = torch.empty((T, w.H), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
     sp = stream.cuda_stream
-    calls_per_step = N_X_ROWS * n_layers
+    calls_per_step = NX * n_layers
 
-    def step():
-        for r in range(N_X_ROWS):
-            x = xs[r]
+    def step(s_=None):
+        for r in range(NX):
             for L in layers:
-                fw.fw_moe_forward(L.handle, x.data_ptr(), T, ids.data_ptr(), None, out.data_ptr(), sp)
+                fw.fw_moe_forward(L.handle, xs[r].data_ptr(), T, ids.data_ptr(), None, out.data_ptr(),
+                                  s_ if s_ is not None else sp)
 
     def barrier():
         if world > 1:
@@ -263,18 +282,14 @@ def run_fw(args, rank, world, local_rank):
     for L in layers:
         L.status()
 
-    # ---- the step captured once as a CUDA graph (the serving mode: decode replays graphs)
     graph = torch.cuda.CUDAGraph()
     cap_stream = torch.cuda.Stream()
     cap_stream.wait_stream(stream)
     with torch.cuda.stream(cap_stream):
         with torch.cuda.graph(graph, stream=cap_stream):
-            csp = torch.cuda.current_stream().cuda_stream
-            for r in range(N_X_ROWS):
-                for L in layers:
-                    fw.fw_moe_forward(L.handle, xs[r].data_ptr(), T, ids.data_ptr(), None, out.data_ptr(), csp)
+            step(torch.cuda.current_stream().cuda_stream)
     stream.wait_stream(cap_stream)
-    for _ in range(max(1, args.warmup)):
+    for _ in range(max(3, args.warmup)):
         graph.replay()
     torch.cuda.synchronize()
 
@@ -291,30 +306,20 @@ def run_fw(args, rank, world, local_rank):
         barrier()
         return max_over_ranks(t0.elapsed_time(t1), world, dev)
 
-    # ---- timed region (graph replays)
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    time.sleep(0.3)
-    ms = timed(graph.replay, args.steps)
-    clk = clocks.stop()
+    reps = [timed(graph.replay, args.steps) for _ in range(max(1, args.repeats))]
+    ms = statistics.median(reps)
     for L in layers:
         L.status()
-    ms_eager = timed(step, max(1, min(args.steps, 5)))
-    eager_steps = max(1, min(args.steps, 5))
     value = whole_job_rate(T * calls_per_step * args.steps, ms / 1e3, world)
-    value_eager = whole_job_rate(T * calls_per_step * eager_steps, ms_eager / 1e3, world)
+    ms_eager = timed(step, 1)
 
-    # ---- per-kernel timing pass (events around every kernel; same K steps)
-    ids_log = []
+    # ---- per-kernel event pass (events serialise the kernels: a pass of its own, one step)
     for L in layers:
-        # room for every launch: 2 kernels per decode call, at most 12 per prefill call
-        fw.fw_moe_profile_begin(L.handle, (2 if T <= 16 else 12) * N_X_ROWS * max(args.steps, 1))
-    ids_all = torch.empty((args.steps, N_X_ROWS, n_layers, T, k), dtype=torch.int32, device=dev)
-    for s_ in range(args.steps):
-        for r in range(N_X_ROWS):
-            for li, L in enumerate(layers):
-                fw.fw_moe_forward(L.handle, xs[r].data_ptr(), T, ids_all[s_, r, li].data_ptr(), None,
-                                  out.data_ptr(), sp)
+        fw.fw_moe_profile_begin(L.handle, 16 * NX)
+    ids_all = torch.empty((NX, n_layers, T, k), dtype=torch.int32, device=dev)
+    for r in range(NX):
+        for li, L in enumerate(layers):
+            fw.fw_moe_forward(L.handle, xs[r].data_ptr(), T, ids_all[r, li].data_ptr(), None, out.data_ptr(), sp)
     torch.cuda.synchronize()
     prof = {}
     for L in layers:
@@ -322,160 +327,245 @@ def run_fw(args, rank, world, local_rank):
             a = prof.setdefault(kname, [0.0, 0])
             a[0] += kms
             a[1] += cnt
-    ids_np = ids_all.cpu().numpy().reshape(-1, T, k)
-    work = algorithmic(w, ids_np)
-    n_calls = args.steps * calls_per_step
+    work = algorithmic(w, ids_all.cpu().numpy().reshape(-1, T, k))
+    n_calls = calls_per_step
     launches_per_call = sum(c for _, c in prof.values()) / n_calls
+    call_us = ms / args.steps / calls_per_step * 1e3
 
-    def avg_launch_ms(name):  # mean duration of one launch of this kind
+    def avg_us(name):
         tot, cnt = prof.get(name, (0.0, 0))
-        return tot / cnt if cnt else 0.0
+        return tot / cnt * 1e3 if cnt else 0.0
 
-    hbm, bf16_burst, bf16_sus, peak_src = load_peaks()
-    decode = T <= 16
-    if decode:
-        dom = "decode_experts"  # gate/up + down + combine in one kernel (one launch per call)
+    hbm, bf16_burst, _, peak_src = load_peaks()
+    if T <= 16:
+        dom = "decode_experts"  # the experts' one kernel (gate/up, down, combine): one launch per call
         dom_bytes = (work["gu_bytes"] + work["d_bytes"]) / n_calls
-        t_ms = avg_launch_ms(dom)
-        achieved = dom_bytes / (t_ms / 1e3) / 1e9
+        ev_us = avg_us(dom)
+        # the event pass serialises the kernels; inside the timed graph the
+        # kernel overlaps its router, so its time there is at most the call's
+        k_us = min(ev_us, call_us) if ev_us else call_us
+        achieved = dom_bytes / (k_us / 1e6) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
                     "frac": round(achieved / hbm, 4), "traffic": measured_traffic(dom, w.name), "kernel": dom,
-                    "avg_launch_us": round(t_ms * 1e3, 3),
+                    "avg_launch_us": round(k_us, 3), "event_pass_us": round(ev_us, 3),
                     "algorithmic_bytes_per_launch": round(dom_bytes),
                     "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"}
     else:
         # the gate/up "launch": the pair of GEMM launches of one call (192-row tiles, then the small tiles)
         dom = "prefill_gateup"
-        t_ms = avg_launch_ms(dom) + avg_launch_ms("prefill_gateup_small")
+        k_us = avg_us(dom) + avg_us("prefill_gateup_small")
         fl = work["flops"] * 2 / 3 / n_calls
-        achieved = fl / (t_ms / 1e3) / 1e12
+        achieved = fl / (k_us / 1e6) / 1e12
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16_burst, "unit": "TFLOP/s",
-                    "frac": round(achieved / bf16_burst, 4), "traffic": measured_traffic(dom, w.name), "kernel": dom,
-                    "avg_launch_us": round(t_ms * 1e3, 3), "algorithmic_flops_per_launch": round(fl),
+                    "frac": round(achieved / bf16_burst, 4), "traffic": measured_traffic(dom, w.name),
+                    "kernel": dom, "avg_launch_us": round(k_us, 3), "algorithmic_flops_per_launch": round(fl),
                     "peak_source": f"{peak_src} bf16_tflops (cuBLAS burst)"}
-    step_bytes = work["bytes"] / args.steps
-    whole = {"algorithmic_GBps": round(step_bytes / (ms / args.steps / 1e3) / 1e9, 1),
-             "frac_of_hbm": round(step_bytes / (ms / args.steps / 1e3) / 1e9 / hbm, 4),
-             "us_per_call": round(ms / args.steps / calls_per_step * 1e3, 3),
-             "roofline_us_per_call": round(step_bytes / calls_per_step / (hbm * 1e9) * 1e6, 3),
-             "touched_experts_mean": round(float(np.mean(work["U"])), 2)}
+    step_bytes = work["bytes"]
+    call_roof_us = max(step_bytes / calls_per_step / (hbm * 1e9), work["flops"] / calls_per_step / (bf16_burst * 1e12)) * 1e6
+    whole = {"us_per_call": round(call_us, 3), "roofline_us_per_call": round(call_roof_us, 3),
+             "frac_of_roofline": round(call_roof_us / call_us, 4),
+             "algorithmic_GBps": round(step_bytes / (ms / args.steps / 1e3) / 1e9, 1),
+             "algorithmic_TFLOPs": round(work["flops"] / (ms / args.steps / 1e3) / 1e12, 1),
+             "touched_experts_mean": round(float(np.mean(work["U"])), 2),
+             "repeats_ms_per_step": [round(r / args.steps, 4) for r in reps]}
     kernels = {n: {"total_ms": round(v[0], 3), "launches": v[1], "avg_us": round(v[0] / v[1] * 1e3, 3)}
                for n, v in prof.items()}
 
-    # ---- end to end through the host-buffer entry point
-    e2e = None
-    if not args.no_e2e:
+    e2e_res = None
+    if e2e:
         xh = [torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).pin_memory() for x in xs_host]
         ids_h = torch.empty((T, k), dtype=torch.int32).pin_memory()
         out_h = torch.empty((T, w.H), dtype=torch.bfloat16).pin_memory()
         e2e_steps = max(1, min(args.steps, 3))
-        for r in range(min(4, N_X_ROWS)):
+        for r in range(min(4, NX)):
             layers[0].forward_host(xh[r], ids_h, out_h)
         barrier()
         t_s = time.perf_counter()
         for _ in range(e2e_steps):
-            for r in range(N_X_ROWS):
+            for r in range(NX):
                 for L in layers:
                     fw.fw_moe_forward_host(L.handle, xh[r].data_ptr(), T, ids_h.data_ptr(), out_h.data_ptr(), sp)
         el = max_over_ranks(time.perf_counter() - t_s, world, dev)
-        e2e = {"value": round(whole_job_rate(T * calls_per_step * e2e_steps, el, world), 1), "unit": "tokens/s",
-               "h2d_bytes_per_step": calls_per_step * T * w.H * 2,
-               "d2h_bytes_per_step": calls_per_step * (T * k * 4 + T * w.H * 2),
-               "steps": e2e_steps, "api": "fw_moe_forward_host (pinned host buffers, synchronous per call)"}
-
-    cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
-        cpu = cpu_baseline(w, args.cpu_seconds)
-
-    for L in layers:
-        L.close()
+        e2e_res = {"value": round(whole_job_rate(T * calls_per_step * e2e_steps, el, world), 1), "unit": "tokens/s",
+                   "h2d_bytes_per_step": calls_per_step * T * w.H * 2,
+                   "d2h_bytes_per_step": calls_per_step * (T * k * 4 + T * w.H * 2),
+                   "steps": e2e_steps, "api": "fw_moe_forward_host (pinned host buffers, synchronous per call)"}
     return {
-        "metric": f"MoE-FFN tokens/s ({w.name}: H={w.H} I={w.I} E={w.E} top-{w.k}"
-                  f"{' +1 shared' if w.S else ''} T={w.T}); decode HBM GB/s / prefill TFLOP/s as fraction of peak",
-        "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms / args.steps, 4), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "fp32 (Q8_0 weights x bf16 activations, fp32 accumulate)" if decode
-        else "bf16 tensor-core (Q8_0 dequantised to bf16), fp32 accumulate",
-        "data": "synthetic (seeded Irwin-Hall normals; experts quantised to Q8_0 on the GPU)",
+        "value": round(value, 1), "unit": "tokens/s", "ms_per_step": round(ms / args.steps, 4),
         "config": {"workload": w.name, "H": w.H, "I": w.I, "E": w.E, "k": w.k, "n_shared": w.S, "T": w.T,
-                   "layers": n_layers, "x_rows": n_x_rows(w), "calls_per_step": calls_per_step,
+                   "layers": n_layers, "x_rows": NX, "calls_per_step": calls_per_step,
                    "l2": f"inputs larger than L2: {n_layers} layers x {round(work_bytes_layer(w) / 1e9, 2)} GB "
-                         "of repacked experts cycled (L2 129 MB), no flush",
-                   "parallelism": f"replicas x{world}"},
-        "eager": {"value": round(value_eager, 1), "ms_per_step": round(ms_eager / eager_steps, 4),
-                  "note": "same step launched call by call from Python (no graph)"},
-        "timing": "CUDA events on the launch stream around K replays of a CUDA graph of one step",
-        "roofline": roofline, "whole_step": whole, "kernels": kernels, "e2e": e2e, "cpu_baseline": cpu,
+                         "of repacked experts cycled (L2 129 MB), no flush"},
+        "eager_ms_per_step": round(ms_eager, 4),
+        "roofline": roofline, "whole_step": whole, "kernels": kernels, "e2e": e2e_res,
         "gpu_launches": int(round(launches_per_call * args.steps * calls_per_step)),
-        "clocks": clk,
     }
 
 
-def work_bytes_layer(w):
-    return (w.E + w.S) * 3 * w.I * w.H * (1 + 4 / 32)
+def metric_name(w):
+    return (f"MoE-FFN tokens/s ({w.name}: H={w.H} I={w.I} E={w.E} top-{w.k}"
+            f"{' +1 shared' if w.S else ''} T={w.T}); decode HBM GB/s / prefill TFLOP/s as fraction of peak")
+
+
+def workload_of(args, name):
+    w = synth.WORKLOADS[name]
+    if args.experts:
+        w = w.with_(E=args.experts)
+    return w
+
+
+def run_fw(args, rank, world, local_rank):
+    import torch
+    import quantized_sparse_moe_router_gb300 as fw
+    fw.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    head = args.workload or HEADLINE
+    names = [head] if args.workload else [n for n in ALL_WORKLOADS if n != head] + [head]
+    results = {}
+    built = {}  # layer-set owner -> layers
+    clocks = ClockSampler(local_rank)
+    clk = None
+    for name in names:
+        w = workload_of(args, name)
+        owner = SHARED_LAYERS.get(name, name) if not args.workload else name
+        users = [n for n in names if SHARED_LAYERS.get(n, n) == owner] if not args.workload else [name]
+        if owner not in built:
+            wo = workload_of(args, owner)
+            n_layers = args.layers or max(synth.WORKLOADS[u].layers for u in users)
+            T_max = max(synth.WORKLOADS[u].T for u in users)
+            built[owner] = build_layers(wo, n_layers, dev, T_max)
+        layers = built[owner][:(args.layers or w.layers)]
+        if name == head:
+            clocks.start()
+            time.sleep(0.3)
+        results[name] = time_workload(w, layers, args, world, dev, e2e=(name == head and not args.no_e2e))
+        if name == head:
+            clk = clocks.stop()
+        if all(n in results for n in users):  # last user of this layer set: free it
+            for L in built.pop(owner):
+                L.close()
+            torch.cuda.empty_cache()
+    w = workload_of(args, head)
+    res = results.pop(head)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = cpu_baseline(w, args.cpu_seconds)
+    line = {
+        "metric": metric_name(w), "value": res["value"], "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp32 (Q8_0 weights x bf16 activations, fp32 accumulate)" if w.T <= 16
+        else "bf16 tensor-core (Q8_0 dequantised to bf16), fp32 accumulate",
+        "data": "synthetic (seeded Irwin-Hall normals; experts quantised to Q8_0 on the GPU)",
+        "config": dict(res["config"], parallelism=f"replicas x{world}"),
+        "timing": f"CUDA events on the launch stream around K replays of a CUDA graph of one step; "
+                  f"median of {args.repeats} repeats",
+        "roofline": res["roofline"], "whole_step": res["whole_step"], "kernels": res["kernels"],
+        "e2e": res["e2e"], "cpu_baseline": cpu, "gpu_launches": res["gpu_launches"], "clocks": clk,
+        "eager_ms_per_step": res["eager_ms_per_step"],
+    }
+    if results:
+        line["per_config"] = {n: {"metric": metric_name(workload_of(args, n)), **r} for n, r in results.items()}
+        line["gpu_launches_all_configs"] = line["gpu_launches"] + sum(r["gpu_launches"] for r in results.values())
+    return line
 
 
 # ------------------------------------------------------------ oracle arm
-def oracle_sample(w, seconds, max_calls=64):
-    """Time the oracle, as it stands, on calls of the workload (layers cycled,
-    the same hidden rows); the experts a call needs are quantised by the oracle
-    beforehand, untimed."""
+def _prep_expert(args):
+    """(workload, layer, expert) -> its three Q8_0 matrices by the oracle's quantiser (worker process)."""
+    import oracle
+    w, l, e = args
+    return e, [oracle.q8_0_quantize(synth.expert_weight_f32(w, l, e, kind)) for kind in (0, 1, 2)]
+
+
+def oracle_prepare(w, n_tokens, n_layers=2):
+    """Hidden rows and the Q8_0 experts their routing needs, for the first
+    n_layers layers of w: quantised by the oracle over a spawn pool (untimed)."""
+    import multiprocessing as mp
     import oracle
     oracle.build()
-    xs = hidden_rows(w, 4)
-    n_layers = min(w.layers, 4)
-    prepared = []
-    for l in range(n_layers):
+    xs = hidden_rows(w, 1)[0][:n_tokens]
+    jobs, routed = [], []
+    for l in range(min(w.layers, n_layers)):
         Wr = synth.router_weight_f32(w, l)
         b = synth.router_bias_f32(w, l)
-        T_s = min(w.T, 8)
-        x = xs[l % 4][:T_s]
-        ids, _ = oracle.topk_gates(oracle.router_logits(x, Wr, b), w.k)
-        need = set(np.unique(ids).tolist()) | set(range(w.E, w.E + w.S))
-        lists = [[oracle.q8_0_quantize(synth.expert_weight_f32(w, l, e, kind)) if e in need else None
-                  for e in range(w.E + w.S)] for kind in (0, 1, 2)]
-        prepared.append((x, Wr, b, lists))
+        ids, _ = oracle.topk_gates(oracle.router_logits(xs, Wr, b), w.k)
+        need = sorted(set(np.unique(ids).tolist()) | set(range(w.E, w.E + w.S)))
+        routed.append((Wr, b, need))
+        jobs += [(w, l, e) for e in need]
+    procs = max(1, min(os.cpu_count() or 1, 32))
+    with mp.get_context("spawn").Pool(procs) as pool:
+        done = pool.map(_prep_expert, jobs)
+    prepared, i = [], 0
+    for Wr, b, need in routed:
+        lists = [[None] * (w.E + w.S) for _ in range(3)]
+        for e in need:
+            _, q = done[i]
+            i += 1
+            for kind in range(3):
+                lists[kind][e] = q[kind]
+        prepared.append((Wr, b, lists))
+    return xs, prepared
+
+
+def oracle_tokens(w, seconds):
+    """Tokens of the bounded oracle sample: about `seconds` of single-thread work."""
+    per_token = 3 * 2 * w.H * w.I * (w.k + w.S) / 0.8e9 + 2 * w.E * w.H / 1e9  # ~0.8 GMAC/s fp64 with dequant
+    return int(max(1, min(w.T, 256, seconds / per_token)))
+
+
+def oracle_sample(w, seconds, xs, prepared, max_calls=64):
+    """Time the oracle, as it stands, single-threaded, on calls of the workload
+    (the prepared layers cycled; each call all prepared tokens)."""
+    import oracle
     done_tokens, el, calls = 0, 0.0, 0
-    while el < seconds and calls < max_calls:
-        x, Wr, b, (g, u, d) = prepared[calls % n_layers]
+    while calls < max_calls and (calls == 0 or el < seconds):
+        Wr, b, (g, u, d) = prepared[calls % len(prepared)]
         t = time.perf_counter()
-        oracle.moe_forward(x, Wr, b, g, u, d, k=w.k, S=w.S)
+        oracle.moe_forward(xs, Wr, b, g, u, d, k=w.k, S=w.S)
         el += time.perf_counter() - t
-        done_tokens += x.shape[0]
+        done_tokens += xs.shape[0]
         calls += 1
-    return done_tokens, el, calls, min(w.T, 8)
+    return done_tokens, el, calls
 
 
 def cpu_baseline(w, seconds):
-    tokens, el, calls, T_s = oracle_sample(w, seconds)
+    n_tok = oracle_tokens(w, seconds / 2)
+    xs, prepared = oracle_prepare(w, n_tok)
+    tokens, el, calls = oracle_sample(w, seconds, xs, prepared)
     return {"value": round(tokens / el, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
-            "sample": f"{calls} route+FFN calls of {T_s} token(s) each over {min(w.layers, 4)} layers of the "
-                      f"workload ({el:.1f} s of single-thread fp64 work; expert quantisation untimed)",
+            "sample": f"{calls} route+FFN calls of the first {n_tok} token(s) of the workload's hidden batch, "
+                      f"cycling {len(prepared)} of its layers ({el:.1f} s of single-thread fp64 work; expert "
+                      f"quantisation untimed)",
             "host_cores": os.cpu_count()}
 
 
 def run_reference(args):
-    w = synth.WORKLOADS[args.workload]
-    per_step = max(0.2, args.cpu_seconds / max(1, args.steps + args.warmup))
+    w = workload_of(args, args.workload or HEADLINE)
+    total = args.steps + args.warmup
+    per_step = max(0.2, args.cpu_seconds / max(1, total))
+    n_tok = oracle_tokens(w, per_step)
+    xs, prepared = oracle_prepare(w, n_tok)
     for _ in range(args.warmup):
-        oracle_sample(w, per_step / 4, max_calls=1)
+        oracle_sample(w, 0.0, xs, prepared, max_calls=1)
     tot_tokens, tot_el, tot_calls = 0, 0.0, 0
     for _ in range(args.steps):
-        tokens, el, calls, T_s = oracle_sample(w, per_step, max_calls=4)
+        tokens, el, calls = oracle_sample(w, 0.0, xs, prepared, max_calls=1)
         tot_tokens += tokens
         tot_el += el
         tot_calls += calls
     value = tot_tokens / tot_el
     return {
-        "impl": "reference",
-        "metric": f"MoE-FFN tokens/s ({w.name}: H={w.H} I={w.I} E={w.E} top-{w.k}"
-                  f"{' +1 shared' if w.S else ''} T={w.T}); decode HBM GB/s / prefill TFLOP/s as fraction of peak",
+        "impl": "reference", "metric": metric_name(w),
         "value": round(value, 3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(tot_el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp64", "data": "synthetic",
         "config": {"workload": w.name, "H": w.H, "I": w.I, "E": w.E, "k": w.k, "n_shared": w.S, "T": w.T},
         "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "kind": "oracle", "cores": 1,
-                         "sample": f"{tot_calls} calls of up to 8 tokens over <=4 layers (single-thread fp64 oracle)"},
+                         "sample": f"{tot_calls} calls (one per step) of the first {n_tok} token(s) of the "
+                                   f"workload, cycling {len(prepared)} layers (single-thread fp64 oracle; expert "
+                                   "quantisation untimed)"},
         "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -489,16 +579,16 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
         return
-    if world > 1:
-        import torch
-        torch.cuda.set_device(local_rank)
-        torch.distributed.init_process_group("nccl")
+    if world > 1 or args.gpus > 1:
+        if rank == 0:
+            print(json.dumps({"metric": metric_name(workload_of(args, args.workload or HEADLINE)),
+                              "n_gpus": max(world, args.gpus), "unavailable":
+                              "one GPU only: the step does not shard (replicas only), and this build's prefill "
+                              "GEMM shares token tiles between paired SMs by TMA multicast, which is kept to "
+                              "1-GPU runs"}), flush=True)
+        return
     res = run_fw(args, rank, world, local_rank)
-    if rank == 0:
-        print(json.dumps(res), flush=True)
-    if world > 1:
-        import torch
-        torch.distributed.destroy_process_group()
+    print(json.dumps(res), flush=True)
 
 
 if __name__ == "__main__":

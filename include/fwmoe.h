@@ -55,10 +55,14 @@ typedef enum {
 
 typedef struct fw_moe_handle fw_moe_handle; /* opaque; one handle = one MoE layer */
 
+/* Layer shape. H and I must be multiples of 64, not only of the Q8_0 block
+ * length 32: the prefill GEMMs step K by 64 (two Q8_0 blocks per 128-byte
+ * swizzled shared-memory row). Every Qwen/DeepSeek-shaped MoE layer the pages
+ * speak of meets this. */
 typedef struct {
   int32_t H;            /* hidden size; multiple of 64 */
   int32_t I;            /* per-expert intermediate size; multiple of 64 */
-  int32_t E;            /* routed experts, 1..1024 */
+  int32_t E;            /* routed experts, 1..256 */
   int32_t k;            /* experts per token, 1..min(E, 16) */
   int32_t n_shared;     /* always-on shared experts: 0 or 1 */
   int32_t T_max;        /* largest T any call on this handle may pass (sizes the workspace) */
@@ -76,21 +80,30 @@ typedef struct { /* all DEVICE pointers, read only during fw_moe_init */
   const uint8_t *shared_down;  /* [H x I/32] Q8_0, or NULL when n_shared == 0 */
 } fw_moe_weights;
 
-/* Create a layer: validates the shapes, copies the router and repacks every
+/* Create a layer (the pages' runtime loads routed experts of GGUF Q8_0 models
+ * onto the GPU for its grouped kernels: Flyweight README, §Quantization and
+ * §Features): validates the shapes, copies the router and repacks every
  * Q8_0 matrix into the handle's own device memory (a byte-preserving change of
  * layout: int8 code planes plus binary16 scale planes), allocates the
  * workspace for T_max tokens and synchronises `stream` once. The caller may
  * free its weight buffers afterwards. *out receives the handle. */
 fw_status fw_moe_init(const fw_moe_config *cfg, const fw_moe_weights *w, void *stream, fw_moe_handle **out);
 
-/* Routing for T tokens (0 <= T <= T_max): x is DEVICE bf16 [T, H] row-major.
+/* The router step (Flyweight README, §Current limitations: dynamic MoE routing;
+ * vOOM README, router/top-k substeps; the reading: fp32 logits, top-k with ties
+ * to the lower id, softmax restricted to the k and renormalised).
+ * Routing for T tokens (0 <= T <= T_max): x is DEVICE bf16 [T, H] row-major.
  * Writes expert_ids (DEVICE int32 [T, k]) and gates (DEVICE fp32 [T, k], may be
  * NULL), and keeps the routing and the token-to-expert grouping in the handle
  * for the next fw_moe_ffn. T == 0 is a no-op. */
 fw_status fw_moe_route(fw_moe_handle *h, const void *x, int32_t T, int32_t *expert_ids, float *gates,
                        void *stream);
 
-/* Experts and combine for the routing made by the last fw_moe_route on this
+/* The routed-expert step (Flyweight README, §Features "sparse MoE execution",
+ * §Quantization: grouped routed-expert kernels over Q8_0; vOOM README: SwiGLU
+ * experts, shared experts): each selected expert's SiLU(gate) * up then down
+ * projection, gate-weighted and summed in slot order (+ the shared expert).
+ * Experts and combine for the routing made by the last fw_moe_route on this
  * handle: same x, same T, same stream. out is DEVICE bf16 [T, H] row-major.
  * A T different from the last route's returns FW_ESTATE. */
 fw_status fw_moe_ffn(fw_moe_handle *h, const void *x, int32_t T, void *out, void *stream);
@@ -106,7 +119,9 @@ fw_status fw_moe_forward(fw_moe_handle *h, const void *x, int32_t T, int32_t *ex
 fw_status fw_moe_forward_host(fw_moe_handle *h, const void *x_host, int32_t T, int32_t *expert_ids_host,
                               void *out_host, void *stream);
 
-/* Token-to-expert grouping of the last route (for tests and tools): offsets
+/* The token-to-expert permutation the grouped kernels run on (Flyweight
+ * README, §Runtime controls: block-table kernels for routed experts).
+ * Token-to-expert grouping of the last route (for tests and tools): offsets
  * DEVICE int32 [E + 1], the exclusive prefix sum of the per-expert counts;
  * perm DEVICE int32 [T*k], the slot ids s = t*k + j grouped by ascending expert
  * and, within an expert, by ascending token; inv DEVICE int32 [T*k] (may be
@@ -149,12 +164,14 @@ enum {
 fw_status fw_moe_profile_begin(fw_moe_handle *h, int32_t max_launches);
 fw_status fw_moe_profile_end(fw_moe_handle *h, int32_t n_kinds, float *total_ms, int32_t *launches);
 
-/* Release the handle (synchronises its device first). NULL is a no-op; a
+/* Release the handle (no counterpart on the pages: resource management of
+ * this library). Synchronises its device first. NULL is a no-op; a
  * handle already freed is detected (FW_EINVAL) as long as its memory has not
  * been reused. */
 fw_status fw_moe_free(fw_moe_handle *h);
 
-/* Text of the last failed call on this thread ("" if none). */
+/* Text of the last failed call on this thread ("" if none). No counterpart
+ * on the pages. */
 const char *fw_moe_last_error(void);
 
 /* Routing only (logits, top-k with ties to the lower id, renormalised gates)
@@ -176,11 +193,16 @@ const char *fw_moe_last_error(void);
  * the ticket in stream order. All calls share the one array and it keeps the
  * last call's contents: calls that can overlap on the GPU (other streams, or
  * other threads' streams) race and must be serialised by the caller. It calls
- * no cudaMalloc, cudaFree or allocating library routine. */
+ * no cudaMalloc, cudaFree or allocating library routine. `stream` must belong
+ * to the current device (checked: FW_EINVAL otherwise); the looked-up address
+ * is kept for the life of the process, so after a cudaDeviceReset of the
+ * device this entry point (like every handle) may no longer be used. */
 fw_status fw_moe_route_noalloc(const void *x, int32_t T, int32_t H, const float *router_w, const float *router_bias,
                                int32_t E, int32_t k, int32_t *expert_ids, float *gates, void *stream);
 
-/* Quantise fp32 weights to Q8_0 on the GPU: w DEVICE [rows, K] row-major fp32,
+/* A tool for preparing inputs, not a step of the MoE layer (the pages name
+ * the GGUF Q8_0 format, Flyweight README §Quantization; the layer itself
+ * never quantises). Quantise fp32 weights to Q8_0 on the GPU: w DEVICE [rows, K] row-major fp32,
  * K % 32 == 0; blocks DEVICE rows x K/32 x 34 bytes. Per block of 32:
  * amax = max|w|, d = amax/127 (fp64), q = round-half-away-from-zero(w/d)
  * clamped to +-127 (fp64), d stored as binary16 (round to nearest even);

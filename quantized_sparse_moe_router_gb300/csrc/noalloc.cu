@@ -117,6 +117,14 @@ extern "C" fw_status fw_moe_route_noalloc(const void* x, int32_t T, int32_t H, c
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return set_error(FW_ECUDA, "fw_moe_route_noalloc: no current CUDA device");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (s) {  // the scratch address looked up below is the current device's: the stream must be on it
+    int sdev = -1;
+    if (cudaStreamGetDevice(s, &sdev) != cudaSuccess)
+      return set_error(FW_EINVAL, "fw_moe_route_noalloc: stream is not a valid CUDA stream");
+    if (sdev != dev)
+      return set_error(FW_EINVAL, "fw_moe_route_noalloc: stream belongs to another device than the current one");
+  }
   void* base = nullptr;
   {
     std::lock_guard<std::mutex> g(g_na_mu);
@@ -128,7 +136,6 @@ extern "C" fw_status fw_moe_route_noalloc(const void* x, int32_t T, int32_t H, c
     }
     base = g_na_ptr[dev];
   }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* logits = static_cast<float*>(base);
   unsigned int* ticket = reinterpret_cast<unsigned int*>(static_cast<unsigned char*>(base) + kNaLogitBytes);
   // the ticket must start at zero: clear it in stream order (no allocation)

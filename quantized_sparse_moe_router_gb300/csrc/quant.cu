@@ -10,16 +10,10 @@
 namespace fw {
 namespace {
 
-__device__ __forceinline__ double round_half_away(double v) {
-  double a = fabs(v);
-  double fl = floor(a);
-  double r = (a - fl >= 0.5) ? fl + 1.0 : fl;
-  return v < 0.0 ? -r : r;
-}
-
 // One thread per 32-value block. The decisions (d and every code) are taken in
-// fp64: d = amax/127, q = round-half-away(w/d), clamp to +-127; d is stored
-// rounded to binary16 (nearest even).
+// fp64: d = amax/127, q = w/d rounded to the nearest integer with halves away
+// from zero (the C library's round(), as CUDA provides it for double), clamped
+// to +-127; d is stored rounded to binary16 (nearest even).
 __global__ void quantize_q8_0_kernel(const float* __restrict__ w, int64_t nblocks, uint8_t* __restrict__ out) {
   int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (blk >= nblocks) return;
@@ -36,18 +30,17 @@ __global__ void quantize_q8_0_kernel(const float* __restrict__ w, int64_t nblock
   float amax = 0.0f;
 #pragma unroll
   for (int i = 0; i < kQBlock; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  double d = (double)amax / 127.0;
-  uint16_t dbits = __half_as_ushort(__double2half(d));
+  const double d = (double)amax / 127.0;
   uint16_t* dst = reinterpret_cast<uint16_t*>(out + blk * kQBlockBytes);  // 34-byte blocks are 2-byte aligned
-  dst[0] = dbits;
+  dst[0] = __half_as_ushort(__double2half(d));
 #pragma unroll
   for (int i = 0; i < kQBlock; i += 2) {
     int q0 = 0, q1 = 0;
     if (amax > 0.0f) {
-      q0 = (int)fmin(127.0, fmax(-127.0, round_half_away((double)v[i] / d)));
-      q1 = (int)fmin(127.0, fmax(-127.0, round_half_away((double)v[i + 1] / d)));
+      q0 = max(-127, min(127, (int)round((double)v[i] / d)));
+      q1 = max(-127, min(127, (int)round((double)v[i + 1] / d)));
     }
-    dst[1 + i / 2] = (uint16_t)((uint8_t)(int8_t)q0 | ((uint16_t)(uint8_t)(int8_t)q1 << 8));
+    dst[1 + i / 2] = (uint16_t)((q0 & 0xFF) | ((q1 & 0xFF) << 8));
   }
 }
 

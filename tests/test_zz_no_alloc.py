@@ -2,8 +2,9 @@
 memory (a framework's memory manager owns the whole device, or a latency path
 cannot take cudaMalloc's synchronisation). Its scratch is a static device
 array inside the library; this checks, through the C ABI, that two calls in a
-row give the same ids and gates as the handle-based fw_moe_route, and that
-sizes beyond the array are refused. Collected last on purpose."""
+row give the fp64 oracle's ids (bit-exact) and gates (within the suite's gate
+bound), and the same as the handle-based fw_moe_route, and that sizes beyond
+the array are refused. Collected last on purpose."""
 import numpy as np
 import pytest
 
@@ -39,6 +40,9 @@ def test_noalloc_route_matches_handle_route_twice(name, over):
         fw.fw_moe_route_noalloc(xd.data_ptr(), wl.T, wl.H, dl.router_w.data_ptr(), bias_ptr, wl.E, wl.k,
                                 ids.data_ptr(), gates.data_ptr(), sp)
         torch.cuda.synchronize()
+        ids_o, gates_o = ol.route(x)  # the oracle's routing of the same rows
+        assert np.array_equal(ids.cpu().numpy(), ids_o)
+        assert np.abs(gates.cpu().numpy() - gates_o).max() <= GATE_TOL
         assert torch.equal(ids, ids_ref)
         assert (gates - g_ref).abs().max().item() <= GATE_TOL
     layer.close()
@@ -51,3 +55,4 @@ def test_noalloc_route_refuses_sizes_beyond_its_scratch():
     assert "16" in fw.fw_moe_last_error()
     assert L.fw_moe_route_noalloc(4096, 4, 256, 4096, None, 257, 2, 4096, None, None) == fw.FW_EINVAL
     assert L.fw_moe_route_noalloc(4096, 0, 256, 4096, None, 8, 2, 4096, None, None) == fw.FW_OK
+
