@@ -67,6 +67,8 @@ def parse(argv=None):
     p.add_argument("--layers", type=int, default=0, help="override the workload's layer count")
     p.add_argument("--experts", type=int, default=0,
                    help="override E (a smaller case for profiling: at T = 1 the expert work per call is the same)")
+    p.add_argument("--tokens", type=int, default=0,
+                   help="override T (with --experts: a smaller case with the same rows per expert, for profiling)")
     p.add_argument("--repeats", type=int, default=REPEATS)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
@@ -411,6 +413,8 @@ def workload_of(args, name):
     w = synth.WORKLOADS[name]
     if args.experts:
         w = w.with_(E=args.experts)
+    if args.tokens:
+        w = w.with_(T=args.tokens)
     return w
 
 
@@ -433,7 +437,7 @@ def run_fw(args, rank, world, local_rank):
         if owner not in built:
             wo = workload_of(args, owner)
             n_layers = args.layers or max(synth.WORKLOADS[u].layers for u in users)
-            T_max = max(synth.WORKLOADS[u].T for u in users)
+            T_max = max(workload_of(args, u).T for u in users)
             built[owner] = build_layers(wo, n_layers, dev, T_max)
         layers = built[owner][:(args.layers or w.layers)]
         if name == head:

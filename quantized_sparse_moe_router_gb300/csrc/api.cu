@@ -5,6 +5,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <unordered_set>
@@ -66,9 +67,10 @@ struct Allocator {
 };
 
 void free_handle_memory(Handle* h) {
-  void* ptrs[] = {h->q_gu, h->st_gu, h->q_d, h->st_d, h->wr3, h->wr, h->bias, h->ids, h->gates,
+  void* ptrs[] = {h->q_gu, h->st_gu, h->q_d, h->st_d, h->q_dc, h->wr3, h->wr, h->bias, h->ids, h->gates,
                   h->logits, h->counts, h->offsets, h->perm, h->inv, h->row_token, h->row_gate, h->uinfo,
-                  h->hist, h->minfo, h->minfo_s, h->xperm, h->hbuf, h->yp, h->meta, h->x_dev, h->out_dev, h->ids_dev};
+                  h->hist, h->minfo, h->minfo_s, h->xperm, h->hbuf, h->yp, h->partial, h->pmask, h->meta,
+                  h->x_dev, h->out_dev, h->ids_dev};
   for (void* p : ptrs)
     if (p) cudaFree(p);
 }
@@ -86,6 +88,16 @@ fw_status check_config(const fw_moe_config* c) {
 }
 
 int decode_limit(const Handle* h) { return h->cfg.decode_T_max ? h->cfg.decode_T_max : kMaxDecodeT; }
+
+// T tokens take the decode kernel: T within the handle's decode limit and a
+// shape that kernel holds; any other T takes the prefill path.
+bool use_decode(const Handle* h, int T) { return T <= decode_limit(h) && decode_supported(h->cfg.H, T); }
+
+// Some T in [1, T_max] takes the prefill path (its tensor maps and buffers are needed).
+bool needs_prefill(const Handle* h) {
+  const int Tm = h->cfg.T_max;
+  return Tm > decode_limit(h) || !decode_supported(h->cfg.H, 1) || (Tm > 1 && !decode_supported(h->cfg.H, 2));
+}
 
 }  // namespace
 
@@ -126,9 +138,15 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
                 prop.major, prop.minor);
 
   e = configure_route_kernels();
-  if (e == cudaSuccess) e = configure_decode_kernels();
-  if (e == cudaSuccess) e = configure_prefill_kernels();
-  if (e != cudaSuccess) return cuda_fail(e, "fw_moe_init: kernel set-up (is the library built for this GPU?)");
+  if (e != cudaSuccess) return cuda_fail(e, "fw_moe_init: router kernel set-up (is the library built for this GPU?)");
+  g_err[0] = 0;
+  e = configure_decode_kernels();
+  if (e != cudaSuccess) {
+    if (g_err[0]) return FW_EUNSUPPORTED;  // the set-up left its own text
+    return cuda_fail(e, "fw_moe_init: decode kernel set-up");
+  }
+  e = configure_prefill_kernels();
+  if (e != cudaSuccess) return cuda_fail(e, "fw_moe_init: prefill kernel set-up");
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   Handle* h = new Handle();
@@ -139,13 +157,19 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
   h->device = dev;
   h->num_sms = prop.multiProcessorCount;
   h->last_T = -1;
+  {
+    const char* s = getenv("FWMOE_TEST_GRID_TIMEOUTS");
+    h->test_grid_timeouts = (s && *s) ? atoi(s) : 0;
+  }
+  const bool pre = needs_prefill(h);
   const int64_t H = cfg->H, I = cfg->I, E = cfg->E, EU = h->EU, k = cfg->k, Tm = cfg->T_max;
   h->rows_max = Tm * (k + h->S);
 
   Allocator A;
   const int64_t n_route_tiles = (Tm + kRouteTileM - 1) / kRouteTileM;
   const int64_t n_mtiles_max = h->rows_max / kTokTile + EU + 1;
-  const size_t hbuf_bytes = (size_t)h->rows_max * I * sizeof(float);
+  const size_t hbuf_bytes = pre ? (size_t)h->rows_max * I * 2 : 256;  // prefill h (bf16)
+  const int64_t T_dec = std::min<int64_t>(Tm, kMaxDecodeT);
   struct {
     void** p;
     size_t bytes;
@@ -154,9 +178,10 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
       {(void**)&h->st_gu, (size_t)(EU * (H / 32) * 2 * I * 2)},
       {(void**)&h->q_d, (size_t)(EU * H * row_bytes(I))},
       {(void**)&h->st_d, (size_t)(EU * (I / 32) * H * 2)},
+      {(void**)&h->q_dc, (size_t)(EU * H * I)},
       {(void**)&h->wr, (size_t)(E * H * 4)},
       {(void**)&h->bias, (size_t)(E * 4)},
-      {(void**)&h->wr3, (size_t)(Tm > decode_limit(h) ? 3 * E * H * 2 : 256)},
+      {(void**)&h->wr3, (size_t)(pre ? 3 * E * H * 2 : 256)},
       {(void**)&h->ids, (size_t)(Tm * k * 4)},
       {(void**)&h->gates, (size_t)(Tm * k * 4)},
       {(void**)&h->logits, (size_t)(std::min<int64_t>(Tm, kMaxDecodeT) * E * 4)},
@@ -170,9 +195,11 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
       {(void**)&h->hist, (size_t)(n_route_tiles * EU * 4)},
       {(void**)&h->minfo, (size_t)(n_mtiles_max * 16)},
       {(void**)&h->minfo_s, (size_t)(EU * 16)},
-      {(void**)&h->xperm, (size_t)(Tm > decode_limit(h) ? h->rows_max * H * 2 : 256)},
+      {(void**)&h->xperm, (size_t)(pre ? h->rows_max * H * 2 : 256)},
       {(void**)&h->hbuf, hbuf_bytes},
-      {(void**)&h->yp, (size_t)(Tm > decode_limit(h) ? h->rows_max * H * 2 : 256)},
+      {(void**)&h->yp, (size_t)(pre ? h->rows_max * H * 2 : 256)},
+      {(void**)&h->partial, (size_t)(h->num_sms * T_dec * H * 4)},
+      {(void**)&h->pmask, (size_t)(h->num_sms * 4)},
       {(void**)&h->meta, sizeof(Meta)},
       {(void**)&h->x_dev, (size_t)(Tm * H * 2)},
       {(void**)&h->out_dev, (size_t)(Tm * H * 2)},
@@ -204,7 +231,7 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
     if (e == cudaSuccess) e = launch_repack(h, 1, (int)E, 1, w->shared_up, s);
     if (e == cudaSuccess) e = launch_repack(h, 2, (int)E, 1, w->shared_down, s);
   }
-  if (e == cudaSuccess && Tm > decode_limit(h)) {
+  if (e == cudaSuccess && pre) {
     // rows past the valid ones of a tile are read (and masked); keep them finite
     e = cudaMemsetAsync(h->xperm, 0, (size_t)h->rows_max * H * 2, s);
     if (e == cudaSuccess) e = cudaMemsetAsync(h->hbuf, 0, hbuf_bytes, s);
@@ -248,8 +275,8 @@ fw_status fw_moe_route(fw_moe_handle* hh, const void* x, int32_t T, int32_t* exp
   if (T == 0) return FW_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
-  cudaError_t e = T <= decode_limit(h) ? launch_route_decode(h, xb, T, expert_ids, gates, true, s)
-                                        : launch_route_prefill(h, xb, T, expert_ids, gates, s);
+  cudaError_t e = use_decode(h, T) ? launch_route_decode(h, xb, T, expert_ids, gates, true, s)
+                                   : launch_route_prefill(h, xb, T, expert_ids, gates, s);
   if (e != cudaSuccess) {
     h->last_T = -1;
     return cuda_fail(e, "fw_moe_route launch");
@@ -268,8 +295,8 @@ fw_status fw_moe_ffn(fw_moe_handle* hh, const void* x, int32_t T, void* out, voi
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
   __nv_bfloat16* ob = static_cast<__nv_bfloat16*>(out);
-  cudaError_t e = T <= decode_limit(h) ? launch_ffn_decode(h, xb, T, ob, false, nullptr, nullptr, s)
-                                        : launch_ffn_prefill(h, xb, T, ob, s);
+  cudaError_t e = use_decode(h, T) ? launch_ffn_decode(h, xb, T, ob, false, nullptr, nullptr, s)
+                                   : launch_ffn_prefill(h, xb, T, ob, s);
   if (e == cudaErrorNotSupported) return fail(FW_EUNSUPPORTED, "fw_moe_ffn: prefill path not available in this build");
   if (e != cudaSuccess) return cuda_fail(e, "fw_moe_ffn launch");
   return FW_OK;
@@ -284,7 +311,7 @@ fw_status fw_moe_forward(fw_moe_handle* hh, const void* x, int32_t T, int32_t* e
     return fail(FW_EINVAL, "fw_moe_forward: expert_ids must be a 4-byte aligned device pointer");
   if (T > 0 && (!out || !aligned(out, 16)))
     return fail(FW_EINVAL, "fw_moe_forward: out must be a 16-byte aligned device pointer");
-  if (T > decode_limit(h)) {
+  if (!use_decode(h, T)) {
     st = fw_moe_route(hh, x, T, expert_ids, gates, stream);
     return st != FW_OK ? st : fw_moe_ffn(hh, x, T, out, stream);
   }

@@ -1,29 +1,43 @@
 // Decode path (T <= 16): the experts of one call as one fused, HBM-bound
-// grouped GEMV kernel.
+// kernel: gate/up, SiLU, down and the gate-weighted combine.
 //
 // The pages' runtime runs routed experts through grouped GPU kernels per
 // quantisation format, Q8_0 among them (Flyweight README, §Quantization), and
 // fuses the gate and up projections so they share one activation load (its
 // CPU expert kernels, §Current limitations). Here every selected expert's
-// Q8_0 rows are streamed from HBM exactly once per call, in large bulk
-// asynchronous copies into a shared-memory ring fed by one producer warp, and
-// dequantised in registers by sixteen consumer warps.
+// Q8_0 bytes are streamed from HBM exactly once per call, in large bulk
+// asynchronous copies into a shared-memory ring fed by one producer warp.
 //
-// One persistent CTA per SM (all resident at once, see launch()):
-//   0. after the router's grid completes (programmatic dependent launch), each
-//      CTA rebuilds the batch's routing from the logits in shared memory
-//      (top-k by rank; deterministic, so every CTA agrees); CTA 0 publishes
-//      it;
-//   1. gate/up: the CTA's slice of the (touched expert, i) units; for each of
-//      the expert's tokens h = SiLU(g) * u -> hbuf (fp32, grouped row order);
-//   2. grid-wide barrier (every h written) -- meanwhile the producer keeps
-//      streaming this CTA's W_down rows into the ring;
-//   3. down + combine: the CTA's output rows in blocks of 16, per block every
-//      touched expert in ascending id (shared last); each lane keeps partial
-//      sums of gate * (W_down h) per token across the experts, one warp
-//      reduction per (row, token) at the end of the block; out[t] (bf16) in a
-//      fixed order, no atomics.
+// The work is cut along I into chunks of 16 units of one expert: the chunk's
+// 16 gate and 16 up rows, and the matching 16 columns of its down matrix
+// (split-K over I). One persistent CTA per SM takes a contiguous range of
+// chunks and, for each, computes h = SiLU(W_gate x) * (W_up x) for the
+// chunk's units and then gate * W_down[:, chunk] h into a partial output of
+// the CTA. So the down projection streams alongside gate/up, and the one
+// grid-wide wait left is for the partial outputs: after it each CTA sums its
+// rows of them over the CTAs in a fixed order (deterministic, no atomics).
+//
+// Gate/up dot products run on integer dot-product instructions: each token's
+// x is held, per 16-element segment, as a 16-bit fixed-point number scaled to
+// the segment's largest exponent (exact for every element within 2^7 of the
+// segment's largest; smaller ones are rounded at 2^-15 of it), split into a
+// signed high and an unsigned low byte plane; the Q8_0 codes (offset binary)
+// multiply both planes with dp4a, and one fp32 multiply-add per segment
+// applies the weight scale and the segment's power of two. The down
+// projection multiplies fp32 h by the exactly dequantised codes in fp32.
+//
+// One CTA per SM, all resident (see launch()):
+//   0. x -> fixed-point planes in shared memory (before the router finishes);
+//   1. after the router's grid completes (programmatic dependent launch), the
+//      batch's routing rebuilt from the logits in shared memory
+//      (deterministic, so every CTA agrees); CTA 0 publishes it;
+//   2. the CTA's chunks: gate/up stages -> h (shared memory), then down
+//      stages -> the CTA's partial output (fp32: shared memory for one token,
+//      registers for several);
+//   3. partial outputs to global memory, grid-wide arrival and bounded wait;
+//   4. each CTA's output rows summed over the CTAs' partials, bf16.
 #include <algorithm>
+#include <cstdio>
 
 #include "routing.cuh"
 
@@ -33,40 +47,43 @@ namespace {
 using namespace dev;
 
 constexpr int kCW = 16;                    // consumer warps
-constexpr int kThreads = (kCW + 1) * 32;   // + one producer warp
+constexpr int kCT = kCW * 32;              // consumer threads
+constexpr int kThreads = kCT + 32;         // + one producer warp
 constexpr int kProducer = kCW;
 constexpr int kMaxStages = 16;
-constexpr int kRowBlock = 16;              // output rows per W_down block
-constexpr int kMaxPer = 2;                 // experts' blocks per W_down stage
-constexpr int kMaxRowsOne = 128;           // output rows per CTA of the one-token instantiation
-constexpr int kStaticChunks = 2;           // gate/up chunks per CTA assigned without a ticket
+constexpr int kChunk = 16;                 // units of I per chunk (one 16-byte segment of a down row)
+constexpr int kRowsMulti = 4;              // several tokens: down rows per consumer thread (H <= 2048)
+constexpr int kMaxHMulti = kRowsMulti * kCT;
+constexpr int kMaxHOne = 16384;            // one token: the partial output row fits in shared memory
+constexpr int kDnRowsMax = 2048;           // down rows per stage at most
 constexpr uint32_t kConsumerBarrier = 1;   // named barrier of the 16 consumer warps
-constexpr int64_t kL2PrefetchMax = 40ll << 20;  // W_down bytes per call prefetched into L2 (L2 is 129 MB)
-
-enum XMode { kXGlobal = 0, kXSmemF32 = 1, kXSmemBf16 = 2 };
+constexpr uint32_t kStageTarget = 36 * 1024;
+constexpr int kRedBatch = 10;              // partial loads in flight per lane in the final sums
+constexpr int kPrefetchAhead = 12;         // stages requested into L2 ahead of the ring
 
 struct DecodeArgs {
-  const uint8_t* q_gu;   // rows of row_bytes(H): codes + 128, then binary16 scales
-  const uint8_t* q_d;    // rows of row_bytes(I)
+  const uint8_t* q_gu;   // [EU][2I] rows of row_bytes(H): codes + 128, then binary16 scales
+  const uint8_t* q_dc;   // [EU][I/16][H][16] down codes (+ 128) by 16-column groups
+  const uint16_t* st_d;  // [EU][I/32][H] down scales
   const __nv_bfloat16* x;
   const float* logits;
-  float* hbuf;           // [rows][I] fp32
+  float* partial;        // [grid][T][H] fp32 partial outputs
+  uint32_t* pmask;       // [grid] tokens each CTA's partial covers
   __nv_bfloat16* out;
   RoutingOut ro;
   Meta* meta;
   int H, I, E, k, S, T;
   int publish;
-  int R;                 // gate/up units per stage (a multiple of kGUGroup dividing 32)
-  int n_per;             // experts per W_down stage (each a block of <= 16 rows), <= kMaxPer
-  uint32_t stage_bytes;  // ring slot size (max of a gate/up and a down stage)
+  int R;                 // gate/up units per stage (even, divides kChunk)
+  int Dr;                // down rows per stage (multiple of 16)
+  uint32_t stage_bytes;
   int stages;
-  int x_mode;
-  int h_smem;            // h staged in shared memory (fp32)
-  uint32_t act_bytes;    // shared-memory area for x, then for h
+  uint32_t off_info, off_acc, off_h, off_ring;  // dynamic shared memory layout (bytes)
+  uint32_t grid_extra;   // arrivals the grid wait expects beyond the grid (0; > 0 only to test the bound)
+  uint64_t grid_wait_ns; // bound of the grid-wide wait
 };
-// (smem layouts of x and h: see x16_from_f32_t)
 
-// ------------------------------------------------------------- packed fp32
+// ------------------------------------------------------------- helpers
 typedef unsigned long long f2;
 
 __device__ __forceinline__ f2 f2_pack(float a, float b) {
@@ -95,7 +112,7 @@ __device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
   return r;
 }
 
-// Four offset-binary codes of a word times four x values (two pairs), added
+// Four offset-binary codes of a word times four h values (two pairs), added
 // to a pair accumulator: the byte permute makes the float 2^23 + q + 128 and
 // one packed subtraction leaves q exactly.
 __device__ __forceinline__ f2 dot4(uint32_t w, f2 x01, f2 x23, f2 acc) {
@@ -106,51 +123,68 @@ __device__ __forceinline__ f2 dot4(uint32_t w, f2 x01, f2 x23, f2 acc) {
   return f2_fma(f2_add(m23, bias), x23, acc);
 }
 
-// sum_{i<16} q_i x_i for one 16-code segment; x as 8 pairs.
-__device__ __forceinline__ float dot16(const uint4 q, const f2 (&x)[8]) {
-  f2 a = dot4(q.x, x[0], x[1], 0ull);
-  f2 b = dot4(q.y, x[2], x[3], 0ull);
-  a = dot4(q.z, x[4], x[5], a);
-  b = dot4(q.w, x[6], x[7], b);
+// sum_{i<16} q_i h_i for one 16-code segment; h as 8 pairs.
+__device__ __forceinline__ float dot16(const uint4 q, const f2 (&h)[8]) {
+  f2 a = dot4(q.x, h[0], h[1], 0ull);
+  f2 b = dot4(q.y, h[2], h[3], 0ull);
+  a = dot4(q.z, h[4], h[5], a);
+  b = dot4(q.w, h[6], h[7], b);
   return f2_hsum(f2_add(a, b));
 }
 
-// Shared-memory vectors (x, h) are stored "segment-transposed" so that lane l
-// reading its 16-element segment l touches consecutive 16-byte words in each
-// of its loads (no bank conflicts): fp32 element e = 16 seg + 4 i + j of a
-// length-K vector sits at i * K/4 + 4 seg + j; bf16 element e = 16 seg + 8 i + j
-// at i * K/2 + 8 seg + j.
-__device__ __forceinline__ void x16_from_f32_t(const float* v, int K, int seg, f2 (&x)[8]) {
+// The same with h read from shared memory (a broadcast) one pair of words at
+// a time, so that few registers hold h.
+__device__ __forceinline__ float dot16_smem(const uint4 q, const float* h) {
+  const float4* hp = reinterpret_cast<const float4*>(h);
+  float4 v0 = hp[0], v1 = hp[1];
+  f2 a = dot4(q.x, f2_pack(v0.x, v0.y), f2_pack(v0.z, v0.w), 0ull);
+  f2 b = dot4(q.y, f2_pack(v1.x, v1.y), f2_pack(v1.z, v1.w), 0ull);
+  v0 = hp[2];
+  v1 = hp[3];
+  a = dot4(q.z, f2_pack(v0.x, v0.y), f2_pack(v0.z, v0.w), a);
+  b = dot4(q.w, f2_pack(v1.x, v1.y), f2_pack(v1.z, v1.w), b);
+  return f2_hsum(f2_add(a, b));
+}
+
+__device__ __forceinline__ void load_h16(const float* p, f2 (&h)[8]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float4 w = *reinterpret_cast<const float4*>(v + i * (K / 4) + seg * 4);
-    x[2 * i] = f2_pack(w.x, w.y);
-    x[2 * i + 1] = f2_pack(w.z, w.w);
+    const float4 v = reinterpret_cast<const float4*>(p)[i];
+    h[2 * i] = f2_pack(v.x, v.y);
+    h[2 * i + 1] = f2_pack(v.z, v.w);
   }
 }
 
-__device__ __forceinline__ void x16_from_bf16(uint4 a, uint4 b, f2 (&x)[8]) {
-  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) x[i] = f2_pack_bits(w[i] << 16, w[i] & 0xFFFF0000u);
+// Integer dot products of four code bytes (unsigned, q + 128) with four
+// signed / unsigned activation bytes, added to c.
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t d;
+  asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
 }
 
-// h written by other CTAs during this kernel: coherent (L2) loads, not the
-// read-only path.
-__device__ __forceinline__ void x16_from_f32_global(const float* p, f2 (&x)[8]) {
-  const float4* q = reinterpret_cast<const float4*>(p);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float4 v = __ldcg(q + i);
-    x[2 * i] = f2_pack(v.x, v.y);
-    x[2 * i + 1] = f2_pack(v.z, v.w);
-  }
+// sum_i (q_i + 128) * xf_i over a 16-code segment, xf = 256 hi + lo.
+__device__ __forceinline__ int seg_dot_i(const uint4 q, const uint4 hi, const uint4 lo) {
+  int sh = dp4a_us(q.x, hi.x, 0);
+  uint32_t sl = dp4a_uu(q.x, lo.x, 0u);
+  sh = dp4a_us(q.y, hi.y, sh);
+  sl = dp4a_uu(q.y, lo.y, sl);
+  sh = dp4a_us(q.z, hi.z, sh);
+  sl = dp4a_uu(q.z, lo.z, sl);
+  sh = dp4a_us(q.w, hi.w, sh);
+  sl = dp4a_uu(q.w, lo.w, sl);
+  return sh * 256 + (int)sl;
 }
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
 __device__ __forceinline__ void consumer_sync() {
-  asm volatile("bar.sync %0, %1;" ::"r"(kConsumerBarrier), "r"(kCW * 32) : "memory");
+  asm volatile("bar.sync %0, %1;" ::"r"(kConsumerBarrier), "r"(kCT) : "memory");
 }
 
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
@@ -161,155 +195,171 @@ __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long
 
 __host__ __device__ inline uint32_t align128(uint32_t v) { return (v + 127) / 128 * 128; }
 
+// One 16-element segment of bf16 x -> 16-bit fixed point at the segment's
+// largest exponent: hi/lo byte planes, the power of two that undoes the
+// scaling, and 128 * sum(xf) (the codes are stored as q + 128). Segments whose
+// largest magnitude is below 2^-112 count as zero.
+__device__ __forceinline__ void x_segment_to_planes(const uint4 a, const uint4 b, uint4& hi, uint4& lo, int2& info) {
+  const uint32_t w[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  uint32_t emax = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) emax = max(emax, max((w[i] >> 7) & 0xFFu, (w[i] >> 23) & 0xFFu));
+  if (emax < 15u) {
+    hi = lo = make_uint4(0u, 0u, 0u, 0u);
+    info = make_int2(0, 0);
+    return;
+  }
+  const float mult = __uint_as_float((268u - emax) << 23);  // 2^(14 - e), e = emax - 127
+  int xf[16];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    xf[2 * i] = __float2int_rn(__uint_as_float(w[i] << 16) * mult);
+    xf[2 * i + 1] = __float2int_rn(__uint_as_float(w[i] & 0xFFFF0000u) * mult);
+    sum += xf[2 * i] + xf[2 * i + 1];
+  }
+  uint32_t h4[4], l4[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    h4[j] = 0u;
+    l4[j] = 0u;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      h4[j] |= ((uint32_t)(xf[4 * j + i] >> 8) & 0xFFu) << (8 * i);
+      l4[j] |= ((uint32_t)xf[4 * j + i] & 0xFFu) << (8 * i);
+    }
+  }
+  hi = make_uint4(h4[0], h4[1], h4[2], h4[3]);
+  lo = make_uint4(l4[0], l4[1], l4[2], l4[3]);
+  info = make_int2((int)((emax - 14u) << 23), 128 * sum);  // float bits of 2^(e - 14), offset term
+}
+
 // ------------------------------------------------------------- the kernel
-// kOne: the single-token instantiation (T = 1, x in shared memory as fp32):
-// its hot code is the T = 1 paths only, which keeps it small for the
-// instruction cache.
-template <bool kOne>
+// kMulti: several tokens (T <= 16, H <= 2048; partial output in registers);
+// otherwise one token (partial output in shared memory).
+template <bool kMulti>
 __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
   __shared__ SmemRouting r;
-  __shared__ int2 stage_units[kMaxStages];  // gate/up units [x, y) held by each ring stage (x < 0: no more)
-  __shared__ float s_half[2][kMaxRowsOne];   // (one token) the two halves of each output row
+  __shared__ uint32_t s_mask;
+  __shared__ volatile int s_abort;  // a consumer gave up a wait: the others stop waiting too
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int H = a.H, I = a.I, T = kOne ? 1 : a.T, R = a.R;
-  const int x_mode = kOne ? (int)kXSmemF32 : a.x_mode;
-  const uint32_t rb_h = (uint32_t)row_bytes(H), rb_i = (uint32_t)row_bytes(I);
-  uint8_t* ring = smem + align128(a.act_bytes);
+  const int H = a.H, I = a.I, T = kMulti ? a.T : 1, R = a.R, Dr = a.Dr;
+  const int nseg = H / 16;
+  const uint32_t rb_h = (uint32_t)row_bytes(H);
+  uint8_t* xhi = smem;                                              // [T][H] int8
+  uint8_t* xlo = smem + (size_t)T * H;                              // [T][H] uint8
+  int2* xinfo = reinterpret_cast<int2*>(smem + a.off_info);         // [T][H/16]
+  float* acc_s = reinterpret_cast<float*>(smem + a.off_acc);        // [H] (one token)
+  float* hbuf = reinterpret_cast<float*>(smem + a.off_h);           // [2][T][16]
+  uint8_t* ring = smem + a.off_ring;
   if (tid == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], kCW);
     }
+    s_abort = 0;
     fence_mbar_init();
   }
   if (warp != kProducer) {
     // x was written before the router kernel started (that launch waits for
-    // the whole stream), so it is staged while the router still runs.
-    // segment-transposed, fp32 or bf16 in shared memory (else read from global)
-    if (x_mode == kXSmemF32) {
-      float* xs = reinterpret_cast<float*>(smem);
-      for (int c = tid; c < T * H / 8; c += kCW * 32) {  // c: 8 bf16 = half a segment
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.x) + c);
-        const int t = c / (H / 8), cc = c % (H / 8), seg = cc >> 1, half = cc & 1;
-        float4 lo4, hi4;
-        bf16x2_to_f32(v.x, lo4.x, lo4.y);
-        bf16x2_to_f32(v.y, lo4.z, lo4.w);
-        bf16x2_to_f32(v.z, hi4.x, hi4.y);
-        bf16x2_to_f32(v.w, hi4.z, hi4.w);
-        float* base = xs + (size_t)t * H + seg * 4;
-        *reinterpret_cast<float4*>(base + (2 * half) * (H / 4)) = lo4;
-        *reinterpret_cast<float4*>(base + (2 * half + 1) * (H / 4)) = hi4;
-      }
-    } else if (x_mode == kXSmemBf16) {
-      __nv_bfloat16* xs = reinterpret_cast<__nv_bfloat16*>(smem);
-      for (int c = tid; c < T * H / 8; c += kCW * 32) {
-        const int t = c / (H / 8), cc = c % (H / 8), seg = cc >> 1, half = cc & 1;
-        *reinterpret_cast<uint4*>(xs + (size_t)t * H + half * (H / 2) + seg * 8) =
-            __ldg(reinterpret_cast<const uint4*>(a.x) + c);
-      }
+    // the whole stream): staged while the router still runs
+    for (int c = tid; c < T * nseg; c += kCT) {
+      const uint4* src = reinterpret_cast<const uint4*>(a.x) + 2 * c;
+      uint4 hi, lo;
+      int2 info;
+      x_segment_to_planes(__ldg(src), __ldg(src + 1), hi, lo, info);
+      reinterpret_cast<uint4*>(xhi)[c] = hi;
+      reinterpret_cast<uint4*>(xlo)[c] = lo;
+      xinfo[c] = info;
     }
+    if (!kMulti)
+      for (int o = tid; o < H; o += kCT) acc_s[o] = 0.f;
   }
-  pdl_wait();  // the router's logits (and its reset of the grid barrier)
-  if (kOne)
-    route_one_in_smem<kThreads>(a.logits, a.E, a.k, a.S, r);
+  pdl_wait();  // the router's logits (and its reset of the grid counter)
+  float* zbuf = reinterpret_cast<float*>(ring);  // the ring is not yet in use
+  if (kMulti)
+    route_in_smem<kThreads>(a.logits, T, a.E, a.k, a.S, r, zbuf);
   else
-    route_in_smem<kThreads>(a.logits, T, a.E, a.k, a.S, r);
+    route_one_in_smem<kThreads>(a.logits, a.E, a.k, a.S, r, zbuf);
   if (a.publish && blockIdx.x == 0) publish_routing<kThreads>(r, T, a.E, a.k, a.S, a.ro);
 
-  const int nU = r.n_unique;
-  // gate/up work, in stages of at most R consecutive units of the nU x I unit
-  // space (never across an expert, since R divides I: a stage is one run of
-  // consecutive interleaved rows of one expert, one copy).
-  //  * one token: the units are split evenly, each CTA a contiguous range
-  //    starting and ending on a kGUGroup boundary (every unit costs the same);
-  //  * several tokens: the cost of a unit is its expert's token count, so
-  //    R-unit chunks are handed out -- CTA b's first kStaticChunks are b,
-  //    b + grid, ..., the rest come from a ticket counter.
-  // (32-bit indices throughout the loops: a 64-bit division is a long
-  // software routine, and these run once per stage in every warp)
-  const int n_units = nU * I;
-  const int64_t n_grp = n_units / kGUGroup;
-  const int lo = (int)(n_grp * blockIdx.x / gridDim.x) * kGUGroup;
-  const int hi = (int)(n_grp * (blockIdx.x + 1) / gridDim.x) * kGUGroup;
-  // down stages: output rows [o0, o1), blocks of 16 rows; per block every touched expert
-  const int o0 = (int)((int64_t)H * blockIdx.x / gridDim.x), o1 = (int)((int64_t)H * (blockIdx.x + 1) / gridDim.x);
-  // (a down stage holds the same 16-row block of up to n_per experts, so that
-  // a warp's dot products for those experts overlap)
-  const int n_blk = (o1 - o0 + kRowBlock - 1) / kRowBlock;
-  const int n_ge = (nU + a.n_per - 1) / a.n_per;
-  const int n_dn = n_ge * n_blk;
+  // this CTA's chunks: [c0, c1) of the nU * I/16 chunks, expert-major
+  const int G = I / kChunk;
+  const int n_ch = r.n_unique * G;
+  const int c0 = (int)((int64_t)n_ch * blockIdx.x / gridDim.x);
+  const int c1 = (int)((int64_t)n_ch * (blockIdx.x + 1) / gridDim.x);
+  const int n_gu = kChunk / R;            // gate/up stages per chunk
+  const int n_dn = (H + Dr - 1) / Dr;     // down stages per chunk
+  if (tid == 0) {
+    uint32_t m = 0;
+    if (c1 > c0) {
+      for (int u = c0 / G; u <= (c1 - 1) / G; ++u) {
+        const int4 ui = r.u[u];
+        for (int p = ui.y; p < ui.y + ui.z; ++p) m |= 1u << r.tok[p];
+      }
+    }
+    s_mask = m;
+  }
+  __syncthreads();
+  const uint32_t cta_mask = s_mask;
 
   if (warp == kProducer) {
     // ------------------------------------------------------ producer
     if (lane == 0) {
-      // Once the ring is full of gate/up stages, ask L2 for all of this CTA's
-      // W_down rows, so that they stream from HBM alongside gate/up instead
-      // of after it -- when the call's W_down fits comfortably in L2.
-      bool pf = (int64_t)nU * H * rb_i <= kL2PrefetchMax;
-      // (several tokens) chunk of the current stage and of the next two: the
-      // ticket for the second is requested two stages ahead, so its round
-      // trip overlaps copies
-      int j = 0, c = blockIdx.x, q0 = blockIdx.x + gridDim.x, q1 = 0;
-      if (!kOne) q1 = (int)atomicAdd(&a.meta->chunk_ctr, 1u) + kStaticChunks * (int)gridDim.x;
-      int su = lo;      // (one token) next unit of the CTA's range
-      bool gu = true;   // still issuing gate/up stages
-      int st = 0;       // j % stages
-      uint32_t ph = 0;  // (j / stages) & 1
-      int ge = 0, blk = 0;  // down stage jd: expert group, row block
-      for (int jd = 0; gu || jd < n_dn;) {
-        if (pf && j == a.stages) {  // the ring is full: the TMA unit has time for it
-          pf = false;
-          for (int u = 0; u < nU; ++u) {
-            const int64_t row = (int64_t)r.u[u].x * H + o0;
-            prefetch_l2(a.q_d + row * rb_i, (uint32_t)(o1 - o0) * rb_i);
-          }
+      int st = 0;
+      uint32_t ph = 0;
+      int j = 0;  // stages issued
+      bool ok = true;
+      const int per_ch = n_gu + n_dn, n_st = (c1 - c0) * per_ch;
+      // Stage x of this CTA (chunk c0 + x / per_ch, step x % per_ch): global
+      // source and bytes of its (first) copy.
+      auto stage_src = [&](int x, const uint8_t*& src, uint32_t& bytes) {
+        const int ch = c0 + x / per_ch, q = x - (x / per_ch) * per_ch;
+        const int u = ch / G, g = ch - u * G;
+        const int e = r.u[u].x;
+        if (q < n_gu) {
+          const int i0 = g * kChunk + q * R;
+          src = a.q_gu + ((int64_t)e * 2 * I + 2 * i0) * rb_h;
+          bytes = (uint32_t)(2 * R) * rb_h;
+        } else {
+          const int r0 = (q - n_gu) * Dr, nr = ::min(Dr, H - r0);
+          src = a.q_dc + (((int64_t)e * G + g) * H + r0) * kChunk;
+          bytes = (uint32_t)nr * kChunk;
+        }
+      };
+      // the stages beyond the ring are asked of L2 ahead of their copies, so
+      // that HBM keeps streaming while the ring waits for its slots
+      int pf = a.stages;
+      for (int x = 0; x < n_st && ok; ++x) {
+        for (; pf < n_st && pf < x + a.stages + kPrefetchAhead; ++pf) {
+          const uint8_t* src;
+          uint32_t bytes;
+          stage_src(pf, src, bytes);
+          prefetch_l2(src, bytes);
         }
         if (j >= a.stages && !mbar_wait(&empty[st], ph ^ 1u)) {
-          report_wait(a.meta, kSiteGuEmpty, j, n_dn);
+          report_wait(a.meta, kSiteGuEmpty, j, x);
+          ok = false;
           break;
         }
         uint8_t* sb = ring + (size_t)st * a.stage_bytes;
-        if (gu) {
-          int u0, u1;
-          if (kOne) {
-            u0 = su;
-            u1 = ::min(hi, (su / R + 1) * R);
-            su = u1;
-          } else {
-            u0 = c * R;
-            u1 = u0 + R;
-            c = q0;
-            q0 = q1;
-            q1 = (int)atomicAdd(&a.meta->chunk_ctr, 1u) + kStaticChunks * (int)gridDim.x;
-          }
-          if (u0 >= (kOne ? hi : n_units)) {
-            gu = false;
-            if (kOne) continue;  // the consumers know the count: this slot goes to the down stages
-            stage_units[st] = make_int2(-1, -1);  // ticketed work: an empty stage tells the consumers
-            mbar_arrive(&full[st]);
-          } else {
-            stage_units[st] = make_int2(u0, u1);
-            const int eu = u0 / I;  // a stage never spans two experts (R divides I)
-            const int e = r.u[eu].x, i0 = u0 - eu * I;
-            const uint32_t bytes = (uint32_t)(u1 - u0) * 2 * rb_h;
-            mbar_arrive_expect_tx(&full[st], bytes);
-            bulk_g2s(sb, a.q_gu + ((int64_t)e * 2 * I + 2 * i0) * rb_h, bytes, &full[st]);
-          }
-        } else {
-          // block-major: all expert groups of block 0, then block 1, ...
-          const int e0 = ge * a.n_per, e1 = ::min(nU, e0 + a.n_per);
-          const int r0 = o0 + blk * kRowBlock, nr = ::min(kRowBlock + 0, o1 - r0);
-          mbar_arrive_expect_tx(&full[st], (uint32_t)(e1 - e0) * nr * rb_i);
-          for (int u = e0; u < e1; ++u)
-            bulk_g2s(sb + (size_t)(u - e0) * kRowBlock * rb_i, a.q_d + ((int64_t)r.u[u].x * H + r0) * rb_i,
-                     (uint32_t)nr * rb_i, &full[st]);
-          ++jd;
-          if (++ge == n_ge) {
-            ge = 0;
-            ++blk;
-          }
+        const uint8_t* src;
+        uint32_t bytes;
+        stage_src(x, src, bytes);
+        const int q = x % per_ch;
+        if (q < n_gu) {  // rows 2 i0 .. 2 (i0 + R) of the interleaved gate/up plane
+          mbar_arrive_expect_tx(&full[st], bytes);
+          bulk_g2s(sb, src, bytes, &full[st]);
+        } else {  // down rows [r0, r0 + nr) of the chunk's column group: codes, then their scales
+          const int ch = c0 + x / per_ch;
+          const int u = ch / G, g = ch - u * G, e = r.u[u].x;
+          const int r0 = (q - n_gu) * Dr, nr = (int)(bytes / kChunk);
+          mbar_arrive_expect_tx(&full[st], (uint32_t)nr * 18u);
+          bulk_g2s(sb, src, bytes, &full[st]);
+          bulk_g2s(sb + (size_t)nr * kChunk, a.st_d + ((int64_t)e * (I / 32) + g / 2) * H + r0, (uint32_t)nr * 2u,
+                   &full[st]);
         }
         ++j;
         if (++st == a.stages) {
@@ -317,127 +367,156 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
           ph ^= 1u;
         }
       }
-      // every copy issued has landed before the CTA may leave
+      // every copy issued has landed before the ring is reused or the CTA leaves
       for (int q = ::max(0, j - a.stages); q < j; ++q)
-        mbar_wait(&full[q % a.stages], (uint32_t)((q / a.stages) & 1));
+        if (!mbar_wait(&full[q % a.stages], (uint32_t)((q / a.stages) & 1))) break;
     }
   } else {
     // ------------------------------------------------------ consumers
-    bool ok = true;  // (x is visible: route_in_smem ends with a CTA barrier)
-
-    // ---- phase 1: gate/up. Every consumer warp passes every stage in order
-    // (no wait is ever more than one phase ahead of its barrier) and computes
-    // its units of the stage's chunk, until the empty stage.
-    const int nseg_h = H / 16;
-    // stages of gate/up work this CTA took (ticketed work: then one empty stage)
-    int n_gu = kOne ? (hi > lo ? (hi + R - 1) / R - lo / R : 0) : 0;
-    int st = 0;       // j % stages
-    uint32_t ph = 0;  // (j / stages) & 1
-    for (int j = 0; ok && (!kOne || j < n_gu); ++j) {
-      if (!mbar_wait(&full[st], ph)) {
-        report_wait(a.meta, kSiteGuFull, j, warp);
-        ok = false;
-        break;
-      }
-      const int2 su = stage_units[st];
-      if (su.x < 0) {
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-        n_gu = j + 1;
-        break;
-      }
-      const int u0 = su.x, u1 = su.y;
-      const uint8_t* sb = ring + (size_t)st * a.stage_bytes;
-      const int eu = u0 / I;  // the stage's expert (a stage never spans two)
-      const int4 ui = r.u[eu];
-      // units alternate over the warps from stage to stage: unit q of stage j
-      // goes to warp (j R + q) mod 16
-      for (int g = u0 + ((warp - j * R) % kCW + kCW) % kCW; g < u1; g += kCW) {
-        // the stage holds rows 2 i0 .. 2 i1 of the expert: per group, kGUGroup
-        // gate rows then their up rows; u0 is group-aligned
-        const int off = (int)(g - u0);
-        const uint8_t* qg_row = sb + (size_t)((off / kGUGroup) * 2 * kGUGroup + off % kGUGroup) * rb_h;
-        const uint8_t* qu_row = qg_row + (size_t)kGUGroup * rb_h;
-        const uint16_t* sg = reinterpret_cast<const uint16_t*>(qg_row + H);
-        const uint16_t* su = reinterpret_cast<const uint16_t*>(qu_row + H);
-        const int i = g - eu * I;
-        auto load_x = [&](int t, int seg, f2(&xv)[8]) {
-          if (x_mode == kXSmemF32) {
-            x16_from_f32_t(reinterpret_cast<const float*>(smem) + (size_t)t * H, H, seg, xv);
-          } else if (x_mode == kXSmemBf16) {
-            const __nv_bfloat16* xb = reinterpret_cast<const __nv_bfloat16*>(smem) + (size_t)t * H;
-            x16_from_bf16(*reinterpret_cast<const uint4*>(xb + seg * 8), *reinterpret_cast<const uint4*>(xb + H / 2 + seg * 8),
-                          xv);
-          } else {
-            const uint4* xp = reinterpret_cast<const uint4*>(a.x + (size_t)t * H + seg * 16);
-            x16_from_bf16(__ldg(xp), __ldg(xp + 1), xv);
-          }
-        };
-        if (T == 1) {
-          // one row: two segments per pass, independent accumulators
-          float ag0 = 0.f, au0 = 0.f, ag1 = 0.f, au1 = 0.f;
-          int seg = lane;
-          for (; seg + 32 < nseg_h; seg += 64) {
-            f2 x0[8], x1[8];
-            load_x(0, seg, x0);
-            load_x(0, seg + 32, x1);
-            const uint4 g0 = *reinterpret_cast<const uint4*>(qg_row + seg * 16);
-            const uint4 v0 = *reinterpret_cast<const uint4*>(qu_row + seg * 16);
-            const uint4 g1 = *reinterpret_cast<const uint4*>(qg_row + (seg + 32) * 16);
-            const uint4 v1 = *reinterpret_cast<const uint4*>(qu_row + (seg + 32) * 16);
-            ag0 = fmaf(half_bits_to_f32(sg[seg >> 1]), dot16(g0, x0), ag0);
-            au0 = fmaf(half_bits_to_f32(su[seg >> 1]), dot16(v0, x0), au0);
-            ag1 = fmaf(half_bits_to_f32(sg[(seg + 32) >> 1]), dot16(g1, x1), ag1);
-            au1 = fmaf(half_bits_to_f32(su[(seg + 32) >> 1]), dot16(v1, x1), au1);
-          }
-          if (seg < nseg_h) {
-            f2 x0[8];
-            load_x(0, seg, x0);
-            const uint4 g0 = *reinterpret_cast<const uint4*>(qg_row + seg * 16);
-            const uint4 v0 = *reinterpret_cast<const uint4*>(qu_row + seg * 16);
-            ag0 = fmaf(half_bits_to_f32(sg[seg >> 1]), dot16(g0, x0), ag0);
-            au0 = fmaf(half_bits_to_f32(su[seg >> 1]), dot16(v0, x0), au0);
-          }
-          const float accg = warp_sum(ag0 + ag1), accu = warp_sum(au0 + au1);
-          if (lane == 0) a.hbuf[(int64_t)ui.y * I + i] = silu(accg) * accu;
-        } else {
-          for (int rr = 0; rr < ui.z; ++rr) {
-            const int pos = ui.y + rr;
-            const int t = r.tok[pos];
-            float accg = 0.f, accu = 0.f;
-            for (int seg = lane; seg < nseg_h; seg += 32) {
-              f2 xv[8];
-              load_x(t, seg, xv);
-              const uint4 qg = *reinterpret_cast<const uint4*>(qg_row + seg * 16);
-              const uint4 qu = *reinterpret_cast<const uint4*>(qu_row + seg * 16);
-              accg = fmaf(half_bits_to_f32(sg[seg >> 1]), dot16(qg, xv), accg);
-              accu = fmaf(half_bits_to_f32(su[seg >> 1]), dot16(qu, xv), accu);
+    // After a wait gives up (ok = false) a warp skips the rest of its waits,
+    // work and arrivals but still passes every consumer barrier, so that the
+    // other warps are never left waiting at one.
+    bool ok = true;
+    float acc[kMulti ? kRowsMulti : 1][kMulti ? kMaxDecodeT : 1];
+#pragma unroll
+    for (int jr = 0; jr < (kMulti ? kRowsMulti : 1); ++jr)
+#pragma unroll
+      for (int t = 0; t < (kMulti ? kMaxDecodeT : 1); ++t) acc[jr][t] = 0.f;
+    int st = 0;
+    uint32_t ph = 0;
+    int jj = 0;  // stages consumed
+    for (int ch = c0; ch < c1; ++ch) {
+      const int4 ui = r.u[ch / G];  // (expert, first grouped row, rows, 0)
+      float* hb = hbuf + ((ch - c0) & 1) * (kMulti ? kMaxDecodeT : 1) * kChunk;
+      // ---- gate/up: unit q of the chunk is computed by warp q, in stage q / R
+      for (int q = 0; q < n_gu; ++q) {
+        ok = ok && !s_abort;
+        if (ok && !mbar_wait(&full[st], ph)) {
+          report_wait(a.meta, kSiteGuFull, jj, warp);
+          ok = false;
+          s_abort = 1;
+        }
+        if (ok && warp / R == q) {
+          const int off = warp - q * R;  // unit within the stage
+          const uint8_t* grow = ring + (size_t)st * a.stage_bytes +
+                                (size_t)((off / kGUGroup) * 2 * kGUGroup + off % kGUGroup) * rb_h;
+          const uint8_t* urow = grow + (size_t)kGUGroup * rb_h;
+          const uint16_t* sg = reinterpret_cast<const uint16_t*>(grow + H);
+          const uint16_t* su = reinterpret_cast<const uint16_t*>(urow + H);
+          for (int m = 0; m < (kMulti ? ui.z : 1); ++m) {
+            const int t = kMulti ? r.tok[ui.y + m] : 0;
+            const uint8_t* xh = xhi + (size_t)t * H;
+            const uint8_t* xl = xlo + (size_t)t * H;
+            const int2* xi = xinfo + (size_t)t * nseg;
+            float ag = 0.f, au = 0.f;
+#pragma unroll(kMulti ? 1 : 2)
+            for (int s = lane; s < nseg; s += 32) {
+              const uint4 qg = *reinterpret_cast<const uint4*>(grow + s * 16);
+              const uint4 qu = *reinterpret_cast<const uint4*>(urow + s * 16);
+              const uint4 vh = *reinterpret_cast<const uint4*>(xh + s * 16);
+              const uint4 vl = *reinterpret_cast<const uint4*>(xl + s * 16);
+              const int2 inf = xi[s];
+              const float f = __int_as_float(inf.x);
+              const int Sg = seg_dot_i(qg, vh, vl) - inf.y;
+              const int Su = seg_dot_i(qu, vh, vl) - inf.y;
+              ag = fmaf((float)Sg, half_bits_to_f32(sg[s >> 1]) * f, ag);
+              au = fmaf((float)Su, half_bits_to_f32(su[s >> 1]) * f, au);
             }
-            accg = warp_sum(accg);
-            accu = warp_sum(accu);
-            if (lane == 0) a.hbuf[(int64_t)pos * I + i] = silu(accg) * accu;
+            ag = warp_sum(ag);
+            au = warp_sum(au);
+            if (lane == 0) hb[m * kChunk + warp] = silu(ag) * au;
           }
         }
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(&empty[st]);
+        ++jj;
+        if (++st == a.stages) {
+          st = 0;
+          ph ^= 1u;
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-      if (++st == a.stages) {
-        st = 0;
-        ph ^= 1u;
+      consumer_sync();  // the chunk's h is complete
+      // ---- down: thread tid takes rows tid, tid + 512, ... of each stage
+      for (int q = 0; q < n_dn; ++q) {
+        ok = ok && !s_abort;
+        if (ok && !mbar_wait(&full[st], ph)) {
+          report_wait(a.meta, kSiteDnFull, jj, warp);
+          ok = false;
+          s_abort = 1;
+        }
+        if (ok) {
+          const uint8_t* sb = ring + (size_t)st * a.stage_bytes;
+          const int r0 = q * Dr, nr = ::min(Dr, H - r0);
+          const uint16_t* sc = reinterpret_cast<const uint16_t*>(sb + (size_t)nr * kChunk);
+          if (kMulti) {
+            // all rows in this one stage (H <= 2048); the expert's tokens ascending
+            uint32_t emask = 0;
+            for (int p = ui.y; p < ui.y + ui.z; ++p) emask |= 1u << r.tok[p];
+#pragma unroll
+            for (int tt = 0; tt < kMaxDecodeT; ++tt) {
+              if ((emask >> tt) & 1u) {
+                const int m = __popc(emask & ((1u << tt) - 1u));
+                const float gate = r.gates[r.slot[ui.y + m]];
+                const float* hm = hb + m * kChunk;
+#pragma unroll
+                for (int jr = 0; jr < kRowsMulti; ++jr) {
+                  const int rr = tid + kCT * jr;
+                  if (rr < nr) {
+                    const uint4 qq = *reinterpret_cast<const uint4*>(sb + (size_t)rr * kChunk);
+                    acc[jr][tt] = fmaf(gate * half_bits_to_f32(sc[rr]), dot16_smem(qq, hm), acc[jr][tt]);
+                  }
+                }
+              }
+            }
+          } else {
+            const float gate = r.gates[r.slot[ui.y]];
+            f2 hv[8];
+            load_h16(hb, hv);
+            for (int rr = tid; rr < nr; rr += kCT) {
+              const uint4 qq = *reinterpret_cast<const uint4*>(sb + (size_t)rr * kChunk);
+              acc_s[r0 + rr] = fmaf(gate * half_bits_to_f32(sc[rr]), dot16(qq, hv), acc_s[r0 + rr]);
+            }
+          }
+        }
+        __syncwarp();
+        if (ok && lane == 0) mbar_arrive(&empty[st]);
+        ++jj;
+        if (++st == a.stages) {
+          st = 0;
+          ph ^= 1u;
+        }
       }
     }
-
-    // ---- phase 2: every CTA's h is written before any CTA reads it. The
-    // arrival is a release (ordering this CTA's h stores, which the consumer
-    // barrier ordered before it), the poll an acquire.
+    // ---- partial output of this CTA to global memory
+    float* part = a.partial + (size_t)blockIdx.x * T * H;
+    if (kMulti) {
+#pragma unroll
+      for (int tt = 0; tt < kMaxDecodeT; ++tt)
+        if ((cta_mask >> tt) & 1u) {
+#pragma unroll
+          for (int jr = 0; jr < kRowsMulti; ++jr) {
+            const int rr = tid + kCT * jr;
+            if (rr < H) __stcg(part + (size_t)tt * H + rr, acc[jr][tt]);
+          }
+        }
+    } else {
+      consumer_sync();  // every row of acc_s is final
+      if (cta_mask)
+        for (int o = tid; o < H; o += kCT) __stcg(part + o, acc_s[o]);
+    }
+    if (tid == 0) a.pmask[blockIdx.x] = cta_mask;
+    // ---- grid-wide: every partial is written before any CTA sums them. The
+    // arrival is a release (ordering the CTA's partial stores, which the
+    // consumer barrier ordered before it), the poll an acquire.
     consumer_sync();
     if (tid == 0) {
       unsigned long long* gb = reinterpret_cast<unsigned long long*>(&a.meta->gbar);
+      const unsigned long long target = (unsigned long long)gridDim.x + a.grid_extra;
       asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(gb) : "memory");
-      if (ld_acquire_u64(gb) < gridDim.x) {
+      if (ld_acquire_u64(gb) < target) {
         const uint64_t t0 = globaltimer_ns();
-        while (ld_acquire_u64(gb) < gridDim.x) {
-          if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        while (ld_acquire_u64(gb) < target) {
+          if (globaltimer_ns() - t0 > a.grid_wait_ns) {
             report_wait(a.meta, kSiteGrid, 0, gridDim.x);
             break;
           }
@@ -445,159 +524,50 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       }
     }
     consumer_sync();
-    if (a.h_smem) {  // x is no longer read: the area now takes h, segment-transposed
-      float* hs = reinterpret_cast<float*>(smem);
-      const int q4 = I / 4;
-      for (int c = tid; c < r.rows * q4; c += kCW * 32) {  // c: 4 floats
-        const int pos = c / q4, cc = c % q4, seg = cc >> 2, i = cc & 3;
-        *reinterpret_cast<float4*>(hs + (size_t)pos * I + i * (I / 4) + seg * 4) =
-            __ldcg(reinterpret_cast<const float4*>(a.hbuf) + c);
-      }
-      consumer_sync();
-    }
-
-    // ---- phase 3: down + combine. Warp w owns row w of every 16-row block;
-    // per block it visits every touched expert (ascending id, shared last)
-    // keeping per-lane partial sums per token, and reduces across the warp
-    // once, at the end of the block. The experts of a stage are processed
-    // together (independent dot products in flight).
-    const float* hsrc = a.h_smem ? reinterpret_cast<const float*>(smem) : a.hbuf;
-    const int nseg_i = I / 16;
-    float part[kMaxDecodeT];
+    // ---- this CTA's output rows [o0, o1): warp w sums the partials of CTAs
+    // [w cpw, (w + 1) cpw), lane = row; then the 16 warp sums in order.
+    uint32_t* s_pm = reinterpret_cast<uint32_t*>(ring);
+    float* red = reinterpret_cast<float*>(ring + align128(gridDim.x * 4u));  // [kCW][T][rows]
+    for (int c = tid; c < (int)gridDim.x; c += kCT) s_pm[c] = __ldcg(a.pmask + c);
+    consumer_sync();
+    const int o0 = (int)((int64_t)H * blockIdx.x / gridDim.x), o1 = (int)((int64_t)H * (blockIdx.x + 1) / gridDim.x);
+    const int nrow = o1 - o0;
+    const int cpw = ((int)gridDim.x + kCW - 1) / kCW;
+    const int cb = warp * cpw, ce = ::min((int)gridDim.x, cb + cpw);
+    for (int rl = lane; rl < nrow; rl += 32) {
+      for (int t = 0; t < T; ++t) {
+        float v = 0.f;
+        for (int c = cb; c < ce; c += kRedBatch) {  // the batch's loads all in flight, then summed in order
+          float pv[kRedBatch];
 #pragma unroll
-    for (int t = 0; t < kMaxDecodeT; ++t) part[t] = 0.f;
-    st = n_gu % a.stages;  // ring position of stage n_gu + jd
-    ph = (uint32_t)(n_gu / a.stages) & 1u;
-    int ge = 0, blk = 0;  // expert group and row block of down stage jd
-    for (int jd = 0; jd < n_dn && ok; ++jd) {
-      if (!mbar_wait(&full[st], ph)) {
-        report_wait(a.meta, kSiteDnFull, n_gu + jd, warp);
-        ok = false;
-        break;
-      }
-      const int e0 = ge * a.n_per, ne = ::min(nU, e0 + a.n_per) - e0;
-      const int r0 = o0 + blk * kRowBlock;
-      const int nr = ::min(kRowBlock + 0, o1 - r0);
-      if (kOne) {
-        // one token: warp w takes rows ra = w & 7 and ra + 8 of the block and
-        // the segments of parity w >> 3, so an h segment is loaded once for
-        // two rows; the two halves of a row are added after the loop
-        const int ra = warp & 7, hf = warp >> 3;
-        if (ra < nr) {
-          const bool has_b = ra + 8 < nr;
-          const uint8_t* sa = ring + (size_t)st * a.stage_bytes + (size_t)ra * rb_i;
-          float da[kMaxPer], db[kMaxPer];
-          const float* hrow[kMaxPer];
+          for (int q = 0; q < kRedBatch; ++q)
+            pv[q] = (c + q < ce && ((s_pm[c + q] >> t) & 1u))
+                        ? __ldcg(a.partial + ((size_t)(c + q) * T + t) * H + o0 + rl)
+                        : 0.f;
 #pragma unroll
-          for (int el = 0; el < kMaxPer; ++el) {
-            da[el] = 0.f;
-            db[el] = 0.f;
-            hrow[el] = hsrc + (size_t)(el < ne ? r.u[e0 + el].y : 0) * I;
-          }
-          for (int seg = 2 * lane + hf; seg < nseg_i; seg += 64) {
-#pragma unroll
-            for (int el = 0; el < kMaxPer; ++el) {
-              if (el < ne) {
-                const uint8_t* qa = sa + (size_t)el * kRowBlock * rb_i;
-                f2 hv[8];
-                if (a.h_smem)
-                  x16_from_f32_t(hrow[el], I, seg, hv);
-                else
-                  x16_from_f32_global(hrow[el] + seg * 16, hv);
-                const uint4 qq = *reinterpret_cast<const uint4*>(qa + seg * 16);
-                da[el] = fmaf(half_bits_to_f32(reinterpret_cast<const uint16_t*>(qa + I)[seg >> 1]), dot16(qq, hv),
-                              da[el]);
-                if (has_b) {
-                  const uint8_t* qb = qa + (size_t)8 * rb_i;
-                  const uint4 qr = *reinterpret_cast<const uint4*>(qb + seg * 16);
-                  db[el] = fmaf(half_bits_to_f32(reinterpret_cast<const uint16_t*>(qb + I)[seg >> 1]), dot16(qr, hv),
-                                db[el]);
-                }
-              }
-            }
-          }
-#pragma unroll
-          for (int el = 0; el < kMaxPer; ++el)
-            if (el < ne) {
-              const float g = r.gates[r.slot[r.u[e0 + el].y]];
-              part[0] = fmaf(g, da[el], part[0]);
-              part[1] = fmaf(g, db[el], part[1]);
-            }
+          for (int q = 0; q < kRedBatch; ++q) v += pv[q];
         }
-      } else if (warp < nr) {
-        const uint8_t* sb = ring + (size_t)st * a.stage_bytes + (size_t)warp * rb_i;
-        if (T == 1) {        } else {
-          for (int el = 0; el < ne; ++el) {
-            const int4 ui = r.u[e0 + el];
-            const uint8_t* qrow = sb + (size_t)el * kRowBlock * rb_i;
-            const uint16_t* sc = reinterpret_cast<const uint16_t*>(qrow + I);
-            for (int m = 0; m < ui.z; ++m) {
-              const int pos = ui.y + m;
-              const float* hr = hsrc + (size_t)pos * I;
-              float d = 0.f;
-              for (int seg = lane; seg < nseg_i; seg += 32) {
-                f2 hv[8];
-                if (a.h_smem)
-                  x16_from_f32_t(hr, I, seg, hv);
-                else
-                  x16_from_f32_global(hr + seg * 16, hv);
-                const uint4 qq = *reinterpret_cast<const uint4*>(qrow + seg * 16);
-                d = fmaf(half_bits_to_f32(sc[seg >> 1]), dot16(qq, hv), d);
-              }
-              const float g = r.gates[r.slot[pos]];
-              const int t = r.tok[pos];
-#pragma unroll
-              for (int tt = 0; tt < kMaxDecodeT; ++tt)
-                if (tt == t) part[tt] = fmaf(g, d, part[tt]);
-            }
-          }
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-      if (ge == n_ge - 1 && kOne) {  // block done: this warp's halves of its two rows
-        const float va = warp_sum(part[0]), vb = warp_sum(part[1]);
-        const int ra = warp & 7, hf = warp >> 3, rr = blk * kRowBlock + ra;
-        if (lane == 0 && ra < nr) s_half[hf][rr] = va;
-        if (lane == 0 && ra + 8 < nr) s_half[hf][rr + 8] = vb;
-        part[0] = 0.f;
-        part[1] = 0.f;
-      } else if (ge == n_ge - 1) {  // block done: one reduction per token, lane t writes token t
-        if (warp < nr) {
-          float mine = 0.f;
-#pragma unroll
-          for (int tt = 0; tt < kMaxDecodeT; ++tt) {
-            if (tt < T) {
-              const float v = warp_sum(part[tt]);
-              if (lane == tt) mine = v;
-            }
-            part[tt] = 0.f;
-          }
-          if (lane < T) a.out[(int64_t)lane * H + r0 + warp] = __float2bfloat16_rn(mine);
-        }
-      }
-      if (++ge == n_ge) {
-        ge = 0;
-        ++blk;
-      }
-      if (++st == a.stages) {
-        st = 0;
-        ph ^= 1u;
+        red[((size_t)warp * T + t) * nrow + rl] = v;
       }
     }
-    if (kOne) {  // every consumer warp gets here (a timed-out wait ends the loop, not the warp)
-      consumer_sync();
-      for (int i = tid; i < o1 - o0; i += kCW * 32) a.out[o0 + i] = __float2bfloat16_rn(s_half[0][i] + s_half[1][i]);
+    consumer_sync();
+    for (int i = tid; i < T * nrow; i += kCT) {
+      const int t = i / nrow, rl = i - t * nrow;
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kCW; ++w) v += red[((size_t)w * T + t) * nrow + rl];
+      a.out[(size_t)t * H + o0 + rl] = __float2bfloat16_rn(v);
     }
   }
   __syncthreads();
 }
 
-// The grid-wide barrier needs every CTA resident: the grid is one CTA per SM
-// and each CTA takes most of an SM's shared memory, so once earlier work has
-// drained all of them are; if something else holds SMs past the wait limit
-// the call reports FW_ETIMEOUT instead of hanging.
-cudaError_t launch(const DecodeArgs& a, unsigned grid, size_t smem, cudaStream_t s) {
+// The grid-wide wait needs every CTA resident: the grid is one CTA per SM
+// and each CTA takes more than half of an SM's shared memory (checked at
+// init), so once earlier work has drained all of them are; if something else
+// holds SMs past the wait bound the call reports FW_ETIMEOUT instead of
+// hanging.
+cudaError_t launch(const DecodeArgs& a, bool multi, unsigned grid, size_t smem, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -608,46 +578,62 @@ cudaError_t launch(const DecodeArgs& a, unsigned grid, size_t smem, cudaStream_t
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const bool one = a.T == 1 && a.x_mode == kXSmemF32 && (a.H + (int)grid - 1) / (int)grid <= kMaxRowsOne;
-  return one ? cudaLaunchKernelEx(&cfg, decode_experts_kernel<true>, a)
-             : cudaLaunchKernelEx(&cfg, decode_experts_kernel<false>, a);
+  return multi ? cudaLaunchKernelEx(&cfg, decode_experts_kernel<true>, a)
+               : cudaLaunchKernelEx(&cfg, decode_experts_kernel<false>, a);
 }
 
-int g_smem_optin = 0;
-constexpr uint32_t kActMax = 80 * 1024;     // x or h in shared memory up to this size
-constexpr uint32_t kStageTarget = 36 * 1024;  // one bulk copy per stage: fewer, larger copies stream faster
+int g_smem_optin = 0;  // dynamic shared memory per CTA the kernels may use
 
 }  // namespace
+
+bool decode_supported(int H, int T) { return T >= 1 && T <= kMaxDecodeT && (T == 1 ? H <= kMaxHOne : H <= kMaxHMulti); }
 
 cudaError_t configure_decode_kernels() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  // the dynamic budget is what the larger static footprint of the two
-  // instantiations leaves (the one-token one also holds the row halves)
   cudaFuncAttributes fa, fb;
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, decode_experts_kernel<false>);
   if (e == cudaSuccess) e = cudaFuncGetAttributes(&fb, decode_experts_kernel<true>);
-  if (e == cudaSuccess) {
-    g_smem_optin -= (int)std::max(fa.sharedSizeBytes, fb.sharedSizeBytes);
-    e = cudaFuncSetAttribute(decode_experts_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_optin);
+  if (e == cudaSuccess) g_smem_optin -= (int)std::max(fa.sharedSizeBytes, fb.sharedSizeBytes);
+  const void* kern[2] = {(const void*)decode_experts_kernel<false>, (const void*)decode_experts_kernel<true>};
+  for (int m = 0; m < 2 && e == cudaSuccess; ++m) {
+    e = cudaFuncSetAttribute(kern[m], cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_optin);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kern[m], cudaFuncAttributePreferredSharedMemoryCarveout,
+                               (int)cudaSharedmemCarveoutMaxShared);
   }
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_experts_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_optin);
+  // one CTA per SM must fit with the least shared memory a launch asks for:
+  // the grid-wide wait relies on every CTA of the grid being resident
+  for (int m = 0; m < 2 && e == cudaSuccess; ++m) {
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern[m], kThreads, (size_t)g_smem_optin / 2 + 1024);
+    if (e == cudaSuccess && n < 1) {
+      cudaFuncAttributes f = m ? fb : fa;
+      char msg[256];
+      snprintf(msg, sizeof(msg),
+               "decode kernel: no CTA of %d threads fits an SM (registers %d, static smem %zu, dynamic %d)",
+               kThreads, f.numRegs, f.sharedSizeBytes, g_smem_optin / 2 + 1024);
+      set_error(FW_EUNSUPPORTED, msg);
+      e = cudaErrorInvalidConfiguration;
+    }
+  }
   return e;
 }
 
 cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfloat16* out, bool publish,
                               int32_t* ids_out, float* gates_out, cudaStream_t s) {
   const int H = h->cfg.H, I = h->cfg.I, k = h->cfg.k, S = h->S;
-  const int rows = T * (k + S);
-  const int grid = h->num_sms;
+  const bool multi = T > 1;
+  const int tcap = multi ? kMaxDecodeT : 1;
   DecodeArgs a;
   a.q_gu = h->q_gu;
-  a.q_d = h->q_d;
+  a.q_dc = h->q_dc;
+  a.st_d = h->st_d;
   a.x = x;
   a.logits = h->logits;
-  a.hbuf = static_cast<float*>(h->hbuf);
+  a.partial = h->partial;
+  a.pmask = h->pmask;
   a.out = out;
   a.ro = RoutingOut{ids_out, gates_out, h->ids,      h->gates,    h->counts, h->offsets,
                     h->perm, h->inv,    h->row_token, h->row_gate, h->uinfo,  h->meta};
@@ -659,26 +645,42 @@ cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfl
   a.S = S;
   a.T = T;
   a.publish = publish ? 1 : 0;
-  const uint32_t x32 = (uint32_t)T * H * 4, x16 = (uint32_t)T * H * 2, hb = (uint32_t)rows * I * 4;
-  a.x_mode = x32 <= 32 * 1024 ? kXSmemF32 : (x16 <= kActMax ? kXSmemBf16 : kXGlobal);
-  a.h_smem = hb <= kActMax;
-  const uint32_t xb = a.x_mode == kXSmemF32 ? x32 : (a.x_mode == kXSmemBf16 ? x16 : 0);
-  a.act_bytes = std::max(xb, a.h_smem ? hb : 0u);
-  const uint32_t unit = (uint32_t)(2 * row_bytes(H));
-  int R = 32;
-  while (R > kGUGroup && (uint32_t)R * unit > kStageTarget) R /= 2;
+  // stages: gate/up R units (2R rows of row_bytes(H)), down Dr rows x 18 bytes
+  const uint32_t rb = (uint32_t)row_bytes(H);
+  int R = kChunk;
+  while (R > kGUGroup && (uint32_t)(2 * R) * rb > kStageTarget) R /= 2;
   a.R = R;
-  const uint32_t dn_block = (uint32_t)(kRowBlock * row_bytes(I));
-  a.n_per = (int)std::max<uint32_t>(1, std::min<uint32_t>(kMaxPer, (uint32_t)R * unit / dn_block));
-  a.stage_bytes = std::max((uint32_t)R * unit, (uint32_t)a.n_per * dn_block);
-  const int64_t ring_bytes = (int64_t)g_smem_optin - align128(a.act_bytes) - 256;
+  const int nd = (H + kDnRowsMax - 1) / kDnRowsMax;
+  a.Dr = multi ? H : ((H + nd - 1) / nd + 15) / 16 * 16;
+  a.stage_bytes = std::max((uint32_t)(2 * R) * rb, align128((uint32_t)a.Dr * 18u));
+  a.stage_bytes = align128(a.stage_bytes);
+  // dynamic shared memory: x planes, segment info, the one-token partial row, h
+  const uint32_t xb = align128((uint32_t)(2 * T * H));
+  a.off_info = xb;
+  a.off_acc = a.off_info + align128((uint32_t)(T * (H / 16) * 8));
+  a.off_h = a.off_acc + (multi ? 0u : align128((uint32_t)H * 4u));
+  a.off_ring = a.off_h + align128((uint32_t)(2 * tcap * kChunk * 4));
+  const int64_t ring_bytes = (int64_t)g_smem_optin - a.off_ring - 256;
   a.stages = (int)std::min<int64_t>(kMaxStages, ring_bytes / a.stage_bytes);
   if (a.stages < 2) return cudaErrorInvalidConfiguration;
+  const int grid = h->num_sms;
+  // the ring also holds the logits while routing and the sums at the end
+  const uint32_t need_end = align128(grid * 4u) + (uint32_t)(kCW * T * ((H + grid - 1) / grid) * 4);
+  if ((uint32_t)a.stages * a.stage_bytes < std::max<uint32_t>(need_end, (uint32_t)(T * h->cfg.E * 4)))
+    return cudaErrorInvalidConfiguration;
+  if (h->test_grid_timeouts > 0) {  // test hook: this call's grid-wide wait cannot be met and gives up fast
+    --h->test_grid_timeouts;
+    a.grid_extra = 1;
+    a.grid_wait_ns = 1000000ull;
+  } else {
+    a.grid_extra = 0;
+    a.grid_wait_ns = kWaitLimitNs;
+  }
   // at least half the SM's shared memory, so that no two CTAs share an SM
-  const size_t smem = std::max<size_t>(align128(a.act_bytes) + (size_t)a.stages * a.stage_bytes,
+  const size_t smem = std::max<size_t>(a.off_ring + (size_t)a.stages * a.stage_bytes,
                                        (size_t)g_smem_optin / 2 + 1024);
   KernelTimer tm(h, FW_KERNEL_DECODE_EXPERTS, s);
-  return launch(a, (unsigned)grid, smem, s);
+  return launch(a, multi, (unsigned)grid, smem, s);
 }
 
 }  // namespace fw

@@ -91,6 +91,7 @@ struct Handle {
   uint16_t* st_gu;    // [EU][H/32][2I] binary16 scales, transposed (prefill)
   uint8_t* q_d;       // [EU][H] rows of row_bytes(I)
   uint16_t* st_d;     // [EU][I/32][H]
+  uint8_t* q_dc;      // [EU][I/16][H][16] down codes by 16-column groups (decode)
   float* wr;          // [E][H]
   float* bias;        // [E] (zeros when none)
   __nv_bfloat16* wr3; // [3][E][H] bf16 planes summing exactly to wr (prefill router), or null
@@ -112,7 +113,10 @@ struct Handle {
   __nv_bfloat16* xperm; // [rows_max][H] x gathered into grouped order (prefill)
   void* hbuf;         // [rows_max][I] fp32 (decode) or bf16 (prefill)
   __nv_bfloat16* yp;  // [rows_max][H] bf16 (prefill)
+  float* partial;     // [num_sms][min(T_max, 16)][H] decode: per-CTA partial outputs
+  uint32_t* pmask;    // [num_sms] decode: tokens each CTA's partial covers
   Meta* meta;
+  int test_grid_timeouts;  // test hook (FWMOE_TEST_GRID_TIMEOUTS at init): decode calls whose grid wait must time out
   // ---- device staging for fw_moe_forward_host
   void* x_dev;
   void* out_dev;
@@ -159,6 +163,9 @@ cudaError_t configure_decode_kernels();
 cudaError_t configure_prefill_kernels();
 cudaError_t prepare_prefill(Handle* h);  // tensor maps; needs the planes and workspace allocated
 // Each returns cudaGetLastError() of its launches.
+// Whether T tokens take the decode kernel for hidden size H (several tokens:
+// H <= 2048, the partial outputs live in registers).
+bool decode_supported(int H, int T);
 cudaError_t launch_quantize_q8_0(const float* w, int64_t rows, int64_t K, uint8_t* blocks, cudaStream_t s);
 cudaError_t launch_repack(const Handle* h, int which, int expert0, int count, const uint8_t* blocks,
                           cudaStream_t s);

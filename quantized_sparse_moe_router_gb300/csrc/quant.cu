@@ -47,6 +47,7 @@ __global__ void quantize_q8_0_kernel(const float* __restrict__ w, int64_t nblock
 struct PlaneView {
   uint8_t* q;      // code plane of this matrix kind, expert 0 (rows: codes, then scales)
   uint16_t* st;    // transposed scale plane
+  uint8_t* qc;     // down only: the codes by 16-column groups (or null)
   int64_t rows;    // rows of one expert's matrix (I for gate/up, H for down)
   int64_t prows;   // rows of one expert in the plane (2I for gate/up, H for down)
   int64_t K;       // row length (H for gate/up, I for down)
@@ -79,6 +80,12 @@ __global__ void repack_kernel(PlaneView p, int expert0, int64_t nblocks, const u
   qd[1] = make_uint4(words[4], words[5], words[6], words[7]);
   reinterpret_cast<uint16_t*>(row + p.K)[b] = in[0];
   p.st[(e * nb + b) * p.prows + plane_row(p, r)] = in[0];
+  if (p.qc) {  // down codes again, by 16-column groups: [e][K/16][rows][16]
+    uint4* c0 = reinterpret_cast<uint4*>(p.qc + ((e * (p.K / 16) + 2 * b) * p.rows + r) * 16);
+    uint4* c1 = reinterpret_cast<uint4*>(p.qc + ((e * (p.K / 16) + 2 * b + 1) * p.rows + r) * 16);
+    *c0 = make_uint4(words[0], words[1], words[2], words[3]);
+    *c1 = make_uint4(words[4], words[5], words[6], words[7]);
+  }
 }
 
 __global__ void export_kernel(PlaneView p, int expert, int64_t nblocks, uint8_t* __restrict__ dst) {
@@ -106,9 +113,11 @@ PlaneView view_of(const Handle* h, int which) {
   PlaneView p;
   const int64_t H = h->cfg.H, I = h->cfg.I;
   p.which = which;
+  p.qc = nullptr;
   if (which == 2) {
     p.q = h->q_d;
     p.st = h->st_d;
+    p.qc = h->q_dc;
     p.rows = H;
     p.prows = H;
     p.K = I;

@@ -62,9 +62,10 @@ __device__ __forceinline__ float warp_gate(float my_z, int k, int lane) {
   return ex / sum;
 }
 
-// The routing of a decode batch in shared memory.
+// The routing of a decode batch in shared memory. The batch's logits are
+// staged in a separate buffer the caller provides (T * E floats), which is
+// free again once the routing is made.
 struct SmemRouting {
-  float z[kMaxDecodeT * kMaxE];  // the batch's logits
   float zsel[kMaxDecodeT * kMaxK];  // selected logits, in rank order
   int ids[kMaxDecodeT * kMaxK];
   float gates[kMaxDecodeT * (kMaxK + 1)];  // by slot; slot T k + t is token t's shared expert (1)
@@ -89,7 +90,7 @@ struct SmemRouting {
 // (warp_topk). Then warp 0 alone groups the pairs (counts, offsets, the
 // table of touched experts, positions) while other warps make the gates.
 template <int NT>
-__device__ void route_in_smem(const float* logits, int T, int E, int k, int S, SmemRouting& r) {
+__device__ void route_in_smem(const float* logits, int T, int E, int k, int S, SmemRouting& r, float* zbuf) {
   static_assert(NT % 32 == 0 && NT >= 64, "whole warps, at least two");
   constexpr int NW = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -97,7 +98,7 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
   const int P = T * E;
   const bool by_rank = 4 * P <= NT;
   if (by_rank)
-    for (int i = tid; i < P; i += NT) r.z[i] = __ldcg(logits + i);
+    for (int i = tid; i < P; i += NT) zbuf[i] = __ldcg(logits + i);
   for (int i = tid; i < EU; i += NT) {
     r.cnt[i] = 0;
     r.mask[i] = 0;
@@ -118,7 +119,7 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
       if (p < P) {
         t = p / E;
         e = p - t * E;
-        const float* zt = r.z + t * E;
+        const float* zt = zbuf + t * E;
         z = zt[e];
 #pragma unroll 4
         for (int f = c; f < E; f += s) {
@@ -227,10 +228,10 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
 // counts and offsets for all experts (read only when CTA 0 publishes) come
 // from comparisons with the k ids.
 template <int NT>
-__device__ void route_one_in_smem(const float* logits, int E, int k, int S, SmemRouting& r) {
+__device__ void route_one_in_smem(const float* logits, int E, int k, int S, SmemRouting& r, float* zbuf) {
   constexpr int NW = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < E; i += NT) r.z[i] = __ldcg(logits + i);
+  for (int i = tid; i < E; i += NT) zbuf[i] = __ldcg(logits + i);
   __syncthreads();
   {
     int s = 32;  // lanes per expert, as many as the block allows
@@ -241,10 +242,10 @@ __device__ void route_one_in_smem(const float* logits, int E, int k, int S, Smem
       int rank = 0;
       float z = 0.f;
       if (e < E) {
-        z = r.z[e];
+        z = zbuf[e];
 #pragma unroll 4
         for (int f = c; f < E; f += s) {
-          const float zf = r.z[f];
+          const float zf = zbuf[f];
           rank += (zf > z) | ((zf == z) & (f < e));
         }
       }

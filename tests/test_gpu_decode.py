@@ -79,6 +79,9 @@ DECODE_CASES = [
     ("tiny", dict(T=3, k=1)),
     ("tiny", dict(T=16, k=8)),                 # k = E
     ("tiny", dict(T=5, S=1)),
+    ("tiny", dict(T=1, H=2304, S=1)),          # one token, H past the several-token limit: two down stages
+    ("tiny", dict(T=1, H=4160, I=192)),        # one token, three down stages (4160 = 3 x 1387 -> 1392-row stages)
+    ("tiny", dict(T=2, H=2304)),               # several tokens with H > 2048: the prefill path takes them
     ("dec1", {}),
     ("dec16", {}),
     ("large1", {}),
@@ -177,4 +180,32 @@ def test_forward_host_matches_device_path():
     out_h = torch.empty((4, wl.H), dtype=torch.bfloat16).pin_memory()
     layer.forward_host(xh, ids_h, out_h)
     assert torch.equal(ids_h, ids.cpu()) and torch.equal(out_h, out.cpu())
+    layer.close()
+
+
+def test_decode_grid_wait_bound_gives_timeout_and_handle_recovers(monkeypatch):
+    """A test hook makes the next two decode calls' grid-wide wait unreachable
+    (one arrival more than the grid): the kernel gives up after its bound
+    (1 ms here), records site 8 and returns; fw_moe_status reports
+    FW_ETIMEOUT; the calls after that are correct again on the same handle.
+    One call of each decode instantiation (one token, several tokens)."""
+    wl = synth.WORKLOADS["tiny"]
+    dl = DeviceLayer(wl, 0, DEV)
+    ol = OracleLayer(wl, 0)
+    monkeypatch.setenv("FWMOE_TEST_GRID_TIMEOUTS", "2")
+    layer = dl.make(T_max=4)
+    monkeypatch.delenv("FWMOE_TEST_GRID_TIMEOUTS")
+    x = hidden_with_margins(wl, 0, ol.Wr, ol.bias)
+    xd = to_device_bf16(x, DEV)
+    for T in (1, 4):
+        layer.forward(xd[:T])
+        with pytest.raises(fw.FwError) as ei:
+            layer.status()
+        assert ei.value.status == fw.FW_ETIMEOUT and "site 8" in str(ei.value)
+    for T in (1, 4):
+        gates = torch.empty((T, wl.k), dtype=torch.float32, device=DEV)
+        ids, out = layer.forward(xd[:T], gates=gates)
+        torch.cuda.synchronize()
+        layer.status()
+        check_against_oracle(dl, ol, layer, x[:T], ids, gates, out)
     layer.close()
