@@ -67,9 +67,9 @@ struct Allocator {
 };
 
 void free_handle_memory(Handle* h) {
-  void* ptrs[] = {h->q_gu, h->st_gu, h->q_d, h->st_d, h->q_dc, h->wr3, h->wr, h->bias, h->ids, h->gates,
+  void* ptrs[] = {h->q_gu, h->q_dc, h->st_d, h->t_gu, h->t_d, h->wr3, h->wr, h->bias, h->ids, h->gates,
                   h->logits, h->counts, h->offsets, h->perm, h->inv, h->row_token, h->row_gate, h->uinfo,
-                  h->hist, h->minfo, h->minfo_s, h->xperm, h->hbuf, h->yp, h->partial, h->pmask, h->meta,
+                  h->hist, h->minfo, h->minfo_s, h->xperm, h->hbuf, h->yp, h->partial, h->zpart, h->meta,
                   h->x_dev, h->out_dev, h->ids_dev};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -162,6 +162,7 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
     h->test_grid_timeouts = (s && *s) ? atoi(s) : 0;
   }
   const bool pre = needs_prefill(h);
+  h->has_prefill = pre ? 1 : 0;
   const int64_t H = cfg->H, I = cfg->I, E = cfg->E, EU = h->EU, k = cfg->k, Tm = cfg->T_max;
   h->rows_max = Tm * (k + h->S);
 
@@ -175,10 +176,10 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
     size_t bytes;
   } req[] = {
       {(void**)&h->q_gu, (size_t)(EU * 2 * I * row_bytes(H))},
-      {(void**)&h->st_gu, (size_t)(EU * (H / 32) * 2 * I * 2)},
-      {(void**)&h->q_d, (size_t)(EU * H * row_bytes(I))},
-      {(void**)&h->st_d, (size_t)(EU * (I / 32) * H * 2)},
       {(void**)&h->q_dc, (size_t)(EU * H * I)},
+      {(void**)&h->st_d, (size_t)(EU * (I / 32) * H * 2)},
+      {(void**)&h->t_gu, (size_t)(pre ? EU * (2 * I / kTileRows) * (H / kTileK) * kTileBytes : 256)},
+      {(void**)&h->t_d, (size_t)(pre ? EU * ((H + kTileRows - 1) / kTileRows) * (I / kTileK) * kTileBytes : 256)},
       {(void**)&h->wr, (size_t)(E * H * 4)},
       {(void**)&h->bias, (size_t)(E * 4)},
       {(void**)&h->wr3, (size_t)(pre ? 3 * E * H * 2 : 256)},
@@ -199,7 +200,7 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
       {(void**)&h->hbuf, hbuf_bytes},
       {(void**)&h->yp, (size_t)(pre ? h->rows_max * H * 2 : 256)},
       {(void**)&h->partial, (size_t)(h->num_sms * T_dec * H * 4)},
-      {(void**)&h->pmask, (size_t)(h->num_sms * 4)},
+      {(void**)&h->zpart, (size_t)(pre ? kRouterMaxSplit * Tm * E * 4 : 256)},
       {(void**)&h->meta, sizeof(Meta)},
       {(void**)&h->x_dev, (size_t)(Tm * H * 2)},
       {(void**)&h->out_dev, (size_t)(Tm * H * 2)},
@@ -222,7 +223,9 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
   if (e == cudaSuccess) e = cudaMemsetAsync(h->meta, 0, sizeof(Meta), s);
   // the scale pads of the code planes are never used, but keep them defined
   if (e == cudaSuccess) e = cudaMemsetAsync(h->q_gu, 0, EU * 2 * I * row_bytes(H), s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(h->q_d, 0, EU * H * row_bytes(I), s);
+  // rows of a last partial down tile (H % 128 != 0) are read and their results dropped: keep them defined
+  if (e == cudaSuccess && pre)
+    e = cudaMemsetAsync(h->t_d, 0, EU * ((H + kTileRows - 1) / kTileRows) * (I / kTileK) * kTileBytes, s);
   if (e == cudaSuccess) e = launch_repack(h, 0, 0, (int)E, w->w_gate, s);
   if (e == cudaSuccess) e = launch_repack(h, 1, 0, (int)E, w->w_up, s);
   if (e == cudaSuccess) e = launch_repack(h, 2, 0, (int)E, w->w_down, s);

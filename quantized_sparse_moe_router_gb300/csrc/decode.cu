@@ -59,7 +59,7 @@ constexpr int kDnRowsMax = 2048;           // down rows per stage at most
 constexpr uint32_t kConsumerBarrier = 1;   // named barrier of the 16 consumer warps
 constexpr uint32_t kStageTarget = 36 * 1024;
 constexpr int kRedBatch = 10;              // partial loads in flight per lane in the final sums
-constexpr int kPrefetchAhead = 12;         // stages requested into L2 ahead of the ring
+constexpr int kMaxGrid = 256;              // CTAs (one per SM) the per-CTA token masks have room for
 
 struct DecodeArgs {
   const uint8_t* q_gu;   // [EU][2I] rows of row_bytes(H): codes + 128, then binary16 scales
@@ -68,7 +68,6 @@ struct DecodeArgs {
   const __nv_bfloat16* x;
   const float* logits;
   float* partial;        // [grid][T][H] fp32 partial outputs
-  uint32_t* pmask;       // [grid] tokens each CTA's partial covers
   __nv_bfloat16* out;
   RoutingOut ro;
   Meta* meta;
@@ -242,7 +241,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
   __shared__ SmemRouting r;
-  __shared__ uint32_t s_mask;
+  __shared__ uint32_t s_emask[kMaxE + 1];  // per touched expert (ascending): its tokens
+  __shared__ uint32_t s_pm[kMaxGrid];       // per CTA: the tokens its partial output covers
   __shared__ volatile int s_abort;  // a consumer gave up a wait: the others stop waiting too
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = a.H, I = a.I, T = kMulti ? a.T : 1, R = a.R, Dr = a.Dr;
@@ -288,22 +288,29 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   // this CTA's chunks: [c0, c1) of the nU * I/16 chunks, expert-major
   const int G = I / kChunk;
   const int n_ch = r.n_unique * G;
-  const int c0 = (int)((int64_t)n_ch * blockIdx.x / gridDim.x);
-  const int c1 = (int)((int64_t)n_ch * (blockIdx.x + 1) / gridDim.x);
+  // (32-bit: a 64-bit division is a long software routine; n_ch * grid < 2^32)
+  const int c0 = (int)((uint32_t)n_ch * blockIdx.x / gridDim.x);
+  const int c1 = (int)((uint32_t)n_ch * (blockIdx.x + 1) / gridDim.x);
   const int n_gu = kChunk / R;            // gate/up stages per chunk
   const int n_dn = (H + Dr - 1) / Dr;     // down stages per chunk
-  if (tid == 0) {
+  // Tokens each CTA's partial output covers (the CTAs' chunk ranges follow
+  // from the routing, which every CTA has): per touched expert, then per CTA.
+  for (int u = tid; u < r.n_unique; u += kThreads) {
+    const int4 ui = r.u[u];
     uint32_t m = 0;
-    if (c1 > c0) {
-      for (int u = c0 / G; u <= (c1 - 1) / G; ++u) {
-        const int4 ui = r.u[u];
-        for (int p = ui.y; p < ui.y + ui.z; ++p) m |= 1u << r.tok[p];
-      }
-    }
-    s_mask = m;
+    for (int p = ui.y; p < ui.y + ui.z; ++p) m |= 1u << r.tok[p];
+    s_emask[u] = m;
   }
   __syncthreads();
-  const uint32_t cta_mask = s_mask;
+  for (int c = tid; c < (int)gridDim.x; c += kThreads) {
+    const int b0 = (int)((uint32_t)n_ch * c / gridDim.x), b1 = (int)((uint32_t)n_ch * (c + 1) / gridDim.x);
+    uint32_t m = 0;
+    if (b1 > b0)
+      for (int u = b0 / G; u <= (b1 - 1) / G; ++u) m |= s_emask[u];
+    s_pm[c] = m;
+  }
+  __syncthreads();
+  const uint32_t cta_mask = s_pm[blockIdx.x];
 
   if (warp == kProducer) {
     // ------------------------------------------------------ producer
@@ -329,16 +336,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
           bytes = (uint32_t)nr * kChunk;
         }
       };
-      // the stages beyond the ring are asked of L2 ahead of their copies, so
-      // that HBM keeps streaming while the ring waits for its slots
-      int pf = a.stages;
+      // (no L2 prefetch ahead of the ring: measured, it only lengthens the
+      // queue the ring's own copies wait in)
       for (int x = 0; x < n_st && ok; ++x) {
-        for (; pf < n_st && pf < x + a.stages + kPrefetchAhead; ++pf) {
-          const uint8_t* src;
-          uint32_t bytes;
-          stage_src(pf, src, bytes);
-          prefetch_l2(src, bytes);
-        }
         if (j >= a.stages && !mbar_wait(&empty[st], ph ^ 1u)) {
           report_wait(a.meta, kSiteGuEmpty, j, x);
           ok = false;
@@ -504,7 +504,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       if (cta_mask)
         for (int o = tid; o < H; o += kCT) __stcg(part + o, acc_s[o]);
     }
-    if (tid == 0) a.pmask[blockIdx.x] = cta_mask;
     // ---- grid-wide: every partial is written before any CTA sums them. The
     // arrival is a release (ordering the CTA's partial stores, which the
     // consumer barrier ordered before it), the poll an acquire.
@@ -526,11 +525,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
     consumer_sync();
     // ---- this CTA's output rows [o0, o1): warp w sums the partials of CTAs
     // [w cpw, (w + 1) cpw), lane = row; then the 16 warp sums in order.
-    uint32_t* s_pm = reinterpret_cast<uint32_t*>(ring);
-    float* red = reinterpret_cast<float*>(ring + align128(gridDim.x * 4u));  // [kCW][T][rows]
-    for (int c = tid; c < (int)gridDim.x; c += kCT) s_pm[c] = __ldcg(a.pmask + c);
-    consumer_sync();
-    const int o0 = (int)((int64_t)H * blockIdx.x / gridDim.x), o1 = (int)((int64_t)H * (blockIdx.x + 1) / gridDim.x);
+    float* red = reinterpret_cast<float*>(ring);  // [kCW][T][rows]
+    const int o0 = (int)((uint32_t)H * blockIdx.x / gridDim.x), o1 = (int)((uint32_t)H * (blockIdx.x + 1) / gridDim.x);
     const int nrow = o1 - o0;
     const int cpw = ((int)gridDim.x + kCW - 1) / kCW;
     const int cb = warp * cpw, ce = ::min((int)gridDim.x, cb + cpw);
@@ -633,7 +629,6 @@ cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfl
   a.x = x;
   a.logits = h->logits;
   a.partial = h->partial;
-  a.pmask = h->pmask;
   a.out = out;
   a.ro = RoutingOut{ids_out, gates_out, h->ids,      h->gates,    h->counts, h->offsets,
                     h->perm, h->inv,    h->row_token, h->row_gate, h->uinfo,  h->meta};
@@ -665,7 +660,8 @@ cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfl
   if (a.stages < 2) return cudaErrorInvalidConfiguration;
   const int grid = h->num_sms;
   // the ring also holds the logits while routing and the sums at the end
-  const uint32_t need_end = align128(grid * 4u) + (uint32_t)(kCW * T * ((H + grid - 1) / grid) * 4);
+  if (grid > kMaxGrid) return cudaErrorInvalidConfiguration;
+  const uint32_t need_end = (uint32_t)(kCW * T * ((H + grid - 1) / grid) * 4);
   if ((uint32_t)a.stages * a.stage_bytes < std::max<uint32_t>(need_end, (uint32_t)(T * h->cfg.E * 4)))
     return cudaErrorInvalidConfiguration;
   if (h->test_grid_timeouts > 0) {  // test hook: this call's grid-wide wait cannot be met and gives up fast

@@ -23,6 +23,7 @@ constexpr int kMaxDecodeT = 16;    // decode path token limit (one lane per toke
 constexpr int kRouteTileM = 32;    // tokens per CTA in the tiled router
 constexpr int kTokTile = 192;      // prefill GEMM token tile (rows of one expert)
 constexpr int kSmallTile = 64;     // tiles of at most this many rows go to the small-tile GEMM
+constexpr int kRouterMaxSplit = 8; // prefill router: K splits at most (partial logits [splits][T_max][E])
 
 // Status bits written by kernels into the handle's device status word.
 constexpr int kStatusTimeout = 1;
@@ -35,6 +36,21 @@ __host__ __device__ inline int64_t scale_pitch_bytes(int64_t K) { return ((K / k
 // scales padded to 16 bytes, so that any run of consecutive rows -- codes and
 // scales -- is one contiguous, 16-byte aligned range.
 __host__ __device__ inline int64_t row_bytes(int64_t K) { return K + scale_pitch_bytes(K); }
+
+// The GEMMs' weight tiles: per (expert, block of 128 plane rows, K step of
+// 64) one contiguous tile -- the 128 rows' 64 codes (+ 128), each row's four
+// 16-byte chunks placed as a 64-byte-swizzled TMA copy would place them
+// (chunk c of row r at position c ^ ((r >> 1) & 3)), then the two Q8_0 scale
+// rows [2][128] binary16 -- so that a CTA's weights for one K step arrive in
+// one bulk copy per block.
+constexpr int kTileRows = 128;
+constexpr int kTileK = 64;
+constexpr int kTileCodeBytes = kTileRows * kTileK;               // 8192
+constexpr int kTileBytes = kTileCodeBytes + 2 * kTileRows * 2;   // 8704
+__host__ __device__ inline int64_t gemm_tile_offset(int64_t e, int64_t mb, int64_t kb, int64_t n_mb, int64_t KT) {
+  return ((e * n_mb + mb) * KT + kb) * (int64_t)kTileBytes;
+}
+__host__ __device__ inline int tile_code_offset(int r, int chunk) { return r * kTileK + ((chunk ^ ((r >> 1) & 3)) << 4); }
 
 // Row of gate/up matrix row i in the interleaved [2I] plane: groups of
 // kGUGroup gate rows followed by the up rows of the same i, so the units
@@ -69,10 +85,6 @@ struct PrefillMaps {
   CUtensorMap a_h;    // hbuf  [rows_max][I] bf16, box 64 x 96, 128B swizzle
   CUtensorMap a_xs;   // the same, box 64 x 64 (small-tile GEMM)
   CUtensorMap a_hs;
-  CUtensorMap q_gu;   // code plane [EU*2I][H] u8 (row stride row_bytes(H)), box 64 x 128, 64B swizzle
-  CUtensorMap s_gu;   // scale plane [EU*H/32][2I] u16, box 128 x 2
-  CUtensorMap q_d;    // [EU*H][I] u8 (row stride row_bytes(I))
-  CUtensorMap s_d;    // [EU*I/32][H] u16
   CUtensorMap w3;     // router planes [3E][H] bf16, box 64 x min(E, 128), 128B swizzle (E <= 256)
 };
 
@@ -85,13 +97,14 @@ struct Handle {
   int device;
   int num_sms;
   int last_T;         // T of the last fw_moe_route, -1 before any
+  int has_prefill;    // some T in [1, T_max] takes the prefill path (its tiles and buffers exist)
   // ---- repacked weights (device)
-  uint8_t* q_gu;      // [EU][2I] rows of row_bytes(H): codes + 128 (offset binary), then scales;
+  uint8_t* q_gu;      // decode: [EU][2I] rows of row_bytes(H): codes + 128 (offset binary), then scales;
                       // gate/up interleaved per kGUGroup rows
-  uint16_t* st_gu;    // [EU][H/32][2I] binary16 scales, transposed (prefill)
-  uint8_t* q_d;       // [EU][H] rows of row_bytes(I)
-  uint16_t* st_d;     // [EU][I/32][H]
-  uint8_t* q_dc;      // [EU][I/16][H][16] down codes by 16-column groups (decode)
+  uint8_t* q_dc;      // decode: [EU][I/16][H][16] down codes by 16-column groups
+  uint16_t* st_d;     // decode: [EU][I/32][H] down scales
+  uint8_t* t_gu;      // prefill: GEMM tiles of the interleaved gate/up rows, [EU][2I/128][H/64] tiles
+  uint8_t* t_d;       // prefill: GEMM tiles of the down rows, [EU][ceil(H/128)][I/64] tiles
   float* wr;          // [E][H]
   float* bias;        // [E] (zeros when none)
   __nv_bfloat16* wr3; // [3][E][H] bf16 planes summing exactly to wr (prefill router), or null
@@ -113,8 +126,8 @@ struct Handle {
   __nv_bfloat16* xperm; // [rows_max][H] x gathered into grouped order (prefill)
   void* hbuf;         // [rows_max][I] fp32 (decode) or bf16 (prefill)
   __nv_bfloat16* yp;  // [rows_max][H] bf16 (prefill)
+  float* zpart;       // [kRouterMaxSplit][T_max][E] prefill router: partial logits of a K split
   float* partial;     // [num_sms][min(T_max, 16)][H] decode: per-CTA partial outputs
-  uint32_t* pmask;    // [num_sms] decode: tokens each CTA's partial covers
   Meta* meta;
   int test_grid_timeouts;  // test hook (FWMOE_TEST_GRID_TIMEOUTS at init): decode calls whose grid wait must time out
   // ---- device staging for fw_moe_forward_host

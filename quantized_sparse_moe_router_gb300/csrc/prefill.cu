@@ -35,7 +35,7 @@
 
 #include <algorithm>
 
-#include "internal.cuh"
+#include "routing.cuh"
 
 namespace fw {
 namespace {
@@ -47,7 +47,6 @@ constexpr int kAStages = 4;                 // tensor-memory A stages (dequant -
 constexpr int kEpiWarps = 4, kProducerWarp = 4, kMmaWarp = 5, kDeqWarp0 = 6, kDeqWarps = 8;
 constexpr int kMmaWarp2 = kDeqWarp0 + kDeqWarps;        // the second MMA issuer (two-block shape)
 constexpr int kThreads = (kMmaWarp2 + 1) * 32;          // 480
-constexpr int kClusterSize = 2;             // CTA pairs share (multicast) each token tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSmemLimit = 227 * 1024; // dynamic shared memory a CTA may have
 
@@ -63,9 +62,8 @@ struct Shape {
   static constexpr int BN = MB_ == 1 ? kTokTile : kSmallTile;    // tokens per tile (MMA N <= BN)
   static constexpr int XBox = MB_ == 1 ? BN / 2 : BN;            // token rows per TMA box
   static constexpr uint32_t XBytes = BN * BK * 2;                // bf16 token tile slot
-  static constexpr uint32_t QBytes = MB * BM * BK;               // int8 codes
-  static constexpr uint32_t SBytes = MB * BM * 2 * 2;            // 2 scale blocks x 128 rows per block
-  static constexpr uint32_t StageBytes = XBytes + QBytes + SBytes;
+  static constexpr uint32_t WBytes = MB * kTileBytes;            // MB weight tiles: codes, then scales
+  static constexpr uint32_t StageBytes = XBytes + WBytes;
   static constexpr int Stages = (int)((kSmemLimit - 2048) / StageBytes) & ~1;
   static constexpr uint32_t SmemBytes = Stages * StageBytes + 1024;
   static constexpr uint32_t AccCols = MB * BN;                   // one accumulator buffer (MB blocks)
@@ -73,6 +71,7 @@ struct Shape {
   static constexpr uint32_t ACols = MB * BK / 2;                 // one A stage: 64 bf16 per row per block
   static_assert(ACol0 + kAStages * ACols <= kTmemCols, "tensor memory budget");
   static_assert(BN % XBox == 0 && BN % 16 == 0 && BN <= 256 && XBox % 8 == 0, "token tile");
+  static_assert(BM == kTileRows && BK == kTileK, "a stage holds whole weight tiles");
   static_assert(Stages >= 4 && Stages % 2 == 0 && kAStages % 2 == 0,
                 "the two dequantising groups own alternate stages");
 };
@@ -80,6 +79,7 @@ struct Shape {
 enum Epi { kEpiSwiGLU = 0, kEpiDownScale = 1 };
 
 struct GemmArgs {
+  const uint8_t* wt;      // the projection's weight tiles [EU][n_mb][K/64]
   const int4* minfo;      // per token tile: (expert, first grouped row, valid rows, 0)
   const int32_t* n_mtiles; // number of tiles in minfo (written by the scan kernel)
   const Meta* meta;
@@ -87,7 +87,7 @@ struct GemmArgs {
   __nv_bfloat16* outp;    // hbuf (SwiGLU, [rows][I]) or yp ([rows][H])
   int K;                  // reduction length (H or I)
   int prows;              // weight rows per expert in the code plane (2I or H)
-  int n_mb;               // ceil(prows / 128)
+  int n_mb;               // ceil(prows / 128): weight tiles per expert and K step
   int out_cols;           // I (SwiGLU) or H
 };
 
@@ -136,37 +136,6 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t adesc, uint64_t
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
-}
-
-// The same box delivered to this CTA and its cluster peer (same shared-memory
-// offsets), completion counted on each CTA's barrier at bar's offset.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
-                                               uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, "
-      "{%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "h"(cta_mask)
-      : "memory");
-}
-
-// Arrive on the barrier at bar's offset in every CTA of cta_mask once this
-// thread's earlier MMAs have completed.
-__device__ __forceinline__ void mma_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-          smem_u32(bar)),
-      "h"(cta_mask)
-      : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-
-__device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
@@ -235,8 +204,7 @@ __device__ __forceinline__ uint32_t deq_pair_bf16(uint32_t bits_lo, uint32_t bit
 // ------------------------------------------------------------- the GEMM
 template <int EPI, int MB>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_b, const __grid_constant__ CUtensorMap map_q,
-                        const __grid_constant__ CUtensorMap map_s, GemmArgs a) {
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_b, GemmArgs a) {
   using G = Shape<MB>;
   constexpr int kStages = G::Stages;
   constexpr int kIssuers = MB;  // MMA-issuing threads: one per weight block
@@ -250,13 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* base = smem_raw + pad;
   uint8_t* sX = base;                            // [kStages][BN rows][128 B], 128B swizzle
-  uint8_t* sQ = sX + kStages * G::XBytes;        // [kStages][MB][128 rows][64 B], 64B swizzle
-  uint8_t* sS = sQ + kStages * G::QBytes;        // [kStages][MB][2][128] binary16
+  uint8_t* sW = sX + kStages * G::XBytes;        // [kStages][MB] weight tiles: [128 rows][64 B] swizzled, [2][128] scales
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kClusterSize * kIssuers);  // both CTAs' MMAs read the multicast token tile
+      mbar_init(&empty[i], kIssuers);
     }
     for (int i = 0; i < kAStages; ++i) {
       mbar_init(&a_full[i], kDeqWarps / 2);  // one group of four warps per stage
@@ -278,20 +245,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // the peer's barriers are initialised before any multicast reaches them
   tc_fence_after();
   const uint32_t tmem_base = s_tmem;
-  const uint32_t crank = cluster_ctarank();
-  const uint16_t kPair = (1u << kClusterSize) - 1u;
 
-  // tiles per cluster: (token tile, pair of MB-block groups), CTA rank r takes
-  // group 2 p + r (a block past the matrix runs but stores nothing)
+  // tiles: (token tile, group of MB weight blocks), token-tile-major, so the
+  // CTAs working on one token tile at the same time read it from L2 (a block
+  // past the matrix is neither loaded nor stored)
   const int n_mbg = (a.n_mb + MB - 1) / MB;
-  const int n_mb2 = (n_mbg + kClusterSize - 1) / kClusterSize;
-  const int n_tiles = *a.n_mtiles * n_mb2;
-  const int cid = blockIdx.x / kClusterSize, ncl = gridDim.x / kClusterSize;
+  const int n_tiles = *a.n_mtiles * n_mbg;
+  const int cid = blockIdx.x, ncl = gridDim.x;
   const int KT = a.K / BK;
-  const int nb = a.K / 32;  // scale blocks per weight row
   bool ok = true;
 
   auto wait = [&](uint64_t* bar, uint32_t parity) -> bool {
@@ -304,25 +267,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       uint32_t it = 0;
-      int4 mi_next = cid < n_tiles ? a.minfo[cid / n_mb2] : make_int4(0, 0, 0, 0);
+      int4 mi_next = cid < n_tiles ? a.minfo[cid / n_mbg] : make_int4(0, 0, 0, 0);
       for (int tile = cid; tile < n_tiles && ok; tile += ncl) {
         const int4 mi = mi_next;
-        const int m0 = ((tile % n_mb2) * kClusterSize + (int)crank) * MB * BM;
+        const int mb0 = (tile % n_mbg) * MB;  // this CTA's first weight block
+        const int nw = ::max(0, ::min(MB, a.n_mb - mb0));  // blocks within the matrix (the rest: no copy, no store)
         const int nx = (mi.z + G::XBox - 1) / G::XBox;
-        if (tile + ncl < n_tiles) mi_next = a.minfo[(tile + ncl) / n_mb2];  // in flight during this tile
+        if (tile + ncl < n_tiles) mi_next = a.minfo[(tile + ncl) / n_mbg];  // in flight during this tile
+        const uint8_t* wsrc = a.wt + gemm_tile_offset(mi.x, mb0, 0, a.n_mb, KT);
         for (int kb = 0; kb < KT && ok; ++kb, ++it) {
           const int s = it % kStages;
           const uint32_t ph = (it / kStages) & 1;
           if (!(ok = wait(&empty[s], ph ^ 1))) break;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)nx * G::XBox * BK * 2 + G::QBytes + G::SBytes);
-          for (int x = (int)crank; x < nx; x += kClusterSize)  // the boxes shared out, each to both CTAs
-            tma_load_2d_mc(sX + s * G::XBytes + x * G::XBox * 128, &map_b, kb * BK, mi.y + x * G::XBox, &full[s],
-                           kPair);
-#pragma unroll
-          for (int b = 0; b < MB; ++b) {
-            tma_load_2d(sQ + s * G::QBytes + b * BM * BK, &map_q, kb * BK, mi.x * a.prows + m0 + b * BM, &full[s]);
-            tma_load_2d(sS + s * G::SBytes + b * BM * 4, &map_s, m0 + b * BM, mi.x * nb + kb * 2, &full[s]);
-          }
+          mbar_arrive_expect_tx(&full[s], (uint32_t)nx * G::XBox * BK * 2 + (uint32_t)nw * kTileBytes);
+          for (int x = 0; x < nx; ++x)
+            tma_load_2d(sX + s * G::XBytes + x * G::XBox * 128, &map_b, kb * BK, mi.y + x * G::XBox, &full[s]);
+          for (int b = 0; b < nw; ++b)  // tile (expert, mb0 + b, kb): one contiguous copy
+            bulk_g2s(sW + s * G::WBytes + b * kTileBytes, wsrc + ((int64_t)b * KT + kb) * kTileBytes, kTileBytes,
+                     &full[s]);
         }
       }
       // copies still in flight after an abort land before the CTA leaves
@@ -338,10 +300,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && (warp == kMmaWarp || kIssuers == 2)) {
       const int q = warp == kMmaWarp ? 0 : 1;
       uint32_t it = 0, tc = 0;
-      int4 mi_next = cid < n_tiles ? a.minfo[cid / n_mb2] : make_int4(0, 0, 0, 0);
+      int4 mi_next = cid < n_tiles ? a.minfo[cid / n_mbg] : make_int4(0, 0, 0, 0);
       for (int tile = cid; tile < n_tiles && ok; tile += ncl, ++tc) {
         const int4 mi = mi_next;
-        if (tile + ncl < n_tiles) mi_next = a.minfo[(tile + ncl) / n_mb2];
+        if (tile + ncl < n_tiles) mi_next = a.minfo[(tile + ncl) / n_mbg];
         const int n_mma = (mi.z + 15) / 16 * 16;
         const uint32_t idesc = idesc_bf16(BM, n_mma);
         const int b = tc & 1;
@@ -358,7 +320,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k)  // block q
             mma_tmem_a(d_tmem + q * G::BN, a0 + q * (BK / 2) + k * 8, sw128_desc(b0 + k * 32), idesc, (kb | k) != 0);
-          mma_commit_mc(&empty[s], kPair);
+          mma_commit(&empty[s]);
           mma_commit(&a_empty[sa]);
         }
         if (ok) mma_commit(&acc_full[b]);
@@ -387,11 +349,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait(&a_empty[sa], ((it / kAStages) & 1) ^ 1))) break;
 #pragma unroll 1
         for (int mb = 0; mb < MB; ++mb) {  // row r of each of the CTA's weight blocks
-          const uint8_t* qrow = sQ + s * G::QBytes + mb * BM * BK + r * 64;
+          const uint8_t* wtile = sW + s * G::WBytes + mb * kTileBytes;
+          const uint8_t* qrow = wtile + r * 64;
           uint4 c[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) c[q] = *reinterpret_cast<const uint4*>(qrow + ((q ^ sw) << 4));
-          const uint16_t* sc = reinterpret_cast<const uint16_t*>(sS + s * G::SBytes + mb * BM * 4);
+          const uint16_t* sc = reinterpret_cast<const uint16_t*>(wtile + kTileCodeBytes);
           const float d0 = half_bits_to_f32(sc[r]), d1 = half_bits_to_f32(sc[BM + r]);
           uint32_t out[32];
 #pragma unroll
@@ -418,11 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ------------------------------------------------ epilogue: TMEM -> registers -> global
     uint32_t tc = 0;
-    int4 mi_next = cid < n_tiles ? a.minfo[cid / n_mb2] : make_int4(0, 0, 0, 0);
+    int4 mi_next = cid < n_tiles ? a.minfo[cid / n_mbg] : make_int4(0, 0, 0, 0);
     for (int tile = cid; tile < n_tiles && ok; tile += ncl, ++tc) {
       const int4 mi = mi_next;
-      if (tile + ncl < n_tiles) mi_next = a.minfo[(tile + ncl) / n_mb2];
-      const int m0 = ((tile % n_mb2) * kClusterSize + (int)crank) * MB * BM;
+      if (tile + ncl < n_tiles) mi_next = a.minfo[(tile + ncl) / n_mbg];
+      const int m0 = (tile % n_mbg) * MB * BM;
       const int b = tc & 1;
       if (!(ok = wait(&acc_full[b], (tc >> 1) & 1))) break;
       tc_fence_after();
@@ -473,7 +436,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync_all();  // no multicast copy or commit of the peer still targets this CTA
   tc_fence_after();
   if (warp == kMmaWarp)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(kTmemCols)
@@ -495,6 +457,7 @@ constexpr int kRPassE = 128;    // experts per pass over x (E > 128: two passes,
 
 struct RouteMmaArgs {
   const float* bias;
+  float* zpart;   // K split over gridDim.y > 1: partial logits [gridDim.y][T][E] (no bias); else null
   int T, H, E, k;
   int32_t* ids;
   float* gates;
@@ -562,7 +525,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const int KT = a.H / kRK;
+  // this CTA's K steps: [kbeg, kbeg + KT) of the H / 64 (the K split is blockIdx.y)
+  const int KT_all = a.H / kRK;
+  const int kbeg = KT_all * blockIdx.y / gridDim.y;
+  const int KT = KT_all * (blockIdx.y + 1) / gridDim.y - kbeg;
   const int NI = n_pass * KT;  // pipeline iterations: (pass, K step)
   // each CTA starts its K loop at its own offset, so the CTAs do not all ask
   // the same L2 lines for the same W_r tile at the same time
@@ -573,7 +539,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     if (lane == 0) {
       for (int i = 0; i < NI && ok; ++i) {
         const int s = i % kRStages, ps = i / KT, kb = i % KT;
-        const int kk = kb + kb0 < KT ? kb + kb0 : kb + kb0 - KT;
+        const int kk = kbeg + (kb + kb0 < KT ? kb + kb0 : kb + kb0 - KT);
         if (!(ok = mbar_wait(&empty[s], ((i / kRStages) & 1) ^ 1))) {
           report_wait(a.meta, kSiteGemm, i, 0);
           break;
@@ -613,6 +579,17 @@ __global__ void __launch_bounds__(kRThreads, 1)
     const int q = warp & 3, row = q * 32 + lane, t = t0 + row;
     if (!mbar_wait(&acc_full, 0)) report_wait(a.meta, kSiteGemm, 0, 2);
     tc_fence_after();
+    if (a.zpart) {  // a K split: this CTA's partial logits, summed (in split order) by the select kernel
+      float* zp = a.zpart + ((size_t)blockIdx.y * a.T + t) * E;
+      for (int c0 = 0; c0 < E; c0 += 32) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + c0, v);
+        if (t < a.T) {
+          const int n = c0 + 32 <= E ? 32 : 16;  // E is a multiple of 16
+          for (int j = 0; j < n; j += 4) *reinterpret_cast<float4*>(zp + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+        }
+      }
+    } else {
     float tv[KS];
     int ti[KS];
 #pragma unroll
@@ -649,15 +626,56 @@ __global__ void __launch_bounds__(kRThreads, 1)
           atomicAdd(&s_cnt[q][ti[j]], 1);
         }
     }
+    }
   }
   tc_fence_before();
   __syncthreads();
-  for (int i = threadIdx.x; i < 4 * E; i += kRThreads) {
-    const int q = i / E, e = i % E, tile = blockIdx.x * 4 + q;
-    if (tile * 32 < a.T) a.hist[(int64_t)tile * E + e] = s_cnt[q][e];
-  }
+  if (!a.zpart)
+    for (int i = threadIdx.x; i < 4 * E; i += kRThreads) {
+      const int q = i / E, e = i % E, tile = blockIdx.x * 4 + q;
+      if (tile * 32 < a.T) a.hist[(int64_t)tile * E + e] = s_cnt[q][e];
+    }
   if (warp == 1)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kRMaxE) : "memory");
+}
+
+// After a K-split router: per token (a warp) the logits summed over the
+// splits in order, plus the bias; the top-k (ties to the lower id), the gates,
+// and the CTA's per-expert counts of its 32 tokens for the scan kernel.
+constexpr int kSelTokens = 32;
+__global__ void __launch_bounds__(kSelTokens * 32) route_select_kernel(RouteMmaArgs a, int ks) {
+  __shared__ int s_cnt[kRMaxE];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, E = a.E, k = a.k;
+  const int t = blockIdx.x * kSelTokens + warp;
+  for (int i = threadIdx.x; i < E; i += kSelTokens * 32) s_cnt[i] = 0;
+  __syncthreads();
+  if (t < a.T) {
+    float zl[kMaxEPerLane];
+#pragma unroll
+    for (int m = 0; m < kMaxEPerLane; ++m) {
+      const int e = lane + 32 * m;
+      float z = -INFINITY;
+      if (e < E) {
+        z = 0.f;
+        for (int q = 0; q < ks; ++q) z += __ldg(a.zpart + ((size_t)q * a.T + t) * E + e);
+        z += a.bias[e];
+      }
+      zl[m] = z;
+    }
+    int id;
+    float zv;
+    warp_topk(zl, E, k, lane, &id, &zv);
+    const float g = warp_gate(zv, k, lane);
+    if (lane < k) {
+      a.ids[t * k + lane] = id;
+      a.gates[t * k + lane] = g;
+      a.ids_out[t * k + lane] = id;
+      if (a.gates_out) a.gates_out[t * k + lane] = g;
+      atomicAdd(&s_cnt[id], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kSelTokens * 32) a.hist[(int64_t)blockIdx.x * E + e] = s_cnt[e];
 }
 
 // W_r (fp32) -> three bf16 planes hi, mid, lo with hi + mid + lo == W_r exactly.
@@ -750,42 +768,11 @@ unsigned grid_for(int64_t n, int threads, int cap) {
 
 
 
-int g_max_clusters[3] = {0, 0, 0};  // CTA pairs of the GEMM resident at once, by MB
-
-template <int MB>
-cudaLaunchConfig_t gemm_config(unsigned grid, cudaStream_t s, cudaLaunchAttribute* attr) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = Shape<MB>::SmemBytes;
-  cfg.stream = s;
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = kClusterSize;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cfg;
-}
-
 template <int EPI, int MB>
-cudaError_t launch_gemm(const CUtensorMap& mb, const CUtensorMap& mq, const CUtensorMap& ms, const GemmArgs& g,
-                        int num_sms, cudaStream_t s) {
-  const unsigned grid = (unsigned)std::min(num_sms / kClusterSize, g_max_clusters[MB]) * kClusterSize;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = gemm_config<MB>(grid, s, attr);
-  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<EPI, MB>, mb, mq, ms, g);
-}
-
-template <int MB>
-cudaError_t max_clusters() {
-  if (g_max_clusters[MB]) return cudaSuccess;
-  cudaLaunchAttribute attr[1];
-  cudaLaunchConfig_t cfg = gemm_config<MB>(kClusterSize, 0, attr);
-  int n = 0;
-  cudaError_t e = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<kEpiSwiGLU, MB>, &cfg);
-  if (e == cudaSuccess) g_max_clusters[MB] = n > 0 ? n : 1;
-  return e;
+cudaError_t launch_gemm(const CUtensorMap& mb, const GemmArgs& g, int num_sms, cudaStream_t s) {
+  // one persistent CTA per SM (its shared memory admits no second)
+  grouped_gemm_kernel<EPI, MB><<<(unsigned)num_sms, kThreads, Shape<MB>::SmemBytes, s>>>(mb, g);
+  return cudaGetLastError();
 }
 
 }  // namespace
@@ -804,8 +791,6 @@ cudaError_t configure_prefill_kernels() {
   if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDownScale, 2>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_mma_kernel<8>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_mma_kernel<16>);
-  if (e == cudaSuccess) e = max_clusters<1>();
-  if (e == cudaSuccess) e = max_clusters<2>();
   return e;
 }
 
@@ -824,18 +809,6 @@ cudaError_t prepare_prefill(Handle* h) {
   if (e == cudaSuccess)
     e = encode_2d(&m->a_hs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->hbuf, I, R, I * 2, BK, Shape<2>::XBox,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
-  if (e == cudaSuccess)
-    e = encode_2d(&m->q_gu, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->q_gu, H, EU * 2 * I, row_bytes(H), BK, BM,
-                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-  if (e == cudaSuccess)
-    e = encode_2d(&m->s_gu, CU_TENSOR_MAP_DATA_TYPE_UINT16, h->st_gu, 2 * I, EU * (H / 32), 2 * I * 2, BM, 2,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-  if (e == cudaSuccess)
-    e = encode_2d(&m->q_d, CU_TENSOR_MAP_DATA_TYPE_UINT8, h->q_d, I, EU * H, row_bytes(I), BK, BM,
-                  CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
-  if (e == cudaSuccess)
-    e = encode_2d(&m->s_d, CU_TENSOR_MAP_DATA_TYPE_UINT16, h->st_d, H, EU * (I / 32), H * 2, BM, 2,
-                  CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
   if (e == cudaSuccess && h->wr3)
     e = encode_2d(&m->w3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->wr3, H, 3 * (uint64_t)h->cfg.E, H * 2, kRK,
                   (uint32_t)std::min(h->cfg.E, kRPassE), CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B);
@@ -872,11 +845,18 @@ cudaError_t launch_route_prefill_mma(Handle* h, const __nv_bfloat16* x, int T, i
   a.hist = h->hist;
   a.meta = h->meta;
   const size_t smem = (size_t)kRStages * (kRM * kRK * 2 + 3 * std::min(E, kRPassE) * kRK * 2) + 1024;
-  const unsigned grid = (unsigned)((T + kRM - 1) / kRM);
+  const int tiles = (T + kRM - 1) / kRM;
+  // split K when the token tiles alone leave most SMs idle (a partial-logit
+  // pass, then a select kernel); the splits are summed in a fixed order
+  int ks = std::min(std::min(h->num_sms / tiles, kRouterMaxSplit), H / kRK);
+  if (ks < 2) ks = 1;
+  a.zpart = ks > 1 ? h->zpart : nullptr;
+  const dim3 grid((unsigned)tiles, (unsigned)ks);
   if (a.k <= 8)
     route_mma_kernel<8><<<grid, kRThreads, smem, s>>>(map_x, h->maps->w3, a);
   else
     route_mma_kernel<16><<<grid, kRThreads, smem, s>>>(map_x, h->maps->w3, a);
+  if (ks > 1) route_select_kernel<<<(unsigned)((T + kSelTokens - 1) / kSelTokens), kSelTokens * 32, 0, s>>>(a, ks);
   return cudaGetLastError();
 }
 
@@ -892,6 +872,7 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
   }
   // each projection: the tiles of more than kSmallTile rows, then the small ones
   GemmArgs g, gs;
+  g.wt = h->t_gu;
   g.minfo = h->minfo;
   g.n_mtiles = &h->meta->n_mtiles;
   g.meta = h->meta;
@@ -907,14 +888,15 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
     gs.n_mtiles = &h->meta->n_stiles;
     {
       KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP, s);
-      err = launch_gemm<kEpiSwiGLU, 1>(h->maps->a_x, h->maps->q_gu, h->maps->s_gu, g, h->num_sms, s);
+      err = launch_gemm<kEpiSwiGLU, 1>(h->maps->a_x, g, h->num_sms, s);
     }
     KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP_SMALL, s);
     if (err == cudaSuccess)
-      err = launch_gemm<kEpiSwiGLU, 2>(h->maps->a_xs, h->maps->q_gu, h->maps->s_gu, gs, h->num_sms, s);
+      err = launch_gemm<kEpiSwiGLU, 2>(h->maps->a_xs, gs, h->num_sms, s);
   }
   {
     g.outp = h->yp;
+    g.wt = h->t_d;
     g.K = I;
     g.prows = H;
     g.n_mb = (H + BM - 1) / BM;
@@ -925,11 +907,11 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
     {
       KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN, s);
       if (err == cudaSuccess)
-        err = launch_gemm<kEpiDownScale, 1>(h->maps->a_h, h->maps->q_d, h->maps->s_d, g, h->num_sms, s);
+        err = launch_gemm<kEpiDownScale, 1>(h->maps->a_h, g, h->num_sms, s);
     }
     KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN_SMALL, s);
     if (err == cudaSuccess)
-      err = launch_gemm<kEpiDownScale, 2>(h->maps->a_hs, h->maps->q_d, h->maps->s_d, gs, h->num_sms, s);
+      err = launch_gemm<kEpiDownScale, 2>(h->maps->a_hs, gs, h->num_sms, s);
   }
   if (err != cudaSuccess) return err;
   {

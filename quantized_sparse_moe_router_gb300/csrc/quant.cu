@@ -44,12 +44,14 @@ __global__ void quantize_q8_0_kernel(const float* __restrict__ w, int64_t nblock
   }
 }
 
+// Where one matrix kind of an expert lives after the repack.
 struct PlaneView {
-  uint8_t* q;      // code plane of this matrix kind, expert 0 (rows: codes, then scales)
-  uint16_t* st;    // transposed scale plane
-  uint8_t* qc;     // down only: the codes by 16-column groups (or null)
+  uint8_t* q;      // gate/up: decode rows [EU][2I] of row_bytes(H) (codes, then scales), interleaved; else null
+  uint8_t* qc;     // down: decode codes by 16-column groups [EU][I/16][H][16]; else null
+  uint16_t* st;    // down: decode scales [EU][I/32][H]; else null
+  uint8_t* tiles;  // GEMM tiles of this projection (gate/up share one plane), or null without a prefill path
   int64_t rows;    // rows of one expert's matrix (I for gate/up, H for down)
-  int64_t prows;   // rows of one expert in the plane (2I for gate/up, H for down)
+  int64_t prows;   // rows of one expert in the GEMM plane (2I for gate/up, H for down)
   int64_t K;       // row length (H for gate/up, I for down)
   int which;       // 0 gate, 1 up, 2 down
 };
@@ -58,9 +60,10 @@ __device__ __forceinline__ int64_t plane_row(const PlaneView& p, int64_t r) {
   return p.which == 0 ? gu_row_gate(r) : (p.which == 1 ? gu_row_up(r) : r);
 }
 
-// One thread per block of one expert range: GGUF block -> code plane + both scale planes.
-// The code planes hold q + 128 (offset binary: q XOR 0x80), which the kernels
-// turn into floats with one byte permute and one subtraction.
+// One thread per GGUF block of one expert range: the block's codes (stored as
+// q + 128, offset binary: q XOR 0x80, which the kernels turn into floats with
+// one byte permute and one subtraction) and scale go to the decode plane of
+// the kind and to the GEMM tile that holds its row and K step.
 __global__ void repack_kernel(PlaneView p, int expert0, int64_t nblocks, const uint8_t* __restrict__ src) {
   int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (blk >= nblocks) return;
@@ -73,39 +76,56 @@ __global__ void repack_kernel(PlaneView p, int expert0, int64_t nblocks, const u
   uint32_t words[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) words[i] = ((uint32_t)in[1 + 2 * i] | ((uint32_t)in[2 + 2 * i] << 16)) ^ 0x80808080u;
-  const int64_t prow = e * p.prows + plane_row(p, r);
-  uint8_t* row = p.q + prow * row_bytes(p.K);
-  uint4* qd = reinterpret_cast<uint4*>(row + b * kQBlock);
-  qd[0] = make_uint4(words[0], words[1], words[2], words[3]);
-  qd[1] = make_uint4(words[4], words[5], words[6], words[7]);
-  reinterpret_cast<uint16_t*>(row + p.K)[b] = in[0];
-  p.st[(e * nb + b) * p.prows + plane_row(p, r)] = in[0];
-  if (p.qc) {  // down codes again, by 16-column groups: [e][K/16][rows][16]
-    uint4* c0 = reinterpret_cast<uint4*>(p.qc + ((e * (p.K / 16) + 2 * b) * p.rows + r) * 16);
-    uint4* c1 = reinterpret_cast<uint4*>(p.qc + ((e * (p.K / 16) + 2 * b + 1) * p.rows + r) * 16);
-    *c0 = make_uint4(words[0], words[1], words[2], words[3]);
-    *c1 = make_uint4(words[4], words[5], words[6], words[7]);
+  const uint4 lo = make_uint4(words[0], words[1], words[2], words[3]);
+  const uint4 hi = make_uint4(words[4], words[5], words[6], words[7]);
+  const int64_t pr = plane_row(p, r);
+  if (p.q) {  // decode gate/up row: codes, then its scales
+    uint8_t* row = p.q + (e * p.prows + pr) * row_bytes(p.K);
+    reinterpret_cast<uint4*>(row + b * kQBlock)[0] = lo;
+    reinterpret_cast<uint4*>(row + b * kQBlock)[1] = hi;
+    reinterpret_cast<uint16_t*>(row + p.K)[b] = in[0];
   }
+  if (p.qc) {  // decode down: the two 16-column groups of the block, and the scale
+    *reinterpret_cast<uint4*>(p.qc + ((e * (p.K / 16) + 2 * b) * p.rows + r) * 16) = lo;
+    *reinterpret_cast<uint4*>(p.qc + ((e * (p.K / 16) + 2 * b + 1) * p.rows + r) * 16) = hi;
+    p.st[(e * nb + b) * p.rows + r] = in[0];
+  }
+  if (!p.tiles) return;  // no prefill path on this handle
+  // GEMM tile (e, row block, K step b / 2): row pr % 128, 16-byte chunks 2 (b & 1) and 2 (b & 1) + 1
+  const int64_t n_mb = (p.prows + kTileRows - 1) / kTileRows, KT = p.K / kTileK;
+  const int rr = (int)(pr % kTileRows), half = (int)(b & 1);
+  uint8_t* t = p.tiles + gemm_tile_offset(e, pr / kTileRows, b / 2, n_mb, KT);
+  *reinterpret_cast<uint4*>(t + tile_code_offset(rr, 2 * half)) = lo;
+  *reinterpret_cast<uint4*>(t + tile_code_offset(rr, 2 * half + 1)) = hi;
+  reinterpret_cast<uint16_t*>(t + kTileCodeBytes)[half * kTileRows + rr] = in[0];
 }
 
+// GGUF blocks of one matrix of one expert, back from the decode planes.
 __global__ void export_kernel(PlaneView p, int expert, int64_t nblocks, uint8_t* __restrict__ dst) {
   int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (blk >= nblocks) return;
   const int64_t nb = p.K / kQBlock;
-  const int64_t r = blk / nb, b = blk % nb;
-  const int64_t prow = (int64_t)expert * p.prows + plane_row(p, r);
-  const uint8_t* row = p.q + prow * row_bytes(p.K);
-  const uint4* qs = reinterpret_cast<const uint4*>(row + b * kQBlock);
-  uint4 a = qs[0], c = qs[1];
-  uint32_t words[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
-#pragma unroll
-  for (int i = 0; i < 8; ++i) words[i] ^= 0x80808080u;  // back from offset binary
+  const int64_t r = blk / nb, b = blk % nb, e = expert;
+  uint4 lo, hi;
+  uint16_t d;
+  if (p.q) {
+    const uint8_t* row = p.q + (e * p.prows + plane_row(p, r)) * row_bytes(p.K);
+    lo = reinterpret_cast<const uint4*>(row + b * kQBlock)[0];
+    hi = reinterpret_cast<const uint4*>(row + b * kQBlock)[1];
+    d = reinterpret_cast<const uint16_t*>(row + p.K)[b];
+  } else {
+    lo = *reinterpret_cast<const uint4*>(p.qc + ((e * (p.K / 16) + 2 * b) * p.rows + r) * 16);
+    hi = *reinterpret_cast<const uint4*>(p.qc + ((e * (p.K / 16) + 2 * b + 1) * p.rows + r) * 16);
+    d = p.st[(e * nb + b) * p.rows + r];
+  }
+  uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
   uint16_t* out = reinterpret_cast<uint16_t*>(dst + blk * kQBlockBytes);
-  out[0] = reinterpret_cast<const uint16_t*>(row + p.K)[b];
+  out[0] = d;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    out[1 + 2 * i] = (uint16_t)(words[i] & 0xFFFF);
-    out[2 + 2 * i] = (uint16_t)(words[i] >> 16);
+    const uint32_t w = words[i] ^ 0x80808080u;  // back from offset binary
+    out[1 + 2 * i] = (uint16_t)(w & 0xFFFF);
+    out[2 + 2 * i] = (uint16_t)(w >> 16);
   }
 }
 
@@ -113,17 +133,19 @@ PlaneView view_of(const Handle* h, int which) {
   PlaneView p;
   const int64_t H = h->cfg.H, I = h->cfg.I;
   p.which = which;
-  p.qc = nullptr;
   if (which == 2) {
-    p.q = h->q_d;
-    p.st = h->st_d;
+    p.q = nullptr;
     p.qc = h->q_dc;
+    p.st = h->st_d;
+    p.tiles = h->has_prefill ? h->t_d : nullptr;
     p.rows = H;
     p.prows = H;
     p.K = I;
   } else {
     p.q = h->q_gu;
-    p.st = h->st_gu;
+    p.qc = nullptr;
+    p.st = nullptr;
+    p.tiles = h->has_prefill ? h->t_gu : nullptr;
     p.rows = I;
     p.prows = 2 * I;
     p.K = H;

@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
   if (!s_last) return;
   __threadfence();
   __shared__ SmemRouting r;
-  __shared__ float zbuf[kMaxDecodeT * kMaxE];
+  __shared__ __align__(16) float zbuf[kMaxDecodeT * kMaxE];
   route_in_smem<kRouteThreads>(a.logits, T, a.E, a.k, a.S, r, zbuf);
   RoutingOut o{a.ids_out, a.gates_out, a.ids,      a.gates,    a.counts, a.offsets,
                a.perm,    a.inv,       a.row_token, a.row_gate, a.uinfo,  a.meta};

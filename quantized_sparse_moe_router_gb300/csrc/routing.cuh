@@ -62,6 +62,25 @@ __device__ __forceinline__ float warp_gate(float my_z, int k, int lane) {
   return ex / sum;
 }
 
+// How many of a row's logits come before logit e (larger, or equal with a
+// lower id), over the float4 words c, c + s, c + 2s, ... of the row (one of s
+// lanes sharing expert e): the lanes with the same c read the same word, the
+// s different c consecutive words, so the loads are free of bank conflicts.
+__device__ __forceinline__ int rank_in_row(const float4* z4, int n4, int c, int s, int e) {
+  const float z = reinterpret_cast<const float*>(z4)[e];
+  int rank = 0;
+#pragma unroll 4
+  for (int i = c; i < n4; i += s) {
+    const float4 v = z4[i];
+    const int f = 4 * i;
+    rank += (v.x > z) | ((v.x == z) & (f < e));
+    rank += (v.y > z) | ((v.y == z) & (f + 1 < e));
+    rank += (v.z > z) | ((v.z == z) & (f + 2 < e));
+    rank += (v.w > z) | ((v.w == z) & (f + 3 < e));
+  }
+  return rank;
+}
+
 // The routing of a decode batch in shared memory. The batch's logits are
 // staged in a separate buffer the caller provides (T * E floats), which is
 // free again once the routing is made.
@@ -96,9 +115,13 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int EU = E + S;
   const int P = T * E;
+  const int E4 = (E + 3) & ~3;  // staged rows padded to whole float4 with -inf (never ranked ahead)
   const bool by_rank = 4 * P <= NT;
   if (by_rank)
-    for (int i = tid; i < P; i += NT) zbuf[i] = __ldcg(logits + i);
+    for (int i = tid; i < T * E4; i += NT) {
+      const int t = i / E4, e = i - t * E4;
+      zbuf[i] = e < E ? __ldcg(logits + t * E + e) : -INFINITY;
+    }
   for (int i = tid; i < EU; i += NT) {
     r.cnt[i] = 0;
     r.mask[i] = 0;
@@ -106,9 +129,8 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
   __syncthreads();
 
   if (by_rank) {
-    // s lanes per pair (a power of two, as many as the block allows); lane c
-    // of a group compares f = c, c + s, ... (same-c lanes read the same word,
-    // distinct c consecutive words: no bank conflicts)
+    // s lanes per pair (a power of two, as many as the block allows), lane c
+    // of a group taking the float4 words c, c + s, ... of the token's row
     int s = 32;
     while (s > 1 && P * s > NT) s >>= 1;
     const int gpw = 32 / s, c = lane & (s - 1);
@@ -119,13 +141,8 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
       if (p < P) {
         t = p / E;
         e = p - t * E;
-        const float* zt = zbuf + t * E;
-        z = zt[e];
-#pragma unroll 4
-        for (int f = c; f < E; f += s) {
-          const float zf = zt[f];
-          rank += (zf > z) | ((zf == z) & (f < e));
-        }
+        z = zbuf[t * E4 + e];
+        rank = rank_in_row(reinterpret_cast<const float4*>(zbuf + t * E4), E4 / 4, c, s, e);
       }
       for (int o = 1; o < s; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
       if (p < P && c == 0 && rank < k) {
@@ -231,7 +248,8 @@ template <int NT>
 __device__ void route_one_in_smem(const float* logits, int E, int k, int S, SmemRouting& r, float* zbuf) {
   constexpr int NW = NT / 32;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  for (int i = tid; i < E; i += NT) zbuf[i] = __ldcg(logits + i);
+  const int E4 = (E + 3) & ~3;  // padded to whole float4 with -inf (never ranked ahead)
+  for (int i = tid; i < E4; i += NT) zbuf[i] = i < E ? __ldcg(logits + i) : -INFINITY;
   __syncthreads();
   {
     int s = 32;  // lanes per expert, as many as the block allows
@@ -243,11 +261,7 @@ __device__ void route_one_in_smem(const float* logits, int E, int k, int S, Smem
       float z = 0.f;
       if (e < E) {
         z = zbuf[e];
-#pragma unroll 4
-        for (int f = c; f < E; f += s) {
-          const float zf = zbuf[f];
-          rank += (zf > z) | ((zf == z) & (f < e));
-        }
+        rank = rank_in_row(reinterpret_cast<const float4*>(zbuf), E4 / 4, c, s, e);
       }
       for (int o = 1; o < s; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
       if (e < E && c == 0 && rank < k) {
