@@ -353,9 +353,9 @@ def time_workload(w, layers, args, world, dev, e2e: bool):
                     "algorithmic_bytes_per_launch": round(dom_bytes),
                     "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"}
     else:
-        # the gate/up "launch": the pair of GEMM launches of one call (192-row tiles, then the small tiles)
+        # the gate/up "launch": the GEMM launches of one call (big, mid and small token tiles)
         dom = "prefill_gateup"
-        k_us = avg_us(dom) + avg_us("prefill_gateup_small")
+        k_us = avg_us(dom) + avg_us("prefill_gateup_mid") + avg_us("prefill_gateup_small")
         fl = work["flops"] * 2 / 3 / n_calls
         achieved = fl / (k_us / 1e6) / 1e12
         roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16_burst, "unit": "TFLOP/s",

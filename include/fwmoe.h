@@ -151,6 +151,8 @@ enum {
   FW_KERNEL_PREFILL_GATHER = 9, /* prefill: x rows gathered into grouped order */
   FW_KERNEL_PREFILL_GATEUP_SMALL = 10, /* prefill gate/up GEMM over the tiles of at most 64 rows */
   FW_KERNEL_PREFILL_DOWN_SMALL = 11,   /* prefill down GEMM over the tiles of at most 64 rows */
+  FW_KERNEL_PREFILL_GATEUP_MID = 12,   /* prefill gate/up GEMM over the tiles of 65 to 96 rows */
+  FW_KERNEL_PREFILL_DOWN_MID = 13,     /* prefill down GEMM over the tiles of 65 to 96 rows */
   FW_KERNEL_KINDS = 16
 };
 

@@ -54,7 +54,7 @@ EXPORTED = ("fw_moe_init", "fw_moe_route", "fw_moe_ffn", "fw_moe_forward", "fw_m
 
 KERNEL_KINDS = ("route_decode", "route_tiles", "route_scan", "route_scatter", "decode_experts", "reserved",
                 "prefill_gateup", "prefill_down", "prefill_combine", "prefill_gather", "prefill_gateup_small",
-                "prefill_down_small")
+                "prefill_down_small", "prefill_gateup_mid", "prefill_down_mid")
 
 
 def lib():

@@ -69,7 +69,7 @@ struct Allocator {
 void free_handle_memory(Handle* h) {
   void* ptrs[] = {h->q_gu, h->q_dc, h->st_d, h->t_gu, h->t_d, h->wr3, h->wr, h->bias, h->ids, h->gates,
                   h->logits, h->counts, h->offsets, h->perm, h->inv, h->row_token, h->row_gate, h->uinfo,
-                  h->hist, h->minfo, h->minfo_s, h->xperm, h->hbuf, h->yp, h->partial, h->zpart, h->meta,
+                  h->hist, h->minfo, h->minfo_m, h->minfo_s, h->xperm, h->hbuf, h->yp, h->partial, h->zpart, h->meta,
                   h->x_dev, h->out_dev, h->ids_dev};
   for (void* p : ptrs)
     if (p) cudaFree(p);
@@ -178,8 +178,8 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
       {(void**)&h->q_gu, (size_t)(EU * 2 * I * row_bytes(H))},
       {(void**)&h->q_dc, (size_t)(EU * H * I)},
       {(void**)&h->st_d, (size_t)(EU * (I / 32) * H * 2)},
-      {(void**)&h->t_gu, (size_t)(pre ? EU * (2 * I / kTileRows) * (H / kTileK) * kTileBytes : 256)},
-      {(void**)&h->t_d, (size_t)(pre ? EU * ((H + kTileRows - 1) / kTileRows) * (I / kTileK) * kTileBytes : 256)},
+      {(void**)&h->t_gu, (size_t)(pre ? EU * gemm_plane_bytes(2 * I / kTileRows, H / kTileK) : 256)},
+      {(void**)&h->t_d, (size_t)(pre ? EU * gemm_plane_bytes((H + kTileRows - 1) / kTileRows, I / kTileK) : 256)},
       {(void**)&h->wr, (size_t)(E * H * 4)},
       {(void**)&h->bias, (size_t)(E * 4)},
       {(void**)&h->wr3, (size_t)(pre ? 3 * E * H * 2 : 256)},
@@ -195,6 +195,7 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
       {(void**)&h->uinfo, (size_t)(EU * 16)},
       {(void**)&h->hist, (size_t)(n_route_tiles * EU * 4)},
       {(void**)&h->minfo, (size_t)(n_mtiles_max * 16)},
+      {(void**)&h->minfo_m, (size_t)(EU * 16)},
       {(void**)&h->minfo_s, (size_t)(EU * 16)},
       {(void**)&h->xperm, (size_t)(pre ? h->rows_max * H * 2 : 256)},
       {(void**)&h->hbuf, hbuf_bytes},
@@ -225,7 +226,7 @@ fw_status fw_moe_init(const fw_moe_config* cfg, const fw_moe_weights* w, void* s
   if (e == cudaSuccess) e = cudaMemsetAsync(h->q_gu, 0, EU * 2 * I * row_bytes(H), s);
   // rows of a last partial down tile (H % 128 != 0) are read and their results dropped: keep them defined
   if (e == cudaSuccess && pre)
-    e = cudaMemsetAsync(h->t_d, 0, EU * ((H + kTileRows - 1) / kTileRows) * (I / kTileK) * kTileBytes, s);
+    e = cudaMemsetAsync(h->t_d, 0, EU * gemm_plane_bytes((H + kTileRows - 1) / kTileRows, I / kTileK), s);
   if (e == cudaSuccess) e = launch_repack(h, 0, 0, (int)E, w->w_gate, s);
   if (e == cudaSuccess) e = launch_repack(h, 1, 0, (int)E, w->w_up, s);
   if (e == cudaSuccess) e = launch_repack(h, 2, 0, (int)E, w->w_down, s);

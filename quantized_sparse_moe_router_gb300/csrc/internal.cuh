@@ -22,7 +22,8 @@ constexpr int kMaxK = 16;          // experts per token
 constexpr int kMaxDecodeT = 16;    // decode path token limit (one lane per token in the combine)
 constexpr int kRouteTileM = 32;    // tokens per CTA in the tiled router
 constexpr int kTokTile = 192;      // prefill GEMM token tile (rows of one expert)
-constexpr int kSmallTile = 64;     // tiles of at most this many rows go to the small-tile GEMM
+constexpr int kMidTile = 96;       // an expert's last tile of at most this many rows goes to the mid-tile GEMM
+constexpr int kSmallTile = 64;     // ... of at most this many, to the small-tile GEMM
 constexpr int kRouterMaxSplit = 8; // prefill router: K splits at most (partial logits [splits][T_max][E])
 
 // Status bits written by kernels into the handle's device status word.
@@ -50,6 +51,8 @@ constexpr int kTileBytes = kTileCodeBytes + 2 * kTileRows * 2;   // 8704
 __host__ __device__ inline int64_t gemm_tile_offset(int64_t e, int64_t mb, int64_t kb, int64_t n_mb, int64_t KT) {
   return ((e * n_mb + mb) * KT + kb) * (int64_t)kTileBytes;
 }
+// bytes of one expert's tiles of a projection with n_mb row blocks and KT K steps
+__host__ __device__ inline int64_t gemm_plane_bytes(int64_t n_mb, int64_t KT) { return n_mb * KT * (int64_t)kTileBytes; }
 __host__ __device__ inline int tile_code_offset(int r, int chunk) { return r * kTileK + ((chunk ^ ((r >> 1) & 3)) << 4); }
 
 // Row of gate/up matrix row i in the interleaved [2I] plane: groups of
@@ -65,8 +68,9 @@ struct Meta {
   uint32_t ticket;      // last-CTA detection in the router (self-resetting)
   int32_t status;       // kStatus* bits
   int32_t T;            // T of the last route
-  int32_t n_mtiles;     // prefill: token tiles of more than kSmallTile rows (minfo)
+  int32_t n_mtiles;     // prefill: token tiles of more than kMidTile rows (minfo)
   int32_t n_stiles;     // prefill: token tiles of at most kSmallTile rows (minfo_s)
+  int32_t n_midtiles;   // prefill: token tiles of kSmallTile+1 .. kMidTile rows (minfo_m)
   uint32_t chunk_ctr;   // decode gate/up chunk tickets handed out (reset by the router)
   int32_t diag[4];      // first failed wait: (site, block, stage, detail); site 0 = none
 };
@@ -81,8 +85,10 @@ struct Timing {
 
 // TMA descriptors of the prefill GEMMs (host copies, passed by value).
 struct PrefillMaps {
-  CUtensorMap a_x;    // xperm [rows_max][H] bf16, box 64 x 96, 128B swizzle
-  CUtensorMap a_h;    // hbuf  [rows_max][I] bf16, box 64 x 96, 128B swizzle
+  CUtensorMap a_x;    // xperm [rows_max][H] bf16, 128B swizzle, box 64 x (the big-tile GEMM's token box)
+  CUtensorMap a_h;    // hbuf  [rows_max][I] bf16, likewise
+  CUtensorMap a_xm;   // the same, box 64 x 96 (mid-tile GEMM)
+  CUtensorMap a_hm;
   CUtensorMap a_xs;   // the same, box 64 x 64 (small-tile GEMM)
   CUtensorMap a_hs;
   CUtensorMap w3;     // router planes [3E][H] bf16, box 64 x min(E, 128), 128B swizzle (E <= 256)
@@ -122,6 +128,7 @@ struct Handle {
   int4* uinfo;        // [EU] (expert, first grouped row, rows, 0) of the experts with rows, ascending id
   int32_t* hist;      // [ceil(T_max/32)][EU] per-tile counts, then per-tile bases
   int4* minfo;        // [rows_max/kTokTile + EU] prefill token tiles: (expert, first row, valid rows, 0)
+  int4* minfo_m;      // [EU] the tiles of kSmallTile+1 .. kMidTile rows (an expert's only or last tile)
   int4* minfo_s;      // [EU] the tiles of at most kSmallTile rows (an expert's only or last tile)
   __nv_bfloat16* xperm; // [rows_max][H] x gathered into grouped order (prefill)
   void* hbuf;         // [rows_max][I] fp32 (decode) or bf16 (prefill)

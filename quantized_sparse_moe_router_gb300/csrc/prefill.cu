@@ -43,24 +43,30 @@ namespace {
 using namespace dev;
 
 constexpr int BM = 128, BK = 64;
-constexpr int kAStages = 4;                 // tensor-memory A stages (dequant -> MMA)
 constexpr int kEpiWarps = 4, kProducerWarp = 4, kMmaWarp = 5, kDeqWarp0 = 6, kDeqWarps = 8;
 constexpr int kMmaWarp2 = kDeqWarp0 + kDeqWarps;        // the second MMA issuer (two-block shape)
 constexpr int kThreads = (kMmaWarp2 + 1) * 32;          // 480
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSmemLimit = 227 * 1024; // dynamic shared memory a CTA may have
 
-// The two shapes of the grouped GEMM. MB = 1: token tiles of up to 192 rows
-// against one 128-row weight block per CTA. MB = 2: tiles of at most 64 rows
-// (an expert's only or last tile) against two weight blocks per CTA, so that
-// a stage carries 16 KB of codes for 8 KB of tokens -- such tiles stream
-// weights more than they multiply, and this keeps twice the code bytes in
-// flight per SM.
-template <int MB_>
+// The three shapes of the grouped GEMM, by the rows of the token tile. A
+// stage brings a K step of the token tile and of MB weight tiles; the SM
+// takes in at most about 65 GB/s from L2 whatever the mix, so the fewer token
+// bytes per weight byte, the closer the weights stream to the HBM rate:
+//   kBig   (tiles of 97..192 rows): one 128-row weight block per CTA -- the
+//          compute-heavy tiles (an expert's full 192-row tiles);
+//   kMid   (65..96 rows): two weight blocks per CTA (12 KB of tokens for
+//          17 KB of codes);
+//   kSmall (1..64 rows): two weight blocks per CTA (8 KB for 17 KB).
+// Accumulators are double-buffered; the rest of tensor memory holds A stages.
+enum TileShape { kBig = 0, kMid = 1, kSmall = 2 };
+
+template <int SH>
 struct Shape {
-  static constexpr int MB = MB_;                                 // 128-row weight blocks per CTA
-  static constexpr int BN = MB_ == 1 ? kTokTile : kSmallTile;    // tokens per tile (MMA N <= BN)
-  static constexpr int XBox = MB_ == 1 ? BN / 2 : BN;            // token rows per TMA box
+  static constexpr int MB = SH == kBig ? 1 : 2;                  // 128-row weight blocks per CTA
+  static constexpr int BN = SH == kBig ? kTokTile : (SH == kMid ? kMidTile : kSmallTile);  // MMA N <= BN
+  // token rows per TMA box
+  static constexpr int XBox = SH == kBig ? BN / 2 : BN;
   static constexpr uint32_t XBytes = BN * BK * 2;                // bf16 token tile slot
   static constexpr uint32_t WBytes = MB * kTileBytes;            // MB weight tiles: codes, then scales
   static constexpr uint32_t StageBytes = XBytes + WBytes;
@@ -69,11 +75,11 @@ struct Shape {
   static constexpr uint32_t AccCols = MB * BN;                   // one accumulator buffer (MB blocks)
   static constexpr uint32_t ACol0 = 2 * AccCols;                 // A stages after the two buffers
   static constexpr uint32_t ACols = MB * BK / 2;                 // one A stage: 64 bf16 per row per block
-  static_assert(ACol0 + kAStages * ACols <= kTmemCols, "tensor memory budget");
+  static constexpr int AStages = (int)((kTmemCols - ACol0) / ACols) & ~1;
+  static_assert(AStages >= 2 && ACol0 + AStages * ACols <= kTmemCols, "tensor memory budget");
   static_assert(BN % XBox == 0 && BN % 16 == 0 && BN <= 256 && XBox % 8 == 0, "token tile");
   static_assert(BM == kTileRows && BK == kTileK, "a stage holds whole weight tiles");
-  static_assert(Stages >= 4 && Stages % 2 == 0 && kAStages % 2 == 0,
-                "the two dequantising groups own alternate stages");
+  static_assert(Stages >= 4 && Stages % 2 == 0, "the two dequantising groups own alternate stages");
 };
 
 enum Epi { kEpiSwiGLU = 0, kEpiDownScale = 1 };
@@ -202,11 +208,12 @@ __device__ __forceinline__ uint32_t deq_pair_bf16(uint32_t bits_lo, uint32_t bit
 }
 
 // ------------------------------------------------------------- the GEMM
-template <int EPI, int MB>
+template <int EPI, int SH>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap map_b, GemmArgs a) {
-  using G = Shape<MB>;
-  constexpr int kStages = G::Stages;
+  using G = Shape<SH>;
+  constexpr int MB = G::MB;
+  constexpr int kStages = G::Stages, kAStages = G::AStages;
   constexpr int kIssuers = MB;  // MMA-issuing threads: one per weight block
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full[kStages], empty[kStages], a_full[kAStages], a_empty[kAStages];
@@ -768,10 +775,10 @@ unsigned grid_for(int64_t n, int threads, int cap) {
 
 
 
-template <int EPI, int MB>
+template <int EPI, int SH>
 cudaError_t launch_gemm(const CUtensorMap& mb, const GemmArgs& g, int num_sms, cudaStream_t s) {
   // one persistent CTA per SM (its shared memory admits no second)
-  grouped_gemm_kernel<EPI, MB><<<(unsigned)num_sms, kThreads, Shape<MB>::SmemBytes, s>>>(mb, g);
+  grouped_gemm_kernel<EPI, SH><<<(unsigned)num_sms, kThreads, Shape<SH>::SmemBytes, s>>>(mb, g);
   return cudaGetLastError();
 }
 
@@ -785,10 +792,12 @@ cudaError_t configure_prefill_kernels() {
     if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return e != cudaSuccess ? e : cudaErrorNotSupported;
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
-  cudaError_t e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiSwiGLU, 1>);
-  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDownScale, 1>);
-  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiSwiGLU, 2>);
-  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDownScale, 2>);
+  cudaError_t e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiSwiGLU, kBig>);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDownScale, kBig>);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiSwiGLU, kMid>);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDownScale, kMid>);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiSwiGLU, kSmall>);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDownScale, kSmall>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_mma_kernel<8>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_mma_kernel<16>);
   return e;
@@ -798,16 +807,22 @@ cudaError_t prepare_prefill(Handle* h) {
   const uint64_t H = h->cfg.H, I = h->cfg.I, EU = h->EU, R = h->rows_max;
   PrefillMaps* m = new PrefillMaps();
   h->maps = m;
-  cudaError_t e = encode_2d(&m->a_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->xperm, H, R, H * 2, BK, Shape<1>::XBox,
+  cudaError_t e = encode_2d(&m->a_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->xperm, H, R, H * 2, BK, Shape<kBig>::XBox,
                             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
   if (e == cudaSuccess)
-    e = encode_2d(&m->a_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->hbuf, I, R, I * 2, BK, Shape<1>::XBox,
+    e = encode_2d(&m->a_h, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->hbuf, I, R, I * 2, BK, Shape<kBig>::XBox,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
   if (e == cudaSuccess)
-    e = encode_2d(&m->a_xs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->xperm, H, R, H * 2, BK, Shape<2>::XBox,
+    e = encode_2d(&m->a_xm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->xperm, H, R, H * 2, BK, Shape<kMid>::XBox,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
   if (e == cudaSuccess)
-    e = encode_2d(&m->a_hs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->hbuf, I, R, I * 2, BK, Shape<2>::XBox,
+    e = encode_2d(&m->a_hm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->hbuf, I, R, I * 2, BK, Shape<kMid>::XBox,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+  if (e == cudaSuccess)
+    e = encode_2d(&m->a_xs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->xperm, H, R, H * 2, BK, Shape<kSmall>::XBox,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
+  if (e == cudaSuccess)
+    e = encode_2d(&m->a_hs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->hbuf, I, R, I * 2, BK, Shape<kSmall>::XBox,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B);
   if (e == cudaSuccess && h->wr3)
     e = encode_2d(&m->w3, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->wr3, H, 3 * (uint64_t)h->cfg.E, H * 2, kRK,
@@ -870,48 +885,50 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
     gather_rows_kernel<<<grid_for(rows, kRowThreads / 32, h->num_sms * 8), kRowThreads, 0, s>>>(x, h->row_token,
                                                                                                rows, H, h->xperm);
   }
-  // each projection: the tiles of more than kSmallTile rows, then the small ones
-  GemmArgs g, gs;
+  // each projection: the big tiles, the mid ones, then the small ones
+  GemmArgs g;
   g.wt = h->t_gu;
-  g.minfo = h->minfo;
-  g.n_mtiles = &h->meta->n_mtiles;
   g.meta = h->meta;
   g.row_gate = h->row_gate;
+  g.outp = static_cast<__nv_bfloat16*>(h->hbuf);
+  g.K = H;
+  g.prows = 2 * I;
+  g.n_mb = (2 * I + BM - 1) / BM;
+  g.out_cols = I;
+  auto lists = [&](GemmArgs base, int shape) {
+    base.minfo = shape == kBig ? h->minfo : (shape == kMid ? h->minfo_m : h->minfo_s);
+    base.n_mtiles = shape == kBig ? &h->meta->n_mtiles : (shape == kMid ? &h->meta->n_midtiles : &h->meta->n_stiles);
+    return base;
+  };
   {
-    g.outp = static_cast<__nv_bfloat16*>(h->hbuf);
-    g.K = H;
-    g.prows = 2 * I;
-    g.n_mb = (2 * I + BM - 1) / BM;
-    g.out_cols = I;
-    gs = g;
-    gs.minfo = h->minfo_s;
-    gs.n_mtiles = &h->meta->n_stiles;
-    {
-      KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP, s);
-      err = launch_gemm<kEpiSwiGLU, 1>(h->maps->a_x, g, h->num_sms, s);
-    }
-    KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP_SMALL, s);
-    if (err == cudaSuccess)
-      err = launch_gemm<kEpiSwiGLU, 2>(h->maps->a_xs, gs, h->num_sms, s);
+    KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP, s);
+    err = launch_gemm<kEpiSwiGLU, kBig>(h->maps->a_x, lists(g, kBig), h->num_sms, s);
   }
   {
-    g.outp = h->yp;
-    g.wt = h->t_d;
-    g.K = I;
-    g.prows = H;
-    g.n_mb = (H + BM - 1) / BM;
-    g.out_cols = H;
-    gs = g;
-    gs.minfo = h->minfo_s;
-    gs.n_mtiles = &h->meta->n_stiles;
-    {
-      KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN, s);
-      if (err == cudaSuccess)
-        err = launch_gemm<kEpiDownScale, 1>(h->maps->a_h, g, h->num_sms, s);
-    }
+    KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP_MID, s);
+    if (err == cudaSuccess) err = launch_gemm<kEpiSwiGLU, kMid>(h->maps->a_xm, lists(g, kMid), h->num_sms, s);
+  }
+  {
+    KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP_SMALL, s);
+    if (err == cudaSuccess) err = launch_gemm<kEpiSwiGLU, kSmall>(h->maps->a_xs, lists(g, kSmall), h->num_sms, s);
+  }
+  g.outp = h->yp;
+  g.wt = h->t_d;
+  g.K = I;
+  g.prows = H;
+  g.n_mb = (H + BM - 1) / BM;
+  g.out_cols = H;
+  {
+    KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN, s);
+    if (err == cudaSuccess) err = launch_gemm<kEpiDownScale, kBig>(h->maps->a_h, lists(g, kBig), h->num_sms, s);
+  }
+  {
+    KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN_MID, s);
+    if (err == cudaSuccess) err = launch_gemm<kEpiDownScale, kMid>(h->maps->a_hm, lists(g, kMid), h->num_sms, s);
+  }
+  {
     KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN_SMALL, s);
-    if (err == cudaSuccess)
-      err = launch_gemm<kEpiDownScale, 2>(h->maps->a_hs, gs, h->num_sms, s);
+    if (err == cudaSuccess) err = launch_gemm<kEpiDownScale, kSmall>(h->maps->a_hs, lists(g, kSmall), h->num_sms, s);
   }
   if (err != cudaSuccess) return err;
   {

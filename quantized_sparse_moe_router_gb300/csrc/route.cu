@@ -247,10 +247,19 @@ __global__ void __launch_bounds__(256) route_tiles_kernel(RouteArgs a, int32_t* 
 constexpr int kScanBatch = 16;
 
 // An expert's token tiles: full kTokTile-row tiles, then the rest -- which
-// goes to the small-tile list when it has at most kSmallTile rows.
+// goes to the small-tile list when it has at most kSmallTile rows, to the
+// mid-tile list when it has at most kMidTile, else it is a big tile too.
+// When the batch has fewer mid tiles than `mid_min` (less than one tile per
+// SM in the mid-tile GEMMs) they join the big tiles instead: a launch that
+// gives each SM at most one tile costs a whole tile's latency, which a few
+// more tiles among the big ones do not.
 __device__ __forceinline__ int big_tiles(int c) {
   const int r = c % kTokTile;
-  return c / kTokTile + (r > kSmallTile ? 1 : 0);
+  return c / kTokTile + (r > kMidTile ? 1 : 0);
+}
+__device__ __forceinline__ int mid_tiles(int c) {
+  const int r = c % kTokTile;
+  return r > kSmallTile && r <= kMidTile ? 1 : 0;
 }
 __device__ __forceinline__ int small_tiles(int c) {
   const int r = c % kTokTile;
@@ -260,12 +269,16 @@ __device__ __forceinline__ int small_tiles(int c) {
 constexpr int kScanThreads = 1024;
 
 __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(RouteArgs a, int32_t* hist, int n_tiles,
-                                                                  int4* minfo, int4* minfo_s) {
+                                                                  int4* minfo, int4* minfo_m, int4* minfo_s,
+                                                                  int mid_min) {
   __shared__ int s_cnt[kMaxE + 2];
   __shared__ int s_off[kMaxE + 2];
   __shared__ int s_nz[kMaxE + 2];
   __shared__ int s_nt[kMaxE + 2];
   __shared__ int s_ns[kMaxE + 2];
+  __shared__ int s_nm[kMaxE + 2];
+  __shared__ int s_nbm[kMaxE + 2];  // big + mid tiles before the expert (mid tiles merged)
+  __shared__ int s_merge;
   __shared__ int s_part[kScanThreads];  // [part][expert]: the part's count (pass 1)
   const int E = a.E, EU = E + a.S, T = a.T, tid = threadIdx.x, lane = tid & 31;
   // thread (part, expert): the experts' per-tile counts are summed by P
@@ -299,7 +312,7 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(RouteArgs a, i
     constexpr int kPer = (kMaxE + 1 + 31) / 32;
     const int per = (EU + 31) / 32, b0 = lane * per;
     int cn[kPer];
-    int sc = 0, sn = 0, st = 0, ss = 0;
+    int sc = 0, sn = 0, st = 0, ss = 0, sm = 0;
 #pragma unroll
     for (int m = 0; m < kPer; ++m) {
       const int i = b0 + m;
@@ -308,20 +321,23 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(RouteArgs a, i
       sn += cn[m] > 0;
       st += big_tiles(cn[m]);
       ss += small_tiles(cn[m]);
+      sm += mid_tiles(cn[m]);
     }
-    int ic = sc, in = sn, it = st, is = ss;
+    int ic = sc, in = sn, it = st, is = ss, im = sm;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const int uc = __shfl_up_sync(0xFFFFFFFFu, ic, o), un = __shfl_up_sync(0xFFFFFFFFu, in, o),
-                ut = __shfl_up_sync(0xFFFFFFFFu, it, o), us = __shfl_up_sync(0xFFFFFFFFu, is, o);
+                ut = __shfl_up_sync(0xFFFFFFFFu, it, o), us = __shfl_up_sync(0xFFFFFFFFu, is, o),
+                um = __shfl_up_sync(0xFFFFFFFFu, im, o);
       if (lane >= o) {
         ic += uc;
         in += un;
         it += ut;
         is += us;
+        im += um;
       }
     }
-    int rc = ic - sc, rn = in - sn, rt = it - st, rs = is - ss;
+    int rc = ic - sc, rn = in - sn, rt = it - st, rs = is - ss, rm = im - sm;
 #pragma unroll
     for (int m = 0; m < kPer; ++m) {
       const int i = b0 + m;
@@ -330,17 +346,23 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(RouteArgs a, i
         s_nz[i] = rn;
         s_nt[i] = rt;
         s_ns[i] = rs;
+        s_nm[i] = rm;
+        s_nbm[i] = rt + rm;
         rc += cn[m];
         rn += cn[m] > 0;
         rt += big_tiles(cn[m]);
         rs += small_tiles(cn[m]);
+        rm += mid_tiles(cn[m]);
       }
     }
     if (lane == 31) {
+      const bool merge = im < mid_min;
+      s_merge = merge;
       s_off[EU] = ic;
       a.meta->n_unique = in;
-      a.meta->n_mtiles = it;
+      a.meta->n_mtiles = merge ? it + im : it;
       a.meta->n_stiles = is;
+      a.meta->n_midtiles = merge ? 0 : im;
       a.meta->T = T;
     }
   }
@@ -350,13 +372,13 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(RouteArgs a, i
     const int cnt = s_cnt[e];
     a.counts[e] = cnt;
     if (cnt > 0) a.uinfo[s_nz[e]] = make_int4(e, s_off[e], cnt, 0);
-    const int nt = big_tiles(cnt);
+    const bool merge = s_merge;
+    const int nt = big_tiles(cnt) + (merge ? mid_tiles(cnt) : 0), t0 = merge ? s_nbm[e] : s_nt[e];
     for (int i = 0; i < nt; ++i)
-      minfo[s_nt[e] + i] = make_int4(e, s_off[e] + kTokTile * i, min(kTokTile, cnt - kTokTile * i), 0);
-    if (small_tiles(cnt)) {
-      const int r0 = cnt / kTokTile * kTokTile;
-      minfo_s[s_ns[e]] = make_int4(e, s_off[e] + r0, cnt - r0, 0);
-    }
+      minfo[t0 + i] = make_int4(e, s_off[e] + kTokTile * i, min(kTokTile, cnt - kTokTile * i), 0);
+    const int r0 = cnt / kTokTile * kTokTile;
+    if (small_tiles(cnt)) minfo_s[s_ns[e]] = make_int4(e, s_off[e] + r0, cnt - r0, 0);
+    if (!merge && mid_tiles(cnt)) minfo_m[s_nm[e]] = make_int4(e, s_off[e] + r0, cnt - r0, 0);
   }
   // per-tile bases: thread (part, expert) starts after the parts before it
   if (e_me < E) {
@@ -498,7 +520,11 @@ cudaError_t launch_route_prefill(Handle* h, const __nv_bfloat16* x, int T, int32
   if (err != cudaSuccess) return err;
   {
     KernelTimer tm(h, FW_KERNEL_ROUTE_SCAN, s);
-    route_scan_kernel<<<1, kScanThreads, 0, s>>>(a, h->hist, n_tiles, h->minfo, h->minfo_s);
+    // the mid-tile GEMMs take two 128-row weight blocks per SM and tile
+    const int64_t mb_gu = (2 * (int64_t)h->cfg.I + 127) / 128, mb_d = ((int64_t)h->cfg.H + 127) / 128;
+    const int n_mbg = (int)::min((mb_gu + 1) / 2, (mb_d + 1) / 2);
+    const int mid_min = (h->num_sms + n_mbg - 1) / n_mbg;
+    route_scan_kernel<<<1, kScanThreads, 0, s>>>(a, h->hist, n_tiles, h->minfo, h->minfo_m, h->minfo_s, mid_min);
   }
   {
     KernelTimer tm(h, FW_KERNEL_ROUTE_SCATTER, s);

@@ -67,6 +67,8 @@ CASES = [
     ("tiny", dict(T=40, H=320, E=8, k=3)),              # H % 256 != 0: partial last down tile
     ("tiny", dict(T=1000, k=2)),                        # 192-row tiles and small last tiles (both GEMM shapes)
     ("tiny", dict(T=700, k=2, I=192, S=1)),             # large remainders (> 64 rows), shared expert, odd blocks
+    ("tiny", dict(T=330, k=2)),                         # about 82 rows per expert: too few mid tiles for their own launch
+    ("tiny", dict(T=470, k=2, S=1)),                    # about 117 rows: big remainders; shared: 2 big + mid
 ]
 
 
@@ -104,6 +106,23 @@ def test_prefill_full_size_4096_zipf():
     ids, _ = check(wl, x, res, ol, parallel=True)
     counts = np.bincount(ids.ravel(), minlength=wl.E)
     assert counts.max() > 2 * 192 and (counts[counts > 0] <= 64).any()  # both GEMM shapes ran
+
+
+def test_prefill_mid_tiles_launch():
+    """About 81 rows on each of 64 experts: more tiles of 65..96 rows than
+    the rule that gives them a launch of their own needs (one tile per SM
+    across the two weight blocks a CTA takes), so the mid-tile GEMMs run
+    them; every token's output."""
+    wl = synth.WORKLOADS["tiny"].with_(T=2600, E=64, k=2, H=1024, I=1024)
+    ol = OracleLayer(wl, 0)
+    x = hidden_with_margins(wl, 0, ol.Wr, ol.bias)
+    _, res = run_layer(wl, x)
+    ids, _ = check(wl, x, res, ol, parallel=True)
+    r = np.bincount(ids.ravel(), minlength=wl.E) % 192
+    n_mid = int(((r > 64) & (r <= 96)).sum())
+    per_tile = min((2 * wl.I // 128 + 1) // 2, (wl.H // 128 + 1) // 2)  # weight-block pairs per tile
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert n_mid * per_tile >= sms, n_mid
 
 
 def test_prefill_full_size_large_2048():
