@@ -24,7 +24,14 @@
 // signed high and an unsigned low byte plane; the Q8_0 codes (offset binary)
 // multiply both planes with dp4a, and one fp32 multiply-add per segment
 // applies the weight scale and the segment's power of two. The down
-// projection multiplies fp32 h by the exactly dequantised codes in fp32.
+// projection does the same with the chunk's h (16 fp32 values per token, made
+// fixed point at their largest exponent: by every thread for one token, once
+// per token into shared memory for several).
+//
+// Chunks are split over the CTAs in contiguous ranges: of equal count for one
+// token; for several, of equal cost, a chunk costing its weight stream plus
+// its expert's token count of arithmetic (a CTA whose range falls on experts
+// with many tokens would otherwise finish last).
 //
 // One CTA per SM, all resident (see launch()):
 //   0. x -> fixed-point planes in shared memory (before the router finishes);
@@ -60,6 +67,14 @@ constexpr uint32_t kConsumerBarrier = 1;   // named barrier of the 16 consumer w
 constexpr uint32_t kStageTarget = 36 * 1024;
 constexpr int kRedBatch = 10;              // partial loads in flight per lane in the final sums
 constexpr int kMaxGrid = 256;              // CTAs (one per SM) the per-CTA token masks have room for
+constexpr int kChunkCost = 4;              // several tokens: a chunk's weight stream, in units of one token's arithmetic
+
+// The chunk's h of one token as 16-bit fixed point (see h16_to_planes).
+struct HPlanes {
+  uint4 hi, lo;
+  int2 info;
+  int2 pad;
+};
 
 struct DecodeArgs {
   const uint8_t* q_gu;   // [EU][2I] rows of row_bytes(H): codes + 128, then binary16 scales
@@ -77,83 +92,12 @@ struct DecodeArgs {
   int Dr;                // down rows per stage (multiple of 16)
   uint32_t stage_bytes;
   int stages;
-  uint32_t off_info, off_acc, off_h, off_ring;  // dynamic shared memory layout (bytes)
+  uint32_t off_info, off_acc, off_h, off_hp, off_ring;  // dynamic shared memory layout (bytes)
   uint32_t grid_extra;   // arrivals the grid wait expects beyond the grid (0; > 0 only to test the bound)
   uint64_t grid_wait_ns; // bound of the grid-wide wait
 };
 
 // ------------------------------------------------------------- helpers
-typedef unsigned long long f2;
-
-__device__ __forceinline__ f2 f2_pack(float a, float b) {
-  f2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ f2 f2_pack_bits(uint32_t a, uint32_t b) {
-  f2 r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(a), "r"(b));
-  return r;
-}
-__device__ __forceinline__ float f2_hsum(f2 v) {
-  float a, b;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
-  return a + b;
-}
-__device__ __forceinline__ f2 f2_add(f2 a, f2 b) {
-  f2 r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ f2 f2_fma(f2 a, f2 b, f2 c) {
-  f2 r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
-
-// Four offset-binary codes of a word times four h values (two pairs), added
-// to a pair accumulator: the byte permute makes the float 2^23 + q + 128 and
-// one packed subtraction leaves q exactly.
-__device__ __forceinline__ f2 dot4(uint32_t w, f2 x01, f2 x23, f2 acc) {
-  const f2 bias = f2_pack(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
-  const f2 m01 = f2_pack_bits(__byte_perm(w, 0x4B000000u, 0x7650), __byte_perm(w, 0x4B000000u, 0x7651));
-  const f2 m23 = f2_pack_bits(__byte_perm(w, 0x4B000000u, 0x7652), __byte_perm(w, 0x4B000000u, 0x7653));
-  acc = f2_fma(f2_add(m01, bias), x01, acc);
-  return f2_fma(f2_add(m23, bias), x23, acc);
-}
-
-// sum_{i<16} q_i h_i for one 16-code segment; h as 8 pairs.
-__device__ __forceinline__ float dot16(const uint4 q, const f2 (&h)[8]) {
-  f2 a = dot4(q.x, h[0], h[1], 0ull);
-  f2 b = dot4(q.y, h[2], h[3], 0ull);
-  a = dot4(q.z, h[4], h[5], a);
-  b = dot4(q.w, h[6], h[7], b);
-  return f2_hsum(f2_add(a, b));
-}
-
-// The same with h read from shared memory (a broadcast) one pair of words at
-// a time, so that few registers hold h.
-__device__ __forceinline__ float dot16_smem(const uint4 q, const float* h) {
-  const float4* hp = reinterpret_cast<const float4*>(h);
-  float4 v0 = hp[0], v1 = hp[1];
-  f2 a = dot4(q.x, f2_pack(v0.x, v0.y), f2_pack(v0.z, v0.w), 0ull);
-  f2 b = dot4(q.y, f2_pack(v1.x, v1.y), f2_pack(v1.z, v1.w), 0ull);
-  v0 = hp[2];
-  v1 = hp[3];
-  a = dot4(q.z, f2_pack(v0.x, v0.y), f2_pack(v0.z, v0.w), a);
-  b = dot4(q.w, f2_pack(v1.x, v1.y), f2_pack(v1.z, v1.w), b);
-  return f2_hsum(f2_add(a, b));
-}
-
-__device__ __forceinline__ void load_h16(const float* p, f2 (&h)[8]) {
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float4 v = reinterpret_cast<const float4*>(p)[i];
-    h[2 * i] = f2_pack(v.x, v.y);
-    h[2 * i + 1] = f2_pack(v.z, v.w);
-  }
-}
-
 // Integer dot products of four code bytes (unsigned, q + 128) with four
 // signed / unsigned activation bytes, added to c.
 __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
@@ -233,6 +177,84 @@ __device__ __forceinline__ void x_segment_to_planes(const uint4 a, const uint4 b
   info = make_int2((int)((emax - 14u) << 23), 128 * sum);  // float bits of 2^(e - 14), offset term
 }
 
+// The chunk's h of one token (16 fp32 values in shared memory) -> the same
+// 16-bit fixed point at its largest exponent as x (byte planes, 2^(e - 14),
+// 128 * sum): the down codes then multiply it with dp4a. Two passes over the
+// values (broadcast reads) keep few registers live. Largest magnitude below
+// 2^-112: zero.
+__device__ __forceinline__ void h16_to_planes(const float* h, uint4& hi, uint4& lo, int2& info) {
+  const float4* h4 = reinterpret_cast<const float4*>(h);
+  uint32_t emax = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float4 v = h4[j];
+    emax = max(emax, max(max((__float_as_uint(v.x) >> 23) & 0xFFu, (__float_as_uint(v.y) >> 23) & 0xFFu),
+                         max((__float_as_uint(v.z) >> 23) & 0xFFu, (__float_as_uint(v.w) >> 23) & 0xFFu)));
+  }
+  if (emax < 15u) {
+    hi = lo = make_uint4(0u, 0u, 0u, 0u);
+    info = make_int2(0, 0);
+    return;
+  }
+  const float mult = __uint_as_float((268u - emax) << 23);  // 2^(14 - e)
+  uint32_t hw[4], lw[4];
+  int sum = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float4 v = h4[j];
+    const int x0 = __float2int_rn(v.x * mult), x1 = __float2int_rn(v.y * mult), x2 = __float2int_rn(v.z * mult),
+              x3 = __float2int_rn(v.w * mult);
+    sum += x0 + x1 + x2 + x3;
+    hw[j] = ((uint32_t)(x0 >> 8) & 0xFFu) | (((uint32_t)(x1 >> 8) & 0xFFu) << 8) | (((uint32_t)(x2 >> 8) & 0xFFu) << 16) |
+            (((uint32_t)(x3 >> 8) & 0xFFu) << 24);
+    lw[j] = ((uint32_t)x0 & 0xFFu) | (((uint32_t)x1 & 0xFFu) << 8) | (((uint32_t)x2 & 0xFFu) << 16) |
+            (((uint32_t)x3 & 0xFFu) << 24);
+  }
+  hi = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  lo = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  info = make_int2((int)((emax - 14u) << 23), 128 * sum);
+}
+
+// The same conversion by one warp (lane j < 16 holds value j), written to
+// shared memory: the several-token path converts each token's h once per
+// chunk instead of once per thread.
+__device__ __forceinline__ void h16_to_planes_warp(const float* h, HPlanes* out, int lane) {
+  const float v = lane < 16 ? h[lane] : 0.f;
+  const uint32_t emax = __reduce_max_sync(0xFFFFFFFFu, (__float_as_uint(v) >> 23) & 0xFFu);
+  int xi = 0;
+  if (emax >= 15u) xi = __float2int_rn(v * __uint_as_float((268u - emax) << 23));  // 2^(14 - e)
+  const int sum = __reduce_add_sync(0xFFFFFFFFu, xi);
+  uint32_t hw = ((uint32_t)(xi >> 8) & 0xFFu) << ((lane & 3) * 8), lw = ((uint32_t)xi & 0xFFu) << ((lane & 3) * 8);
+  hw |= __shfl_xor_sync(0xFFFFFFFFu, hw, 1);
+  lw |= __shfl_xor_sync(0xFFFFFFFFu, lw, 1);
+  hw |= __shfl_xor_sync(0xFFFFFFFFu, hw, 2);
+  lw |= __shfl_xor_sync(0xFFFFFFFFu, lw, 2);
+  if (lane < 16 && (lane & 3) == 0) {
+    reinterpret_cast<uint32_t*>(&out->hi)[lane >> 2] = hw;
+    reinterpret_cast<uint32_t*>(&out->lo)[lane >> 2] = lw;
+  }
+  if (lane == 0) out->info = emax >= 15u ? make_int2((int)((emax - 14u) << 23), 128 * sum) : make_int2(0, 0);
+}
+
+// Four consecutive fp32 columns of this thread's tensor-memory lane (the
+// several-token path keeps its partial output there: 64 per thread would not
+// fit in registers beside the rest).
+__device__ __forceinline__ float4 tmem_ld4(uint32_t taddr) {
+  uint32_t r0, r1, r2, r3;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  return make_float4(__uint_as_float(r0), __uint_as_float(r1), __uint_as_float(r2), __uint_as_float(r3));
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, float4 v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(taddr), "r"(__float_as_uint(v.x)),
+               "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)), "r"(__float_as_uint(v.w))
+               : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+constexpr uint32_t kTmemCols = 512;  // several tokens: 16 warps x (16 tokens x 4 rows) fp32, by lane quarter
+
 // ------------------------------------------------------------- the kernel
 // kMulti: several tokens (T <= 16, H <= 2048; partial output in registers);
 // otherwise one token (partial output in shared memory).
@@ -243,7 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   __shared__ SmemRouting r;
   __shared__ uint32_t s_emask[kMaxE + 1];  // per touched expert (ascending): its tokens
   __shared__ uint32_t s_pm[kMaxGrid];       // per CTA: the tokens its partial output covers
+  __shared__ int s_c0[kMaxGrid + 1];         // per CTA: its first chunk (s_c0[grid] = all chunks)
+  __shared__ uint32_t s_pref[kMaxE + 2];     // several tokens: chunk cost before each touched expert
   __shared__ volatile int s_abort;  // a consumer gave up a wait: the others stop waiting too
+  __shared__ uint32_t s_tmem;        // several tokens: tensor-memory base of the partial outputs
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = a.H, I = a.I, T = kMulti ? a.T : 1, R = a.R, Dr = a.Dr;
   const int nseg = H / 16;
@@ -253,6 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   int2* xinfo = reinterpret_cast<int2*>(smem + a.off_info);         // [T][H/16]
   float* acc_s = reinterpret_cast<float*>(smem + a.off_acc);        // [H] (one token)
   float* hbuf = reinterpret_cast<float*>(smem + a.off_h);           // [2][T][16]
+  HPlanes* hpl = reinterpret_cast<HPlanes*>(smem + a.off_hp);       // [T] (several tokens)
   uint8_t* ring = smem + a.off_ring;
   if (tid == 0) {
     for (int s = 0; s < a.stages; ++s) {
@@ -261,6 +287,12 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
     }
     s_abort = 0;
     fence_mbar_init();
+  }
+  if (kMulti && warp == 0) {  // one CTA per SM: the 512 columns are free
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (warp != kProducer) {
     // x was written before the router kernel started (that launch waits for
@@ -288,9 +320,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   // this CTA's chunks: [c0, c1) of the nU * I/16 chunks, expert-major
   const int G = I / kChunk;
   const int n_ch = r.n_unique * G;
-  // (32-bit: a 64-bit division is a long software routine; n_ch * grid < 2^32)
-  const int c0 = (int)((uint32_t)n_ch * blockIdx.x / gridDim.x);
-  const int c1 = (int)((uint32_t)n_ch * (blockIdx.x + 1) / gridDim.x);
   const int n_gu = kChunk / R;            // gate/up stages per chunk
   const int n_dn = (H + Dr - 1) / Dr;     // down stages per chunk
   // Tokens each CTA's partial output covers (the CTAs' chunk ranges follow
@@ -301,9 +330,55 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
     for (int p = ui.y; p < ui.y + ui.z; ++p) m |= 1u << r.tok[p];
     s_emask[u] = m;
   }
+  if (kMulti) {
+    // A chunk costs its weight stream plus its expert's token count of
+    // arithmetic: kChunkCost + n. CTA b takes the chunks whose starting cost
+    // lies in [b C / grid, (b + 1) C / grid), C the total. Prefix costs per
+    // expert by one warp (C < 2^32), the bounds by a thread per CTA.
+    if (warp == 0) {
+      const int nu = r.n_unique, per = (nu + 31) / 32, u0 = lane * per;
+      uint32_t run = 0;
+      for (int u = u0; u < ::min(nu, u0 + per); ++u) run += (uint32_t)(kChunkCost + r.u[u].z) * G;
+      uint32_t inc = run;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += v;
+      }
+      uint32_t p = inc - run;
+      for (int u = u0; u < ::min(nu, u0 + per); ++u) {
+        s_pref[u] = p;
+        p += (uint32_t)(kChunkCost + r.u[u].z) * G;
+      }
+      if (lane == 31) s_pref[nu] = inc;
+    }
+    __syncthreads();
+    const uint64_t C = s_pref[r.n_unique], grid = gridDim.x;
+    for (int b = tid; b <= (int)grid; b += kThreads) {
+      // first chunk c with cost(c) * grid >= b * C (once per call: 64-bit)
+      const uint64_t target = (uint64_t)b * C;
+      int lo = 0, hi = r.n_unique;  // expert: the last u with s_pref[u] * grid <= target
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_pref[mid] * grid <= target) lo = mid; else hi = mid;
+      }
+      int c = n_ch;
+      if (b < (int)grid && r.n_unique > 0) {
+        const uint64_t w = (uint64_t)(kChunkCost + r.u[lo].z) * grid;
+        const uint64_t rem = target - s_pref[lo] * grid;
+        c = ::min(lo * G + (int)((rem + w - 1) / w), n_ch);
+      }
+      s_c0[b] = c;
+    }
+  } else {
+    // one token: every chunk costs the same, equal counts
+    // (32-bit: a 64-bit division is a long software routine; n_ch * grid < 2^32)
+    for (int b = tid; b <= (int)gridDim.x; b += kThreads) s_c0[b] = (int)((uint32_t)n_ch * b / gridDim.x);
+  }
   __syncthreads();
+  const int c0 = s_c0[blockIdx.x], c1 = s_c0[blockIdx.x + 1];
   for (int c = tid; c < (int)gridDim.x; c += kThreads) {
-    const int b0 = (int)((uint32_t)n_ch * c / gridDim.x), b1 = (int)((uint32_t)n_ch * (c + 1) / gridDim.x);
+    const int b0 = s_c0[c], b1 = s_c0[c + 1];
     uint32_t m = 0;
     if (b1 > b0)
       for (int u = b0 / G; u <= (b1 - 1) / G; ++u) m |= s_emask[u];
@@ -377,11 +452,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
     // work and arrivals but still passes every consumer barrier, so that the
     // other warps are never left waiting at one.
     bool ok = true;
-    float acc[kMulti ? kRowsMulti : 1][kMulti ? kMaxDecodeT : 1];
-#pragma unroll
-    for (int jr = 0; jr < (kMulti ? kRowsMulti : 1); ++jr)
-#pragma unroll
-      for (int t = 0; t < (kMulti ? kMaxDecodeT : 1); ++t) acc[jr][t] = 0.f;
+    // several tokens: this thread's partial output rows tid + 512 jr of token
+    // t in its tensor-memory lane, column (warp / 4) 64 + 4 t + jr
+    uint32_t tacc = 0;
+    if (kMulti) {
+      tc_fence_after();
+      tacc = s_tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(warp >> 2) * 64u;
+#pragma unroll 1
+      for (int t = 0; t < kMaxDecodeT; ++t) tmem_st4(tacc + 4 * t, make_float4(0.f, 0.f, 0.f, 0.f));
+    }
     int st = 0;
     uint32_t ph = 0;
     int jj = 0;  // stages consumed
@@ -396,6 +475,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
           ok = false;
           s_abort = 1;
         }
+        ok = __all_sync(0xFFFFFFFFu, ok);  // warp-uniform (tensor-memory accesses are warp-wide)
         if (ok && warp / R == q) {
           const int off = warp - q * R;  // unit within the stage
           const uint8_t* grow = ring + (size_t)st * a.stage_bytes +
@@ -436,6 +516,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
         }
       }
       consumer_sync();  // the chunk's h is complete
+      if (kMulti) {  // each token's h -> fixed-point planes, a warp per token
+        for (int m = warp; m < ui.z; m += kCW) h16_to_planes_warp(hb + m * kChunk, hpl + m, lane);
+        consumer_sync();
+      }
+      uint4 dhh = make_uint4(0u, 0u, 0u, 0u), dhl = dhh;  // one token: the chunk's h planes
+      int2 dhinf = make_int2(0, 0);
+      float dgf = 0.f;
       // ---- down: thread tid takes rows tid, tid + 512, ... of each stage
       for (int q = 0; q < n_dn; ++q) {
         ok = ok && !s_abort;
@@ -444,37 +531,47 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
           ok = false;
           s_abort = 1;
         }
+        ok = __all_sync(0xFFFFFFFFu, ok);
         if (ok) {
           const uint8_t* sb = ring + (size_t)st * a.stage_bytes;
           const int r0 = q * Dr, nr = ::min(Dr, H - r0);
           const uint16_t* sc = reinterpret_cast<const uint16_t*>(sb + (size_t)nr * kChunk);
           if (kMulti) {
-            // all rows in this one stage (H <= 2048); the expert's tokens ascending
-            uint32_t emask = 0;
-            for (int p = ui.y; p < ui.y + ui.z; ++p) emask |= 1u << r.tok[p];
+            // all rows in this one stage (H <= 2048); the expert's tokens in
+            // ascending order: the row products, then the token's four
+            // partial sums read, added to and written back to tensor memory
+            for (int m = 0; m < ui.z; ++m) {
+              const int t = r.tok[ui.y + m];
+              const uint4 hh = hpl[m].hi, hl = hpl[m].lo;
+              const int2 inf = hpl[m].info;
+              const float gf = r.gates[r.slot[ui.y + m]] * __int_as_float(inf.x);
+              float d[kRowsMulti];
 #pragma unroll
-            for (int tt = 0; tt < kMaxDecodeT; ++tt) {
-              if ((emask >> tt) & 1u) {
-                const int m = __popc(emask & ((1u << tt) - 1u));
-                const float gate = r.gates[r.slot[ui.y + m]];
-                const float* hm = hb + m * kChunk;
-#pragma unroll
-                for (int jr = 0; jr < kRowsMulti; ++jr) {
-                  const int rr = tid + kCT * jr;
-                  if (rr < nr) {
-                    const uint4 qq = *reinterpret_cast<const uint4*>(sb + (size_t)rr * kChunk);
-                    acc[jr][tt] = fmaf(gate * half_bits_to_f32(sc[rr]), dot16_smem(qq, hm), acc[jr][tt]);
-                  }
+              for (int jr = 0; jr < kRowsMulti; ++jr) {
+                const int rr = tid + kCT * jr;
+                d[jr] = 0.f;
+                if (rr < nr) {
+                  const uint4 qq = *reinterpret_cast<const uint4*>(sb + (size_t)rr * kChunk);
+                  d[jr] = (float)(seg_dot_i(qq, hh, hl) - inf.y) * (gf * half_bits_to_f32(sc[rr]));
                 }
               }
+              float4 v = tmem_ld4(tacc + 4 * t);
+              v.x += d[0];
+              v.y += d[1];
+              v.z += d[2];
+              v.w += d[3];
+              tmem_st4(tacc + 4 * t, v);
             }
           } else {
-            const float gate = r.gates[r.slot[ui.y]];
-            f2 hv[8];
-            load_h16(hb, hv);
+            // (the chunk's h planes: the same in every down stage of the chunk)
+            if (q == 0) {
+              h16_to_planes(hb, dhh, dhl, dhinf);
+              dgf = r.gates[r.slot[ui.y]] * __int_as_float(dhinf.x);
+            }
             for (int rr = tid; rr < nr; rr += kCT) {
               const uint4 qq = *reinterpret_cast<const uint4*>(sb + (size_t)rr * kChunk);
-              acc_s[r0 + rr] = fmaf(gate * half_bits_to_f32(sc[rr]), dot16(qq, hv), acc_s[r0 + rr]);
+              const int S = seg_dot_i(qq, dhh, dhl) - dhinf.y;
+              acc_s[r0 + rr] = fmaf((float)S, dgf * half_bits_to_f32(sc[rr]), acc_s[r0 + rr]);
             }
           }
         }
@@ -490,13 +587,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
     // ---- partial output of this CTA to global memory
     float* part = a.partial + (size_t)blockIdx.x * T * H;
     if (kMulti) {
-#pragma unroll
       for (int tt = 0; tt < kMaxDecodeT; ++tt)
         if ((cta_mask >> tt) & 1u) {
+          const float4 v = tmem_ld4(tacc + 4 * tt);
+          const float vv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int jr = 0; jr < kRowsMulti; ++jr) {
             const int rr = tid + kCT * jr;
-            if (rr < H) __stcg(part + (size_t)tt * H + rr, acc[jr][tt]);
+            if (rr < H) __stcg(part + (size_t)tt * H + rr, vv[jr]);
           }
         }
     } else {
@@ -523,39 +621,61 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       }
     }
     consumer_sync();
-    // ---- this CTA's output rows [o0, o1): warp w sums the partials of CTAs
-    // [w cpw, (w + 1) cpw), lane = row; then the 16 warp sums in order.
-    float* red = reinterpret_cast<float*>(ring);  // [kCW][T][rows]
+    // ---- this CTA's output rows [o0, o1). For each token, the CTAs whose
+    // partials hold it (ascending); each (token, row) pair is summed over that
+    // list by P threads taking consecutive parts of it (a part's loads all in
+    // flight, then added in order), then the P part sums in order.
     const int o0 = (int)((uint32_t)H * blockIdx.x / gridDim.x), o1 = (int)((uint32_t)H * (blockIdx.x + 1) / gridDim.x);
-    const int nrow = o1 - o0;
-    const int cpw = ((int)gridDim.x + kCW - 1) / kCW;
-    const int cb = warp * cpw, ce = ::min((int)gridDim.x, cb + cpw);
-    for (int rl = lane; rl < nrow; rl += 32) {
-      for (int t = 0; t < T; ++t) {
-        float v = 0.f;
-        for (int c = cb; c < ce; c += kRedBatch) {  // the batch's loads all in flight, then summed in order
-          float pv[kRedBatch];
-#pragma unroll
-          for (int q = 0; q < kRedBatch; ++q)
-            pv[q] = (c + q < ce && ((s_pm[c + q] >> t) & 1u))
-                        ? __ldcg(a.partial + ((size_t)(c + q) * T + t) * H + o0 + rl)
-                        : 0.f;
-#pragma unroll
-          for (int q = 0; q < kRedBatch; ++q) v += pv[q];
-        }
-        red[((size_t)warp * T + t) * nrow + rl] = v;
+    const int nrow = o1 - o0, pairs = T * nrow;
+    const int P = ::max(1, ::min(kCW, kCT / ::max(1, pairs)));
+    float* red = reinterpret_cast<float*>(ring);                       // [P][pairs]: P pairs <= max(kCT, pairs)
+    int* lists = reinterpret_cast<int*>(ring) + ::max(kCT, pairs);     // [T][grid]
+    __shared__ int s_len[kMaxDecodeT];
+    for (int t = warp; t < T; t += kCW) {  // a warp per token: its CTAs by ballot, ascending
+      int n = 0;
+      for (int c0 = 0; c0 < (int)gridDim.x; c0 += 32) {
+        const int c = c0 + lane;
+        const bool has = c < (int)gridDim.x && ((s_pm[c] >> t) & 1u);
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, has);
+        if (has) lists[t * gridDim.x + n + __popc(bal & ((1u << lane) - 1u))] = c;
+        n += __popc(bal);
       }
+      if (lane == 0) s_len[t] = n;
     }
     consumer_sync();
-    for (int i = tid; i < T * nrow; i += kCT) {
+    for (int i = tid; i < P * pairs; i += kCT) {
+      const int part = i / pairs, pr = i - part * pairs;
+      const int t = pr / nrow, rl = pr - t * nrow;
+      const int len = s_len[t], q0 = len * part / P, q1 = len * (part + 1) / P;
+      const int* lt = lists + t * gridDim.x;
+      float v = 0.f;
+      for (int q = q0; q < q1; q += kRedBatch) {
+        float pv[kRedBatch];
+#pragma unroll
+        for (int j = 0; j < kRedBatch; ++j)
+          pv[j] = q + j < q1 ? __ldcg(a.partial + ((size_t)lt[q + j] * T + t) * H + o0 + rl) : 0.f;
+#pragma unroll
+        for (int j = 0; j < kRedBatch; ++j) v += pv[j];
+      }
+      red[part * pairs + pr] = v;
+    }
+    consumer_sync();
+    for (int i = tid; i < pairs; i += kCT) {
       const int t = i / nrow, rl = i - t * nrow;
       float v = 0.f;
-#pragma unroll
-      for (int w = 0; w < kCW; ++w) v += red[((size_t)w * T + t) * nrow + rl];
+      for (int part = 0; part < P; ++part) v += red[part * pairs + i];
       a.out[(size_t)t * H + o0 + rl] = __float2bfloat16_rn(v);
     }
   }
-  __syncthreads();
+  if (kMulti) {
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0)
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(s_tmem), "r"(kTmemCols) : "memory");
+  } else {
+    __syncthreads();
+  }
 }
 
 // The grid-wide wait needs every CTA resident: the grid is one CTA per SM
@@ -654,14 +774,16 @@ cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfl
   a.off_info = xb;
   a.off_acc = a.off_info + align128((uint32_t)(T * (H / 16) * 8));
   a.off_h = a.off_acc + (multi ? 0u : align128((uint32_t)H * 4u));
-  a.off_ring = a.off_h + align128((uint32_t)(2 * tcap * kChunk * 4));
+  a.off_hp = a.off_h + align128((uint32_t)(2 * tcap * kChunk * 4));
+  a.off_ring = a.off_hp + (multi ? align128((uint32_t)(tcap * sizeof(HPlanes))) : 0u);
   const int64_t ring_bytes = (int64_t)g_smem_optin - a.off_ring - 256;
   a.stages = (int)std::min<int64_t>(kMaxStages, ring_bytes / a.stage_bytes);
   if (a.stages < 2) return cudaErrorInvalidConfiguration;
   const int grid = h->num_sms;
   // the ring also holds the logits while routing and the sums at the end
   if (grid > kMaxGrid) return cudaErrorInvalidConfiguration;
-  const uint32_t need_end = (uint32_t)(kCW * T * ((H + grid - 1) / grid) * 4);
+  // the final sums: part sums (at most max(kCT, T rows) floats), then the per-token CTA lists
+  const uint32_t need_end = (uint32_t)((std::max(kCT, T * ((H + grid - 1) / grid)) + T * grid) * 4);
   if ((uint32_t)a.stages * a.stage_bytes < std::max<uint32_t>(need_end, (uint32_t)(T * h->cfg.E * 4)))
     return cudaErrorInvalidConfiguration;
   if (h->test_grid_timeouts > 0) {  // test hook: this call's grid-wide wait cannot be met and gives up fast

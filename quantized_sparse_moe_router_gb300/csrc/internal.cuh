@@ -297,6 +297,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   return mbar_wait_slow(bar, parity);
 }
 
+// Ordering of tensor-core (tcgen05) operations around thread synchronisation.
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
 // One bulk asynchronous copy global -> shared (16-byte aligned, size % 16 == 0),
 // completion counted in bytes on `bar`.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {

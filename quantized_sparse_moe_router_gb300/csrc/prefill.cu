@@ -22,15 +22,14 @@
 // tokens are B (N = the tile's rows rounded up to 16; K-major bf16 in shared
 // memory, 128-byte swizzle, loaded by TMA). So the bf16 weights never pass
 // through shared memory, and a partial token tile costs only the MMA columns
-// it uses. Two shapes of the kernel: token tiles of up to 192 rows against
-// one 128-row weight block per CTA, and the tiles of at most 64 rows (an
-// expert's only or last tile) against two blocks per CTA.
+// it uses. Three shapes of the kernel, by the rows of the token tile (up to
+// 192, 96 or 64), against one or two 128-row weight blocks per CTA.
 //
-// One persistent CTA per SM (pairs share each token tile by TMA multicast),
-// 15 warps: 0-3 epilogue (TMEM lane quarters), 4 TMA producer, 5 MMA issuer
-// (and TMEM owner), 6-13 dequantisers (two groups of four, one per lane
-// quarter, taking alternate stages; a thread converts the 64 codes of its
-// weight row in the stage), 14 the second MMA issuer of the two-block shape.
+// One persistent CTA per SM, 15 warps: 0-3 epilogue (TMEM lane quarters), 4
+// TMA producer, 5 MMA issuer (and TMEM owner), 6-13 dequantisers (two groups
+// of four, one per lane quarter, taking alternate stages; a thread converts
+// the 64 codes of its weight row in each block of the stage), 14 the second
+// MMA issuer of the two-block shapes.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -149,8 +148,6 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                : "memory");
 }
 
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
@@ -179,6 +176,7 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
       : "memory");
 }
+
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -340,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------ dequantisers: int8 x scale -> bf16 -> TMEM (A)
     // Two groups of four warps (one per TMEM lane quarter) take alternate
     // stages, so the conversion of one stage overlaps the next; a thread
-    // converts the 64 codes (two Q8_0 blocks) of its row.
+    // converts the 64 codes (two Q8_0 blocks) of its row in each weight block.
     const int quarter = warp & 3, group = (warp - kDeqWarp0) >> 2;
     const int r = quarter * 32 + lane;  // weight row of the tile = TMEM lane
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
@@ -804,7 +802,7 @@ cudaError_t configure_prefill_kernels() {
 }
 
 cudaError_t prepare_prefill(Handle* h) {
-  const uint64_t H = h->cfg.H, I = h->cfg.I, EU = h->EU, R = h->rows_max;
+  const uint64_t H = h->cfg.H, I = h->cfg.I, R = h->rows_max;
   PrefillMaps* m = new PrefillMaps();
   h->maps = m;
   cudaError_t e = encode_2d(&m->a_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, h->xperm, H, R, H * 2, BK, Shape<kBig>::XBox,
