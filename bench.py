@@ -17,9 +17,11 @@ once as a CUDA graph and replayed. value = tokens x layer-calls per second.
 Every workload cycles more layers than L2 holds (no flush needed). Timing: CUDA
 events around K graph replays, repeated 5 times, median.
 
-The path does not shard: this build runs on one GPU (its prefill GEMM shares
-token tiles between paired SMs by TMA multicast within the GPU), so --gpus N
-with N > 1 reports that it is unavailable instead of running.
+The path does not shard: under torch.distributed.run with N processes (one
+per GPU) every rank runs an independent replica of the same workload on its
+own GPU (weak scaling; the only collectives are the barriers around the timed
+region and the max over ranks of its time). --gpus N > 1 without such a launch
+reports that it is unavailable.
 
 --impl reference times the fp64 oracle on the host cores instead (rank 0),
 on a bounded sample of the same workload.
@@ -583,16 +585,22 @@ def main():
         if rank == 0:
             print(json.dumps(run_reference(args)), flush=True)
         return
-    if world > 1 or args.gpus > 1:
-        if rank == 0:
-            print(json.dumps({"metric": metric_name(workload_of(args, args.workload or HEADLINE)),
-                              "n_gpus": max(world, args.gpus), "unavailable":
-                              "one GPU only: the step does not shard (replicas only), and this build's prefill "
-                              "GEMM shares token tiles between paired SMs by TMA multicast, which is kept to "
-                              "1-GPU runs"}), flush=True)
+    if args.gpus > 1 and world == 1:
+        print(json.dumps({"metric": metric_name(workload_of(args, args.workload or HEADLINE)),
+                          "n_gpus": args.gpus, "unavailable":
+                          "replicas only: launch one process per GPU with torch.distributed.run"}), flush=True)
         return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     res = run_fw(args, rank, world, local_rank)
-    print(json.dumps(res), flush=True)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
 
 
 if __name__ == "__main__":

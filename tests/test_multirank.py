@@ -53,3 +53,16 @@ def test_reference_arm_prints_on_rank0_only():
     d = json.loads(lines[0])
     assert d["impl"] == "reference" and d["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] == 0
     assert d["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_gpus_above_one_without_a_launcher_is_reported_unavailable():
+    """--gpus N > 1 run as one process (no torch.distributed.run): one JSON
+    line saying the replicas need one process per GPU, exit 0, no GPU work."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--workload", "tiny"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT,
+                       env={k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")})
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2 and "unavailable" in d and "replicas" in d["unavailable"]
