@@ -14,8 +14,8 @@
 //             D = deq(W_gu rows) . X_tile^T; epilogue h = SiLU(gate) * up
 //             -> hbuf (bf16, grouped order)
 //   GEMM 2:   per (token tile, 128 output features):
-//             Yp = gate_of_row * (deq(W_down rows) . h_tile^T) -> yp (bf16)
-//   combine:  out[t] = sum_j Yp[inv[t*k + j]] (+ shared row), fixed order
+//             Yp = deq(W_down rows) . h_tile^T -> yp (bf16)
+//   combine:  out[t] = sum_j g[t, j] Yp[inv[t*k + j]] (+ shared row), fixed order
 //
 // The weights are the MMA's A operand (M = 128 rows, read from tensor
 // memory, written there by the dequantising warps with tcgen05.st); the
@@ -81,14 +81,13 @@ struct Shape {
   static_assert(Stages >= 4 && Stages % 2 == 0, "the two dequantising groups own alternate stages");
 };
 
-enum Epi { kEpiSwiGLU = 0, kEpiDownScale = 1 };
+enum Epi { kEpiSwiGLU = 0, kEpiDown = 1 };
 
 struct GemmArgs {
   const uint8_t* wt;      // the projection's weight tiles [EU][n_mb][K/64]
   const int4* minfo;      // per token tile: (expert, first grouped row, valid rows, 0)
   const int32_t* n_mtiles; // number of tiles in minfo (written by the scan kernel)
   const Meta* meta;
-  const float* row_gate;  // kEpiDownScale
   __nv_bfloat16* outp;    // hbuf (SwiGLU, [rows][I]) or yp ([rows][H])
   int K;                  // reduction length (H or I)
   int prows;              // weight rows per expert in the code plane (2I or H)
@@ -421,11 +420,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 *reinterpret_cast<uint32_t*>(a.outp + (int64_t)(mi.y + c) * a.out_cols + i) = pack_bf16x2(hv, hn);
             }
           } else {
+            // (the row gates are applied in the combine)
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
               const bool valid = c0 + j < mi.z;
-              const float g = valid ? __ldg(a.row_gate + mi.y + c0 + j) : 0.f;
-              const float y = g * v[j];
+              const float y = v[j];
               const float yn = __shfl_down_sync(0xFFFFFFFFu, y, 1);
               if ((lane & 1) == 0 && valid && prow < a.out_cols)
                 *reinterpret_cast<uint32_t*>(a.outp + (int64_t)(mi.y + c0 + j) * a.out_cols + prow) = pack_bf16x2(y, yn);
@@ -714,11 +713,14 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const __nv_bfl
   }
 }
 
-// out[t] = sum over the token's slots j (ascending) of Yp[inv[t*k + j]], then
-// the shared expert's row; fp32 sum, one bf16 rounding. One CTA per token,
+// out[t] = sum over the token's slots j (ascending) of g[t, j] Yp[inv[t*k + j]],
+// then the shared expert's row (weight 1); fp32 sum, one bf16 rounding. (The
+// gate is applied here rather than in the down GEMM's epilogue, which is on
+// the GEMM's critical path.) One CTA per token,
 // a thread per 16-byte chunk (all of a chunk's k + S row loads in flight).
 __global__ void __launch_bounds__(kRowThreads) combine_kernel(const __nv_bfloat16* __restrict__ yp,
-                                                              const int32_t* __restrict__ inv, int T, int k, int S,
+                                                              const int32_t* __restrict__ inv,
+                                                              const float* __restrict__ gates, int T, int k, int S,
                                                               int H, __nv_bfloat16* __restrict__ out) {
   const int chunks = H / 8;
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
@@ -729,14 +731,15 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(const __nv_bfloat1
 #pragma unroll 4
       for (int j = 0; j < k + S; ++j) {
         const int slot = j < k ? t * k + j : T * k + t;
+        const float g = j < k ? __ldg(gates + slot) : 1.0f;
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(yp + (int64_t)inv[slot] * H) + c);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           float lo, hi;
           bf16x2_to_f32(w[q], lo, hi);
-          acc[2 * q] += lo;
-          acc[2 * q + 1] += hi;
+          acc[2 * q] = fmaf(g, lo, acc[2 * q]);
+          acc[2 * q + 1] = fmaf(g, hi, acc[2 * q + 1]);
         }
       }
       uint4 o;
@@ -791,11 +794,11 @@ cudaError_t configure_prefill_kernels() {
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   cudaError_t e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiSwiGLU, kBig>);
-  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDownScale, kBig>);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDown, kBig>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiSwiGLU, kMid>);
-  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDownScale, kMid>);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDown, kMid>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiSwiGLU, kSmall>);
-  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDownScale, kSmall>);
+  if (e == cudaSuccess) e = allow_max_dynamic_smem(grouped_gemm_kernel<kEpiDown, kSmall>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_mma_kernel<8>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_mma_kernel<16>);
   return e;
@@ -887,7 +890,6 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
   GemmArgs g;
   g.wt = h->t_gu;
   g.meta = h->meta;
-  g.row_gate = h->row_gate;
   g.outp = static_cast<__nv_bfloat16*>(h->hbuf);
   g.K = H;
   g.prows = 2 * I;
@@ -918,20 +920,20 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
   g.out_cols = H;
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN, s);
-    if (err == cudaSuccess) err = launch_gemm<kEpiDownScale, kBig>(h->maps->a_h, lists(g, kBig), h->num_sms, s);
+    if (err == cudaSuccess) err = launch_gemm<kEpiDown, kBig>(h->maps->a_h, lists(g, kBig), h->num_sms, s);
   }
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN_MID, s);
-    if (err == cudaSuccess) err = launch_gemm<kEpiDownScale, kMid>(h->maps->a_hm, lists(g, kMid), h->num_sms, s);
+    if (err == cudaSuccess) err = launch_gemm<kEpiDown, kMid>(h->maps->a_hm, lists(g, kMid), h->num_sms, s);
   }
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN_SMALL, s);
-    if (err == cudaSuccess) err = launch_gemm<kEpiDownScale, kSmall>(h->maps->a_hs, lists(g, kSmall), h->num_sms, s);
+    if (err == cudaSuccess) err = launch_gemm<kEpiDown, kSmall>(h->maps->a_hs, lists(g, kSmall), h->num_sms, s);
   }
   if (err != cudaSuccess) return err;
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_COMBINE, s);
-    combine_kernel<<<(unsigned)std::min(T, h->num_sms * 16), kRowThreads, 0, s>>>(h->yp, h->inv, T, k, S, H, out);
+    combine_kernel<<<(unsigned)std::min(T, h->num_sms * 16), kRowThreads, 0, s>>>(h->yp, h->inv, h->gates, T, k, S, H, out);
   }
   return cudaGetLastError();
 }
