@@ -61,7 +61,7 @@ constexpr int kMaxStages = 16;
 constexpr int kChunk = 16;                 // units of I per chunk (one 16-byte segment of a down row)
 constexpr int kRowsMulti = 4;              // several tokens: down rows per consumer thread (H <= 2048)
 constexpr int kMaxHMulti = kRowsMulti * kCT;
-constexpr int kMaxHOne = 16384;            // one token: the partial output row fits in shared memory
+constexpr int kMaxHOne = 14336;            // one token: x planes, the fp32 partial row and two ring stages fit in shared memory
 constexpr int kDnRowsMax = 2048;           // down rows per stage at most
 constexpr uint32_t kConsumerBarrier = 1;   // named barrier of the 16 consumer warps
 constexpr uint32_t kStageTarget = 36 * 1024;

@@ -219,6 +219,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_abort;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the next GEMM of the call may start on SMs this grid leaves (its tiles
+  // are independent of this grid's; see launch_gemm)
+  pdl_launch_dependents();
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* base = smem_raw + pad;
   uint8_t* sX = base;                            // [kStages][BN rows][128 B], 128B swizzle
@@ -413,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const float mine = gate_lane ? v[j] : v[16 + j];
               const float other = __shfl_xor_sync(0xFFFFFFFFu, gate_lane ? v[16 + j] : v[j], 2);
               const float g = gate_lane ? mine : other, u = gate_lane ? other : mine;
-              const float hv = g * __frcp_rn(1.0f + __expf(-g)) * u;
+              const float hv = __fdividef(g, 1.0f + __expf(-g)) * u;  // h is rounded to bf16 next
               const float hn = __shfl_xor_sync(0xFFFFFFFFu, hv, 1);
               const int c = c0 + jt + j;
               if ((lane & 1) == 0 && c < mi.z && i < a.out_cols)
@@ -777,10 +780,26 @@ unsigned grid_for(int64_t n, int threads, int cap) {
 
 
 template <int EPI, int SH>
-cudaError_t launch_gemm(const CUtensorMap& mb, const GemmArgs& g, int num_sms, cudaStream_t s) {
-  // one persistent CTA per SM (its shared memory admits no second)
-  grouped_gemm_kernel<EPI, SH><<<(unsigned)num_sms, kThreads, Shape<SH>::SmemBytes, s>>>(mb, g);
-  return cudaGetLastError();
+cudaError_t launch_gemm(const CUtensorMap& mb, const GemmArgs& g, int num_sms, bool overlap, cudaStream_t s) {
+  // One persistent CTA per SM (its shared memory admits no second). With
+  // `overlap` the launch is a programmatic dependent of the previous GEMM of
+  // the same projection: its CTAs take the SMs that grid's CTAs leave while
+  // the last of them still run (their tiles and outputs are disjoint, and
+  // nothing here reads what the previous grid writes, so there is no wait);
+  // the first GEMM of each projection is an ordinary launch, which starts
+  // only after all earlier work of the stream (the gather, or all gate/up
+  // GEMMs) has completed.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)num_sms);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Shape<SH>::SmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = overlap ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<EPI, SH>, mb, g);
 }
 
 }  // namespace
@@ -902,15 +921,15 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
   };
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP, s);
-    err = launch_gemm<kEpiSwiGLU, kBig>(h->maps->a_x, lists(g, kBig), h->num_sms, s);
+    err = launch_gemm<kEpiSwiGLU, kBig>(h->maps->a_x, lists(g, kBig), h->num_sms, false, s);
   }
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP_MID, s);
-    if (err == cudaSuccess) err = launch_gemm<kEpiSwiGLU, kMid>(h->maps->a_xm, lists(g, kMid), h->num_sms, s);
+    if (err == cudaSuccess) err = launch_gemm<kEpiSwiGLU, kMid>(h->maps->a_xm, lists(g, kMid), h->num_sms, true, s);
   }
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP_SMALL, s);
-    if (err == cudaSuccess) err = launch_gemm<kEpiSwiGLU, kSmall>(h->maps->a_xs, lists(g, kSmall), h->num_sms, s);
+    if (err == cudaSuccess) err = launch_gemm<kEpiSwiGLU, kSmall>(h->maps->a_xs, lists(g, kSmall), h->num_sms, true, s);
   }
   g.outp = h->yp;
   g.wt = h->t_d;
@@ -920,15 +939,15 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
   g.out_cols = H;
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN, s);
-    if (err == cudaSuccess) err = launch_gemm<kEpiDown, kBig>(h->maps->a_h, lists(g, kBig), h->num_sms, s);
+    if (err == cudaSuccess) err = launch_gemm<kEpiDown, kBig>(h->maps->a_h, lists(g, kBig), h->num_sms, false, s);
   }
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN_MID, s);
-    if (err == cudaSuccess) err = launch_gemm<kEpiDown, kMid>(h->maps->a_hm, lists(g, kMid), h->num_sms, s);
+    if (err == cudaSuccess) err = launch_gemm<kEpiDown, kMid>(h->maps->a_hm, lists(g, kMid), h->num_sms, true, s);
   }
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_DOWN_SMALL, s);
-    if (err == cudaSuccess) err = launch_gemm<kEpiDown, kSmall>(h->maps->a_hs, lists(g, kSmall), h->num_sms, s);
+    if (err == cudaSuccess) err = launch_gemm<kEpiDown, kSmall>(h->maps->a_hs, lists(g, kSmall), h->num_sms, true, s);
   }
   if (err != cudaSuccess) return err;
   {

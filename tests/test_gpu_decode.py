@@ -82,6 +82,10 @@ DECODE_CASES = [
     ("tiny", dict(T=1, H=2304, S=1)),          # one token, H past the several-token limit: two down stages
     ("tiny", dict(T=1, H=4160, I=192)),        # one token, three down stages (4160 = 3 x 1387 -> 1392-row stages)
     ("tiny", dict(T=2, H=2304)),               # several tokens with H > 2048: the prefill path takes them
+    ("tiny", dict(T=1, H=14336, I=128)),       # one token at the largest H the decode kernel takes (two ring stages)
+    ("tiny", dict(T=1, H=16384, I=128)),       # one token past it: the prefill path takes it
+    ("tiny", dict(T=4, E=32, k=16)),           # the largest k
+    ("tiny", dict(T=16, E=32, k=16, S=1)),     # largest k and T together, with a shared expert
     ("dec1", {}),
     ("dec16", {}),
     ("large1", {}),

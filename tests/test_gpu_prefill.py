@@ -69,6 +69,8 @@ CASES = [
     ("tiny", dict(T=700, k=2, I=192, S=1)),             # large remainders (> 64 rows), shared expert, odd blocks
     ("tiny", dict(T=330, k=2)),                         # about 82 rows per expert: too few mid tiles for their own launch
     ("tiny", dict(T=470, k=2, S=1)),                    # about 117 rows: big remainders; shared: 2 big + mid
+    ("tiny", dict(T=40, E=32, k=16)),                   # the largest k (tensor-core router, 16-long top-k lists)
+    ("tiny", dict(T=300, E=256, k=8)),                  # the largest E: 256 experts, most with a handful of rows
 ]
 
 
