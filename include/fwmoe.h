@@ -66,7 +66,10 @@ typedef struct {
   int32_t k;            /* experts per token, 1..min(E, 16) */
   int32_t n_shared;     /* always-on shared experts: 0 or 1 */
   int32_t T_max;        /* largest T any call on this handle may pass (sizes the workspace) */
-  int32_t decode_T_max; /* T <= this takes the decode (grouped GEMV) path; 0 = 16; at most 16 */
+  int32_t decode_T_max; /* T <= this takes the decode (grouped GEMV) path; 0 = 16; at most 16.
+                         * The decode kernel holds a call's x in shared memory: one token
+                         * up to H = 14336, several up to H = 2048; calls past that take
+                         * the prefill path whatever their T. */
 } fw_moe_config;
 
 typedef struct { /* all DEVICE pointers, read only during fw_moe_init */
