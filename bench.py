@@ -457,6 +457,10 @@ def run_fw(args, rank, world, local_rank):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
         cpu = cpu_baseline(w, args.cpu_seconds)
+        # the 4096-token prefill's baseline on its first 256 tokens (one call, about 25 s)
+        pre = "pre4096" if "pre4096" in results else None
+        if pre:
+            results[pre]["cpu_baseline"] = cpu_baseline_tokens(workload_of(args, pre), 256)
     line = {
         "metric": metric_name(w), "value": res["value"], "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
@@ -544,6 +548,17 @@ def cpu_baseline(w, seconds):
             "sample": f"{calls} route+FFN calls of the first {n_tok} token(s) of the workload's hidden batch, "
                       f"cycling {len(prepared)} of its layers ({el:.1f} s of single-thread fp64 work; expert "
                       f"quantisation untimed)",
+            "host_cores": os.cpu_count()}
+
+
+def cpu_baseline_tokens(w, n_tok):
+    """The oracle on one call of the workload's first n_tok tokens (one layer)."""
+    n_tok = min(n_tok, w.T)
+    xs, prepared = oracle_prepare(w, n_tok, n_layers=1)
+    tokens, el, calls = oracle_sample(w, 0.0, xs, prepared, max_calls=1)
+    return {"value": round(tokens / el, 3), "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"one route+FFN call of the first {n_tok} tokens of the workload's hidden batch "
+                      f"({el:.1f} s of single-thread fp64 work; expert quantisation untimed)",
             "host_cores": os.cpu_count()}
 
 
