@@ -9,6 +9,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "../../include/fwmoe.h"
 
 namespace fw {
@@ -321,6 +323,27 @@ __device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
 // prologue, and wait for the previous kernel's results.
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launch as a programmatic dependent of the previous kernel in the stream:
+// it may start while that kernel's last CTAs still run. Every kernel launched
+// so waits (pdl_wait) before it reads or writes global memory, so it
+// completes only after its predecessor has -- a chain of such kernels keeps
+// the stream's order for all that came before.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                             Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 r;

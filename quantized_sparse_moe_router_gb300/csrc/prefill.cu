@@ -93,6 +93,7 @@ struct GemmArgs {
   int prows;              // weight rows per expert in the code plane (2I or H)
   int n_mb;               // ceil(prows / 128): weight tiles per expert and K step
   int out_cols;           // I (SwiGLU) or H
+  int wait_prev;          // launched as a dependent that reads its predecessor's output (the gather's)
 };
 
 // ------------------------------------------------------------- PTX helpers
@@ -220,7 +221,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   // the next GEMM of the call may start on SMs this grid leaves (its tiles
-  // are independent of this grid's; see launch_gemm)
+  // are independent of this grid's; see launch_gemm) -- once this grid's own
+  // inputs are complete
+  if (a.wait_prev) pdl_wait();
   pdl_launch_dependents();
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* base = smem_raw + pad;
@@ -506,6 +509,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
   __shared__ float s_bias[kRMaxE];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int E = a.E, k = a.k, t0 = blockIdx.x * kRM;
+  pdl_launch_dependents();  // the select kernel may start early: it waits for this grid before reading
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* sX = smem_raw + pad;                 // [kRStages][128 tokens][128 B]
   const int BR = E < kRPassE ? E : kRPassE;      // W_r rows per pass
@@ -652,23 +656,28 @@ __global__ void __launch_bounds__(kRThreads, 1)
 constexpr int kSelTokens = 32;
 __global__ void __launch_bounds__(kSelTokens * 32) route_select_kernel(RouteMmaArgs a, int ks) {
   __shared__ int s_cnt[kRMaxE];
+  pdl_wait();  // the partial logits
+  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, E = a.E, k = a.k;
   const int t = blockIdx.x * kSelTokens + warp;
   for (int i = threadIdx.x; i < E; i += kSelTokens * 32) s_cnt[i] = 0;
   __syncthreads();
   if (t < a.T) {
+    // the K splits summed in order, then the bias; a split's loads for all of
+    // the lane's experts in flight together
     float zl[kMaxEPerLane];
 #pragma unroll
-    for (int m = 0; m < kMaxEPerLane; ++m) {
-      const int e = lane + 32 * m;
-      float z = -INFINITY;
-      if (e < E) {
-        z = 0.f;
-        for (int q = 0; q < ks; ++q) z += __ldg(a.zpart + ((size_t)q * a.T + t) * E + e);
-        z += a.bias[e];
-      }
-      zl[m] = z;
+    for (int m = 0; m < kMaxEPerLane; ++m) zl[m] = 0.f;
+    for (int q = 0; q < ks; ++q) {
+      const float* zq = a.zpart + ((size_t)q * a.T + t) * E;
+      float v[kMaxEPerLane];
+#pragma unroll
+      for (int m = 0; m < kMaxEPerLane; ++m) v[m] = lane + 32 * m < E ? __ldg(zq + lane + 32 * m) : 0.f;
+#pragma unroll
+      for (int m = 0; m < kMaxEPerLane; ++m) zl[m] += v[m];
     }
+#pragma unroll
+    for (int m = 0; m < kMaxEPerLane; ++m) zl[m] = lane + 32 * m < E ? zl[m] + a.bias[lane + 32 * m] : -INFINITY;
     int id;
     float zv;
     warp_topk(zl, E, k, lane, &id, &zv);
@@ -708,6 +717,8 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const __nv_bfl
                                                                   const int32_t* __restrict__ row_token, int rows,
                                                                   int H, __nv_bfloat16* __restrict__ xperm) {
   const int chunks = H / 8, lane = threadIdx.x & 31;
+  pdl_wait();  // the scatter's row tokens
+  pdl_launch_dependents();
   const int nw = gridDim.x * (kRowThreads / 32);
   for (int pos = blockIdx.x * (kRowThreads / 32) + (threadIdx.x >> 5); pos < rows; pos += nw) {
     const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)row_token[pos] * H);
@@ -782,13 +793,13 @@ unsigned grid_for(int64_t n, int threads, int cap) {
 template <int EPI, int SH>
 cudaError_t launch_gemm(const CUtensorMap& mb, const GemmArgs& g, int num_sms, bool overlap, cudaStream_t s) {
   // One persistent CTA per SM (its shared memory admits no second). With
-  // `overlap` the launch is a programmatic dependent of the previous GEMM of
-  // the same projection: its CTAs take the SMs that grid's CTAs leave while
-  // the last of them still run (their tiles and outputs are disjoint, and
-  // nothing here reads what the previous grid writes, so there is no wait);
-  // the first GEMM of each projection is an ordinary launch, which starts
-  // only after all earlier work of the stream (the gather, or all gate/up
-  // GEMMs) has completed.
+  // `overlap` the launch is a programmatic dependent of the kernel before it:
+  // its CTAs take the SMs that grid's CTAs leave while the last of them still
+  // run. The mid and small GEMMs of a projection follow the GEMM before them
+  // and read nothing it writes (disjoint tiles and outputs), so they do not
+  // wait; the gate/up big-tile GEMM follows the gather and waits for it
+  // (wait_prev) before anything else. The down big-tile GEMM is an ordinary
+  // launch: it reads the h of all three gate/up GEMMs.
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)num_sms);
   cfg.blockDim = dim3(kThreads);
@@ -891,8 +902,11 @@ cudaError_t launch_route_prefill_mma(Handle* h, const __nv_bfloat16* x, int T, i
     route_mma_kernel<8><<<grid, kRThreads, smem, s>>>(map_x, h->maps->w3, a);
   else
     route_mma_kernel<16><<<grid, kRThreads, smem, s>>>(map_x, h->maps->w3, a);
-  if (ks > 1) route_select_kernel<<<(unsigned)((T + kSelTokens - 1) / kSelTokens), kSelTokens * 32, 0, s>>>(a, ks);
-  return cudaGetLastError();
+  cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess && ks > 1)
+    err = launch_dependent(route_select_kernel, dim3((unsigned)((T + kSelTokens - 1) / kSelTokens)),
+                           dim3(kSelTokens * 32), 0, s, a, ks);
+  return err;
 }
 
 cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bfloat16* out, cudaStream_t s) {
@@ -902,9 +916,10 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
   cudaError_t err;
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_GATHER, s);
-    gather_rows_kernel<<<grid_for(rows, kRowThreads / 32, h->num_sms * 8), kRowThreads, 0, s>>>(x, h->row_token,
-                                                                                               rows, H, h->xperm);
+    err = launch_dependent(gather_rows_kernel, dim3(grid_for(rows, kRowThreads / 32, h->num_sms * 8)),
+                           dim3(kRowThreads), 0, s, x, (const int32_t*)h->row_token, rows, H, h->xperm);
   }
+  if (err != cudaSuccess) return err;
   // each projection: the big tiles, the mid ones, then the small ones
   GemmArgs g;
   g.wt = h->t_gu;
@@ -914,6 +929,7 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
   g.prows = 2 * I;
   g.n_mb = (2 * I + BM - 1) / BM;
   g.out_cols = I;
+  g.wait_prev = 0;
   auto lists = [&](GemmArgs base, int shape) {
     base.minfo = shape == kBig ? h->minfo : (shape == kMid ? h->minfo_m : h->minfo_s);
     base.n_mtiles = shape == kBig ? &h->meta->n_mtiles : (shape == kMid ? &h->meta->n_midtiles : &h->meta->n_stiles);
@@ -921,7 +937,9 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
   };
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP, s);
-    err = launch_gemm<kEpiSwiGLU, kBig>(h->maps->a_x, lists(g, kBig), h->num_sms, false, s);
+    GemmArgs gb = lists(g, kBig);
+    gb.wait_prev = 1;
+    err = launch_gemm<kEpiSwiGLU, kBig>(h->maps->a_x, gb, h->num_sms, true, s);
   }
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_GATEUP_MID, s);

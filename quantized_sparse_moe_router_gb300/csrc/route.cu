@@ -280,6 +280,8 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(RouteArgs a, i
   __shared__ int s_nbm[kMaxE + 2];  // big + mid tiles before the expert (mid tiles merged)
   __shared__ int s_merge;
   __shared__ int s_part[kScanThreads];  // [part][expert]: the part's count (pass 1)
+  pdl_wait();  // the per-tile counts of the router
+  pdl_launch_dependents();
   const int E = a.E, EU = E + a.S, T = a.T, tid = threadIdx.x, lane = tid & 31;
   // thread (part, expert): the experts' per-tile counts are summed by P
   // threads each over consecutive tile ranges (a few batched loads instead
@@ -402,6 +404,8 @@ __global__ void __launch_bounds__(kScanThreads) route_scan_kernel(RouteArgs a, i
 __global__ void __launch_bounds__(256) route_scatter_kernel(RouteArgs a, const int32_t* hist) {
   __shared__ uint32_t s_mask[kMaxE];
   __shared__ int s_ids[kRouteTileM * kMaxK];
+  pdl_wait();  // the scan's offsets and per-tile bases
+  pdl_launch_dependents();
   const int tid = threadIdx.x, T = a.T, k = a.k, E = a.E;
   const int t0 = blockIdx.x * kRouteTileM;
   const int nt = min(kRouteTileM, T - t0);
@@ -524,13 +528,15 @@ cudaError_t launch_route_prefill(Handle* h, const __nv_bfloat16* x, int T, int32
     const int64_t mb_gu = (2 * (int64_t)h->cfg.I + 127) / 128, mb_d = ((int64_t)h->cfg.H + 127) / 128;
     const int n_mbg = (int)::min((mb_gu + 1) / 2, (mb_d + 1) / 2);
     const int mid_min = (h->num_sms + n_mbg - 1) / n_mbg;
-    route_scan_kernel<<<1, kScanThreads, 0, s>>>(a, h->hist, n_tiles, h->minfo, h->minfo_m, h->minfo_s, mid_min);
+    err = launch_dependent(route_scan_kernel, dim3(1), dim3(kScanThreads), 0, s, a, h->hist, n_tiles, h->minfo,
+                           h->minfo_m, h->minfo_s, mid_min);
   }
+  if (err != cudaSuccess) return err;
   {
     KernelTimer tm(h, FW_KERNEL_ROUTE_SCATTER, s);
-    route_scatter_kernel<<<n_tiles, 256, 0, s>>>(a, h->hist);
+    err = launch_dependent(route_scatter_kernel, dim3(n_tiles), dim3(256), 0, s, a, (const int32_t*)h->hist);
   }
-  return cudaGetLastError();
+  return err;
 }
 
 cudaError_t launch_get_permutation(const Handle* h, int T, int32_t* offsets, int32_t* perm, int32_t* inv,
