@@ -67,7 +67,10 @@ constexpr uint32_t kConsumerBarrier = 1;   // named barrier of the 16 consumer w
 constexpr uint32_t kStageTarget = 36 * 1024;
 constexpr int kRedBatch = 10;              // partial loads in flight per lane in the final sums
 constexpr int kMaxGrid = 256;              // CTAs (one per SM) the per-CTA token masks have room for
-constexpr int kChunkCost = 4;              // several tokens: a chunk's weight stream, in units of one token's arithmetic
+#ifndef FW_CHUNK_COST
+#define FW_CHUNK_COST 4
+#endif
+constexpr int kChunkCost = FW_CHUNK_COST;  // several tokens: a chunk's weight stream, in units of one token's arithmetic
 
 // The chunk's h of one token as 16-bit fixed point (see h16_to_planes).
 struct HPlanes {
@@ -295,8 +298,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (warp != kProducer) {
-    // x was written before the router kernel started (that launch waits for
-    // the whole stream): staged while the router still runs
+    // x is complete: the router lets this grid launch only after everything
+    // before it in the stream has completed. Staged while the router still runs.
     for (int c = tid; c < T * nseg; c += kCT) {
       const uint4* src = reinterpret_cast<const uint4*>(a.x) + 2 * c;
       uint4 hi, lo;
@@ -621,6 +624,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       }
     }
     consumer_sync();
+    // every partial is written: the next call's router may launch (it waits
+    // for this grid's completion before touching memory)
+    pdl_launch_dependents();
     // ---- this CTA's output rows [o0, o1). For each token, the CTAs whose
     // partials hold it (ascending); each (token, row) pair is summed over that
     // list by P threads taking consecutive parts of it (a part's loads all in

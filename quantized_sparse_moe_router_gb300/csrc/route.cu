@@ -52,7 +52,13 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int e = blockIdx.x;
   const int T = a.T, H = a.H;
-  pdl_launch_dependents();  // the expert kernels wait for this grid's completion before reading
+  // Launched as a programmatic dependent of whatever came before it (the
+  // previous call's expert kernel, typically): wait for it to complete before
+  // touching memory (x may be its output; the grid counter is its own), and
+  // only then let this call's expert kernel start (it stages x before its own
+  // wait for this grid).
+  pdl_wait();
+  pdl_launch_dependents();
   if (blockIdx.x == 0 && tid == 0) {  // fresh grid barrier and chunk tickets for this call's expert kernel
     a.meta->gbar = 0;
     a.meta->chunk_ctr = 0;
@@ -495,8 +501,7 @@ cudaError_t launch_route_decode(Handle* h, const __nv_bfloat16* x, int T, int32_
                                 bool select, cudaStream_t s) {
   RouteArgs a = route_args(h, x, T, ids_out, gates_out);
   KernelTimer tm(h, FW_KERNEL_ROUTE_DECODE, s);
-  route_decode_kernel<<<h->cfg.E, kRouteThreads, 0, s>>>(a, select ? 1 : 0);
-  return cudaGetLastError();
+  return launch_dependent(route_decode_kernel, dim3(h->cfg.E), dim3(kRouteThreads), 0, s, a, select ? 1 : 0);
 }
 
 cudaError_t launch_route_prefill(Handle* h, const __nv_bfloat16* x, int T, int32_t* ids_out, float* gates_out,
