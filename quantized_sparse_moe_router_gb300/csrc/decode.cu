@@ -67,10 +67,16 @@ constexpr uint32_t kConsumerBarrier = 1;   // named barrier of the 16 consumer w
 constexpr uint32_t kStageTarget = 36 * 1024;
 constexpr int kRedBatch = 10;              // partial loads in flight per lane in the final sums
 constexpr int kMaxGrid = 256;              // CTAs (one per SM) the per-CTA token masks have room for
-#ifndef FW_CHUNK_COST
-#define FW_CHUNK_COST 4
+// Several tokens: the cost of a chunk is kChunkCost (its weight stream) plus
+// kTokCost per token of its expert (the arithmetic). Measured at 16 tokens
+// (per call): 1 + 1 n 112.6 us, 2 + n 120.6, 4 + n 135.7, 8 + n 151.1,
+// 0 + n 128.5, 1 + 2 n 117.4, 1 + 4 n 122.0.
+#ifndef FW_GU_UNROLL
+#define FW_GU_UNROLL 1
 #endif
-constexpr int kChunkCost = FW_CHUNK_COST;  // several tokens: a chunk's weight stream, in units of one token's arithmetic
+constexpr int kGuUnroll = FW_GU_UNROLL;
+constexpr int kChunkCost = 1;
+constexpr int kTokCost = 1;
 
 // The chunk's h of one token as 16-bit fixed point (see h16_to_planes).
 struct HPlanes {
@@ -335,13 +341,13 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   }
   if (kMulti) {
     // A chunk costs its weight stream plus its expert's token count of
-    // arithmetic: kChunkCost + n. CTA b takes the chunks whose starting cost
+    // arithmetic: kChunkCost + kTokCost n. CTA b takes the chunks whose starting cost
     // lies in [b C / grid, (b + 1) C / grid), C the total. Prefix costs per
     // expert by one warp (C < 2^32), the bounds by a thread per CTA.
     if (warp == 0) {
       const int nu = r.n_unique, per = (nu + 31) / 32, u0 = lane * per;
       uint32_t run = 0;
-      for (int u = u0; u < ::min(nu, u0 + per); ++u) run += (uint32_t)(kChunkCost + r.u[u].z) * G;
+      for (int u = u0; u < ::min(nu, u0 + per); ++u) run += (uint32_t)(kChunkCost + kTokCost * r.u[u].z) * G;
       uint32_t inc = run;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -351,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       uint32_t p = inc - run;
       for (int u = u0; u < ::min(nu, u0 + per); ++u) {
         s_pref[u] = p;
-        p += (uint32_t)(kChunkCost + r.u[u].z) * G;
+        p += (uint32_t)(kChunkCost + kTokCost * r.u[u].z) * G;
       }
       if (lane == 31) s_pref[nu] = inc;
     }
@@ -367,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       }
       int c = n_ch;
       if (b < (int)grid && r.n_unique > 0) {
-        const uint64_t w = (uint64_t)(kChunkCost + r.u[lo].z) * grid;
+        const uint64_t w = (uint64_t)(kChunkCost + kTokCost * r.u[lo].z) * grid;
         const uint64_t rem = target - s_pref[lo] * grid;
         c = ::min(lo * G + (int)((rem + w - 1) / w), n_ch);
       }
@@ -492,7 +498,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
             const uint8_t* xl = xlo + (size_t)t * H;
             const int2* xi = xinfo + (size_t)t * nseg;
             float ag = 0.f, au = 0.f;
-#pragma unroll(kMulti ? 1 : 2)
+#pragma unroll(kMulti ? kGuUnroll : 2)
             for (int s = lane; s < nseg; s += 32) {
               const uint4 qg = *reinterpret_cast<const uint4*>(grow + s * 16);
               const uint4 qu = *reinterpret_cast<const uint4*>(urow + s * 16);
