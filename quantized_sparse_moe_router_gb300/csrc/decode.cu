@@ -71,10 +71,6 @@ constexpr int kMaxGrid = 256;              // CTAs (one per SM) the per-CTA toke
 // kTokCost per token of its expert (the arithmetic). Measured at 16 tokens
 // (per call): 1 + 1 n 112.6 us, 2 + n 120.6, 4 + n 135.7, 8 + n 151.1,
 // 0 + n 128.5, 1 + 2 n 117.4, 1 + 4 n 122.0.
-#ifndef FW_GU_UNROLL
-#define FW_GU_UNROLL 1
-#endif
-constexpr int kGuUnroll = FW_GU_UNROLL;
 constexpr int kChunkCost = 1;
 constexpr int kTokCost = 1;
 
@@ -498,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
             const uint8_t* xl = xlo + (size_t)t * H;
             const int2* xi = xinfo + (size_t)t * nseg;
             float ag = 0.f, au = 0.f;
-#pragma unroll(kMulti ? kGuUnroll : 2)
+#pragma unroll(kMulti ? 1 : 2)
             for (int s = lane; s < nseg; s += 32) {
               const uint4 qg = *reinterpret_cast<const uint4*>(grow + s * 16);
               const uint4 qu = *reinterpret_cast<const uint4*>(urow + s * 16);

@@ -195,11 +195,14 @@ __device__ __forceinline__ f2 f2_pack_bits(uint32_t a, uint32_t b) {
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(a), "r"(b));
   return r;
 }
-// (q_lo + c, q_hi + c) * d, both exact, rounded once to a bf16 pair (low half = first)
-__device__ __forceinline__ uint32_t deq_pair_bf16(uint32_t bits_lo, uint32_t bits_hi, f2 bias, f2 dd) {
-  f2 m = f2_pack_bits(bits_lo, bits_hi), q, w;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(q) : "l"(m), "l"(bias));
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(w) : "l"(q), "l"(dd));
+
+// The code byte placed by a byte permute in bits 8..15 of the float
+// 2^23 + 256 (q + 128); with d' = d / 256, fma(m, d', -(2^15 + 2^7) d) is
+// q d exactly (every product and the constant fit in fp32's 24 bits), then
+// one rounding to bf16: one packed op fewer than subtract-then-multiply.
+__device__ __forceinline__ uint32_t deq_pair_fma(uint32_t bits_lo, uint32_t bits_hi, f2 dd, f2 cc) {
+  f2 m = f2_pack_bits(bits_lo, bits_hi), w;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(w) : "l"(m), "l"(dd), "l"(cc));
   uint32_t r;
   asm("{\n\t.reg .f32 a, b;\n\tmov.b64 {a, b}, %1;\n\tcvt.rn.bf16x2.f32 %0, b, a;\n\t}" : "=r"(r) : "l"(w));
   return r;
@@ -347,7 +350,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quarter = warp & 3, group = (warp - kDeqWarp0) >> 2;
     const int r = quarter * 32 + lane;  // weight row of the tile = TMEM lane
     const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
-    const f2 bias = f2_pack(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
     const int sw = (r >> 1) & 3;                        // 64-byte swizzle of this row
     uint32_t it = 0;
     for (int tile = cid; tile < n_tiles && ok; tile += ncl) {
@@ -367,17 +369,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint16_t* sc = reinterpret_cast<const uint16_t*>(wtile + kTileCodeBytes);
           const float d0 = half_bits_to_f32(sc[r]), d1 = half_bits_to_f32(sc[BM + r]);
           uint32_t out[32];
+          const float e0 = d0 * 0.00390625f, e1 = d1 * 0.00390625f;       // d / 256
+          const float k0 = d0 * -32896.0f, k1 = d1 * -32896.0f;           // -(2^15 + 2^7) d
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const f2 dd = q < 2 ? f2_pack(d0, d0) : f2_pack(d1, d1);
+            const f2 dd = q < 2 ? f2_pack(e0, e0) : f2_pack(e1, e1);
+            const f2 cc = q < 2 ? f2_pack(k0, k0) : f2_pack(k1, k1);
             const uint32_t w4[4] = {c[q].x, c[q].y, c[q].z, c[q].w};
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const uint32_t w = w4[i];
-              out[8 * q + 2 * i] = deq_pair_bf16(__byte_perm(w, 0x4B000000u, 0x7650), __byte_perm(w, 0x4B000000u, 0x7651),
-                                                 bias, dd);
-              out[8 * q + 2 * i + 1] = deq_pair_bf16(__byte_perm(w, 0x4B000000u, 0x7652),
-                                                     __byte_perm(w, 0x4B000000u, 0x7653), bias, dd);
+              out[8 * q + 2 * i] = deq_pair_fma(__byte_perm(w, 0x4B000000u, 0x7504), __byte_perm(w, 0x4B000000u, 0x7514),
+                                                dd, cc);
+              out[8 * q + 2 * i + 1] = deq_pair_fma(__byte_perm(w, 0x4B000000u, 0x7524),
+                                                    __byte_perm(w, 0x4B000000u, 0x7534), dd, cc);
             }
           }
           tmem_st32(tmem_base + lane_addr + G::ACol0 + sa * G::ACols + mb * (BK / 2), out);

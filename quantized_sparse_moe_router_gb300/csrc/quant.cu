@@ -61,8 +61,9 @@ __device__ __forceinline__ int64_t plane_row(const PlaneView& p, int64_t r) {
 }
 
 // One thread per GGUF block of one expert range: the block's codes (stored as
-// q + 128, offset binary: q XOR 0x80, which the kernels turn into floats with
-// one byte permute and one subtraction) and scale go to the decode plane of
+// q + 128, offset binary: q XOR 0x80, which the decode kernel multiplies as
+// unsigned bytes and the GEMM turns into floats with a byte permute and one
+// fused multiply-add) and scale go to the decode plane of
 // the kind and to the GEMM tile that holds its row and K step.
 __global__ void repack_kernel(PlaneView p, int expert0, int64_t nblocks, const uint8_t* __restrict__ src) {
   int64_t blk = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
