@@ -40,7 +40,7 @@
 //      (deterministic, so every CTA agrees); CTA 0 publishes it;
 //   2. the CTA's chunks: gate/up stages -> h (shared memory), then down
 //      stages -> the CTA's partial output (fp32: shared memory for one token,
-//      registers for several);
+//      tensor memory for several);
 //   3. partial outputs to global memory, grid-wide arrival and bounded wait;
 //   4. each CTA's output rows summed over the CTAs' partials, bf16.
 #include <algorithm>
