@@ -384,7 +384,7 @@ __device__ __forceinline__ void report(Meta* m, int bits) { atomicOr(&m->status,
 // Sites of bounded waits, recorded with the first timeout (see Meta::diag).
 enum WaitSite {
   kSiteGuX = 1, kSiteGuFull = 2, kSiteGuEmpty = 3, kSiteDnH = 4, kSiteDnFull = 5, kSiteDnEmpty = 6,
-  kSiteGemm = 7, kSiteGrid = 8
+  kSiteGemm = 7, kSiteGrid = 8, kSiteRouteX = 9
 };
 
 static __device__ __noinline__ void report_wait(Meta* m, int site, int64_t stage, int detail) {

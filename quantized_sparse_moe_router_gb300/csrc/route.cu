@@ -37,6 +37,7 @@ struct RouteArgs {
 };
 
 constexpr int kRouteThreads = 256;
+constexpr int kRouteXStage = 64 * 1024;  // x staged in shared memory by one bulk copy when it fits
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kRouteUnroll = 8;  // float4 loads of the router row in flight per lane
 
@@ -46,9 +47,11 @@ constexpr int kRouteUnroll = 8;  // float4 loads of the router row in flight per
 // makes the gates and groups the (token, slot) pairs and publishes them;
 // without it the logits are the only output (the expert kernels rebuild the
 // routing from them).
-__global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a, int select) {
+__global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a, int select, int staged) {
+  extern __shared__ __align__(128) uint8_t x_s[];  // [T][H] bf16 when staged
   __shared__ float s_part[kRouteWarps][kMaxDecodeT];
   __shared__ bool s_last;
+  __shared__ __align__(8) uint64_t xbar;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int e = blockIdx.x;
   const int T = a.T, H = a.H;
@@ -62,6 +65,25 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
   if (blockIdx.x == 0 && tid == 0) {  // fresh grid barrier and chunk tickets for this call's expert kernel
     a.meta->gbar = 0;
     a.meta->chunk_ctr = 0;
+  }
+  // Several tokens: all of x (up to 64 KB) into shared memory by one bulk
+  // copy; read from there by every warp (as loads of 8 bytes from global
+  // memory by each thread it took 7.5 us at 16 tokens, the copy about 1).
+  const __nv_bfloat16* xs = a.x;
+  if (staged) {
+    const uint32_t bytes = (uint32_t)(T * H * 2);
+    if (tid == 0) {
+      mbar_init(&xbar, 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&xbar, bytes);
+      bulk_g2s(x_s, a.x, bytes, &xbar);
+    }
+    __syncthreads();
+    if (!mbar_wait(&xbar, 0)) {  // bounded: report, and leave the logits as they are
+      if (tid == 0) report_wait(a.meta, kSiteRouteX, blockIdx.x, 0);
+      return;
+    }
+    xs = reinterpret_cast<const __nv_bfloat16*>(x_s);
   }
   {
     float acc[kMaxDecodeT];
@@ -82,7 +104,8 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
 #pragma unroll
           for (int t = 0; t < kMaxDecodeT; ++t) {
             if (t < T) {
-              uint2 xv = __ldg(reinterpret_cast<const uint2*>(a.x + (int64_t)t * H + h));
+              const uint2 xv = staged ? *reinterpret_cast<const uint2*>(xs + (int64_t)t * H + h)
+                                      : __ldg(reinterpret_cast<const uint2*>(xs + (int64_t)t * H + h));
               float x0, x1, x2, x3;
               bf16x2_to_f32(xv.x, x0, x1);
               bf16x2_to_f32(xv.y, x2, x3);
@@ -486,6 +509,8 @@ cudaError_t configure_route_kernels() {
   // reconfigured between the two.
   cudaError_t e = cudaFuncSetAttribute(route_decode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
                                        (int)cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(route_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteXStage);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_tiles_kernel<1>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_tiles_kernel<2>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_tiles_kernel<3>);
@@ -501,7 +526,11 @@ cudaError_t launch_route_decode(Handle* h, const __nv_bfloat16* x, int T, int32_
                                 bool select, cudaStream_t s) {
   RouteArgs a = route_args(h, x, T, ids_out, gates_out);
   KernelTimer tm(h, FW_KERNEL_ROUTE_DECODE, s);
-  return launch_dependent(route_decode_kernel, dim3(h->cfg.E), dim3(kRouteThreads), 0, s, a, select ? 1 : 0);
+  // x by one bulk copy into shared memory for several tokens (16-byte aligned, fits)
+  const size_t xbytes = (size_t)T * h->cfg.H * 2;
+  const int staged = T > 1 && xbytes <= (size_t)kRouteXStage && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+  return launch_dependent(route_decode_kernel, dim3(h->cfg.E), dim3(kRouteThreads), staged ? xbytes : 0, s, a,
+                          select ? 1 : 0, staged);
 }
 
 cudaError_t launch_route_prefill(Handle* h, const __nv_bfloat16* x, int T, int32_t* ids_out, float* gates_out,
