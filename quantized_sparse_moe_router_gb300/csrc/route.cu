@@ -118,12 +118,32 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
         }
       }
     }
+    if (T <= 2) {
 #pragma unroll
-    for (int t = 0; t < kMaxDecodeT; ++t) {
-      if (t < T) {
-        float v = warp_sum(acc[t]);
-        if (lane == 0) s_part[warp][t] = v;
+      for (int t = 0; t < 2; ++t) {
+        if (t < T) {
+          float v = warp_sum(acc[t]);
+          if (lane == 0) s_part[warp][t] = v;
+        }
       }
+    } else {
+      // the 16 sums of the warp by recursive halving: at each step a lane
+      // keeps one half of its values (by its lane bit), sends the other to
+      // its partner and adds what it receives -- 16 shuffles, not 16 x 5;
+      // lane pair (2 t', 2 t' + 1) ends with token t's sum, t from the lane bits
+#pragma unroll
+      for (int m = 16, half = 8; m >= 2; m >>= 1, half >>= 1) {
+        const bool hi = (lane & m) != 0;
+#pragma unroll
+        for (int i = 0; i < half; ++i) {
+          const float send = hi ? acc[i] : acc[i + half];
+          const float keep = hi ? acc[i + half] : acc[i];
+          acc[i] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, m);
+        }
+      }
+      acc[0] += __shfl_xor_sync(0xFFFFFFFFu, acc[0], 1);
+      const int t = ((lane >> 4) & 1) * 8 + ((lane >> 3) & 1) * 4 + ((lane >> 2) & 1) * 2 + ((lane >> 1) & 1);
+      if ((lane & 1) == 0 && t < T) s_part[warp][t] = acc[0];
     }
   }
   __syncthreads();
