@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   if (kMulti)
     route_in_smem<kThreads>(a.logits, T, a.E, a.k, a.S, r, zbuf);
   else
-    route_one_in_smem<kThreads>(a.logits, a.E, a.k, a.S, r, zbuf);
+    route_one_in_smem<kThreads>(a.logits, a.E, a.k, a.S, r);
   if (a.publish && blockIdx.x == 0) publish_routing<kThreads>(r, T, a.E, a.k, a.S, a.ro);
 
   // this CTA's chunks: [c0, c1) of the nU * I/16 chunks, expert-major

@@ -14,41 +14,50 @@ constexpr int kMaxE = 256;               // experts supported by the register la
 constexpr int kMaxEPerLane = kMaxE / 32;
 constexpr int kMaxRowsDecode = kMaxDecodeT * (kMaxK + 1);
 
+// Order-preserving key of a logit: a larger float has a larger key, -0 keys
+// as +0 (the two compare equal), and NaN keys as 0, below every number.
+__device__ __forceinline__ uint32_t topk_key(float z) {
+  uint32_t u = __float_as_uint(z);
+  if (u == 0x80000000u) u = 0u;
+  const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return (u & 0x7FFFFFFFu) > 0x7F800000u ? 0u : key;
+}
+__device__ __forceinline__ float topk_value(uint32_t key) {
+  return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
 // One warp selects the k largest of z[0..E) (lane l holds z[l + 32 m]), ties
 // to the lower id, in descending order; lane j < k ends with (id_j, z_j).
+// Per round: each lane's best remaining entry (64-bit (key, kMaxEPerLane - m):
+// ties inside the lane go to the lower id), the warp's largest key by one
+// integer reduction, and among the lanes holding it the lowest id by a second
+// one -- two reductions a round where a shuffle tree over (value, id) takes ten.
+// Entries past E sit below every logit and taken ones below those.
+__device__ __forceinline__ uint64_t max64(uint64_t a, uint64_t b) { return a > b ? a : b; }
 __device__ __forceinline__ void warp_topk(const float (&zl)[kMaxEPerLane], int E, int k, int lane, int* out_id,
                                           float* out_z) {
-  uint32_t taken = 0;  // bit m: z[lane + 32 m] already selected
+  static_assert(kMaxEPerLane == 8, "the tree below takes eight entries a lane");
+  uint64_t v[kMaxEPerLane];
+#pragma unroll
+  for (int m = 0; m < kMaxEPerLane; ++m) {
+    const uint32_t key = lane + 32 * m < E ? topk_key(zl[m]) : 0u;
+    v[m] = ((uint64_t)key << 32) | (uint32_t)(kMaxEPerLane - m);
+  }
   int my_id = -1;
   float my_z = 0.0f;
   for (int j = 0; j < k; ++j) {
-    float bv = -INFINITY;
-    int bi = 0x7FFFFFFF;
-#pragma unroll
-    for (int m = 0; m < kMaxEPerLane; ++m) {
-      int e = lane + 32 * m;
-      if (e < E && !((taken >> m) & 1u)) {
-        float v = zl[m];
-        if (v > bv || (v == bv && e < bi)) {
-          bv = v;
-          bi = e;
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-      int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-      if (ov > bv || (ov == bv && oi < bi)) {
-        bv = ov;
-        bi = oi;
-      }
-    }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    const uint64_t best = max64(max64(max64(v[0], v[1]), max64(v[2], v[3])), max64(max64(v[4], v[5]), max64(v[6], v[7])));
+    const uint32_t bk = (uint32_t)(best >> 32);
+    const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, bk);
+    const int bm = kMaxEPerLane - (int)(uint32_t)best;
+    const uint32_t id = __reduce_min_sync(0xFFFFFFFFu, bk == top && best != 0 ? (uint32_t)(lane + 32 * bm) : 0xFFFFFFFFu);
     if (lane == j) {
-      my_id = bi;
-      my_z = bv;
+      my_id = (int)id;
+      my_z = topk_value(top);
     }
+    const int tm = (int)(id & 31u) == lane ? (int)(id >> 5) : -1;  // this lane's entry taken
+#pragma unroll
+    for (int m = 0; m < kMaxEPerLane; ++m) v[m] = m == tm ? 0ull : v[m];
   }
   *out_id = my_id;
   *out_z = my_z;
@@ -240,34 +249,27 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
   __syncthreads();
 }
 
-// The same for one token (T = 1), with less work and code: the k selected
-// experts each get one grouped row, so the grouping is a sort of k ids; the
-// counts and offsets for all experts (read only when CTA 0 publishes) come
-// from comparisons with the k ids.
+// The same for one token (T = 1), with less work and code: warp 0 selects
+// straight from the logits (the other warps wait at the barrier); the k
+// selected experts each get one grouped row, so the grouping is a sort of k
+// ids; the counts and offsets for all experts (read only when CTA 0
+// publishes) come from comparisons with the k ids.
 template <int NT>
-__device__ void route_one_in_smem(const float* logits, int E, int k, int S, SmemRouting& r, float* zbuf) {
-  constexpr int NW = NT / 32;
+__device__ void route_one_in_smem(const float* logits, int E, int k, int S, SmemRouting& r) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int E4 = (E + 3) & ~3;  // padded to whole float4 with -inf (never ranked ahead)
-  for (int i = tid; i < E4; i += NT) zbuf[i] = i < E ? __ldcg(logits + i) : -INFINITY;
-  __syncthreads();
-  {
-    int s = 32;  // lanes per expert, as many as the block allows
-    while (s > 1 && E * s > NT) s >>= 1;
-    const int gpw = 32 / s, c = lane & (s - 1);
-    for (int b = warp * gpw; b < E; b += NW * gpw) {  // warp-uniform trip count
-      const int e = b + lane / s;
-      int rank = 0;
-      float z = 0.f;
-      if (e < E) {
-        z = zbuf[e];
-        rank = rank_in_row(reinterpret_cast<const float4*>(zbuf), E4 / 4, c, s, e);
-      }
-      for (int o = 1; o < s; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
-      if (e < E && c == 0 && rank < k) {
-        r.ids[rank] = e;
-        r.zsel[rank] = z;
-      }
+  if (warp == 0) {
+    float zl[kMaxEPerLane];
+#pragma unroll
+    for (int m = 0; m < kMaxEPerLane; ++m) {
+      const int e = lane + 32 * m;
+      zl[m] = e < E ? __ldcg(logits + e) : -INFINITY;
+    }
+    int id;
+    float zv;
+    warp_topk(zl, E, k, lane, &id, &zv);
+    if (lane < k) {
+      r.ids[lane] = id;
+      r.zsel[lane] = zv;
     }
   }
   __syncthreads();
