@@ -314,28 +314,45 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
     if (!kMulti)
       for (int o = tid; o < H; o += kCT) acc_s[o] = 0.f;
   }
-  pdl_wait();  // the router's logits (and its reset of the grid counter)
-  float* zbuf = reinterpret_cast<float*>(ring);  // the ring is not yet in use
-  if (kMulti)
-    route_in_smem<kThreads>(a.logits, T, a.E, a.k, a.S, r, zbuf);
-  else
-    route_one_in_smem<kThreads>(a.logits, a.E, a.k, a.S, r);
-  if (a.publish && blockIdx.x == 0) publish_routing<kThreads>(r, T, a.E, a.k, a.S, a.ro);
-
-  // this CTA's chunks: [c0, c1) of the nU * I/16 chunks, expert-major
   const int G = I / kChunk;
-  const int n_ch = r.n_unique * G;
   const int n_gu = kChunk / R;            // gate/up stages per chunk
   const int n_dn = (H + Dr - 1) / Dr;     // down stages per chunk
-  // Tokens each CTA's partial output covers (the CTAs' chunk ranges follow
-  // from the routing, which every CTA has): per touched expert, then per CTA.
-  for (int u = tid; u < r.n_unique; u += kThreads) {
-    const int4 ui = r.u[u];
-    uint32_t m = 0;
-    for (int p = ui.y; p < ui.y + ui.z; ++p) m |= 1u << r.tok[p];
-    s_emask[u] = m;
+  if (!kMulti) {
+    // One token touches k + S experts whatever the logits, so its chunk ranges
+    // (equal counts) and which CTAs' partial outputs hold it are known before
+    // the routing is. (32-bit: n_ch * grid < 2^32.)
+    const uint32_t n1 = (uint32_t)((a.k + a.S) * G);
+    for (int c = tid; c < (int)gridDim.x; c += kThreads)
+      s_pm[c] = n1 * (uint32_t)(c + 1) / gridDim.x > n1 * (uint32_t)c / gridDim.x ? 1u : 0u;
   }
+  pdl_wait();  // the router's logits (and its reset of the grid counter)
+  float* zbuf = reinterpret_cast<float*>(ring);  // the ring is not yet in use
   if (kMulti) {
+    route_in_smem<kThreads>(a.logits, T, a.E, a.k, a.S, r, zbuf);
+  } else {
+    route_one_in_smem<kThreads>(a.logits, a.E, a.k, a.S, r);
+    // the gates are first read in a down stage, after a consumer barrier
+    if (warp == 0) route_one_gates(a.k, a.S, r, lane);
+  }
+  if (a.publish && blockIdx.x == 0) {
+    if (!kMulti) {
+      route_one_tables<kThreads>(a.E, a.k, a.S, r);
+      __syncthreads();
+    }
+    publish_routing<kThreads>(r, T, a.E, a.k, a.S, a.ro);
+  }
+
+  // this CTA's chunks: [c0, c1) of the nU * I/16 chunks, expert-major
+  const int n_ch = r.n_unique * G;
+  int c0, c1;
+  if (kMulti) {
+    // Tokens each CTA's partial output covers (the CTAs' chunk ranges follow
+    // from the routing, which every CTA has): per touched expert its token
+    // mask, then per CTA.
+    for (int u = tid; u < r.n_unique; u += kThreads) {
+      const int e = r.u[u].x;
+      s_emask[u] = e < a.E ? r.mask[e] : (1u << T) - 1u;
+    }
     // A chunk costs its weight stream plus its expert's token count of
     // arithmetic: kChunkCost + kTokCost n. CTA b takes the chunks whose starting cost
     // lies in [b C / grid, (b + 1) C / grid), C the total. Prefix costs per
@@ -369,27 +386,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       }
       int c = n_ch;
       if (b < (int)grid && r.n_unique > 0) {
+        // rem < w G: the quotient is at most G, and rem + w fits 32 bits
         const uint64_t w = (uint64_t)(kChunkCost + kTokCost * r.u[lo].z) * grid;
         const uint64_t rem = target - s_pref[lo] * grid;
-        c = ::min(lo * G + (int)((rem + w - 1) / w), n_ch);
+        c = ::min(lo * G + (int)(((uint32_t)rem + (uint32_t)w - 1u) / (uint32_t)w), n_ch);
       }
       s_c0[b] = c;
     }
+    __syncthreads();
+    c0 = s_c0[blockIdx.x];
+    c1 = s_c0[blockIdx.x + 1];
+    for (int c = tid; c < (int)gridDim.x; c += kThreads) {
+      const int b0 = s_c0[c], b1 = s_c0[c + 1];
+      uint32_t m = 0;
+      if (b1 > b0)
+        for (int u = b0 / G; u <= (b1 - 1) / G; ++u) m |= s_emask[u];
+      s_pm[c] = m;
+    }
+    __syncthreads();
   } else {
-    // one token: every chunk costs the same, equal counts
-    // (32-bit: a 64-bit division is a long software routine; n_ch * grid < 2^32)
-    for (int b = tid; b <= (int)gridDim.x; b += kThreads) s_c0[b] = (int)((uint32_t)n_ch * b / gridDim.x);
+    c0 = (int)((uint32_t)n_ch * blockIdx.x / gridDim.x);
+    c1 = (int)((uint32_t)n_ch * (blockIdx.x + 1) / gridDim.x);
   }
-  __syncthreads();
-  const int c0 = s_c0[blockIdx.x], c1 = s_c0[blockIdx.x + 1];
-  for (int c = tid; c < (int)gridDim.x; c += kThreads) {
-    const int b0 = s_c0[c], b1 = s_c0[c + 1];
-    uint32_t m = 0;
-    if (b1 > b0)
-      for (int u = b0 / G; u <= (b1 - 1) / G; ++u) m |= s_emask[u];
-    s_pm[c] = m;
-  }
-  __syncthreads();
   const uint32_t cta_mask = s_pm[blockIdx.x];
 
   if (warp == kProducer) {

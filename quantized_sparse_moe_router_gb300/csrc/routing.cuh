@@ -15,52 +15,56 @@ constexpr int kMaxEPerLane = kMaxE / 32;
 constexpr int kMaxRowsDecode = kMaxDecodeT * (kMaxK + 1);
 
 // Order-preserving key of a logit: a larger float has a larger key, -0 keys
-// as +0 (the two compare equal), and NaN keys as 0, below every number.
+// as +0 (the two compare equal), and NaN keys as 1, with the padding past E,
+// below every number (whose keys are at least that of -inf, 0x007FFFFF).
 __device__ __forceinline__ uint32_t topk_key(float z) {
   uint32_t u = __float_as_uint(z);
   if (u == 0x80000000u) u = 0u;
   const uint32_t key = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-  return (u & 0x7FFFFFFFu) > 0x7F800000u ? 0u : key;
+  return (u & 0x7FFFFFFFu) > 0x7F800000u ? 1u : key;
 }
 __device__ __forceinline__ float topk_value(uint32_t key) {
   return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
 }
 
-// One warp selects the k largest of z[0..E) (lane l holds z[l + 32 m]), ties
-// to the lower id, in descending order; lane j < k ends with (id_j, z_j).
-// Per round: each lane's best remaining entry (64-bit (key, kMaxEPerLane - m):
-// ties inside the lane go to the lower id), the warp's largest key by one
-// integer reduction, and among the lanes holding it the lowest id by a second
-// one -- two reductions a round where a shuffle tree over (value, id) takes ten.
-// Entries past E sit below every logit and taken ones below those.
-__device__ __forceinline__ uint64_t max64(uint64_t a, uint64_t b) { return a > b ? a : b; }
-__device__ __forceinline__ void warp_topk(const float (&zl)[kMaxEPerLane], int E, int k, int lane, int* out_id,
-                                          float* out_z) {
-  static_assert(kMaxEPerLane == 8, "the tree below takes eight entries a lane");
-  uint64_t v[kMaxEPerLane];
+// One warp selects the k largest of z[0..E) (lane l holds z[l + 32 m], m <
+// MPL), ties to the lower id, in descending order; lane j < k ends with
+// (id_j, z_j). Per round two integer warp reductions: the largest key, then
+// the lowest id holding it (each lane offers its lowest); the chosen entry's
+// key becomes 0, below everything left (k <= E, so a key >= 1 always remains).
+template <int MPL>
+__device__ __forceinline__ void warp_topk_n(const float (&zl)[kMaxEPerLane], int E, int k, int lane, int* out_id,
+                                            float* out_z) {
+  uint32_t key[MPL];
 #pragma unroll
-  for (int m = 0; m < kMaxEPerLane; ++m) {
-    const uint32_t key = lane + 32 * m < E ? topk_key(zl[m]) : 0u;
-    v[m] = ((uint64_t)key << 32) | (uint32_t)(kMaxEPerLane - m);
-  }
+  for (int m = 0; m < MPL; ++m) key[m] = lane + 32 * m < E ? topk_key(zl[m]) : 1u;
   int my_id = -1;
   float my_z = 0.0f;
   for (int j = 0; j < k; ++j) {
-    const uint64_t best = max64(max64(max64(v[0], v[1]), max64(v[2], v[3])), max64(max64(v[4], v[5]), max64(v[6], v[7])));
-    const uint32_t bk = (uint32_t)(best >> 32);
-    const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, bk);
-    const int bm = kMaxEPerLane - (int)(uint32_t)best;
-    const uint32_t id = __reduce_min_sync(0xFFFFFFFFu, bk == top && best != 0 ? (uint32_t)(lane + 32 * bm) : 0xFFFFFFFFu);
+    uint32_t best = key[0];
+#pragma unroll
+    for (int m = 1; m < MPL; ++m) best = max(best, key[m]);
+    const uint32_t top = __reduce_max_sync(0xFFFFFFFFu, best);
+    uint32_t cand = 0xFFFFFFFFu;
+#pragma unroll
+    for (int m = MPL - 1; m >= 0; --m) cand = key[m] == top ? (uint32_t)(lane + 32 * m) : cand;
+    const uint32_t id = __reduce_min_sync(0xFFFFFFFFu, cand);
     if (lane == j) {
       my_id = (int)id;
       my_z = topk_value(top);
     }
-    const int tm = (int)(id & 31u) == lane ? (int)(id >> 5) : -1;  // this lane's entry taken
 #pragma unroll
-    for (int m = 0; m < kMaxEPerLane; ++m) v[m] = m == tm ? 0ull : v[m];
+    for (int m = 0; m < MPL; ++m) key[m] = (uint32_t)(lane + 32 * m) == id ? 0u : key[m];
   }
   *out_id = my_id;
   *out_z = my_z;
+}
+__device__ __forceinline__ void warp_topk(const float (&zl)[kMaxEPerLane], int E, int k, int lane, int* out_id,
+                                          float* out_z) {
+  if (E <= 128)
+    warp_topk_n<4>(zl, E, k, lane, out_id, out_z);
+  else
+    warp_topk_n<kMaxEPerLane>(zl, E, k, lane, out_id, out_z);
 }
 
 // Gates of the selection held by lanes 0..k-1: exp(z_j - z_0) / sum.
@@ -115,8 +119,10 @@ struct SmemRouting {
 // (token, expert) pair counts, split over a group of lanes, the logits that
 // come before it (larger, or equal with a lower id); ranks below k are the
 // top-k in order. Otherwise one warp per token takes the k largest in turn
-// (warp_topk). Then warp 0 alone groups the pairs (counts, offsets, the
-// table of touched experts, positions) while other warps make the gates.
+// (warp_topk). Either way each selected pair sets its token's bit in its
+// expert's mask. Then warp 0 alone groups the pairs (counts as popcounts of
+// the masks, offsets, the table of touched experts, positions) while the
+// other warps make the gates.
 template <int NT>
 __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, SmemRouting& r, float* zbuf) {
   static_assert(NT % 32 == 0 && NT >= 64, "whole warps, at least two");
@@ -131,10 +137,7 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
       const int t = i / E4, e = i - t * E4;
       zbuf[i] = e < E ? __ldcg(logits + t * E + e) : -INFINITY;
     }
-  for (int i = tid; i < EU; i += NT) {
-    r.cnt[i] = 0;
-    r.mask[i] = 0;
-  }
+  for (int i = tid; i < EU; i += NT) r.mask[i] = 0;
   __syncthreads();
 
   if (by_rank) {
@@ -157,6 +160,7 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
       if (p < P && c == 0 && rank < k) {
         r.ids[t * k + rank] = e;
         r.zsel[t * k + rank] = z;
+        atomicOr(&r.mask[e], 1u << t);
       }
     }
   } else {
@@ -170,23 +174,16 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
       int id;
       float zv;
       warp_topk(zl, E, k, lane, &id, &zv);
-      const float g = warp_gate(zv, k, lane);
-      if (lane < k) {
+      if (lane < k) {  // k distinct experts: no two lanes share a mask word
         r.ids[t * k + lane] = id;
-        r.gates[t * k + lane] = g;
+        r.zsel[t * k + lane] = zv;
+        atomicOr(&r.mask[id], 1u << t);
       }
     }
   }
   __syncthreads();
 
   if (warp == 0) {
-    for (int p = lane; p < T * k; p += 32) {
-      const int ee = r.ids[p];
-      atomicAdd(&r.cnt[ee], 1);
-      atomicOr(&r.mask[ee], 1u << (p / k));
-    }
-    if (S && lane == 0) r.cnt[E] = T;
-    __syncwarp();
     // lane l owns the consecutive experts [l per, l per + per), in registers;
     // both scans (rows and touched experts) in one pass of shuffles
     constexpr int kPer = (kMaxE + 1 + 31) / 32;
@@ -196,7 +193,7 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
 #pragma unroll
     for (int m = 0; m < kPer; ++m) {
       const int i = b0 + m;
-      cn[m] = (m < per && i < EU) ? r.cnt[i] : 0;
+      cn[m] = (m < per && i < EU) ? (i < E ? __popc(r.mask[i]) : T) : 0;
       sc += cn[m];
       sn += cn[m] > 0;
     }
@@ -214,6 +211,7 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
     for (int m = 0; m < kPer; ++m) {
       const int i = b0 + m;
       if (m < per && i < EU) {
+        r.cnt[i] = cn[m];
         r.off[i] = rc;
         if (cn[m] > 0) r.u[rn++] = make_int4(i, rc, cn[m], 0);
         rc += cn[m];
@@ -239,7 +237,7 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
         r.slot[pos] = T * k + t;
         r.gates[T * k + t] = 1.0f;
       }
-  } else if (by_rank) {
+  } else {
     for (int t = warp - 1; t < T; t += NW - 1) {
       const float zj = lane < k ? r.zsel[t * k + lane] : 0.f;
       const float g = warp_gate(zj, k, lane);
@@ -250,13 +248,14 @@ __device__ void route_in_smem(const float* logits, int T, int E, int k, int S, S
 }
 
 // The same for one token (T = 1), with less work and code: warp 0 selects
-// straight from the logits (the other warps wait at the barrier); the k
-// selected experts each get one grouped row, so the grouping is a sort of k
-// ids; the counts and offsets for all experts (read only when CTA 0
-// publishes) come from comparisons with the k ids.
+// straight from the logits and sorts the k ids (each selected expert gets one
+// grouped row), then one block barrier. The gates (route_one_gates) and the
+// counts and offsets over all experts (route_one_tables, read only when the
+// routing is published) are left to the caller, off the path to the first
+// weight copy.
 template <int NT>
 __device__ void route_one_in_smem(const float* logits, int E, int k, int S, SmemRouting& r) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (warp == 0) {
     float zl[kMaxEPerLane];
 #pragma unroll
@@ -267,20 +266,13 @@ __device__ void route_one_in_smem(const float* logits, int E, int k, int S, Smem
     int id;
     float zv;
     warp_topk(zl, E, k, lane, &id, &zv);
+    // lane j < k: the expert of rank j, its row among the k ids in ascending order
+    const int e = lane < k ? id : 0x7FFFFFFF;
+    int pos = 0;
+    for (int m = 0; m < k; ++m) pos += __shfl_sync(0xFFFFFFFFu, e, m) < e;
     if (lane < k) {
       r.ids[lane] = id;
       r.zsel[lane] = zv;
-    }
-  }
-  __syncthreads();
-  if (warp == 0) {
-    // lane j < k: the expert of rank j, its row among the k ids in ascending order
-    const int e = lane < k ? r.ids[lane] : 0x7FFFFFFF;
-    int pos = 0;
-    for (int m = 0; m < k; ++m) pos += __shfl_sync(0xFFFFFFFFu, e, m) < e;
-    const float g = warp_gate(lane < k ? r.zsel[lane] : 0.f, k, lane);
-    if (lane < k) {
-      r.gates[lane] = g;
       r.u[pos] = make_int4(e, pos, 1, 0);
       r.tok[pos] = 0;
       r.slot[pos] = lane;
@@ -290,28 +282,41 @@ __device__ void route_one_in_smem(const float* logits, int E, int k, int S, Smem
         r.u[k] = make_int4(E, k, 1, 0);
         r.tok[k] = 0;
         r.slot[k] = k;
-        r.gates[k] = 1.0f;
       }
       r.n_unique = k + S;
       r.rows = k + S;
     }
-  } else {
-    for (int i = tid - 32; i <= E + S; i += NT - 32) {  // offsets [EU + 1], counts [EU]
-      int before = 0, hit = 0;
-      for (int m = 0; m < k; ++m) {
-        const int em = r.ids[m];
-        before += em < i;
-        hit += em == i;
-      }
-      if (i >= E) {  // the shared expert's row comes after the k routed ones
-        before = k + (i > E ? 1 : 0);
-        hit = i == E ? 1 : 0;
-      }
-      r.off[i] = before;
-      if (i < E + S) r.cnt[i] = hit;
-    }
   }
   __syncthreads();
+}
+
+// One warp, after route_one_in_smem: the gates of the k selected experts (and
+// 1 for the shared expert's slot).
+__device__ __forceinline__ void route_one_gates(int k, int S, SmemRouting& r, int lane) {
+  const float g = warp_gate(lane < k ? r.zsel[lane] : 0.f, k, lane);
+  if (lane < k) r.gates[lane] = g;
+  if (S && lane == 0) r.gates[k] = 1.0f;
+}
+
+// Whole block, after route_one_in_smem: counts [E + S] and offsets [E + S + 1]
+// over all experts, by comparison with the k ids (the shared expert's row
+// comes after the k routed ones).
+template <int NT>
+__device__ void route_one_tables(int E, int k, int S, SmemRouting& r) {
+  for (int i = threadIdx.x; i <= E + S; i += NT) {
+    int before = 0, hit = 0;
+    for (int m = 0; m < k; ++m) {
+      const int em = r.ids[m];
+      before += em < i;
+      hit += em == i;
+    }
+    if (i >= E) {
+      before = k + (i > E ? 1 : 0);
+      hit = i == E ? 1 : 0;
+    }
+    r.off[i] = before;
+    if (i < E + S) r.cnt[i] = hit;
+  }
 }
 
 // Publish a routing computed by route_in_smem (whole block).
