@@ -625,6 +625,28 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       if (cta_mask)
         for (int o = tid; o < H; o += kCT) __stcg(part + o, acc_s[o]);
     }
+    // ---- this CTA's output rows [o0, o1) (summed after the grid-wide wait).
+    // For each token, the CTAs whose partials hold it (ascending), made here
+    // while other CTAs still stream (the ring is free: every stage is consumed;
+    // the sums clamp the CTA index all the same, should a wait have given up
+    // with a copy still in flight)
+    const int o0 = (int)((uint32_t)H * blockIdx.x / gridDim.x), o1 = (int)((uint32_t)H * (blockIdx.x + 1) / gridDim.x);
+    const int nrow = o1 - o0, pairs = T * nrow;
+    const int P = ::max(1, ::min(kCW, kCT / ::max(1, pairs)));
+    float* red = reinterpret_cast<float*>(ring);                       // [P][pairs]: P pairs <= max(kCT, pairs)
+    int* lists = reinterpret_cast<int*>(ring) + ::max(kCT, pairs);     // [T][grid]
+    __shared__ int s_len[kMaxDecodeT];
+    for (int t = warp; t < T; t += kCW) {  // a warp per token: its CTAs by ballot, ascending
+      int n = 0;
+      for (int c0 = 0; c0 < (int)gridDim.x; c0 += 32) {
+        const int c = c0 + lane;
+        const bool has = c < (int)gridDim.x && ((s_pm[c] >> t) & 1u);
+        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, has);
+        if (has) lists[t * gridDim.x + n + __popc(bal & ((1u << lane) - 1u))] = c;
+        n += __popc(bal);
+      }
+      if (lane == 0) s_len[t] = n;
+    }
     // ---- grid-wide: every partial is written before any CTA sums them. The
     // arrival is a release (ordering the CTA's partial stores, which the
     // consumer barrier ordered before it), the poll an acquire.
@@ -647,28 +669,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
     // every partial is written: the next call's router may launch (it waits
     // for this grid's completion before touching memory)
     pdl_launch_dependents();
-    // ---- this CTA's output rows [o0, o1). For each token, the CTAs whose
-    // partials hold it (ascending); each (token, row) pair is summed over that
-    // list by P threads taking consecutive parts of it (a part's loads all in
-    // flight, then added in order), then the P part sums in order.
-    const int o0 = (int)((uint32_t)H * blockIdx.x / gridDim.x), o1 = (int)((uint32_t)H * (blockIdx.x + 1) / gridDim.x);
-    const int nrow = o1 - o0, pairs = T * nrow;
-    const int P = ::max(1, ::min(kCW, kCT / ::max(1, pairs)));
-    float* red = reinterpret_cast<float*>(ring);                       // [P][pairs]: P pairs <= max(kCT, pairs)
-    int* lists = reinterpret_cast<int*>(ring) + ::max(kCT, pairs);     // [T][grid]
-    __shared__ int s_len[kMaxDecodeT];
-    for (int t = warp; t < T; t += kCW) {  // a warp per token: its CTAs by ballot, ascending
-      int n = 0;
-      for (int c0 = 0; c0 < (int)gridDim.x; c0 += 32) {
-        const int c = c0 + lane;
-        const bool has = c < (int)gridDim.x && ((s_pm[c] >> t) & 1u);
-        const uint32_t bal = __ballot_sync(0xFFFFFFFFu, has);
-        if (has) lists[t * gridDim.x + n + __popc(bal & ((1u << lane) - 1u))] = c;
-        n += __popc(bal);
-      }
-      if (lane == 0) s_len[t] = n;
-    }
-    consumer_sync();
+    // ---- each (token, row) pair of this CTA's rows is summed over its
+    // token's list by P threads taking consecutive parts of it (a part's loads
+    // all in flight, then added in order), then the P part sums in order.
     for (int i = tid; i < P * pairs; i += kCT) {
       const int part = i / pairs, pr = i - part * pairs;
       const int t = pr / nrow, rl = pr - t * nrow;
@@ -679,7 +682,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
         float pv[kRedBatch];
 #pragma unroll
         for (int j = 0; j < kRedBatch; ++j)
-          pv[j] = q + j < q1 ? __ldcg(a.partial + ((size_t)lt[q + j] * T + t) * H + o0 + rl) : 0.f;
+          pv[j] = q + j < q1 ? __ldcg(a.partial + ((size_t)::min((unsigned)lt[q + j], gridDim.x - 1u) * T + t) * H + o0 + rl)
+                             : 0.f;
 #pragma unroll
         for (int j = 0; j < kRedBatch; ++j) v += pv[j];
       }

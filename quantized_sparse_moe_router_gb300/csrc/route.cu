@@ -59,7 +59,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
   // previous call's expert kernel, typically): wait for it to complete before
   // touching memory (x may be its output; the grid counter is its own), and
   // only then let this call's expert kernel start (it stages x before its own
-  // wait for this grid).
+  // wait for this grid). The router row is a weight, written by nothing in
+  // the stream: it starts coming into L2 before the wait.
+  if (tid == 0) prefetch_l2(a.wr + (int64_t)e * H, (uint32_t)(H * 4));
   pdl_wait();
   pdl_launch_dependents();
   if (blockIdx.x == 0 && tid == 0) {  // fresh grid barrier and chunk tickets for this call's expert kernel
