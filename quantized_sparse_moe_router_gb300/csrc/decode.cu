@@ -285,6 +285,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   float* hbuf = reinterpret_cast<float*>(smem + a.off_h);           // [2][T][16]
   HPlanes* hpl = reinterpret_cast<HPlanes*>(smem + a.off_hp);       // [T] (several tokens)
   uint8_t* ring = smem + a.off_ring;
+  // The next kernel in the stream (the next call's router) may launch at
+  // once: it waits for this grid's completion before touching memory, and
+  // meanwhile its CTAs, where they fit beside this one, prefetch their weights.
+  pdl_launch_dependents();
   if (tid == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(&full[s], 1);
@@ -666,9 +670,6 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
       }
     }
     consumer_sync();
-    // every partial is written: the next call's router may launch (it waits
-    // for this grid's completion before touching memory)
-    pdl_launch_dependents();
     // ---- each (token, row) pair of this CTA's rows is summed over its
     // token's list by P threads taking consecutive parts of it (a part's loads
     // all in flight, then added in order), then the P part sums in order.

@@ -41,16 +41,21 @@ constexpr int kRouteXStage = 64 * 1024;  // x staged in shared memory by one bul
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kRouteUnroll = 8;  // float4 loads of the router row in flight per lane
 
-// Grid: E CTAs of 8 warps; CTA e computes z[t][e] for the T <= 16 tokens, its
+// Grid: E CTAs of 8 warps; CTA e computes z[t][e] for the T <= kT tokens, its
 // warps splitting H with all of a lane's loads issued before any use. With
-// `select`, the last CTA to finish (atomic ticket, no waiting) also selects,
-// makes the gates and groups the (token, slot) pairs and publishes them;
-// without it the logits are the only output (the expert kernels rebuild the
-// routing from them).
-__global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a, int select, int staged) {
+// kSelect (the route-only entry point), the last CTA to finish (atomic ticket,
+// no waiting) also selects, makes the gates and groups the (token, slot) pairs
+// and publishes them; without it the logits are the only output (the expert
+// kernels rebuild the routing from them), and the kernel holds no routing
+// tables in shared memory. With kT = 2 it also holds two accumulators a
+// thread instead of 16: so sized, its CTAs fit beside a one-token expert
+// kernel's, which lets them launch, and prefetch their rows, while that
+// kernel still runs.
+template <bool kSelect, int kT>
+__global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a, int staged) {
+  static_assert(kT == 2 || kT == kMaxDecodeT, "two tokens, or the decode limit");
   extern __shared__ __align__(128) uint8_t x_s[];  // [T][H] bf16 when staged
-  __shared__ float s_part[kRouteWarps][kMaxDecodeT];
-  __shared__ bool s_last;
+  __shared__ float s_part[kRouteWarps][kT];
   __shared__ __align__(8) uint64_t xbar;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int e = blockIdx.x;
@@ -88,9 +93,9 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
     xs = reinterpret_cast<const __nv_bfloat16*>(x_s);
   }
   {
-    float acc[kMaxDecodeT];
+    float acc[kT];
 #pragma unroll
-    for (int t = 0; t < kMaxDecodeT; ++t) acc[t] = 0.0f;
+    for (int t = 0; t < kT; ++t) acc[t] = 0.0f;
     const float* wrow = a.wr + (int64_t)e * H;
     for (int base = 4 * tid; base < H; base += 4 * kRouteThreads * kRouteUnroll) {
       float4 w[kRouteUnroll];
@@ -104,7 +109,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
         int h = base + 4 * kRouteThreads * u;
         if (h < H) {
 #pragma unroll
-          for (int t = 0; t < kMaxDecodeT; ++t) {
+          for (int t = 0; t < kT; ++t) {
             if (t < T) {
               const uint2 xv = staged ? *reinterpret_cast<const uint2*>(xs + (int64_t)t * H + h)
                                       : __ldg(reinterpret_cast<const uint2*>(xs + (int64_t)t * H + h));
@@ -120,7 +125,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
         }
       }
     }
-    if (T <= 2) {
+    if (kT == 2 || T <= 2) {
 #pragma unroll
       for (int t = 0; t < 2; ++t) {
         if (t < T) {
@@ -128,7 +133,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
           if (lane == 0) s_part[warp][t] = v;
         }
       }
-    } else {
+    } else if constexpr (kT == kMaxDecodeT) {
       // the 16 sums of the warp by recursive halving: at each step a lane
       // keeps one half of its values (by its lane bit), sends the other to
       // its partner and adds what it receives -- 16 shuffles, not 16 x 5;
@@ -154,20 +159,22 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
 #pragma unroll
     for (int w = 0; w < kRouteWarps; ++w) z += s_part[w][tid];
     a.logits[tid * a.E + e] = z + a.bias[e];
-    if (select) __threadfence();
+    if (kSelect) __threadfence();
   }
-  if (!select) return;
-  __syncthreads();
-  if (tid == 0) s_last = atomicInc(&a.meta->ticket, gridDim.x - 1) == gridDim.x - 1;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  __shared__ SmemRouting r;
-  __shared__ __align__(16) float zbuf[kMaxDecodeT * kMaxE];
-  route_in_smem<kRouteThreads>(a.logits, T, a.E, a.k, a.S, r, zbuf);
-  RoutingOut o{a.ids_out, a.gates_out, a.ids,      a.gates,    a.counts, a.offsets,
-               a.perm,    a.inv,       a.row_token, a.row_gate, a.uinfo,  a.meta};
-  publish_routing<kRouteThreads>(r, T, a.E, a.k, a.S, o);
+  if constexpr (kSelect) {
+    __shared__ bool s_last;
+    __syncthreads();
+    if (tid == 0) s_last = atomicInc(&a.meta->ticket, gridDim.x - 1) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    __shared__ SmemRouting r;
+    __shared__ __align__(16) float zbuf[kMaxDecodeT * kMaxE];
+    route_in_smem<kRouteThreads>(a.logits, T, a.E, a.k, a.S, r, zbuf);
+    RoutingOut o{a.ids_out, a.gates_out, a.ids,      a.gates,    a.counts, a.offsets,
+                 a.perm,    a.inv,       a.row_token, a.row_gate, a.uinfo,  a.meta};
+    publish_routing<kRouteThreads>(r, T, a.E, a.k, a.S, o);
+  }
 }
 
 // ------------------------------------------------------ prefill router
@@ -529,10 +536,15 @@ cudaError_t configure_route_kernels() {
   // The decode router runs on the SMs that the expert kernel (all of shared
   // memory) takes next: with the same carve-out an SM need not be
   // reconfigured between the two.
-  cudaError_t e = cudaFuncSetAttribute(route_decode_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                       (int)cudaSharedmemCarveoutMaxShared);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(route_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteXStage);
+  void (*const routers[4])(RouteArgs, int) = {route_decode_kernel<false, 2>, route_decode_kernel<true, 2>,
+                                               route_decode_kernel<false, kMaxDecodeT>,
+                                               route_decode_kernel<true, kMaxDecodeT>};
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 4 && e == cudaSuccess; ++i) {
+    e = cudaFuncSetAttribute(routers[i], cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(routers[i], cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteXStage);
+  }
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_tiles_kernel<1>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_tiles_kernel<2>);
   if (e == cudaSuccess) e = allow_max_dynamic_smem(route_tiles_kernel<3>);
@@ -551,8 +563,13 @@ cudaError_t launch_route_decode(Handle* h, const __nv_bfloat16* x, int T, int32_
   // x by one bulk copy into shared memory for several tokens (16-byte aligned, fits)
   const size_t xbytes = (size_t)T * h->cfg.H * 2;
   const int staged = T > 1 && xbytes <= (size_t)kRouteXStage && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
-  return launch_dependent(route_decode_kernel, dim3(h->cfg.E), dim3(kRouteThreads), staged ? xbytes : 0, s, a,
-                          select ? 1 : 0, staged);
+  const dim3 grid(h->cfg.E), block(kRouteThreads);
+  const size_t dyn = staged ? xbytes : 0;
+  if (T <= 2)
+    return select ? launch_dependent(route_decode_kernel<true, 2>, grid, block, dyn, s, a, staged)
+                  : launch_dependent(route_decode_kernel<false, 2>, grid, block, dyn, s, a, staged);
+  return select ? launch_dependent(route_decode_kernel<true, kMaxDecodeT>, grid, block, dyn, s, a, staged)
+                : launch_dependent(route_decode_kernel<false, kMaxDecodeT>, grid, block, dyn, s, a, staged);
 }
 
 cudaError_t launch_route_prefill(Handle* h, const __nv_bfloat16* x, int T, int32_t* ids_out, float* gates_out,
