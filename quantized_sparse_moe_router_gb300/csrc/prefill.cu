@@ -716,6 +716,7 @@ __global__ void split_router_kernel(const float* __restrict__ wr, int64_t n, __n
 // ------------------------------------------------------------- gather, combine
 // One warp per row, 16 bytes per lane per step (no per-element division).
 constexpr int kRowThreads = 256;
+constexpr int kGatherBatch = 8;  // 16-byte chunks of a row a lane has in flight
 
 // xperm[pos] = x[row_token[pos]].
 __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const __nv_bfloat16* __restrict__ x,
@@ -724,41 +725,72 @@ __global__ void __launch_bounds__(kRowThreads) gather_rows_kernel(const __nv_bfl
   const int chunks = H / 8, lane = threadIdx.x & 31;
   pdl_wait();  // the scatter's row tokens
   pdl_launch_dependents();
+  // warp w copies rows w, w + nw, ...: their tokens 32 at a time (one load a
+  // lane, then shuffles), and each row's 16-byte chunks kGatherBatch a lane
+  // in flight before any store
   const int nw = gridDim.x * (kRowThreads / 32);
-  for (int pos = blockIdx.x * (kRowThreads / 32) + (threadIdx.x >> 5); pos < rows; pos += nw) {
-    const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)row_token[pos] * H);
-    uint4* dst = reinterpret_cast<uint4*>(xperm + (int64_t)pos * H);
-    for (int c = lane; c < chunks; c += 32) dst[c] = __ldg(src + c);
+  for (int p0 = blockIdx.x * (kRowThreads / 32) + (threadIdx.x >> 5); p0 < rows; p0 += 32 * nw) {
+    const int mine = p0 + lane * nw;
+    const int tok_l = mine < rows ? row_token[mine] : 0;
+    const int nr = ::min(32, (rows - p0 + nw - 1) / nw);
+    for (int i = 0; i < nr; ++i) {
+      const int tok = __shfl_sync(0xFFFFFFFFu, tok_l, i);
+      const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)tok * H);
+      uint4* dst = reinterpret_cast<uint4*>(xperm + (int64_t)(p0 + i * nw) * H);
+      for (int c0 = lane; c0 < chunks; c0 += 32 * kGatherBatch) {
+        uint4 v[kGatherBatch];
+#pragma unroll
+        for (int u = 0; u < kGatherBatch; ++u)
+          if (c0 + 32 * u < chunks) v[u] = __ldg(src + c0 + 32 * u);
+#pragma unroll
+        for (int u = 0; u < kGatherBatch; ++u)
+          if (c0 + 32 * u < chunks) dst[c0 + 32 * u] = v[u];
+      }
+    }
   }
 }
 
 // out[t] = sum over the token's slots j (ascending) of g[t, j] Yp[inv[t*k + j]],
 // then the shared expert's row (weight 1); fp32 sum, one bf16 rounding. (The
 // gate is applied here rather than in the down GEMM's epilogue, which is on
-// the GEMM's critical path.) One CTA per token,
-// a thread per 16-byte chunk (all of a chunk's k + S row loads in flight).
+// the GEMM's critical path.) One CTA per token: its rows and gates into shared
+// memory, then a thread per 16-byte chunk with all of the chunk's k + S <= kN
+// row loads in flight before the sum (in slot order).
+template <int kN>
 __global__ void __launch_bounds__(kRowThreads) combine_kernel(const __nv_bfloat16* __restrict__ yp,
                                                               const int32_t* __restrict__ inv,
                                                               const float* __restrict__ gates, int T, int k, int S,
                                                               int H, __nv_bfloat16* __restrict__ out) {
-  const int chunks = H / 8;
+  __shared__ int s_row[kN];
+  __shared__ float s_g[kN];
+  const int chunks = H / 8, n = k + S;
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    if (threadIdx.x < n) {
+      const int j = threadIdx.x, slot = j < k ? t * k + j : T * k + t;
+      s_row[j] = inv[slot];
+      s_g[j] = j < k ? gates[slot] : 1.0f;
+    }
+    __syncthreads();
     for (int c = threadIdx.x; c < chunks; c += kRowThreads) {
+      uint4 v[kN];
+#pragma unroll
+      for (int j = 0; j < kN; ++j)
+        if (j < n) v[j] = __ldg(reinterpret_cast<const uint4*>(yp + (int64_t)s_row[j] * H) + c);
       float acc[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-#pragma unroll 4
-      for (int j = 0; j < k + S; ++j) {
-        const int slot = j < k ? t * k + j : T * k + t;
-        const float g = j < k ? __ldg(gates + slot) : 1.0f;
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(yp + (int64_t)inv[slot] * H) + c);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float lo, hi;
-          bf16x2_to_f32(w[q], lo, hi);
-          acc[2 * q] = fmaf(g, lo, acc[2 * q]);
-          acc[2 * q + 1] = fmaf(g, hi, acc[2 * q + 1]);
+      for (int j = 0; j < kN; ++j) {
+        if (j < n) {
+          const float g = s_g[j];
+          const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float lo, hi;
+            bf16x2_to_f32(w[q], lo, hi);
+            acc[2 * q] = fmaf(g, lo, acc[2 * q]);
+            acc[2 * q + 1] = fmaf(g, hi, acc[2 * q + 1]);
+          }
         }
       }
       uint4 o;
@@ -768,6 +800,7 @@ __global__ void __launch_bounds__(kRowThreads) combine_kernel(const __nv_bfloat1
       o.w = pack_bf16x2(acc[6], acc[7]);
       reinterpret_cast<uint4*>(out + (int64_t)t * H)[c] = o;
     }
+    __syncthreads();  // s_row and s_g are rewritten for the next token
   }
 }
 
@@ -975,7 +1008,11 @@ cudaError_t launch_ffn_prefill(Handle* h, const __nv_bfloat16* x, int T, __nv_bf
   if (err != cudaSuccess) return err;
   {
     KernelTimer tm(h, FW_KERNEL_PREFILL_COMBINE, s);
-    combine_kernel<<<(unsigned)std::min(T, h->num_sms * 16), kRowThreads, 0, s>>>(h->yp, h->inv, h->gates, T, k, S, H, out);
+    const unsigned cgrid = (unsigned)std::min(T, h->num_sms * 16);
+    if (k + S <= 9)
+      combine_kernel<9><<<cgrid, kRowThreads, 0, s>>>(h->yp, h->inv, h->gates, T, k, S, H, out);
+    else
+      combine_kernel<kMaxK + 1><<<cgrid, kRowThreads, 0, s>>>(h->yp, h->inv, h->gates, T, k, S, H, out);
   }
   return cudaGetLastError();
 }
