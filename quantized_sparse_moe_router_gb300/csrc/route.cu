@@ -41,21 +41,29 @@ constexpr int kRouteXStage = 64 * 1024;  // x staged in shared memory by one bul
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kRouteUnroll = 8;  // float4 loads of the router row in flight per lane
 
-// Grid: E CTAs of 8 warps; CTA e computes z[t][e] for the T <= kT tokens, its
-// warps splitting H with all of a lane's loads issued before any use. With
-// kSelect (the route-only entry point), the last CTA to finish (atomic ticket,
-// no waiting) also selects, makes the gates and groups the (token, slot) pairs
-// and publishes them; without it the logits are the only output (the expert
-// kernels rebuild the routing from them), and the kernel holds no routing
-// tables in shared memory. With kT = 2 it also holds two accumulators a
-// thread instead of 16: so sized, its CTAs fit beside a one-token expert
-// kernel's, which lets them launch, and prefetch their rows, while that
-// kernel still runs.
-template <bool kSelect, int kT>
-__global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a, int staged) {
+// Grid: E CTAs of kNT / 32 warps; CTA e computes z[t][e] for the T <= kT
+// tokens, its warps splitting H with all of a lane's loads issued before any
+// use. With kSelect (the route-only entry point), the last CTA to finish
+// (atomic ticket, no waiting) also selects, makes the gates and groups the
+// (token, slot) pairs and publishes them; without it the logits are the only
+// output (the expert kernels rebuild the routing from them), and the kernel
+// holds no routing tables in shared memory.
+//
+// kNT = 128 (one or two tokens, H <= kSmallRouterH, no selection): four
+// warps of two accumulators a thread and four row loads in flight a lane, at
+// most 32 registers. So sized, two of its CTAs fit in what a one-token
+// expert CTA leaves of an SM (the registers of each scheduler's share of
+// warps included), which lets them launch, and prefetch their rows, while
+// that kernel still runs. At larger H the eight-warp form, though it cannot
+// launch early, is faster (7,168: 3.5 against 5.6 us after the wait).
+constexpr int kSmallRouterH = 2048;
+template <bool kSelect, int kT, int kNT>
+__global__ void __launch_bounds__(kNT, kNT == 128 ? 16 : 1) route_decode_kernel(RouteArgs a, int staged) {
   static_assert(kT == 2 || kT == kMaxDecodeT, "two tokens, or the decode limit");
+  static_assert(kNT == kRouteThreads || (kNT == 128 && kT == 2 && !kSelect), "the small form: two tokens, no selection");
+  constexpr int kNW = kNT / 32, kU = kNT == 128 ? 4 : kRouteUnroll;
   extern __shared__ __align__(128) uint8_t x_s[];  // [T][H] bf16 when staged
-  __shared__ float s_part[kRouteWarps][kT];
+  __shared__ float s_part[kNW][kT];
   __shared__ __align__(8) uint64_t xbar;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int e = blockIdx.x;
@@ -97,16 +105,16 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
 #pragma unroll
     for (int t = 0; t < kT; ++t) acc[t] = 0.0f;
     const float* wrow = a.wr + (int64_t)e * H;
-    for (int base = 4 * tid; base < H; base += 4 * kRouteThreads * kRouteUnroll) {
-      float4 w[kRouteUnroll];
+    for (int base = 4 * tid; base < H; base += 4 * kNT * kU) {
+      float4 w[kU];
 #pragma unroll
-      for (int u = 0; u < kRouteUnroll; ++u) {
-        int h = base + 4 * kRouteThreads * u;
+      for (int u = 0; u < kU; ++u) {
+        int h = base + 4 * kNT * u;
         w[u] = h < H ? __ldg(reinterpret_cast<const float4*>(wrow + h)) : make_float4(0.f, 0.f, 0.f, 0.f);
       }
 #pragma unroll
-      for (int u = 0; u < kRouteUnroll; ++u) {
-        int h = base + 4 * kRouteThreads * u;
+      for (int u = 0; u < kU; ++u) {
+        int h = base + 4 * kNT * u;
         if (h < H) {
 #pragma unroll
           for (int t = 0; t < kT; ++t) {
@@ -157,7 +165,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
   if (tid < T) {
     float z = 0.f;
 #pragma unroll
-    for (int w = 0; w < kRouteWarps; ++w) z += s_part[w][tid];
+    for (int w = 0; w < kNW; ++w) z += s_part[w][tid];
     a.logits[tid * a.E + e] = z + a.bias[e];
     if (kSelect) __threadfence();
   }
@@ -170,10 +178,10 @@ __global__ void __launch_bounds__(kRouteThreads) route_decode_kernel(RouteArgs a
     __threadfence();
     __shared__ SmemRouting r;
     __shared__ __align__(16) float zbuf[kMaxDecodeT * kMaxE];
-    route_in_smem<kRouteThreads>(a.logits, T, a.E, a.k, a.S, r, zbuf);
+    route_in_smem<kNT>(a.logits, T, a.E, a.k, a.S, r, zbuf);
     RoutingOut o{a.ids_out, a.gates_out, a.ids,      a.gates,    a.counts, a.offsets,
                  a.perm,    a.inv,       a.row_token, a.row_gate, a.uinfo,  a.meta};
-    publish_routing<kRouteThreads>(r, T, a.E, a.k, a.S, o);
+    publish_routing<kNT>(r, T, a.E, a.k, a.S, o);
   }
 }
 
@@ -536,11 +544,12 @@ cudaError_t configure_route_kernels() {
   // The decode router runs on the SMs that the expert kernel (all of shared
   // memory) takes next: with the same carve-out an SM need not be
   // reconfigured between the two.
-  void (*const routers[4])(RouteArgs, int) = {route_decode_kernel<false, 2>, route_decode_kernel<true, 2>,
-                                               route_decode_kernel<false, kMaxDecodeT>,
-                                               route_decode_kernel<true, kMaxDecodeT>};
+  void (*const routers[5])(RouteArgs, int) = {
+      route_decode_kernel<false, 2, 128>, route_decode_kernel<false, 2, kRouteThreads>,
+      route_decode_kernel<true, 2, kRouteThreads>, route_decode_kernel<false, kMaxDecodeT, kRouteThreads>,
+      route_decode_kernel<true, kMaxDecodeT, kRouteThreads>};
   cudaError_t e = cudaSuccess;
-  for (int i = 0; i < 4 && e == cudaSuccess; ++i) {
+  for (int i = 0; i < 5 && e == cudaSuccess; ++i) {
     e = cudaFuncSetAttribute(routers[i], cudaFuncAttributePreferredSharedMemoryCarveout,
                              (int)cudaSharedmemCarveoutMaxShared);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(routers[i], cudaFuncAttributeMaxDynamicSharedMemorySize, kRouteXStage);
@@ -563,13 +572,17 @@ cudaError_t launch_route_decode(Handle* h, const __nv_bfloat16* x, int T, int32_
   // x by one bulk copy into shared memory for several tokens (16-byte aligned, fits)
   const size_t xbytes = (size_t)T * h->cfg.H * 2;
   const int staged = T > 1 && xbytes <= (size_t)kRouteXStage && (reinterpret_cast<uintptr_t>(x) & 15) == 0;
-  const dim3 grid(h->cfg.E), block(kRouteThreads);
+  const dim3 grid(h->cfg.E);
   const size_t dyn = staged ? xbytes : 0;
+  const dim3 block(kRouteThreads);
+  if (T <= 2 && !select && h->cfg.H <= kSmallRouterH)
+    return launch_dependent(route_decode_kernel<false, 2, 128>, grid, dim3(128), dyn, s, a, staged);
   if (T <= 2)
-    return select ? launch_dependent(route_decode_kernel<true, 2>, grid, block, dyn, s, a, staged)
-                  : launch_dependent(route_decode_kernel<false, 2>, grid, block, dyn, s, a, staged);
-  return select ? launch_dependent(route_decode_kernel<true, kMaxDecodeT>, grid, block, dyn, s, a, staged)
-                : launch_dependent(route_decode_kernel<false, kMaxDecodeT>, grid, block, dyn, s, a, staged);
+    return select ? launch_dependent(route_decode_kernel<true, 2, kRouteThreads>, grid, block, dyn, s, a, staged)
+                  : launch_dependent(route_decode_kernel<false, 2, kRouteThreads>, grid, block, dyn, s, a, staged);
+  return select ? launch_dependent(route_decode_kernel<true, kMaxDecodeT, kRouteThreads>, grid, block, dyn, s, a, staged)
+                : launch_dependent(route_decode_kernel<false, kMaxDecodeT, kRouteThreads>, grid, block, dyn, s, a,
+                                   staged);
 }
 
 cudaError_t launch_route_prefill(Handle* h, const __nv_bfloat16* x, int T, int32_t* ids_out, float* gates_out,
