@@ -811,6 +811,16 @@ cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfl
   a.stages = (int)std::min<int64_t>(kMaxStages, ring_bytes / a.stage_bytes);
   if (a.stages < 2) return cudaErrorInvalidConfiguration;
   const int grid = h->num_sms;
+  if (!multi) {
+    // One token: a CTA streams about ceil((k + S) I/16 / grid) chunks of
+    // n_gu + n_dn stages. A ring deeper than a third of that only front-loads
+    // the requests: every CTA's first stages then queue behind everyone's
+    // later ones (1-token call at H = 2048, nine stages a CTA: ring of 2
+    // stages 20.0 us, 3: 18.0, 4: 18.3, 5: 18.4; at H = 7168, 96 stages a
+    // CTA, the deepest ring is fastest).
+    const int64_t per_cta = ((int64_t)(k + S) * (I / kChunk) + grid - 1) / grid * (kChunk / R + (H + a.Dr - 1) / a.Dr);
+    a.stages = (int)std::min<int64_t>(a.stages, std::max<int64_t>(3, (per_cta + 2) / 3));
+  }
   // the ring also holds the logits while routing and the sums at the end
   if (grid > kMaxGrid) return cudaErrorInvalidConfiguration;
   // the final sums: part sums (at most max(kCT, T rows) floats), then the per-token CTA lists
