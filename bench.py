@@ -253,6 +253,20 @@ def work_bytes_layer(w):
     return (w.E + w.S) * 3 * w.I * w.H * (1 + 4 / 32)
 
 
+def gemm_roofline(fl, gb, k_us, hbm, bf16, peak_src):
+    """Roofline of a GEMM launch doing fl FLOPs over gb algorithmic bytes in k_us: bound by
+    whichever of the two takes longer at its peak (bf16 TFLOP/s, HBM GB/s); the other beside it."""
+    tf = fl / (k_us / 1e6) / 1e12
+    bw = gb / (k_us / 1e6) / 1e9
+    tensor_side = {"achieved": round(tf, 1), "peak": bf16, "unit": "TFLOP/s", "frac": round(tf / bf16, 4),
+                   "algorithmic_flops_per_launch": round(fl), "peak_source": f"{peak_src} bf16_tflops (cuBLAS burst)"}
+    hbm_side = {"achieved": round(bw, 1), "peak": hbm, "unit": "GB/s", "frac": round(bw / hbm, 4),
+                "algorithmic_bytes_per_launch": round(gb), "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"}
+    if fl / (bf16 * 1e12) >= gb / (hbm * 1e9):
+        return {"bound": "tensor", **tensor_side, "hbm": hbm_side}
+    return {"bound": "hbm", **hbm_side, "tensor": tensor_side}
+
+
 # ------------------------------------------------------------ fw arm
 def time_workload(w, layers, args, world, dev, e2e: bool):
     """Time one workload on its layers: graph of one step, REPEATS x K replays,
@@ -355,15 +369,15 @@ def time_workload(w, layers, args, world, dev, e2e: bool):
                     "algorithmic_bytes_per_launch": round(dom_bytes),
                     "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"}
     else:
-        # the gate/up "launch": the GEMM launches of one call (big, mid and small token tiles)
+        # the gate/up "launch": the GEMM launches of one call (big, mid and small token tiles).
+        # Its bound is the binding one of its own work: its FLOPs at the bf16 peak or its
+        # bytes (the touched experts' gate/up weights once, x in, h out) at the HBM peak;
+        # the other is reported beside it.
         dom = "prefill_gateup"
         k_us = avg_us(dom) + avg_us("prefill_gateup_mid") + avg_us("prefill_gateup_small")
-        fl = work["flops"] * 2 / 3 / n_calls
-        achieved = fl / (k_us / 1e6) / 1e12
-        roofline = {"bound": "tensor", "achieved": round(achieved, 1), "peak": bf16_burst, "unit": "TFLOP/s",
-                    "frac": round(achieved / bf16_burst, 4), "traffic": measured_traffic(dom, w.name),
-                    "kernel": dom, "avg_launch_us": round(k_us, 3), "algorithmic_flops_per_launch": round(fl),
-                    "peak_source": f"{peak_src} bf16_tflops (cuBLAS burst)"}
+        roofline = gemm_roofline(work["flops"] * 2 / 3 / n_calls, work["gu_bytes"] / n_calls, k_us, hbm, bf16_burst,
+                                 peak_src)
+        roofline.update({"traffic": measured_traffic(dom, w.name), "kernel": dom, "avg_launch_us": round(k_us, 3)})
     step_bytes = work["bytes"]
     call_roof_us = max(step_bytes / calls_per_step / (hbm * 1e9), work["flops"] / calls_per_step / (bf16_burst * 1e12)) * 1e6
     whole = {"us_per_call": round(call_us, 3), "roofline_us_per_call": round(call_roof_us, 3),

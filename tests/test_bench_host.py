@@ -49,3 +49,17 @@ def test_measured_traffic_requires_matching_source(tmp_path, monkeypatch):
 
 def test_whole_job_rate_is_aggregate():
     assert bench.whole_job_rate(100.0, 2.0, 4) == 200.0
+
+
+def test_gemm_roofline_takes_the_binding_bound():
+    # a weight-streaming GEMM (few FLOPs a byte) is HBM-bound, a token-heavy one tensor-bound;
+    # achieved and frac follow from the work and the time, and the other bound is reported beside
+    import bench
+    hbm, bf16 = 6789.0, 1905.7
+    r = bench.gemm_roofline(fl=1.08e12, gb=8.2e9, k_us=1700.0, hbm=hbm, bf16=bf16, peak_src="measured")
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s"
+    assert abs(r["achieved"] - 8.2e9 / 1700e-6 / 1e9) < 0.1 and abs(r["frac"] - r["achieved"] / hbm) < 1e-4
+    assert r["tensor"]["unit"] == "TFLOP/s" and abs(r["tensor"]["achieved"] - 1.08e12 / 1700e-6 / 1e12) < 0.1
+    r = bench.gemm_roofline(fl=2.06e11, gb=0.5e9, k_us=305.0, hbm=hbm, bf16=bf16, peak_src="measured")
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["hbm"]["unit"] == "GB/s"
+    assert abs(r["frac"] - 2.06e11 / 305e-6 / 1e12 / bf16) < 1e-4
