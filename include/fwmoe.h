@@ -136,6 +136,29 @@ fw_status fw_moe_get_permutation(fw_moe_handle *h, int32_t *offsets, int32_t *pe
  * DEVICE memory of rows x K/32 x 34 bytes. Round-trips fw_moe_init's input. */
 fw_status fw_moe_export_q8_0(fw_moe_handle *h, int32_t expert, int32_t which, uint8_t *blocks, void *stream);
 
+/* A chain of layer calls captured once as one CUDA graph and replayed by a
+ * single launch (Flyweight README, §Current limitations: host
+ * synchronisation points of dynamic MoE routing, persistent layer kernels
+ * listed as incomplete; §Features: CUDA-graph replay of decode). No call of
+ * fw_moe_forward synchronises with the host -- routing, grouping and tile
+ * lists stay on the device for both paths -- so n of them capture into one
+ * graph. Call i runs fw_moe_forward(layers[i], x[i], T, expert_ids[i], NULL,
+ * out[i]): x[i] and out[i] DEVICE bf16 [T, H_i], 16-byte aligned (out[i] may be
+ * x[i + 1], chaining the layers); expert_ids[i] DEVICE int32 [T, k_i]. The
+ * handles, T and every pointer are fixed at capture; the buffers' contents
+ * are read at each launch. Capture runs on a stream of its own on the current
+ * device, which must be every layer's. Replays of one graph, and other work
+ * on its layers, must not overlap (they share each handle's workspace).
+ * Errors: FW_EINVAL for arguments (before any CUDA call), FW_ESTATE if a layer
+ * is profiling, else what a capture or instantiation reports. */
+typedef struct fw_moe_graph fw_moe_graph;
+fw_status fw_moe_graph_create(fw_moe_handle *const *layers, int32_t n, int32_t T, const void *const *x,
+                              void *const *out, int32_t *const *expert_ids, fw_moe_graph **graph);
+/* Enqueue one replay of the chain on `stream`. */
+fw_status fw_moe_graph_launch(fw_moe_graph *graph, void *stream);
+/* Release the graph (not its layers). NULL is a no-op. */
+fw_status fw_moe_graph_destroy(fw_moe_graph *graph);
+
 /* Synchronise `stream`, read and clear the handle's device status word.
  * FW_OK, FW_ETIMEOUT or FW_EDEVICE. */
 fw_status fw_moe_status(fw_moe_handle *h, void *stream);

@@ -50,7 +50,8 @@ _lib = None
 
 EXPORTED = ("fw_moe_init", "fw_moe_route", "fw_moe_ffn", "fw_moe_forward", "fw_moe_forward_host",
             "fw_moe_get_permutation", "fw_moe_export_q8_0", "fw_moe_status", "fw_moe_free", "fw_moe_last_error",
-            "fw_q8_0_quantize", "fw_moe_profile_begin", "fw_moe_profile_end", "fw_moe_route_noalloc")
+            "fw_q8_0_quantize", "fw_moe_profile_begin", "fw_moe_profile_end", "fw_moe_route_noalloc",
+            "fw_moe_graph_create", "fw_moe_graph_launch", "fw_moe_graph_destroy")
 
 KERNEL_KINDS = ("route_decode", "route_tiles", "route_scan", "route_scatter", "decode_experts", "reserved",
                 "prefill_gateup", "prefill_down", "prefill_combine", "prefill_gather", "prefill_gateup_small",
@@ -80,6 +81,9 @@ def lib():
             "fw_moe_profile_begin": [vp, i32],
             "fw_moe_profile_end": [vp, i32, vp, vp],
             "fw_moe_route_noalloc": [vp, i32, i32, vp, vp, i32, i32, vp, vp, vp],
+            "fw_moe_graph_create": [vp, i32, i32, vp, vp, vp, ctypes.POINTER(vp)],
+            "fw_moe_graph_launch": [vp, vp],
+            "fw_moe_graph_destroy": [vp],
         }
         for name, args in sig.items():
             f = getattr(L, name)
@@ -139,6 +143,24 @@ def fw_moe_free(h):
     _check(lib().fw_moe_free(h), "fw_moe_free")
 
 
+def fw_moe_graph_create(handles, T, xs, outs, ids) -> int:
+    """handles, xs, outs, ids: sequences of raw pointers (one per call)."""
+    n = len(handles)
+    arr = lambda seq: (ctypes.c_void_p * n)(*seq)
+    g = ctypes.c_void_p()
+    _check(lib().fw_moe_graph_create(arr(handles), n, T, arr(xs), arr(outs), arr(ids), ctypes.byref(g)),
+           "fw_moe_graph_create")
+    return g.value
+
+
+def fw_moe_graph_launch(g, stream):
+    _check(lib().fw_moe_graph_launch(g, stream), "fw_moe_graph_launch")
+
+
+def fw_moe_graph_destroy(g):
+    _check(lib().fw_moe_graph_destroy(g), "fw_moe_graph_destroy")
+
+
 def fw_q8_0_quantize(w, rows, K, blocks, stream):
     _check(lib().fw_q8_0_quantize(w, rows, K, blocks, stream), "fw_q8_0_quantize")
 
@@ -185,6 +207,32 @@ def quantize_q8_0(w, out=None, stream=None):
         out = torch.empty((rows, K // 32 * 34), dtype=torch.uint8, device=w.device)
     fw_q8_0_quantize(_ptr(w), rows, K, _ptr(out), _stream(stream))
     return out
+
+
+class MoEGraph:
+    """A chain of layer calls captured once as one CUDA graph and replayed by one
+    launch (fw_moe_graph_* in include/fwmoe.h): call i is layers[i].forward of
+    xs[i] into outs[i] with expert ids into ids[i] (outs[i] may be xs[i + 1])."""
+
+    def __init__(self, layers, xs, outs, ids):
+        T = xs[0].shape[0]
+        self.graph = fw_moe_graph_create([L.handle for L in layers], T, [_ptr(x) for x in xs],
+                                         [_ptr(o) for o in outs], [_ptr(i) for i in ids])
+        self._keep = (list(layers), list(xs), list(outs), list(ids))  # the graph reads them at each launch
+
+    def launch(self, stream=None):
+        fw_moe_graph_launch(self.graph, _stream(stream))
+
+    def close(self):
+        if self.graph:
+            g, self.graph = self.graph, None
+            fw_moe_graph_destroy(g)
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 class MoELayer:

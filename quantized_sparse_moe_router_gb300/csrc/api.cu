@@ -8,6 +8,7 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <new>
 #include <unordered_set>
 #include <vector>
 
@@ -332,6 +333,103 @@ fw_status fw_moe_forward(fw_moe_handle* hh, const void* x, int32_t T, int32_t* e
     h->last_T = -1;
     return cuda_fail(e, "fw_moe_forward launch");
   }
+  return FW_OK;
+}
+
+}  // extern "C"
+
+namespace fw {
+namespace {
+constexpr uint32_t kGraphMagic = 0x4772614Du;  // "MarG"
+struct Graph {
+  uint32_t magic;
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+std::unordered_set<Graph*> g_live_graphs;  // under g_live_mu; a pointer is checked here before it is read
+bool live_graph(Graph* g) {
+  std::lock_guard<std::mutex> lk(g_live_mu);
+  return g && g_live_graphs.count(g) && g->magic == kGraphMagic;
+}
+}  // namespace
+}  // namespace fw
+
+extern "C" {
+
+fw_status fw_moe_graph_create(fw_moe_handle* const* layers, int32_t n, int32_t T, const void* const* x,
+                              void* const* out, int32_t* const* expert_ids, fw_moe_graph** graph) {
+  if (!graph) return fail(FW_EINVAL, "fw_moe_graph_create: graph is null");
+  *graph = nullptr;
+  if (!layers || !x || !out || !expert_ids || n < 1 || T < 1)
+    return fail(FW_EINVAL, "fw_moe_graph_create: needs n >= 1 layers, T >= 1 and the x, out and expert_ids arrays");
+  for (int i = 0; i < n; ++i) {
+    Handle* h = reinterpret_cast<Handle*>(layers[i]);
+    if (!live(h)) return fail(FW_EINVAL, "fw_moe_graph_create: layer %d is not a live handle", i);
+    if (T > h->cfg.T_max) return fail(FW_EINVAL, "fw_moe_graph_create: T=%d above layer %d's T_max=%d", T, i, h->cfg.T_max);
+    if (!x[i] || !aligned(x[i], 16) || !out[i] || !aligned(out[i], 16) || !expert_ids[i] || !aligned(expert_ids[i], 4))
+      return fail(FW_EINVAL, "fw_moe_graph_create: call %d: x and out must be 16-byte, expert_ids 4-byte aligned", i);
+    if (h->timing) return fail(FW_ESTATE, "fw_moe_graph_create: layer %d is profiling", i);
+  }
+  cudaStream_t cs;
+  cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return cuda_fail(e, "fw_moe_graph_create: stream");
+  e = cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal);
+  if (e != cudaSuccess) {
+    cudaStreamDestroy(cs);
+    return cuda_fail(e, "fw_moe_graph_create: begin capture");
+  }
+  fw_status st = FW_OK;
+  char why[sizeof(g_err) + 64] = "";
+  for (int i = 0; i < n && st == FW_OK; ++i) {
+    st = fw_moe_forward(layers[i], x[i], T, expert_ids[i], nullptr, out[i], cs);
+    if (st != FW_OK) snprintf(why, sizeof(why), "fw_moe_graph_create: call %d: %s", i, g_err);
+  }
+  cudaGraph_t g = nullptr;
+  e = cudaStreamEndCapture(cs, &g);  // ends the capture whatever happened inside it
+  cudaStreamDestroy(cs);
+  if (st != FW_OK || e != cudaSuccess) {
+    if (g) cudaGraphDestroy(g);
+    if (st != FW_OK) return fail(st, "%s", why);
+    return cuda_fail(e, "fw_moe_graph_create: end capture");
+  }
+  cudaGraphExec_t ge = nullptr;
+  e = cudaGraphInstantiate(&ge, g, 0);
+  if (e != cudaSuccess) {
+    cudaGraphDestroy(g);
+    return cuda_fail(e, "fw_moe_graph_create: instantiate");
+  }
+  Graph* gr = new (std::nothrow) Graph{kGraphMagic, g, ge};
+  if (!gr) {
+    cudaGraphExecDestroy(ge);
+    cudaGraphDestroy(g);
+    return fail(FW_ENOMEM, "fw_moe_graph_create: out of host memory");
+  }
+  {
+    std::lock_guard<std::mutex> lk(g_live_mu);
+    g_live_graphs.insert(gr);
+  }
+  *graph = reinterpret_cast<fw_moe_graph*>(gr);
+  return FW_OK;
+}
+
+fw_status fw_moe_graph_launch(fw_moe_graph* graph, void* stream) {
+  Graph* g = reinterpret_cast<Graph*>(graph);
+  if (!live_graph(g)) return fail(FW_EINVAL, "fw_moe_graph_launch: not a live graph");
+  cudaError_t e = cudaGraphLaunch(g->exec, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? FW_OK : cuda_fail(e, "fw_moe_graph_launch");
+}
+
+fw_status fw_moe_graph_destroy(fw_moe_graph* graph) {
+  Graph* g = reinterpret_cast<Graph*>(graph);
+  if (!g) return FW_OK;
+  {
+    std::lock_guard<std::mutex> lk(g_live_mu);
+    if (!g_live_graphs.erase(g)) return fail(FW_EINVAL, "fw_moe_graph_destroy: not a live graph");
+  }
+  g->magic = 0;
+  cudaGraphExecDestroy(g->exec);
+  cudaGraphDestroy(g->graph);
+  delete g;
   return FW_OK;
 }
 

@@ -110,3 +110,19 @@ def test_noalloc_router_rejects_bad_arguments_before_any_device_call():
     assert call(ids=4098) == fw.FW_EINVAL and call(g=4098) == fw.FW_EINVAL and call(b=4098) == fw.FW_EINVAL
     assert "alignment" in fw.fw_moe_last_error()
     assert call(T=0, x=None, w=None, ids=None) == fw.FW_OK  # nothing to route
+
+
+def test_graph_calls_reject_bad_arguments_on_the_host():
+    L = fw.lib()
+    g = ctypes.c_void_p()
+    assert L.fw_moe_graph_create(None, 1, 1, None, None, None, None) == fw.FW_EINVAL
+    assert L.fw_moe_graph_create(None, 0, 1, None, None, None, ctypes.byref(g)) == fw.FW_EINVAL
+    assert g.value is None
+    one = (ctypes.c_void_p * 1)(4096)
+    rc = L.fw_moe_graph_create(one, 1, 1, one, one, one, ctypes.byref(g))
+    assert rc == fw.FW_EINVAL and "not a live handle" in fw.fw_moe_last_error()
+    assert L.fw_moe_graph_create(one, 1, 0, one, one, one, ctypes.byref(g)) == fw.FW_EINVAL
+    assert L.fw_moe_graph_launch(None, None) == fw.FW_EINVAL
+    assert L.fw_moe_graph_launch(777, None) == fw.FW_EINVAL  # checked against the live set, not read
+    assert L.fw_moe_graph_destroy(None) == fw.FW_OK  # NULL is a no-op
+    assert L.fw_moe_graph_destroy(777) == fw.FW_EINVAL
