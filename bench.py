@@ -13,7 +13,7 @@ as the headline.
 A step of a workload is one pass of the whole hot path (route, experts,
 combine) over every layer of the workload for each of its hidden batches
 (64 rows for T = 1, fewer batches for larger T), all on one stream, captured
-once as a CUDA graph and replayed. value = tokens x layer-calls per second.
+once as a CUDA graph by the library (fw_moe_graph_create) and replayed. value = tokens x layer-calls per second.
 Every workload cycles more layers than L2 holds (no flush needed). Timing: CUDA
 events around K graph replays, repeated 5 times, median.
 
@@ -300,15 +300,13 @@ def time_workload(w, layers, args, world, dev, e2e: bool):
     for L in layers:
         L.status()
 
-    graph = torch.cuda.CUDAGraph()
-    cap_stream = torch.cuda.Stream()
-    cap_stream.wait_stream(stream)
-    with torch.cuda.stream(cap_stream):
-        with torch.cuda.graph(graph, stream=cap_stream):
-            step(torch.cuda.current_stream().cuda_stream)
-    stream.wait_stream(cap_stream)
+    # the step as one CUDA graph through the library's own capture (fw_moe_graph_create):
+    # the same calls as step(), replayed by one fw_moe_graph_launch
+    order = [(xs[r], L) for r in range(NX) for L in layers]
+    graph = fw.MoEGraph([L for _, L in order], [x for x, _ in order], [out] * len(order), [ids] * len(order))
+    replay = lambda: graph.launch(sp)
     for _ in range(max(3, args.warmup)):
-        graph.replay()
+        replay()
     torch.cuda.synchronize()
 
     def timed(fn, n):
@@ -324,12 +322,13 @@ def time_workload(w, layers, args, world, dev, e2e: bool):
         barrier()
         return max_over_ranks(t0.elapsed_time(t1), world, dev)
 
-    reps = [timed(graph.replay, args.steps) for _ in range(max(1, args.repeats))]
+    reps = [timed(replay, args.steps) for _ in range(max(1, args.repeats))]
     ms = statistics.median(reps)
     for L in layers:
         L.status()
     value = whole_job_rate(T * calls_per_step * args.steps, ms / 1e3, world)
     ms_eager = timed(step, 1)
+    graph.close()
 
     # ---- per-kernel event pass (events serialise the kernels: a pass of its own, one step)
     for L in layers:
@@ -483,8 +482,8 @@ def run_fw(args, rank, world, local_rank):
         else "bf16 tensor-core (Q8_0 dequantised to bf16), fp32 accumulate",
         "data": "synthetic (seeded Irwin-Hall normals; experts quantised to Q8_0 on the GPU)",
         "config": dict(res["config"], parallelism=f"replicas x{world}"),
-        "timing": f"CUDA events on the launch stream around K replays of a CUDA graph of one step; "
-                  f"median of {args.repeats} repeats",
+        "timing": f"CUDA events on the launch stream around K replays of one step's CUDA graph "
+                  f"(fw_moe_graph_create / fw_moe_graph_launch); median of {args.repeats} repeats",
         "roofline": res["roofline"], "whole_step": res["whole_step"], "kernels": res["kernels"],
         "e2e": res["e2e"], "cpu_baseline": cpu, "gpu_launches": res["gpu_launches"], "clocks": clk,
         "eager_ms_per_step": res["eager_ms_per_step"],
