@@ -59,6 +59,10 @@ def load(path: str):
     L.oracle_moe_forward.argtypes = [i64] * 6 + [vp] * 9
     L.oracle_moe_forward.restype = ctypes.c_int
     L.oracle_moe_experts.argtypes = [i64] * 6 + [vp] * 7
+    L.oracle_q8_activations.argtypes = [vp, i64, i64, vp, vp, vp]
+    L.oracle_q8_activations.restype = ctypes.c_int
+    L.oracle_moe_experts_q8act.argtypes = [i64] * 6 + [vp] * 7
+    L.oracle_moe_experts_q8act.restype = ctypes.c_int
     L.oracle_moe_experts.restype = ctypes.c_int
     return L
 
@@ -183,8 +187,20 @@ def moe_forward(x_bits, Wr, bias, w_gate, w_up, w_down, k: int, S: int = 0):
     return ids, gates, out
 
 
-def moe_experts(x_bits, ids, gates, w_gate, w_up, w_down, E: int, S: int = 0):
-    """Expert part only, from given routing. Returns out [T,H] fp64."""
+def q8_activations(v: np.ndarray, blk: int):
+    """Q8 activations of fp32 v (1-D, len % blk == 0): (q*d fp64, q int8, d fp32 per block)."""
+    v = _c(np.asarray(v, dtype=np.float32).ravel(), np.float32)
+    n = v.size
+    out = np.empty(n, dtype=np.float64)
+    q = np.empty(n, dtype=np.int8)
+    d = np.empty(max(n // blk, 1), dtype=np.float32)
+    if lib().oracle_q8_activations(_p(v), n, blk, _p(out), _p(q), _p(d)) != 0:
+        raise ValueError("oracle_q8_activations: bad sizes")
+    return out, q, d[:n // blk]
+
+
+def moe_experts(x_bits, ids, gates, w_gate, w_up, w_down, E: int, S: int = 0, act_q8: bool = False):
+    """Expert part only, from given routing (act_q8: with Q8 activations). Returns out [T,H] fp64."""
     x_bits = _c(x_bits, np.uint16)
     ids = _c(ids, np.int32)
     gates = _c(gates, np.float64)
@@ -199,7 +215,8 @@ def moe_experts(x_bits, ids, gates, w_gate, w_up, w_down, E: int, S: int = 0):
     u_arr, k2 = _ptr_array(w_up)
     d_arr, k3 = _ptr_array(w_down)
     out = np.empty((T, H), dtype=np.float64)
-    rc = lib().oracle_moe_experts(T, H, I, E, k, S, _p(x_bits), _p(ids), _p(gates), g_arr, u_arr, d_arr, _p(out))
+    fn = lib().oracle_moe_experts_q8act if act_q8 else lib().oracle_moe_experts
+    rc = fn(T, H, I, E, k, S, _p(x_bits), _p(ids), _p(gates), g_arr, u_arr, d_arr, _p(out))
     if rc != 0:
         raise ValueError(f"oracle_moe_experts failed: {rc}")
     return out

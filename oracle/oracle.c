@@ -284,3 +284,78 @@ int oracle_moe_forward(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, in
   if (!gates) free(g);
   return rc;
 }
+
+/* ------------------------------------------------------- Q8 activations */
+
+int oracle_q8_activations(const float *v, int64_t n, int64_t blk, double *out, int8_t *q, float *d) {
+  if (n < 0 || blk <= 0 || n % blk) return -1;
+  for (int64_t b = 0; b < n / blk; ++b) {
+    const float *x = v + b * blk;
+    float amax = 0.0f;
+    for (int64_t i = 0; i < blk; ++i) {
+      float a = fabsf(x[i]);
+      if (a > amax) amax = a;
+    }
+    float db = amax / 127.0f; /* fp32 division */
+    if (d) d[b] = db;
+    for (int64_t i = 0; i < blk; ++i) {
+      double qi = 0.0;
+      if (amax > 0.0f) {
+        float r = x[i] / db; /* fp32 division; its exact value decides the code */
+        qi = round_half_away((double)r);
+        if (qi > 127.0) qi = 127.0;
+        if (qi < -127.0) qi = -127.0;
+      }
+      if (q) q[b * blk + i] = (int8_t)qi;
+      out[b * blk + i] = qi * (double)db;
+    }
+  }
+  return 0;
+}
+
+/* One expert on one token, Q8 activations: x8 is the token's already
+ * quantised x (fp64 [H]); h goes through the same rule in blocks of 16. */
+static void expert_ffn_q8act(const uint8_t *wg, const uint8_t *wu, const uint8_t *wd, int64_t H, int64_t I,
+                             const double *x8, double *y) {
+  float *a32 = (float *)malloc(sizeof(float) * (size_t)I);
+  double *a8 = (double *)malloc(sizeof(double) * (size_t)I);
+  for (int64_t i = 0; i < I; ++i) {
+    double g = q8_0_row_dot(wg, i, H, x8);
+    double u = q8_0_row_dot(wu, i, H, x8);
+    a32[i] = (float)(g / (1.0 + exp(-g)) * u); /* SiLU(g) * u, rounded to fp32 */
+  }
+  oracle_q8_activations(a32, I, 16, a8, NULL, NULL);
+  for (int64_t o = 0; o < H; ++o) y[o] = q8_0_row_dot(wd, o, I, a8);
+  free(a32);
+  free(a8);
+}
+
+int oracle_moe_experts_q8act(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, int64_t S, const uint16_t *x,
+                             const int32_t *ids, const double *gates, const uint8_t *const *w_gate,
+                             const uint8_t *const *w_up, const uint8_t *const *w_down, double *out) {
+  if (!sizes_ok(T, H, I, E, k, S) || I % 16) return -1;
+  float *x32 = (float *)malloc(sizeof(float) * (size_t)H);
+  double *x8 = (double *)malloc(sizeof(double) * (size_t)H);
+  double *y = (double *)malloc(sizeof(double) * (size_t)H);
+  int rc = 0;
+  for (int64_t t = 0; t < T && rc == 0; ++t) {
+    for (int64_t h = 0; h < H; ++h) x32[h] = (float)oracle_bf16_to_double(x[t * H + h]); /* exact */
+    oracle_q8_activations(x32, H, ORACLE_Q8_0_BLOCK, x8, NULL, NULL);
+    double *ot = out + t * H;
+    for (int64_t h = 0; h < H; ++h) ot[h] = 0.0;
+    for (int64_t j = 0; j < k + S && rc == 0; ++j) {
+      const int64_t e = j < k ? ids[t * k + j] : E + (j - k); /* then the always-on expert, weight 1 */
+      if (!w_gate[e] || !w_up[e] || !w_down[e]) {
+        rc = -2;
+        break;
+      }
+      expert_ffn_q8act(w_gate[e], w_up[e], w_down[e], H, I, x8, y);
+      const double g = j < k ? gates[t * k + j] : 1.0;
+      for (int64_t h = 0; h < H; ++h) ot[h] += g * y[h];
+    }
+  }
+  free(x32);
+  free(x8);
+  free(y);
+  return rc;
+}

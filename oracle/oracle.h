@@ -90,6 +90,24 @@ int oracle_moe_experts(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, in
                        const int32_t *ids, const double *gates, const uint8_t *const *w_gate,
                        const uint8_t *const *w_up, const uint8_t *const *w_down, double *out);
 
+/* Q8 activations (the Flyweight README, 0.2.0, §Quantization: Q8-activation
+ * dp4a group-decode kernels, and §Current limitations: the int8 MMQ path;
+ * the pages give no formula, and the reading used here is the Q8_0 rule
+ * applied to an activation vector in fp32): v [n] fp32 is cut into blocks of
+ * blk values (n % blk == 0); per block d = amax/127 and q =
+ * round-half-away-from-zero(v/d) clamped to [-127, 127], the division and d
+ * both in fp32 (an all-zero block: d = 0, q = 0). out [n] = q*d (exact in fp64);
+ * q [n] and d [n/blk] may be NULL. Returns 0, -1 on bad sizes. */
+int oracle_q8_activations(const float *v, int64_t n, int64_t blk, double *out, int8_t *q, float *d);
+
+/* The expert part with Q8 activations: each token's x (bf16 -> fp32) through
+ * oracle_q8_activations in blocks of 32 before the gate/up projections, and
+ * each expert's h = SiLU(g)*u (rounded to fp32) in blocks of 16 before the
+ * down projection; otherwise as oracle_moe_experts. */
+int oracle_moe_experts_q8act(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, int64_t S, const uint16_t *x,
+                             const int32_t *ids, const double *gates, const uint8_t *const *w_gate,
+                             const uint8_t *const *w_up, const uint8_t *const *w_down, double *out);
+
 #ifdef __cplusplus
 }
 #endif

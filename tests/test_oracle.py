@@ -324,3 +324,95 @@ def test_generator_bf16_is_round_to_nearest_even_of_f32():
     bits = synth.normal_bf16_bits(9, 4, 10000, 0.37)
     ref = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(bits, ref)
+
+
+# ------------------------------------------------------- Q8 activations
+def test_q8_activations_closed_forms():
+    # amax 127 gives d = 1 and codes round(v), ties away from zero
+    v = np.array([127, 2.5, -2.5, 0.5, -0.5, 126.5, 0.49, -0.51] + [1.5] * 24, np.float32)
+    out, q, d = oracle.q8_activations(v, 32)
+    assert d.tolist() == [1.0]
+    assert q[:8].tolist() == [127, 3, -3, 1, -1, 127, 0, -1] and set(q[8:].tolist()) == {2}
+    assert np.array_equal(out, q.astype(np.float64))
+    # an all-zero block: d = 0, codes 0, values 0; blocks are independent
+    v = np.concatenate([np.zeros(16, np.float32), np.full(16, 3.0, np.float32)])
+    out, q, d = oracle.q8_activations(v, 16)
+    assert d[0] == 0.0 and not q[:16].any() and not out[:16].any()
+    assert d[1] == np.float32(3.0) / np.float32(127.0) and set(q[16:].tolist()) == {127}
+    # values already on the grid q * 2^-7 with amax = 127 * 2^-7 come back exactly
+    codes = np.arange(-127, 129, 8)[:32].clip(-127, 127).astype(np.float32)
+    codes[0] = -127.0
+    v = codes * np.float32(2.0 ** -7)
+    out, q, d = oracle.q8_activations(v, 32)
+    assert d[0] == np.float32(2.0 ** -7) and np.array_equal(q.astype(np.float32), codes)
+    assert np.array_equal(out, v.astype(np.float64))
+
+
+def test_q8_activations_error_bound():
+    rng = np.random.default_rng(5)
+    v = (rng.standard_normal(64 * 32) * rng.choice([1e-3, 1.0, 40.0], 64).repeat(32)).astype(np.float32)
+    out, q, d = oracle.q8_activations(v, 32)
+    vb = v.reshape(64, 32).astype(np.float64)
+    amax = np.abs(vb).max(axis=1)
+    assert np.all(np.abs(q) <= 127) and np.all(np.abs(q.reshape(64, 32)).max(axis=1) == 127)
+    assert np.allclose(d, amax / 127, rtol=2 ** -23, atol=0)          # d = amax/127 to fp32 rounding
+    err = np.abs(out.reshape(64, 32) - vb)
+    assert np.all(err <= d[:, None].astype(np.float64) * (0.5 + 1e-6))  # half a step, fp32 division slack
+
+
+def test_q8act_experts_with_identity_weights_elementwise():
+    """One expert whose gate, up and down matrices are s * identity (s = 127 * 2^-8: Q8_0 stores it
+    exactly, d = 2^-8, code 127) reduces the Q8-activation step to element-wise operations: x on the
+    2^-7 grid passes the x quantiser unchanged, g = u = s x, h = SiLU(g) u rounded to fp32 and
+    quantised in blocks of 16 (here two blocks of very different size), y[o] = s h8[o] for o < I."""
+    H, I = 64, 32
+    s = 127 * 2.0 ** -8
+    wg = np.zeros((I, H), np.float32)
+    wg[np.arange(I), np.arange(I)] = s
+    wd = np.zeros((H, I), np.float32)
+    wd[np.arange(I), np.arange(I)] = s
+    qg, qd = oracle.q8_0_quantize(wg), oracle.q8_0_quantize(wd)
+    codes = np.concatenate([np.arange(-120, 120, 15)[:16], np.arange(-8, 8)[:16], np.arange(-127, 127, 4)[:32]])
+    codes[0], codes[32] = -127, -127                     # every 32-block of x has amax 127 * 2^-7
+    x = (codes.astype(np.float32) * np.float32(2.0 ** -7))
+    x_bits = (x.view(np.uint32) >> 16).astype(np.uint16)[None, :]   # exact in bf16 (7-bit codes)
+    ids = np.zeros((1, 1), np.int32)
+    gates = np.ones((1, 1))
+    out = oracle.moe_experts(x_bits, ids, gates, [qg], [qg], [qd], E=1, S=0, act_q8=True)[0]
+    g = s * x[:I].astype(np.float64)
+    h32 = (g / (1.0 + np.exp(-g)) * g).astype(np.float32)
+    want = np.zeros(H)
+    for b in range(I // 16):
+        blk = h32[16 * b:16 * b + 16]
+        db = np.float32(np.abs(blk).max()) / np.float32(127.0)
+        r = (blk / db).astype(np.float64)                  # fp32 quotients
+        qb = np.sign(r) * np.floor(np.abs(r) + 0.5)        # ties away (r is exact in fp64)
+        want[16 * b:16 * b + 16] = s * qb * np.float64(db)
+    assert np.allclose(out, want, rtol=1e-12, atol=1e-15)
+    # the two h blocks differ in scale by far more than a code step: one 32-wide block would not match
+    assert np.abs(h32[:16]).max() > 20 * np.abs(h32[16:]).max()
+
+
+def test_q8act_experts_quantise_x_in_blocks_of_32():
+    """Off the grid, x goes through the (separately pinned) activation quantiser in blocks of 32
+    before the projections: with identity weights the output follows element by element."""
+    H, I = 64, 32
+    s = 127 * 2.0 ** -8
+    wg = np.zeros((I, H), np.float32)
+    wg[np.arange(I), np.arange(I)] = s
+    wd = np.zeros((H, I), np.float32)
+    wd[np.arange(I), np.arange(I)] = s
+    qg, qd = oracle.q8_0_quantize(wg), oracle.q8_0_quantize(wd)
+    rng = np.random.default_rng(11)
+    x32 = (rng.standard_normal(H) * np.repeat([0.7, 0.05], 32)).astype(np.float32)
+    u = x32.view(np.uint32)
+    x_bits = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)[None, :]  # to bf16, nearest even
+    xb = (x_bits[0].astype(np.uint32) << 16).view(np.float32)          # the bf16 values, exactly
+    x8 = oracle.q8_activations(xb, 32)[0]
+    assert not np.array_equal(x8, xb.astype(np.float64))              # the quantiser does change x here
+    out = oracle.moe_experts(x_bits, np.zeros((1, 1), np.int32), np.ones((1, 1)), [qg], [qg], [qd], E=1, S=0,
+                             act_q8=True)[0]
+    g = s * x8[:I]
+    h8 = oracle.q8_activations((g / (1.0 + np.exp(-g)) * g).astype(np.float32), 16)[0]
+    want = np.concatenate([s * h8, np.zeros(H - I)])
+    assert np.allclose(out, want, rtol=1e-12, atol=1e-15)
