@@ -214,13 +214,16 @@ void oracle_permutation(const int32_t *ids, int64_t T, int64_t k, int64_t E, int
 
 /* ------------------------------------------------------------------ experts */
 
+/* SiLU(g) * u, SiLU(a) = a / (1 + e^-a). */
+static double silu_times(double g, double u) { return g / (1.0 + exp(-g)) * u; }
+
 void oracle_expert_ffn(const uint8_t *wg, const uint8_t *wu, const uint8_t *wd, int64_t H, int64_t I,
                        const double *x, double *y) {
   double *a = (double *)malloc(sizeof(double) * (size_t)I);
   for (int64_t i = 0; i < I; ++i) {
     double g = q8_0_row_dot(wg, i, H, x);
     double u = q8_0_row_dot(wu, i, H, x);
-    a[i] = g / (1.0 + exp(-g)) * u; /* SiLU(g) * u */
+    a[i] = silu_times(g, u);
   }
   for (int64_t o = 0; o < H; ++o) y[o] = q8_0_row_dot(wd, o, I, a);
   free(a);
@@ -322,7 +325,7 @@ static void expert_ffn_q8act(const uint8_t *wg, const uint8_t *wu, const uint8_t
   for (int64_t i = 0; i < I; ++i) {
     double g = q8_0_row_dot(wg, i, H, x8);
     double u = q8_0_row_dot(wu, i, H, x8);
-    a32[i] = (float)(g / (1.0 + exp(-g)) * u); /* SiLU(g) * u, rounded to fp32 */
+    a32[i] = (float)silu_times(g, u); /* rounded to fp32 */
   }
   oracle_q8_activations(a32, I, 16, a8, NULL, NULL);
   for (int64_t o = 0; o < H; ++o) y[o] = q8_0_row_dot(wd, o, I, a8);
