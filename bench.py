@@ -74,6 +74,8 @@ def parse(argv=None):
     p.add_argument("--repeats", type=int, default=REPEATS)
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--act-q8", action="store_true",
+                   help="Q8 activations on the decode path (an option of the layer; the default is bf16)")
     p.add_argument("--cpu-seconds", type=float, default=15.0,
                    help="host time budget of the oracle baseline (and of the whole reference arm)")
     return p.parse_args(argv)
@@ -195,7 +197,7 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------- layers
-def build_layers(w, n_layers, device, T_max):
+def build_layers(w, n_layers, device, T_max, act_q8=False):
     """n_layers seeded layers of workload w's shapes, quantised to Q8_0 on the GPU."""
     import torch
     import quantized_sparse_moe_router_gb300 as fw
@@ -217,7 +219,7 @@ def build_layers(w, n_layers, device, T_max):
                    "w_gate": q[0][:E], "w_up": q[1][:E], "w_down": q[2][:E]}
         if S:
             weights.update(shared_gate=q[0][E], shared_up=q[1][E], shared_down=q[2][E])
-        layers.append(fw.MoELayer(H, I, E, w.k, n_shared=S, T_max=T_max, weights=weights))
+        layers.append(fw.MoELayer(H, I, E, w.k, n_shared=S, T_max=T_max, weights=weights, act_q8=act_q8))
         del q, Wr, weights
     del tmp
     torch.cuda.synchronize()
@@ -453,7 +455,7 @@ def run_fw(args, rank, world, local_rank):
             wo = workload_of(args, owner)
             n_layers = args.layers or max(synth.WORKLOADS[u].layers for u in users)
             T_max = max(workload_of(args, u).T for u in users)
-            built[owner] = build_layers(wo, n_layers, dev, T_max)
+            built[owner] = build_layers(wo, n_layers, dev, T_max, act_q8=args.act_q8)
         layers = built[owner][:(args.layers or w.layers)]
         if name == head:
             clocks.start()
@@ -478,10 +480,11 @@ def run_fw(args, rank, world, local_rank):
         "metric": metric_name(w), "value": res["value"], "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["ms_per_step"], "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "fp32 (Q8_0 weights x bf16 activations, fp32 accumulate)" if w.T <= 16
+        "dtype": ("int32 dot products (Q8_0 weights x Q8 activations), fp32 scales and sums" if args.act_q8
+                  else "fp32 (Q8_0 weights x bf16 activations, fp32 accumulate)") if w.T <= 16
         else "bf16 tensor-core (Q8_0 dequantised to bf16), fp32 accumulate",
         "data": "synthetic (seeded Irwin-Hall normals; experts quantised to Q8_0 on the GPU)",
-        "config": dict(res["config"], parallelism=f"replicas x{world}"),
+        "config": dict(res["config"], parallelism=f"replicas x{world}", activations="q8" if args.act_q8 else "bf16"),
         "timing": f"CUDA events on the launch stream around K replays of one step's CUDA graph "
                   f"(fw_moe_graph_create / fw_moe_graph_launch); median of {args.repeats} repeats",
         "roofline": res["roofline"], "whole_step": res["whole_step"], "kernels": res["kernels"],

@@ -70,6 +70,13 @@ typedef struct {
                          * The decode kernel holds a call's x in shared memory: one token
                          * up to H = 14336, several up to H = 2048; calls past that take
                          * the prefill path whatever their T. */
+  int32_t act_q8;       /* 0: bf16 activations (the default step). 1: Q8 activations on the
+                         * decode path (the Flyweight README, §Quantization: Q8-activation
+                         * dp4a decode kernels): each token's x quantised per 32-block and
+                         * each expert's h = SiLU(g)*u per 16-block by the Q8_0 rule in fp32
+                         * (d = amax/127, codes round-half-away(v/d)), integer dot products
+                         * with the Q8_0 weights, scales applied per block. The prefill path
+                         * keeps bf16 activations (sm_103a has no int8 tensor-core MMA). */
 } fw_moe_config;
 
 typedef struct { /* all DEVICE pointers, read only during fw_moe_init */

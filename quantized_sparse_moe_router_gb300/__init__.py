@@ -27,7 +27,8 @@ STATUS_NAMES = {0: "FW_OK", -1: "FW_EINVAL", -2: "FW_ENOMEM", -3: "FW_ECUDA", -4
 
 class FwMoeConfig(ctypes.Structure):
     _fields_ = [("H", ctypes.c_int32), ("I", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
-                ("n_shared", ctypes.c_int32), ("T_max", ctypes.c_int32), ("decode_T_max", ctypes.c_int32)]
+                ("n_shared", ctypes.c_int32), ("T_max", ctypes.c_int32), ("decode_T_max", ctypes.c_int32),
+                ("act_q8", ctypes.c_int32)]
 
 
 class FwMoeWeights(ctypes.Structure):
@@ -245,9 +246,9 @@ class MoELayer:
     after construction.
     """
 
-    def __init__(self, H, I, E, k, n_shared=0, T_max=16, decode_T_max=0, weights=None, stream=None):
+    def __init__(self, H, I, E, k, n_shared=0, T_max=16, decode_T_max=0, weights=None, stream=None, act_q8=False):
         self.H, self.I, self.E, self.k, self.S, self.T_max = H, I, E, k, n_shared, T_max
-        cfg = FwMoeConfig(H, I, E, k, n_shared, T_max, decode_T_max)
+        cfg = FwMoeConfig(H, I, E, k, n_shared, T_max, decode_T_max, 1 if act_q8 else 0)
         w = FwMoeWeights()
         for name, _ in FwMoeWeights._fields_:
             t = weights.get(name) if weights else None

@@ -85,6 +85,7 @@ fw_status check_config(const fw_moe_config* c) {
   if (c->T_max < 1 || c->T_max > (1 << 20)) return fail(FW_EINVAL, "T_max=%d must be in [1, 2^20]", c->T_max);
   if (c->decode_T_max < 0 || c->decode_T_max > kMaxDecodeT)
     return fail(FW_EINVAL, "decode_T_max=%d must be in [0, 16]", c->decode_T_max);
+  if (c->act_q8 != 0 && c->act_q8 != 1) return fail(FW_EINVAL, "act_q8=%d must be 0 or 1", c->act_q8);
   return FW_OK;
 }
 

@@ -129,6 +129,30 @@ __device__ __forceinline__ int seg_dot_i(const uint4 q, const uint4 hi, const ui
   return sh * 256 + (int)sl;
 }
 
+// The same with Q8 activations: one signed plane, sum_i (q_i + 128) * x8_i.
+__device__ __forceinline__ int seg_dot_q8(const uint4 q, const uint4 x8) {
+  int s = dp4a_us(q.x, x8.x, 0);
+  s = dp4a_us(q.y, x8.y, s);
+  s = dp4a_us(q.z, x8.z, s);
+  return dp4a_us(q.w, x8.w, s);
+}
+template <bool kQ8>
+__device__ __forceinline__ int seg_dot(const uint4 q, const uint4 hi, const uint4 lo) {
+  if constexpr (kQ8)
+    return seg_dot_q8(q, hi);
+  else
+    return seg_dot_i(q, hi, lo);
+}
+
+// Q8 code of v in a block of scale d (d > 0): round-half-away of the fp32
+// quotient, clamped to [-127, 127].
+__device__ __forceinline__ int q8_code(float v, float d) {
+  return ::max(-127, ::min(127, (int)roundf(__fdiv_rn(v, d))));
+}
+__device__ __forceinline__ uint32_t pack_s8x4(int a, int b, int c, int d) {
+  return ((uint32_t)a & 0xFFu) | (((uint32_t)b & 0xFFu) << 8) | (((uint32_t)c & 0xFFu) << 16) | ((uint32_t)d << 24);
+}
+
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + expf(-g)); }
 
 __device__ __forceinline__ void consumer_sync() {
@@ -180,6 +204,38 @@ __device__ __forceinline__ void x_segment_to_planes(const uint4 a, const uint4 b
   hi = make_uint4(h4[0], h4[1], h4[2], h4[3]);
   lo = make_uint4(l4[0], l4[1], l4[2], l4[3]);
   info = make_int2((int)((emax - 14u) << 23), 128 * sum);  // float bits of 2^(e - 14), offset term
+}
+
+// Q8 activations: one 32-value block of bf16 x (four 16-byte words) -> two
+// segments of signed codes, each with the block's scale d = amax/127 (fp32
+// division) as its float and 128 * sum(codes); an all-zero block: zeros.
+__device__ __forceinline__ void x_block_to_q8(const uint4 a, const uint4 b, const uint4 c, const uint4 e, uint4& q0,
+                                              uint4& q1, int2& i0, int2& i1) {
+  const uint32_t w[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w, e.x, e.y, e.z, e.w};
+  float amax = 0.f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i)
+    amax = fmaxf(amax, fmaxf(fabsf(__uint_as_float(w[i] << 16)), fabsf(__uint_as_float(w[i] & 0xFFFF0000u))));
+  if (amax == 0.f) {
+    q0 = q1 = make_uint4(0u, 0u, 0u, 0u);
+    i0 = i1 = make_int2(0, 0);
+    return;
+  }
+  const float d = __fdiv_rn(amax, 127.0f);
+  uint32_t p[8];
+  int s0 = 0, s1 = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int c0 = q8_code(__uint_as_float(w[2 * j] << 16), d), c1 = q8_code(__uint_as_float(w[2 * j] & 0xFFFF0000u), d);
+    const int c2 = q8_code(__uint_as_float(w[2 * j + 1] << 16), d),
+              c3 = q8_code(__uint_as_float(w[2 * j + 1] & 0xFFFF0000u), d);
+    p[j] = pack_s8x4(c0, c1, c2, c3);
+    if (j < 4) s0 += c0 + c1 + c2 + c3; else s1 += c0 + c1 + c2 + c3;
+  }
+  q0 = make_uint4(p[0], p[1], p[2], p[3]);
+  q1 = make_uint4(p[4], p[5], p[6], p[7]);
+  i0 = make_int2(__float_as_int(d), 128 * s0);
+  i1 = make_int2(__float_as_int(d), 128 * s1);
 }
 
 // The chunk's h of one token (16 fp32 values in shared memory) -> the same
@@ -241,6 +297,52 @@ __device__ __forceinline__ void h16_to_planes_warp(const float* h, HPlanes* out,
   if (lane == 0) out->info = emax >= 15u ? make_int2((int)((emax - 14u) << 23), 128 * sum) : make_int2(0, 0);
 }
 
+// Q8 activations: the chunk's h of one token (16 fp32 values) -> signed codes
+// at d = amax/127, (float bits of d, 128 * sum); all zero: zeros.
+__device__ __forceinline__ void h16_to_q8(const float* h, uint4& q, int2& info) {
+  const float4* h4 = reinterpret_cast<const float4*>(h);
+  float amax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float4 v = h4[j];
+    amax = fmaxf(amax, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+  if (amax == 0.f) {
+    q = make_uint4(0u, 0u, 0u, 0u);
+    info = make_int2(0, 0);
+    return;
+  }
+  const float d = __fdiv_rn(amax, 127.0f);
+  uint32_t p[4];
+  int sum = 0;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float4 v = h4[j];
+    const int c0 = q8_code(v.x, d), c1 = q8_code(v.y, d), c2 = q8_code(v.z, d), c3 = q8_code(v.w, d);
+    sum += c0 + c1 + c2 + c3;
+    p[j] = pack_s8x4(c0, c1, c2, c3);
+  }
+  q = make_uint4(p[0], p[1], p[2], p[3]);
+  info = make_int2(__float_as_int(d), 128 * sum);
+}
+__device__ __forceinline__ void h16_to_q8_warp(const float* h, HPlanes* out, int lane) {
+  const float v = lane < 16 ? h[lane] : 0.f;
+  // |v| as unsigned bits orders like |v| itself
+  const float amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(v) & 0x7FFFFFFFu));
+  int c = 0;
+  float d = 0.f;
+  if (amax > 0.f) {
+    d = __fdiv_rn(amax, 127.0f);
+    c = lane < 16 ? q8_code(v, d) : 0;
+  }
+  const int sum = __reduce_add_sync(0xFFFFFFFFu, c);
+  uint32_t qw = ((uint32_t)c & 0xFFu) << ((lane & 3) * 8);
+  qw |= __shfl_xor_sync(0xFFFFFFFFu, qw, 1);
+  qw |= __shfl_xor_sync(0xFFFFFFFFu, qw, 2);
+  if (lane < 16 && (lane & 3) == 0) reinterpret_cast<uint32_t*>(&out->hi)[lane >> 2] = qw;
+  if (lane == 0) out->info = make_int2(__float_as_int(d), 128 * sum);
+}
+
 // Four consecutive fp32 columns of this thread's tensor-memory lane (the
 // several-token path keeps its partial output there: 64 per thread would not
 // fit in registers beside the rest).
@@ -263,7 +365,7 @@ constexpr uint32_t kTmemCols = 512;  // several tokens: 16 warps x (16 tokens x 
 // ------------------------------------------------------------- the kernel
 // kMulti: several tokens (T <= 16, H <= 2048; partial output in registers);
 // otherwise one token (partial output in shared memory).
-template <bool kMulti>
+template <bool kMulti, bool kQ8>
 __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[kMaxStages], empty[kMaxStages];
@@ -274,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   __shared__ uint32_t s_pref[kMaxE + 2];     // several tokens: chunk cost before each touched expert
   __shared__ volatile int s_abort;  // a consumer gave up a wait: the others stop waiting too
   __shared__ uint32_t s_tmem;        // several tokens: tensor-memory base of the partial outputs
+  __shared__ HPlanes s_hq;           // one token, Q8 activations: the chunk's h codes
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int H = a.H, I = a.I, T = kMulti ? a.T : 1, R = a.R, Dr = a.Dr;
   const int nseg = H / 16;
@@ -306,14 +409,62 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
   if (warp != kProducer) {
     // x is complete: the router lets this grid launch only after everything
     // before it in the stream has completed. Staged while the router still runs.
-    for (int c = tid; c < T * nseg; c += kCT) {
-      const uint4* src = reinterpret_cast<const uint4*>(a.x) + 2 * c;
-      uint4 hi, lo;
-      int2 info;
-      x_segment_to_planes(__ldg(src), __ldg(src + 1), hi, lo, info);
-      reinterpret_cast<uint4*>(xhi)[c] = hi;
-      reinterpret_cast<uint4*>(xlo)[c] = lo;
-      xinfo[c] = info;
+    if constexpr (kQ8 && kMulti) {
+      // Q8 activations, one plane, several tokens: a thread per 32-value
+      // block (two segments); the work is spread over all threads already
+      for (int c = tid; c < T * nseg / 2; c += kCT) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.x) + 4 * c;
+        uint4 q0, q1;
+        int2 i0, i1;
+        x_block_to_q8(__ldg(src), __ldg(src + 1), __ldg(src + 2), __ldg(src + 3), q0, q1, i0, i1);
+        reinterpret_cast<uint4*>(xhi)[2 * c] = q0;
+        reinterpret_cast<uint4*>(xhi)[2 * c + 1] = q1;
+        xinfo[2 * c] = i0;
+        xinfo[2 * c + 1] = i1;
+      }
+    } else if constexpr (kQ8) {
+      // Q8 activations, one plane, one token: four values a thread (a block
+      // a thread would leave most threads idle), a 32-value block
+      // over eight lanes (its amax and each 16-value segment's code sum by
+      // shuffles within the group); whole warps, so the trip count is uniform
+      const int n4 = T * H / 4;
+      for (int c0 = warp * 32; c0 < n4; c0 += kCW * 32) {
+        const int c = c0 + lane;
+        const bool in = c < n4;  // n4 is a multiple of 8: a group is all in or all out
+        const uint2 v = in ? __ldg(reinterpret_cast<const uint2*>(a.x) + c) : make_uint2(0u, 0u);
+        const float f0 = __uint_as_float(v.x << 16), f1 = __uint_as_float(v.x & 0xFFFF0000u),
+                    f2 = __uint_as_float(v.y << 16), f3 = __uint_as_float(v.y & 0xFFFF0000u);
+        float amax = fmaxf(fmaxf(fabsf(f0), fabsf(f1)), fmaxf(fabsf(f2), fabsf(f3)));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+        int q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+        float d = 0.f;
+        if (amax > 0.f) {
+          d = __fdiv_rn(amax, 127.0f);
+          q0 = q8_code(f0, d);
+          q1 = q8_code(f1, d);
+          q2 = q8_code(f2, d);
+          q3 = q8_code(f3, d);
+        }
+        int sum = q0 + q1 + q2 + q3;
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 1);
+        sum += __shfl_xor_sync(0xFFFFFFFFu, sum, 2);  // the 16-value segment's four lanes
+        if (in) {
+          reinterpret_cast<uint32_t*>(xhi)[c] = pack_s8x4(q0, q1, q2, q3);
+          if ((lane & 3) == 0) xinfo[c >> 2] = make_int2(__float_as_int(d), 128 * sum);
+        }
+      }
+    } else {
+      for (int c = tid; c < T * nseg; c += kCT) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.x) + 2 * c;
+        uint4 hi, lo;
+        int2 info;
+        x_segment_to_planes(__ldg(src), __ldg(src + 1), hi, lo, info);
+        reinterpret_cast<uint4*>(xhi)[c] = hi;
+        reinterpret_cast<uint4*>(xlo)[c] = lo;
+        xinfo[c] = info;
+      }
     }
     if (!kMulti)
       for (int o = tid; o < H; o += kCT) acc_s[o] = 0.f;
@@ -521,11 +672,11 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
               const uint4 qg = *reinterpret_cast<const uint4*>(grow + s * 16);
               const uint4 qu = *reinterpret_cast<const uint4*>(urow + s * 16);
               const uint4 vh = *reinterpret_cast<const uint4*>(xh + s * 16);
-              const uint4 vl = *reinterpret_cast<const uint4*>(xl + s * 16);
+              const uint4 vl = kQ8 ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4*>(xl + s * 16);
               const int2 inf = xi[s];
               const float f = __int_as_float(inf.x);
-              const int Sg = seg_dot_i(qg, vh, vl) - inf.y;
-              const int Su = seg_dot_i(qu, vh, vl) - inf.y;
+              const int Sg = seg_dot<kQ8>(qg, vh, vl) - inf.y;
+              const int Su = seg_dot<kQ8>(qu, vh, vl) - inf.y;
               ag = fmaf((float)Sg, half_bits_to_f32(sg[s >> 1]) * f, ag);
               au = fmaf((float)Su, half_bits_to_f32(su[s >> 1]) * f, au);
             }
@@ -543,8 +694,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
         }
       }
       consumer_sync();  // the chunk's h is complete
+      if constexpr (!kMulti && kQ8) {  // one token, Q8: its h codes once, by one warp (sixteen divisions)
+        if (warp == 0) h16_to_q8_warp(hb, &s_hq, lane);
+        consumer_sync();
+      }
       if (kMulti) {  // each token's h -> fixed-point planes, a warp per token
-        for (int m = warp; m < ui.z; m += kCW) h16_to_planes_warp(hb + m * kChunk, hpl + m, lane);
+        for (int m = warp; m < ui.z; m += kCW) {
+          if constexpr (kQ8)
+            h16_to_q8_warp(hb + m * kChunk, hpl + m, lane);
+          else
+            h16_to_planes_warp(hb + m * kChunk, hpl + m, lane);
+        }
         consumer_sync();
       }
       uint4 dhh = make_uint4(0u, 0u, 0u, 0u), dhl = dhh;  // one token: the chunk's h planes
@@ -579,7 +739,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
                 d[jr] = 0.f;
                 if (rr < nr) {
                   const uint4 qq = *reinterpret_cast<const uint4*>(sb + (size_t)rr * kChunk);
-                  d[jr] = (float)(seg_dot_i(qq, hh, hl) - inf.y) * (gf * half_bits_to_f32(sc[rr]));
+                  d[jr] = (float)(seg_dot<kQ8>(qq, hh, hl) - inf.y) * (gf * half_bits_to_f32(sc[rr]));
                 }
               }
               float4 v = tmem_ld4(tacc + 4 * t);
@@ -592,12 +752,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
           } else {
             // (the chunk's h planes: the same in every down stage of the chunk)
             if (q == 0) {
-              h16_to_planes(hb, dhh, dhl, dhinf);
+              if constexpr (kQ8) {  // quantised by warp 0 after the chunk's gate/up
+                dhh = s_hq.hi;
+                dhinf = s_hq.info;
+              } else {
+                h16_to_planes(hb, dhh, dhl, dhinf);
+              }
               dgf = r.gates[r.slot[ui.y]] * __int_as_float(dhinf.x);
             }
             for (int rr = tid; rr < nr; rr += kCT) {
               const uint4 qq = *reinterpret_cast<const uint4*>(sb + (size_t)rr * kChunk);
-              const int S = seg_dot_i(qq, dhh, dhl) - dhinf.y;
+              const int S = seg_dot<kQ8>(qq, dhh, dhl) - dhinf.y;
               acc_s[r0 + rr] = fmaf((float)S, dgf * half_bits_to_f32(sc[rr]), acc_s[r0 + rr]);
             }
           }
@@ -714,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_experts_kernel(DecodeArgs 
 // init), so once earlier work has drained all of them are; if something else
 // holds SMs past the wait bound the call reports FW_ETIMEOUT instead of
 // hanging.
-cudaError_t launch(const DecodeArgs& a, bool multi, unsigned grid, size_t smem, cudaStream_t s) {
+cudaError_t launch(const DecodeArgs& a, bool multi, bool q8, unsigned grid, size_t smem, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kThreads);
@@ -725,8 +890,11 @@ cudaError_t launch(const DecodeArgs& a, bool multi, unsigned grid, size_t smem, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return multi ? cudaLaunchKernelEx(&cfg, decode_experts_kernel<true>, a)
-               : cudaLaunchKernelEx(&cfg, decode_experts_kernel<false>, a);
+  if (q8)
+    return multi ? cudaLaunchKernelEx(&cfg, decode_experts_kernel<true, true>, a)
+                 : cudaLaunchKernelEx(&cfg, decode_experts_kernel<false, true>, a);
+  return multi ? cudaLaunchKernelEx(&cfg, decode_experts_kernel<true, false>, a)
+               : cudaLaunchKernelEx(&cfg, decode_experts_kernel<false, false>, a);
 }
 
 int g_smem_optin = 0;  // dynamic shared memory per CTA the kernels may use
@@ -739,12 +907,17 @@ cudaError_t configure_decode_kernels() {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&g_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  cudaFuncAttributes fa, fb;
-  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, decode_experts_kernel<false>);
-  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fb, decode_experts_kernel<true>);
-  if (e == cudaSuccess) g_smem_optin -= (int)std::max(fa.sharedSizeBytes, fb.sharedSizeBytes);
-  const void* kern[2] = {(const void*)decode_experts_kernel<false>, (const void*)decode_experts_kernel<true>};
-  for (int m = 0; m < 2 && e == cudaSuccess; ++m) {
+  const void* kern[4] = {(const void*)decode_experts_kernel<false, false>,
+                         (const void*)decode_experts_kernel<true, false>,
+                         (const void*)decode_experts_kernel<false, true>, (const void*)decode_experts_kernel<true, true>};
+  cudaFuncAttributes fk[4];
+  size_t static_max = 0;
+  for (int m = 0; m < 4 && e == cudaSuccess; ++m) {
+    e = cudaFuncGetAttributes(&fk[m], kern[m]);
+    static_max = std::max(static_max, fk[m].sharedSizeBytes);
+  }
+  if (e == cudaSuccess) g_smem_optin -= (int)static_max;
+  for (int m = 0; m < 4 && e == cudaSuccess; ++m) {
     e = cudaFuncSetAttribute(kern[m], cudaFuncAttributeMaxDynamicSharedMemorySize, g_smem_optin);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(kern[m], cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -752,11 +925,11 @@ cudaError_t configure_decode_kernels() {
   }
   // one CTA per SM must fit with the least shared memory a launch asks for:
   // the grid-wide wait relies on every CTA of the grid being resident
-  for (int m = 0; m < 2 && e == cudaSuccess; ++m) {
+  for (int m = 0; m < 4 && e == cudaSuccess; ++m) {
     int n = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern[m], kThreads, (size_t)g_smem_optin / 2 + 1024);
     if (e == cudaSuccess && n < 1) {
-      cudaFuncAttributes f = m ? fb : fa;
+      const cudaFuncAttributes& f = fk[m];
       char msg[256];
       snprintf(msg, sizeof(msg),
                "decode kernel: no CTA of %d threads fits an SM (registers %d, static smem %zu, dynamic %d)",
@@ -801,7 +974,8 @@ cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfl
   a.stage_bytes = std::max((uint32_t)(2 * R) * rb, align128((uint32_t)a.Dr * 18u));
   a.stage_bytes = align128(a.stage_bytes);
   // dynamic shared memory: x planes, segment info, the one-token partial row, h
-  const uint32_t xb = align128((uint32_t)(2 * T * H));
+  const bool q8 = h->cfg.act_q8 != 0;  // Q8 activations: one code plane instead of two
+  const uint32_t xb = align128((uint32_t)((q8 ? 1 : 2) * T * H));
   a.off_info = xb;
   a.off_acc = a.off_info + align128((uint32_t)(T * (H / 16) * 8));
   a.off_h = a.off_acc + (multi ? 0u : align128((uint32_t)H * 4u));
@@ -839,7 +1013,7 @@ cudaError_t launch_ffn_decode(Handle* h, const __nv_bfloat16* x, int T, __nv_bfl
   const size_t smem = std::max<size_t>(a.off_ring + (size_t)a.stages * a.stage_bytes,
                                        (size_t)g_smem_optin / 2 + 1024);
   KernelTimer tm(h, FW_KERNEL_DECODE_EXPERTS, s);
-  return launch(a, multi, (unsigned)grid, smem, s);
+  return launch(a, multi, q8, (unsigned)grid, smem, s);
 }
 
 }  // namespace fw

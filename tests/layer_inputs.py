@@ -88,11 +88,11 @@ class DeviceLayer:
                      shared_down=self.q[KIND_DOWN][E])
         return d
 
-    def make(self, T_max, decode_T_max=0):
+    def make(self, T_max, decode_T_max=0, act_q8=False):
         import quantized_sparse_moe_router_gb300 as fw
         w = self.w
         return fw.MoELayer(w.H, w.I, w.E, w.k, n_shared=w.S, T_max=T_max, decode_T_max=decode_T_max,
-                           weights=self.weights())
+                           weights=self.weights(), act_q8=act_q8)
 
 
 class OracleLayer:

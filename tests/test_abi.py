@@ -35,7 +35,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def _cfg(**kw):
-    d = dict(H=256, I=128, E=8, k=2, n_shared=0, T_max=4, decode_T_max=0)
+    d = dict(H=256, I=128, E=8, k=2, n_shared=0, T_max=4, decode_T_max=0, act_q8=0)
     d.update(kw)
     return fw.FwMoeConfig(**d)
 
@@ -44,7 +44,7 @@ def _cfg(**kw):
     (dict(H=96), fw.FW_EUNSUPPORTED), (dict(I=0), fw.FW_EUNSUPPORTED), (dict(E=0), fw.FW_EUNSUPPORTED),
     (dict(E=300), fw.FW_EUNSUPPORTED), (dict(k=0), fw.FW_EINVAL), (dict(k=9), fw.FW_EINVAL),
     (dict(k=17, E=32), fw.FW_EINVAL), (dict(n_shared=2), fw.FW_EINVAL), (dict(T_max=0), fw.FW_EINVAL),
-    (dict(decode_T_max=17), fw.FW_EINVAL),
+    (dict(decode_T_max=17), fw.FW_EINVAL), (dict(act_q8=2), fw.FW_EINVAL),
 ])
 def test_init_rejects_bad_config(bad, status):
     h = ctypes.c_void_p()
