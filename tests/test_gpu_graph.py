@@ -93,3 +93,24 @@ def test_graph_refuses_a_profiling_layer():
     assert ei.value.status == fw.FW_ESTATE
     fw.fw_moe_profile_end(layer.handle)
     layer.close()
+
+
+def test_graph_of_q8_activation_layers_matches_direct_calls():
+    """The graph captures whatever each layer does: Q8-activation decode layers replay bit for bit."""
+    wl = synth.WORKLOADS["tiny"].with_(T=3, S=1)
+    n = 2
+    layers = [DeviceLayer(wl, l, DEV).make(T_max=16, act_q8=True) for l in range(n)]
+    ol0 = OracleLayer(wl, 0)
+    x = hidden_with_margins(wl, 0, ol0.Wr, ol0.bias)
+    bufs = [to_device_bf16(x, DEV)] + [torch.zeros((wl.T, wl.H), dtype=torch.bfloat16, device=DEV) for _ in range(n)]
+    ids = [torch.empty((wl.T, wl.k), dtype=torch.int32, device=DEV) for _ in range(n)]
+    g = fw.MoEGraph(layers, bufs[:n], bufs[1:], ids)
+    g.launch()
+    torch.cuda.synchronize()
+    ids_d, outs_d = direct_chain(layers, bufs[0], wl.T, wl.H, wl.k)
+    torch.cuda.synchronize()
+    for i in range(n):
+        assert torch.equal(ids[i], ids_d[i]) and torch.equal(bufs[i + 1], outs_d[i])
+    g.close()
+    for L in layers:
+        L.close()
