@@ -365,7 +365,9 @@ def time_workload(w, layers, args, world, dev, e2e: bool):
         k_us = min(ev_us, call_us) if ev_us else call_us
         achieved = dom_bytes / (k_us / 1e6) / 1e9
         roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
-                    "frac": round(achieved / hbm, 4), "traffic": measured_traffic(dom, w.name), "kernel": dom,
+                    "frac": round(achieved / hbm, 4),
+                    # the committed captures are of the bf16-activation kernel: none for the Q8 one
+                    "traffic": None if args.act_q8 else measured_traffic(dom, w.name), "kernel": dom,
                     "avg_launch_us": round(k_us, 3), "event_pass_us": round(ev_us, 3),
                     "algorithmic_bytes_per_launch": round(dom_bytes),
                     "peak_source": f"{peak_src} hbm_gbs (STREAM-style copy)"}
